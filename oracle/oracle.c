@@ -1,0 +1,550 @@
+/*
+ * oracle.c -- plain, slow, scalar CPU oracle for batch speculative-decoding
+ * verification and the ragged-to-rectangular realignment it forces.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the library's product path may link,
+ * load or call this file; only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg do.  It shares no code, header, table or constant with the
+ * CUDA path: every definition below is restated from the pages it cites.
+ *
+ * Pages cited (by title and section):
+ *   [CF]  "Correctness Forensics for Batch Speculative Decoding: Diagnosing the
+ *         Ragged Tensor Problem" (source-linked summary of arXiv 2510.22876v4)
+ *   [ZS]  "Chapter 10 Speculative Decoding (Code Walkthrough)" (zero-to-sglang)
+ *   [SDR] "Design Document -- speculative-decoding-real"
+ *   [AL]  "Speculative decoding: proposals and verified output" (Atlas lesson)
+ *
+ * Arithmetic: probabilities in fp64 (double); logits are read exactly from
+ * their storage type (fp32, bf16 or fp16 bit patterns) into double.
+ *
+ * Pins: every function here is checked in tests/test_oracle_*.py against
+ * values the pages print, closed forms, brute force on tiny inputs and planted
+ * mistakes (the oracle_set_mutant switch below).  The length-grouping policy
+ * (oracle_group_by_length) is this project's own construction because the
+ * pages give the EXSPEC scheduling appendix as a heading with no body: its
+ * parity is UNPINNED by the pages (it is only checked against an independent
+ * brute-force restatement of the same policy).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ */
+/* storage types of the logits                                         */
+/* ------------------------------------------------------------------ */
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2 };
+
+/* IEEE binary16 -> double, from the format's definition (1 sign bit, 5
+   exponent bits with bias 15, 10 fraction bits; exponent 0 = subnormal,
+   exponent 31 = inf / NaN). */
+static double half_bits_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(m | 0x400), e - 25);
+    return sign ? -v : v;
+}
+
+/* bfloat16 is the upper half of an IEEE binary32. */
+static double bf16_bits_to_double(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double logit_at(const void *x, int dtype, int64_t i)
+{
+    if (dtype == ORACLE_F32)
+        return (double)((const float *)x)[i];
+    if (dtype == ORACLE_BF16)
+        return bf16_bits_to_double(((const uint16_t *)x)[i]);
+    return half_bits_to_double(((const uint16_t *)x)[i]);
+}
+
+/* ------------------------------------------------------------------ */
+/* planted mistakes, used only by the tests to show that the pins catch */
+/* them; 0 = the correct oracle                                          */
+/* ------------------------------------------------------------------ */
+enum {
+    MUT_NONE = 0,
+    MUT_TIE_HIGHEST = 1,      /* argmax keeps the highest index among ties  */
+    MUT_ROW_SHIFT = 2,        /* proposal j checked against row j+1         */
+    MUT_RESAMPLE_FROM_P = 3,  /* correction drawn from p, not the residual  */
+    MUT_BONUS_FROM_DRAFT = 4, /* bonus drawn from the last draft row        */
+    MUT_NO_CLAMP = 5,         /* residual p-q without the positive part     */
+    MUT_CDF_GE = 6,           /* inverse CDF tests C_i >= target            */
+    MUT_SKIP_KV_SHIFT = 7,    /* realign updates lengths but moves no KV    */
+    MUT_STALE_POSITIONS = 8,  /* position/mask rebuild writes nothing       */
+    MUT_BONUS_ALWAYS = 9,     /* bonus appended even after a rejection      */
+    MUT_SHIFT_ONE_SHORT = 10  /* KV run moved one row short                 */
+};
+static int g_mutant = MUT_NONE;
+void oracle_set_mutant(int m) { g_mutant = m; }
+
+/* ------------------------------------------------------------------ */
+/* O1  greedy verification                                              */
+/* ------------------------------------------------------------------ */
+
+/* Index of the largest value of row x[off .. off+V): the lowest index among
+   equal maxima, and a NaN counts as larger than every number (the first NaN
+   wins).  The pages name tie-breaking as a source of divergence without fixing
+   it ([CF] §4.2); lowest-index is the reading taken here. */
+static int argmax_row(const void *x, int dtype, int64_t off, int V)
+{
+    int best = 0;
+    double bv = logit_at(x, dtype, off);
+    for (int v = 1; v < V; ++v) {
+        if (isnan(bv))
+            break;
+        double xv = logit_at(x, dtype, off + v);
+        int better = isnan(xv) || xv > bv;
+        if (g_mutant == MUT_TIE_HIGHEST)
+            better = better || xv == bv;
+        if (better) {
+            best = v;
+            bv = xv;
+        }
+    }
+    return best;
+}
+
+/*
+ * Greedy commitment of one verification round for every sequence of a batch,
+ * restating the teaching function greedy_commit ([ZS] §4.1) and steps 4-6 of
+ * the standard greedy algorithm ([SDR] "Standard Greedy Algorithm"):
+ *   - row j of sequence b (j < k_b) verifies proposal j; row k_b gives the
+ *     bonus ([ZS] §3.3: with confirmed prefix L, rows L-1 .. L+k-2 verify and
+ *     row L+k-1 gives the extra token; here those rows arrive as j = 0..k);
+ *   - the argmax t of row j is committed; the round stops after it when t is
+ *     EOS, when the output budget is reached, or when t differs from the
+ *     proposal (t is then the correction);
+ *   - after all k_b proposals are accepted the argmax of row k_b is the bonus,
+ *     drawn from the target ([CF] App. D).
+ *
+ * logits       [B, k+1, V] in `dtype`
+ * draft_tokens [B, k]
+ * draft_len    [B] or NULL (NULL: every sequence has k proposals)
+ * eos_id       token that ends a sequence, or negative for none
+ * remaining    [B] output budget or NULL (NULL: unlimited); 0 commits nothing
+ * out_tokens   [B, k+1] committed tokens, -1 after the last one
+ * n_accept     [B] committed tokens that are accepted proposals
+ * n_emit       [B] committed tokens (accepted + correction/bonus)
+ */
+void oracle_verify_greedy(const void *logits, int dtype, int B, int k, int V,
+                          const int32_t *draft_tokens, const int32_t *draft_len,
+                          int32_t eos_id, const int32_t *remaining,
+                          int32_t *out_tokens, int32_t *n_accept, int32_t *n_emit)
+{
+    for (int b = 0; b < B; ++b) {
+        int kb = draft_len ? draft_len[b] : k;
+        int64_t rem = remaining ? remaining[b] : INT64_MAX;
+        int32_t *out = out_tokens + (int64_t)b * (k + 1);
+        int ne = 0, na = 0, stopped = 0;
+        for (int i = 0; i <= k; ++i)
+            out[i] = -1;
+        if (rem > 0) {
+            for (int j = 0; j < kb; ++j) {
+                int row = (g_mutant == MUT_ROW_SHIFT) ? j + 1 : j;
+                int t = argmax_row(logits, dtype, ((int64_t)b * (k + 1) + row) * V, V);
+                int match = (t == draft_tokens[(int64_t)b * k + j]);
+                out[ne++] = t;
+                if (match)
+                    na++;
+                if ((eos_id >= 0 && t == eos_id) || ne == rem || !match) {
+                    stopped = 1;
+                    break;
+                }
+            }
+            if (!stopped || g_mutant == MUT_BONUS_ALWAYS) {
+                if (ne < k + 1 && ne < rem)
+                    out[ne++] = argmax_row(logits, dtype, ((int64_t)b * (k + 1) + kb) * V, V);
+            }
+        }
+        n_accept[b] = na;
+        n_emit[b] = ne;
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* O2  stochastic verification                                           */
+/* ------------------------------------------------------------------ */
+
+/* p = softmax(x / T) of one row in fp64: m = max z, p_v = e^(z_v - m) / sum.
+   Returns 1 when the row holds a non-finite logit or the sum is not finite. */
+static int softmax_row(const void *x, int dtype, int64_t off, int V, double T, double *p)
+{
+    int bad = 0;
+    double m = -INFINITY;
+    for (int v = 0; v < V; ++v) {
+        double z = logit_at(x, dtype, off + v) / T;
+        p[v] = z;
+        if (!isfinite(z))
+            bad = 1;
+        if (z > m)
+            m = z;
+    }
+    double s = 0.0;
+    for (int v = 0; v < V; ++v) {
+        p[v] = exp(p[v] - m);
+        s += p[v];
+    }
+    for (int v = 0; v < V; ++v)
+        p[v] /= s;
+    if (!isfinite(s) || s <= 0.0)
+        bad = 1;
+    return bad;
+}
+
+/* Inverse CDF of the weights w[0..V) at uniform u in [0,1): the smallest i
+   whose sequential fp64 prefix sum C_i exceeds u * sum(w).  If rounding leaves
+   no such i, the last index with positive weight.  A zero-weight index is
+   therefore never returned. */
+static int inverse_cdf(const double *w, int V, double u)
+{
+    double total = 0.0;
+    for (int i = 0; i < V; ++i)
+        total += w[i];
+    double target = u * total;
+    double c = 0.0;
+    for (int i = 0; i < V; ++i) {
+        c += w[i];
+        int hit = (g_mutant == MUT_CDF_GE) ? (c >= target) : (c > target);
+        if (hit)
+            return i;
+    }
+    for (int i = V - 1; i >= 0; --i)
+        if (w[i] > 0.0)
+            return i;
+    return V - 1;
+}
+
+/*
+ * Stochastic verification of one round ([ZS] §5.1; [AL] "The mechanism" steps
+ * 2-4 and "Acceptance and rejection correction"):
+ *   - p_j = softmax(x_j / T) of target row j; q_j = draft_probs[b, j, :];
+ *   - proposal y = d_j is accepted iff u_{b,j} < p_j(y) / q_j(y), which is
+ *     acceptance with probability min(1, p/q) since u < 1;
+ *   - on the first rejection the correction is drawn from the normalised
+ *     positive residual r = max(0, p_j - q_j) / sum(...) and the round stops;
+ *     the residual is used only when its sum is positive ([AL] "Assumptions";
+ *     [ZS] "check numerical validity"); otherwise the draw is from p_j and
+ *     flag bit 2 is set;
+ *   - after k_b acceptances the bonus is drawn from p_{k_b}, the target
+ *     ([CF] App. D), never from the draft;
+ *   - one uniform per ratio test (columns 0..k-1) and a single uniform for
+ *     the one draw of the round (column k) -- this layout is this project's
+ *     reading: the page draws them with separate torch.rand / multinomial;
+ *   - EOS and the output budget stop the round as in greedy commitment.
+ * Flags per sequence: 1 = a tested proposal had q(y) = 0 (the page says such a
+ * symbol cannot be proposed; IEEE then gives +inf -> accept when p > 0, or
+ * NaN -> reject when p = 0), 2 = zero residual mass, 4 = a non-finite logit in
+ * a row that was used.
+ *
+ * out_residual [B, V] (or NULL): the normalised distribution the final draw
+ * came from (residual, or p on zero residual, or the bonus row's p); rows of
+ * sequences that drew nothing are left untouched.
+ */
+void oracle_verify_sample(const void *logits, int dtype, double temperature,
+                          const float *draft_probs, const int32_t *draft_tokens,
+                          const float *uniforms, int B, int k, int V,
+                          const int32_t *draft_len, int32_t eos_id,
+                          const int32_t *remaining, int32_t *out_tokens,
+                          int32_t *n_accept, int32_t *n_emit, double *out_residual,
+                          uint32_t *flags)
+{
+    double *p = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    double *w = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    for (int b = 0; b < B; ++b) {
+        int kb = draft_len ? draft_len[b] : k;
+        int64_t rem = remaining ? remaining[b] : INT64_MAX;
+        int32_t *out = out_tokens + (int64_t)b * (k + 1);
+        const float *u = uniforms + (int64_t)b * (k + 1);
+        uint32_t fl = 0;
+        int ne = 0, na = 0, stopped = 0, draw_row = -1, draw_residual = 0;
+        for (int i = 0; i <= k; ++i)
+            out[i] = -1;
+        if (rem > 0) {
+            for (int j = 0; j < kb; ++j) {
+                int y = draft_tokens[(int64_t)b * k + j];
+                const float *q = draft_probs + ((int64_t)b * k + j) * V;
+                if (softmax_row(logits, dtype, ((int64_t)b * (k + 1) + j) * V, V, temperature, p))
+                    fl |= 4;
+                if (q[y] == 0.0f)
+                    fl |= 1;
+                double ratio = p[y] / (double)q[y];
+                if ((double)u[j] < ratio) {
+                    out[ne++] = y;
+                    na++;
+                    if ((eos_id >= 0 && y == eos_id) || ne == rem) {
+                        stopped = 1;
+                        break;
+                    }
+                    continue;
+                }
+                /* first rejection: correction from the positive residual */
+                double total = 0.0;
+                for (int v = 0; v < V; ++v) {
+                    double d = p[v] - (double)q[v];
+                    w[v] = (g_mutant == MUT_NO_CLAMP) ? d : (d > 0.0 ? d : 0.0);
+                    total += w[v];
+                }
+                if (g_mutant == MUT_RESAMPLE_FROM_P || !(total > 0.0)) {
+                    if (!(total > 0.0))
+                        fl |= 2;
+                    memcpy(w, p, sizeof(double) * (size_t)V);
+                }
+                draw_row = j;
+                draw_residual = 1;
+                stopped = 1;
+                break;
+            }
+            if (!stopped) {
+                /* bonus from the target row k_b */
+                if (g_mutant == MUT_BONUS_FROM_DRAFT && kb > 0) {
+                    const float *q = draft_probs + ((int64_t)b * k + kb - 1) * V;
+                    for (int v = 0; v < V; ++v)
+                        w[v] = (double)q[v];
+                } else {
+                    if (softmax_row(logits, dtype, ((int64_t)b * (k + 1) + kb) * V, V, temperature, p))
+                        fl |= 4;
+                    memcpy(w, p, sizeof(double) * (size_t)V);
+                }
+                draw_row = kb;
+            }
+            if (draw_row >= 0) {
+                out[ne++] = inverse_cdf(w, V, (double)u[k]);
+                if (out_residual) {
+                    double total = 0.0;
+                    for (int v = 0; v < V; ++v)
+                        total += w[v];
+                    for (int v = 0; v < V; ++v)
+                        out_residual[(int64_t)b * V + v] = w[v] / total;
+                }
+            }
+        }
+        (void)draw_residual;
+        n_accept[b] = na;
+        n_emit[b] = ne;
+        if (flags)
+            flags[b] = fl;
+    }
+    free(p);
+    free(w);
+}
+
+/* fp64 softmax of one logits row, exported for the tests' tolerance
+   accounting (they recompute p/q and CDF boundaries next to a mismatch). */
+int oracle_softmax_row(const void *logits, int dtype, int64_t row, int V, double T, double *p)
+{
+    return softmax_row(logits, dtype, row * V, V, T, p);
+}
+
+/* ------------------------------------------------------------------ */
+/* O3  realignment plan and KV shift                                      */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Unpad-append-repad ([CF] §3.2 and App. B), stated on per-sequence lengths.
+ * Layout: sequence b is left-padded, its confirmed tokens occupy slots
+ * pad_b .. pad_b + len_b - 1 of a common width W = pad_b + len_b (rectangular
+ * alignment, invariant I1), and min_b pad_b = 0.  After a round that commits
+ * n_b tokens: len'_b = len_b + n_b, the new width is W' = max_b len'_b (repad to
+ * the new maximum length) and pad'_b = W' - len'_b.
+ * Returns 0, or 2 when I1 does not hold on input (or a length is < 1), 3 when
+ * a run would start beyond the buffer (W + n_b - 1 > S or n_b < 0), 1 when the
+ * new width does not fit (W' > S).  Outputs are written only on 0.
+ */
+int oracle_realign_plan(int B, int S, const int32_t *len, const int32_t *pad,
+                        const int32_t *n_emit, int32_t *len_new, int32_t *pad_new,
+                        int32_t *width_new)
+{
+    if (B <= 0)
+        return 0;
+    int64_t W = (int64_t)pad[0] + len[0];
+    int64_t min_pad = pad[0];
+    for (int b = 0; b < B; ++b) {
+        if (len[b] < 1 || pad[b] < 0 || (int64_t)pad[b] + len[b] != W)
+            return 2;
+        if (pad[b] < min_pad)
+            min_pad = pad[b];
+    }
+    if (min_pad != 0)
+        return 2;
+    int64_t Wn = 0;
+    for (int b = 0; b < B; ++b) {
+        if (n_emit[b] < 0 || W + n_emit[b] - 1 > S)
+            return 3;
+        int64_t ln = (int64_t)len[b] + n_emit[b];
+        if (ln > Wn)
+            Wn = ln;
+    }
+    if (Wn > S)
+        return 1;
+    for (int b = 0; b < B; ++b) {
+        int64_t ln = (int64_t)len[b] + n_emit[b];
+        int64_t pn = Wn - ln;
+        len_new[b] = (int32_t)ln;
+        pad_new[b] = (int32_t)pn;
+    }
+    *width_new = (int32_t)Wn;
+    return 0;
+}
+
+/*
+ * Move the KV run of one (layer, K/V, sequence, head) slab.  A slab is S rows
+ * of row_bytes each.  After the round, sequence b's valid KV covers positions
+ * 0 .. len'_b - 2: the rows that were there, the row of the previous last token
+ * and the rows of the accepted proposals, all target-computed; the committed
+ * correction or bonus token has no KV until the next forward ([CF] App. D;
+ * [ZS] §5.2).  The run of len'_b - 1 rows moves from slot pad_b to slot pad'_b
+ * with memmove semantics; no other byte changes (stale slots stay as they are
+ * and are masked).  Relocating retained entries and dropping rejected ones is
+ * [CF] App. B's description of EQSPEC realignment.
+ */
+void oracle_shift_slab(uint8_t *slab, int64_t row_bytes, int pad_old, int pad_new, int n_rows)
+{
+    if (g_mutant == MUT_SKIP_KV_SHIFT)
+        return;
+    if (g_mutant == MUT_SHIFT_ONE_SHORT && n_rows > 0)
+        n_rows -= 1;
+    if (pad_old == pad_new || n_rows <= 0)
+        return;
+    memmove(slab + (int64_t)pad_new * row_bytes, slab + (int64_t)pad_old * row_bytes,
+            (size_t)((int64_t)n_rows * row_bytes));
+}
+
+/* Plan and shift on a contiguous left-padded cache kv[L, 2, B, H, S, D] whose
+   elements are elt_bytes wide.  Returns the plan's status; kv is untouched
+   unless it is 0. */
+int oracle_realign_kv(void *kv, int elt_bytes, int L, int B, int H, int S, int D,
+                      const int32_t *len, const int32_t *pad, const int32_t *n_emit,
+                      int32_t *len_new, int32_t *pad_new, int32_t *width_new)
+{
+    if (B <= 0)
+        return 0;
+    int32_t *ln = (int32_t *)malloc(sizeof(int32_t) * (size_t)B);
+    int32_t *pn = (int32_t *)malloc(sizeof(int32_t) * (size_t)B);
+    int32_t *po = (int32_t *)malloc(sizeof(int32_t) * (size_t)B);
+    int32_t wn = 0;
+    memcpy(po, pad, sizeof(int32_t) * (size_t)B); /* outputs may alias inputs */
+    int st = oracle_realign_plan(B, S, len, pad, n_emit, ln, pn, &wn);
+    if (st == 0) {
+        int64_t row_bytes = (int64_t)D * elt_bytes;
+        int64_t slab_bytes = row_bytes * S;
+        for (int l = 0; l < L; ++l)
+            for (int c = 0; c < 2; ++c)
+                for (int b = 0; b < B; ++b)
+                    for (int h = 0; h < H; ++h) {
+                        int64_t slab = (((int64_t)l * 2 + c) * B + b) * H + h;
+                        oracle_shift_slab((uint8_t *)kv + slab * slab_bytes, row_bytes, po[b],
+                                          pn[b], ln[b] - 1);
+                    }
+        memcpy(len_new, ln, sizeof(int32_t) * (size_t)B);
+        memcpy(pad_new, pn, sizeof(int32_t) * (size_t)B);
+        *width_new = wn;
+    }
+    free(ln);
+    free(pn);
+    free(po);
+    return st;
+}
+
+/* ------------------------------------------------------------------ */
+/* O4  position IDs and attention mask                                    */
+/* ------------------------------------------------------------------ */
+
+/* Recompute the mask and the positions of every row from the new padding:
+   mask[b, s] = 1 for s >= pad'_b (0 in the left padding), and positions are
+   recomputed from the mask ([CF] App. B) as cumsum(mask) - 1, clamped at 0 in
+   the padding.  Slots at or beyond the new width keep counting, so the next
+   round's query slots need no rewrite. */
+void oracle_rebuild_pos_mask(int B, int S, const int32_t *pad_new, int32_t *pos, uint8_t *mask)
+{
+    if (g_mutant == MUT_STALE_POSITIONS)
+        return;
+    for (int b = 0; b < B; ++b) {
+        int64_t csum = 0;
+        for (int s = 0; s < S; ++s) {
+            uint8_t m = (s >= pad_new[b]) ? 1 : 0;
+            mask[(int64_t)b * S + s] = m;
+            csum += m;
+            int64_t p = csum - 1;
+            pos[(int64_t)b * S + s] = (int32_t)(p < 0 ? 0 : p);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* O5  same-length grouping (policy UNPINNED by the pages)                  */
+/* ------------------------------------------------------------------ */
+
+/*
+ * EXSPEC keeps sequences ragged and batches sequences of identical current
+ * length so realignment can be skipped ([CF] §3.2).  The pages give no
+ * algorithm (the appendix is a bare heading), so this policy is this project's
+ * construction:
+ *   - L* = the most frequent length among active sequences, ties to the
+ *     smaller length;
+ *   - members: active sequences of length L* in ascending index, at most B;
+ *     count_equal = their number;
+ *   - the remaining slots are filled with the other active sequences in
+ *     ascending (|len - L*|, index);
+ *   - slots beyond the number of active sequences hold -1;
+ *   - group_len = L*, or -1 when no sequence is active.
+ */
+void oracle_group_by_length(int N, const int32_t *len, const uint8_t *active, int B,
+                            int32_t *out_idx, int32_t *count_equal, int32_t *group_len)
+{
+    int64_t best_len = -1, best_cnt = 0;
+    for (int i = 0; i < N; ++i) {
+        if (active && !active[i])
+            continue;
+        int64_t cnt = 0;
+        for (int j = 0; j < N; ++j)
+            if ((!active || active[j]) && len[j] == len[i])
+                cnt++;
+        if (cnt > best_cnt || (cnt == best_cnt && len[i] < best_len)) {
+            best_cnt = cnt;
+            best_len = len[i];
+        }
+    }
+    for (int s = 0; s < B; ++s)
+        out_idx[s] = -1;
+    *group_len = (int32_t)best_len;
+    int n = 0;
+    uint8_t *taken = (uint8_t *)calloc((size_t)(N > 0 ? N : 1), 1);
+    for (int i = 0; i < N && n < B; ++i)
+        if ((!active || active[i]) && len[i] == best_len) {
+            out_idx[n++] = i;
+            taken[i] = 1;
+        }
+    *count_equal = n;
+    while (n < B) {
+        int pick = -1;
+        int64_t pick_d = 0;
+        for (int i = 0; i < N; ++i) {
+            if ((active && !active[i]) || taken[i])
+                continue;
+            int64_t d = llabs((int64_t)len[i] - best_len);
+            if (pick < 0 || d < pick_d) {
+                pick = i;
+                pick_d = d;
+            }
+        }
+        if (pick < 0)
+            break;
+        out_idx[n++] = pick;
+        taken[pick] = 1;
+    }
+    free(taken);
+}
