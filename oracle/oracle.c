@@ -248,7 +248,7 @@ static int inverse_cdf(const double *w, int V, double u)
  * Flags per sequence: 1 = a tested proposal had q(y) = 0 (the page says such a
  * symbol cannot be proposed; IEEE then gives +inf -> accept when p > 0, or
  * NaN -> reject when p = 0), 2 = zero residual mass, 4 = a non-finite logit in
- * a row that was used.
+ * a row that was used, 8 = a proposal outside [0, V) (rejected).
  *
  * out_residual [B, V] (or NULL): the normalised distribution the final draw
  * came from (residual, or p on zero residual, or the bonus row's p); rows of
@@ -279,10 +279,15 @@ void oracle_verify_sample(const void *logits, int dtype, double temperature,
                 const float *q = draft_probs + ((int64_t)b * k + j) * V;
                 if (softmax_row(logits, dtype, ((int64_t)b * (k + 1) + j) * V, V, temperature, p))
                     fl |= 4;
-                if (q[y] == 0.0f)
+                /* a proposal outside the vocabulary has no probability under
+                   either model: flag 8 and treat it as rejected */
+                int valid = y >= 0 && y < V;
+                if (!valid)
+                    fl |= 8;
+                if (valid && q[y] == 0.0f)
                     fl |= 1;
-                double ratio = p[y] / (double)q[y];
-                if ((double)u[j] < ratio) {
+                double ratio = valid ? p[y] / (double)q[y] : 0.0;
+                if (valid && (double)u[j] < ratio) {
                     out[ne++] = y;
                     na++;
                     if ((eos_id >= 0 && y == eos_id) || ne == rem) {

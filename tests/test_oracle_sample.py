@@ -216,3 +216,16 @@ def test_stop_rules_match_greedy_commitment():
     assert ne[0] == 0 and (out[0] == -1).all()
     out, na, ne, _, _ = oracle.verify_sample(x, DT_F32, q, d, u, draft_len=np.array([1], np.int32))
     assert list(out[0, :ne[0]]) == [1, 3] and na[0] == 1
+
+
+def test_out_of_vocabulary_proposal_is_rejected_and_flagged():
+    V = 4
+    p = np.array([0.1, 0.2, 0.3, 0.4])
+    x = np.log(p).astype(np.float32)[None, None].repeat(2, axis=1)
+    q = np.full((1, 1, V), 0.25, np.float32)
+    for y in (-1, V, 10**6):
+        out, na, ne, fl, res = oracle.verify_sample(x, DT_F32, q, np.array([[y]], np.int32),
+                                                    np.array([[0.0, 0.5]], np.float32), want_residual=True)
+        assert fl[0] & 8 and na[0] == 0 and ne[0] == 1
+        # drawn from the residual max(0, p - q) = [0, 0, 0.05, 0.15]
+        assert np.allclose(res[0], [0, 0, 0.25, 0.75], atol=1e-6)
