@@ -1,0 +1,526 @@
+"""Benchmark: verify + realign rounds/s on synthetic inputs, one JSON line.
+
+A step is one speculative round of the hot path over one batch:
+    spec_verify_greedy (or spec_verify_sample)  -> commits per sequence
+    spec_realign_kv                              -> KV compaction / shift
+    spec_rebuild_pos_mask                        -> position IDs + mask
+Between steps (outside the timed events) the harness plays the target model:
+it draws the next round's logits and proposals, writes the KV of the k+1
+query slots, and flushes L2 by writing a 256 MiB buffer.  Each step is
+bracketed by CUDA events on the launching stream; the reported time is the
+sum over the K timed steps (barrier + synchronize on both sides, max over
+ranks).  `--impl reference` times the CPU oracle on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify+realign rounds/sec at B=4..256; achieved HBM GB/s vs GB300 peak"
+
+# workloads (synthetic stand-ins for the pages' SpecBench / Multi30k runs)
+WORKLOADS = {
+    "c1": dict(cfg="c1", mode="greedy"),
+    "c2": dict(cfg="c2", mode="greedy"),
+    "c3": dict(cfg="c3", mode="sample"),
+    "c4": dict(cfg="c4", mode="greedy"),
+    "c5": dict(cfg="c5", mode="greedy"),
+    "c5s": dict(cfg="c5", mode="sample"),
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c2")
+    ap.add_argument("--alpha", type=float, default=None)
+    ap.add_argument("--k", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--seed", type=int, default=1002)
+    return ap.parse_args()
+
+
+def workload_params(args):
+    from specgen import CONFIGS
+
+    w = WORKLOADS[args.workload]
+    c = dict(CONFIGS[w["cfg"]])
+    c["mode"] = w["mode"]
+    if args.workload == "c4":
+        c["k"] = args.k or 8
+        c["prompt"] = c["pool_len"]
+    if args.k:
+        c["k"] = args.k
+    if c["mode"] == "greedy":
+        c["alpha"] = args.alpha if args.alpha is not None else max(c["alphas"])
+    else:
+        c["alpha"] = None
+    return c
+
+
+def describe(c):
+    kv = f"{c['L']}x2x{c['B']}x{c['H']}x{c['S']}x{c['D']} {c['kv_dtype']}"
+    s = f"{c['mode']} round: B={c['B']} k={c['k']} V={c['V']} {c['logit_dtype']} logits"
+    s += f", alpha={c['alpha']}" if c["alpha"] is not None else f", draft=target+N(0,{c['noise']})"
+    return s + f"; KV {kv}; prompts U{list(c['prompt'])}"
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (also exercised on CPU with gloo in the tests)
+# ---------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+def rank_seed(base, rank):
+    """Each rank verifies and realigns its own independent batch."""
+    return base + 7919 * rank
+
+
+def max_over_ranks(x, pg_active, device=None):
+    if not pg_active:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(units_per_rank, max_time_s, n_ranks):
+    """Whole-job throughput: units processed by all ranks / slowest rank's time."""
+    return units_per_rank * n_ranks / max_time_s
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax = float(p[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# peaks and the committed ncu traffic record
+# ---------------------------------------------------------------------------
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        return float(json.load(open(p))["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_source_digest():
+    import hashlib
+
+    h = hashlib.sha256()
+    for fn in ("realign.cu", "spec_common.cuh"):
+        h.update(open(os.path.join(ROOT, "speculative_decoding_verification_28_gb300", "csrc", fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic_ratio(workload):
+    """DRAM bytes / algorithmic bytes of the shift kernel from the committed
+    ncu summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", f"kv_shift_{workload}.txt")
+    if not os.path.exists(p):
+        return None
+    rec = {}
+    for line in open(p):
+        if ":" in line and not line.startswith(" "):
+            k_, v = line.split(":", 1)
+            rec[k_.strip()] = v.strip()
+    if rec.get("source digest") != kernel_source_digest():
+        return None
+    try:
+        return float(rec["dram bytes / algorithmic bytes"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+class Round:
+    """State of one left-padded batch on the device plus the harness that
+    plays the target model between rounds."""
+
+    def __init__(self, c, seed, device):
+        import torch
+
+        import speculative_decoding_verification_28_gb300 as sv
+        from specgen import prompt_lengths
+        from specgen import torch_gen
+
+        self.c, self.dev, self.sv, self.tg = c, device, sv, torch_gen
+        self.kv_dt = {"bf16": torch.bfloat16, "f32": torch.float32}[c["kv_dtype"]]
+        self.lg_dt = {"bf16": torch.bfloat16, "f32": torch.float32}[c["logit_dtype"]]
+        B, S, k = c["B"], c["S"], c["k"]
+        self.g = torch.Generator(device=device).manual_seed(seed)
+        self.rng = np.random.default_rng(seed)
+        self.kv = torch.empty((c["L"], 2, B, c["H"], S, c["D"]), dtype=self.kv_dt, device=device)
+        self.pos = torch.empty((B, S), dtype=torch.int32, device=device)
+        self.mask = torch.empty((B, S), dtype=torch.uint8, device=device)
+        self.tokens = torch.randint(0, c["V"], (B, S), device=device, dtype=torch.int32, generator=self.g)
+        self.ws = sv.Workspace(B, k, c["V"], device)
+        self.flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=device)
+        self.prompt_lengths = prompt_lengths
+        self.reset()
+
+    def reset(self):
+        import torch
+
+        c = self.c
+        ln = self.prompt_lengths(c["B"], *c["prompt"], seed=self.rng)
+        W = int(ln.max())
+        self.ln = torch.from_numpy(ln).to(self.dev)
+        self.pad = torch.from_numpy((W - ln).astype(np.int32)).to(self.dev)
+        self.W = W
+        self.tg.kv_fill(self.kv, self.tokens, self.pad, self.ln - 1, junk=False)
+        self.sv.spec_rebuild_pos_mask(self.pad, self.pos, self.mask)
+
+    def prepare(self):
+        """The target forward of this round (untimed): logits, proposals and
+        the KV of the query slots; then an L2 flush."""
+        import torch
+
+        c = self.c
+        if self.W + c["k"] + 1 > c["S"]:
+            self.reset()
+        B, k, V = c["B"], c["k"], c["V"]
+        if c["mode"] == "greedy":
+            self.x, self.d = self.tg.greedy_round_inputs(B, k, V, c["alpha"], c["sigma"], self.g, self.lg_dt, self.dev)
+        else:
+            self.x, self.q, self.d, self.u = self.tg.sample_round_inputs(B, k, V, c["noise"], self.g, self.lg_dt,
+                                                                         self.dev)
+        last = torch.gather(self.tokens, 1, (self.ln.long() - 1).unsqueeze(1))
+        self.tg.kv_write_query(self.kv, torch.cat([last, self.d], 1).contiguous(), self.pos, self.W)
+        self.flush.zero_()
+
+    def verify(self):
+        if self.c["mode"] == "greedy":
+            return self.sv.spec_verify_greedy(self.x, self.d, workspace=self.ws)[2]
+        return self.sv.spec_verify_sample(self.x, self.q, self.d, self.u, workspace=self.ws)[2]
+
+    def realign(self, ne):
+        return self.sv.spec_realign_kv(self.kv, self.ln, self.pad, ne, workspace=self.ws)
+
+    def posmask(self, pad_new):
+        self.sv.spec_rebuild_pos_mask(pad_new, self.pos, self.mask, pad_old=self.pad)
+
+    def advance(self, ne, ln_new, pad_new, width):
+        """Untimed bookkeeping after a round: returns rows moved (for bytes)."""
+        ln0, pad0, n = self.ln.cpu().numpy(), self.pad.cpu().numpy(), ne.cpu().numpy()
+        ln1, pad1 = ln_new.cpu().numpy(), pad_new.cpu().numpy()
+        moved_rows = int(((ln1 - 1) * (pad1 != pad0)).sum())
+        self.ln, self.pad, self.W = ln_new, pad_new, int(width.item())
+        return moved_rows, int(n.sum()), (ln0, pad0, n)
+
+    def row_bytes_all_slabs(self):
+        c = self.c
+        return c["L"] * 2 * c["H"] * c["D"] * (2 if c["kv_dtype"] == "bf16" else 4)
+
+
+def run_ours(args, c, rank, local_rank, world):
+    import torch
+
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    pg = world > 1
+    if pg:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    st = torch.cuda.current_stream(dev)
+    R = Round(c, rank_seed(args.seed, rank), dev)
+
+    def one_step(timed):
+        R.prepare()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ev[0].record(st)
+        ne = R.verify()
+        ev[1].record(st)
+        ln_new, pad_new, width, err = R.realign(ne)
+        ev[2].record(st)
+        R.posmask(pad_new)
+        ev[3].record(st)
+        torch.cuda.synchronize(dev)
+        assert int(err.item()) == 0, "realign error"
+        moved, emitted, _ = R.advance(ne, ln_new, pad_new, width)
+        return [ev[i].elapsed_time(ev[i + 1]) for i in range(3)], moved, emitted
+
+    for _ in range(args.warmup):
+        one_step(False)
+    if pg:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    per = []
+    moved_rows = []
+    emitted = 0
+    with ClockSampler(local_rank) as clk:
+        for _ in range(args.steps):
+            t, m, e = one_step(True)
+            per.append(t)
+            moved_rows.append(m)
+            emitted += e
+    torch.cuda.synchronize(dev)
+    if pg:
+        dist.barrier()
+    per = np.array(per)  # ms [steps, 3]
+    total_s = per.sum() / 1e3
+    total_s = max_over_ranks(total_s, pg, dev)
+    value = aggregate(args.steps, total_s, world)
+
+    # roofline of the dominant kernel: the KV shift (timed together with its
+    # one-CTA plan kernel, so the achieved figure is a lower bound)
+    row_all = R.row_bytes_all_slabs()
+    alg_bytes = np.array(moved_rows, dtype=np.float64) * row_all * 2  # read + write
+    realign_ms = per[:, 1]
+    mean_alg = float(alg_bytes.mean())
+    achieved = float(alg_bytes.sum() / (realign_ms.sum() / 1e3) / 1e9)
+    peak, peak_src = hbm_peak()
+    ratio = ncu_traffic_ratio(args.workload)
+    roofline = {"bound": "hbm", "kernel": "kv_shift_bulk_kernel (+ realign_plan_kernel in the same timing)",
+                "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                "traffic": None if ratio is None else round(ratio * mean_alg),
+                "algorithmic_bytes_per_launch": round(mean_alg)}
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "rounds/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(float(per.sum(1).mean()), 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": c["logit_dtype"] if c["mode"] == "greedy" else "f32 arithmetic on " + c["logit_dtype"] + " logits",
+        "data": "synthetic (seeded; stands in for SpecBench/Multi30k-shaped rounds)",
+        "config": {"workload": f"{args.workload}: " + describe(c),
+                   "l2": "flushed between steps (256 MiB write, outside the timed events)",
+                   "timed": "library calls only; the harness target forward runs between steps",
+                   "parallelism": f"independent batch per GPU x{world}"},
+        "roofline": roofline,
+        "per_call_us": {"verify": round(float(per[:, 0].mean()) * 1e3, 2),
+                        "realign": round(float(per[:, 1].mean()) * 1e3, 2),
+                        "pos_mask": round(float(per[:, 2].mean()) * 1e3, 2)},
+        "tokens_per_round": round(emitted / args.steps / c["B"], 4),
+        "gpu_launches": args.steps * (4 if c["mode"] == "greedy" else 5),
+        "clocks": clk.summary(),
+    }
+    if not args.no_e2e:
+        line["e2e"] = run_e2e(args, R, st, dev, pg, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = run_cpu_baseline(c, args, R)
+    if pg:
+        dist.destroy_process_group()
+    return line
+
+
+def run_e2e(args, R, st, dev, pg, world):
+    """Same rounds through the public API with HOST inputs and outputs: the
+    timed region of every step includes the pinned host->device copy of the
+    round's logits and proposals and the device->host copy of its results."""
+    import torch
+
+    c = R.c
+    steps = max(1, args.steps)
+    hx = torch.empty(tuple(R.x.shape), dtype=R.x.dtype).pin_memory()
+    hd = torch.empty(tuple(R.d.shape), dtype=torch.int32).pin_memory()
+    extra = []
+    if c["mode"] == "sample":
+        hq = torch.empty(tuple(R.q.shape), dtype=torch.float32).pin_memory()
+        hu = torch.empty(tuple(R.u.shape), dtype=torch.float32).pin_memory()
+        extra = [hq, hu]
+    B = c["B"]
+    h_out = torch.empty((B, c["k"] + 1), dtype=torch.int32).pin_memory()
+    h_small = torch.empty((4, B), dtype=torch.int32).pin_memory()
+    h_w = torch.empty(2, dtype=torch.int32).pin_memory()
+    total = 0.0
+    h2d = d2h = 0
+    for _ in range(steps):
+        R.prepare()
+        hx.copy_(R.x)
+        hd.copy_(R.d)
+        if extra:
+            extra[0].copy_(R.q)
+            extra[1].copy_(R.u)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        R.x.copy_(hx, non_blocking=True)
+        R.d.copy_(hd, non_blocking=True)
+        if extra:
+            R.q.copy_(extra[0], non_blocking=True)
+            R.u.copy_(extra[1], non_blocking=True)
+        if c["mode"] == "greedy":
+            out, na, ne = R.sv.spec_verify_greedy(R.x, R.d, workspace=R.ws)
+        else:
+            out, na, ne, _, _ = R.sv.spec_verify_sample(R.x, R.q, R.d, R.u, workspace=R.ws)
+        ln_new, pad_new, width, err = R.realign(ne)
+        R.posmask(pad_new)
+        h_out.copy_(out, non_blocking=True)
+        h_small[0].copy_(na, non_blocking=True)
+        h_small[1].copy_(ne, non_blocking=True)
+        h_small[2].copy_(ln_new, non_blocking=True)
+        h_small[3].copy_(pad_new, non_blocking=True)
+        h_w[0].copy_(width[0], non_blocking=True)
+        h_w[1].copy_(err[0], non_blocking=True)
+        e1.record(st)
+        torch.cuda.synchronize(dev)
+        total += e0.elapsed_time(e1) / 1e3
+        assert int(h_w[1]) == 0
+        R.advance(ne, ln_new, pad_new, width)
+        h2d = hx.numel() * hx.element_size() + hd.numel() * 4 + sum(t.numel() * 4 for t in extra)
+        d2h = h_out.numel() * 4 + h_small.numel() * 4 + h_w.numel() * 4
+    total = max_over_ranks(total, pg, dev)
+    return {"value": round(aggregate(steps, total, world), 3), "unit": "rounds/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_rounds(c, n_rounds, seed, kv_host=None, state=None, R=None):
+    """n_rounds full rounds of the CPU oracle on the host (single thread):
+    verification on the round's logits, realignment of the host copy of the
+    cache, position/mask rebuild.  Returns (seconds in oracle calls, kv)."""
+    import oracle
+    from specgen import greedy_round_inputs, prompt_lengths, sample_round_inputs
+
+    rng = np.random.default_rng(seed)
+    B, k, V, S = c["B"], c["k"], c["V"], c["S"]
+    dt = {"bf16": oracle.DT_BF16, "f32": oracle.DT_F32}[c["logit_dtype"]]
+    if kv_host is None:
+        if R is not None:
+            kv_host = R.kv.view(-1).view(__import__("torch").int16).cpu().numpy().view(np.uint16)
+            kv_host = kv_host.reshape(tuple(R.kv.shape)) if c["kv_dtype"] == "bf16" else R.kv.cpu().numpy()
+        else:
+            kv_host = np.zeros((c["L"], 2, B, c["H"], S, c["D"]),
+                               np.uint16 if c["kv_dtype"] == "bf16" else np.float32)
+    ln = prompt_lengths(B, *c["prompt"], seed=rng)
+    pad = (int(ln.max()) - ln).astype(np.int32)
+    pos = np.zeros((B, S), np.int32)
+    mask = np.zeros((B, S), np.uint8)
+    spent = 0.0
+    for r in range(n_rounds):
+        if int(ln[0] + pad[0]) + k + 1 > S:
+            ln = prompt_lengths(B, *c["prompt"], seed=rng)
+            pad = (int(ln.max()) - ln).astype(np.int32)
+        if c["mode"] == "greedy":
+            x, d = greedy_round_inputs(B, k, V, c["alpha"], c["sigma"], seed=rng, dtype=c["logit_dtype"])
+            t0 = time.perf_counter()
+            _, _, ne = oracle.verify_greedy(x, dt, d)
+        else:
+            x, q, d, u = sample_round_inputs(B, k, V, c["noise"], seed=rng, dtype=c["logit_dtype"])
+            t0 = time.perf_counter()
+            _, _, ne, _, _ = oracle.verify_sample(x, dt, q, d, u)
+        st, ln, pad2, w = oracle.realign_kv(kv_host, ln, pad, ne)
+        oracle.rebuild_pos_mask(S, pad2, pos, mask)
+        spent += time.perf_counter() - t0
+        assert st == 0
+        pad = pad2
+    return spent, kv_host
+
+
+def run_cpu_baseline(c, args, R):
+    n = 4 if c["B"] * c["S"] >= 256 * 4096 else 16
+    spent, _ = oracle_rounds(c, n, args.seed + 1, R=R)
+    return {"value": round(n / spent, 4), "unit": "rounds/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} full rounds of the same workload (oracle verify + realign of a host copy of the "
+                      f"cache + pos/mask), single-threaded C, inputs generated outside the timing"}
+
+
+def run_reference(args, c):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return None
+    per = []
+    kv = None
+    for i in range(args.warmup + args.steps):
+        spent, kv = oracle_rounds(c, 1, args.seed + 31 * i, kv_host=kv)
+        if i >= args.warmup:
+            per.append(spent)
+    total = float(np.sum(per))
+    v = args.steps / total
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "rounds/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 oracle",
+            "data": "synthetic", "config": {"workload": f"{args.workload}: " + describe(c)},
+            "cpu_baseline": {"value": round(v, 4), "unit": "rounds/s", "cores": 1, "kind": "oracle",
+                             "sample": "each step one full round of the workload on the host"},
+            "e2e": {"value": round(v, 4), "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    c = workload_params(args)
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, c)
+    else:
+        line = run_ours(args, c, rank, local_rank, world)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

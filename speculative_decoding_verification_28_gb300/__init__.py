@@ -1,0 +1,29 @@
+"""GB300 (sm_103a) library for the data-parallel hot path of batch
+speculative decoding: greedy and stochastic verification of k draft tokens
+against k+1 target logit rows, realignment of a contiguous left-padded KV
+cache with its position IDs and attention mask, and same-length grouping.
+
+The C ABI is include/specverify.h (libspecverify.so); this package is a thin
+ctypes binding with the same function names.
+"""
+from .api import (  # noqa: F401
+    FLAG_BAD_TOKEN,
+    FLAG_NONFINITE,
+    FLAG_Q_ZERO,
+    FLAG_ZERO_RESIDUAL,
+    MAX_GROUP_N,
+    MAX_K,
+    REALIGN_CAPACITY,
+    REALIGN_EMIT,
+    REALIGN_LAYOUT,
+    REALIGN_OK,
+    REALIGN_TIMEOUT,
+    SpecError,
+    Workspace,
+    spec_group_by_length,
+    spec_realign_kv,
+    spec_rebuild_pos_mask,
+    spec_verify_greedy,
+    spec_verify_sample,
+    spec_workspace_bytes,
+)

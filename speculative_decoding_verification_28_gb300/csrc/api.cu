@@ -1,0 +1,224 @@
+// api.cu -- the extern "C" entry points of include/specverify.h: host-side
+// argument checks (nothing is launched on an error) and kernel launches.
+#include <limits.h>
+
+#include "spec_common.cuh"
+#include "spec_launch.h"
+
+using namespace spec;
+
+namespace {
+
+bool dtype_ok(int dt) { return dt == SPEC_F32 || dt == SPEC_BF16 || dt == SPEC_F16; }
+int dtype_bytes(int dt) { return dt == SPEC_F32 ? 4 : 2; }
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_workspace(void *ws, size_t have, size_t need)
+{
+    if (need == 0)
+        return SPEC_OK;
+    if (!ws || have < need || !aligned(ws, 256))
+        return SPEC_EWORKSPACE;
+    return SPEC_OK;
+}
+
+int launched(cudaError_t e) { return e == cudaSuccess ? SPEC_OK : SPEC_ECUDA; }
+
+int check_verify_common(const void *logits, int dt, int B, int k, int V, const int32_t *draft,
+                        const int32_t *out_tokens, const int32_t *n_accept, const int32_t *n_emit)
+{
+    if (B < 0 || k < 0 || k > SPEC_MAX_K || V < 1)
+        return SPEC_EINVAL;
+    if (!dtype_ok(dt))
+        return SPEC_EDTYPE;
+    if (B == 0)
+        return SPEC_OK;
+    if (!logits || (k > 0 && !draft) || !out_tokens || !n_accept || !n_emit)
+        return SPEC_EINVAL;
+    const long long units = (long long)B * (k + 1) * verify_chunks(V);
+    if (units > INT_MAX)
+        return SPEC_EINVAL;
+    if (!aligned(logits, dtype_bytes(dt)) || !aligned(out_tokens, 4) || !aligned(n_accept, 4) ||
+        !aligned(n_emit, 4) || (draft && !aligned(draft, 4)))
+        return SPEC_EALIGN;
+    return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_workspace_bytes(int B, int k, int V)
+{
+    if (B <= 0)
+        return 0;
+    k = k < 0 ? 0 : (k > SPEC_MAX_K ? SPEC_MAX_K : k);
+    V = V < 1 ? 1 : V;
+    return make_layout(B, k, V).total;
+}
+
+int spec_workspace_init(void *workspace, size_t bytes, void *cuda_stream)
+{
+    if (bytes == 0)
+        return SPEC_OK;
+    if (!workspace)
+        return SPEC_EWORKSPACE;
+    return launched(cudaMemsetAsync(workspace, 0, bytes, (cudaStream_t)cuda_stream));
+}
+
+const char *spec_status_str(int status)
+{
+    switch (status) {
+    case SPEC_OK:
+        return "ok";
+    case SPEC_EINVAL:
+        return "invalid argument (null pointer, negative size or k out of range)";
+    case SPEC_EDTYPE:
+        return "unknown spec_dtype";
+    case SPEC_EWORKSPACE:
+        return "workspace missing, misaligned (256 B) or smaller than spec_workspace_bytes()";
+    case SPEC_ECUDA:
+        return "a CUDA launch failed";
+    case SPEC_EALIGN:
+        return "a pointer lacks the alignment of its element type";
+    default:
+        return "unknown status";
+    }
+}
+
+int spec_verify_greedy(const void *target_logits, spec_dtype dt, int B, int k, int V,
+                       const int32_t *draft_tokens, const int32_t *draft_len, int32_t eos_id,
+                       const int32_t *remaining, int32_t *out_tokens, int32_t *n_accept, int32_t *n_emit,
+                       void *workspace, size_t workspace_bytes, void *cuda_stream)
+{
+    int rc = check_verify_common(target_logits, dt, B, k, V, draft_tokens, out_tokens, n_accept, n_emit);
+    if (rc != SPEC_OK || B == 0)
+        return rc;
+    rc = check_workspace(workspace, workspace_bytes, spec_workspace_bytes(B, k, V));
+    if (rc != SPEC_OK)
+        return rc;
+    VerifyArgs a{};
+    a.logits = target_logits;
+    a.B = B;
+    a.k = k;
+    a.V = V;
+    a.C = verify_chunks(V);
+    a.draft = draft_tokens;
+    a.draft_len = draft_len;
+    a.eos = eos_id;
+    a.remaining = remaining;
+    a.out_tokens = out_tokens;
+    a.n_accept = n_accept;
+    a.n_emit = n_emit;
+    a.ws = workspace;
+    return launched(launch_verify_greedy(a, dt, (cudaStream_t)cuda_stream));
+}
+
+int spec_verify_sample(const void *target_logits, spec_dtype dt, float temperature, const float *draft_probs,
+                       const int32_t *draft_tokens, const float *uniforms, int B, int k, int V,
+                       const int32_t *draft_len, int32_t eos_id, const int32_t *remaining, int32_t *out_tokens,
+                       int32_t *n_accept, int32_t *n_emit, float *out_residual, uint32_t *flags,
+                       void *workspace, size_t workspace_bytes, void *cuda_stream)
+{
+    int rc = check_verify_common(target_logits, dt, B, k, V, draft_tokens, out_tokens, n_accept, n_emit);
+    if (rc != SPEC_OK || B == 0)
+        return rc;
+    if (!(temperature > 0.0f) || !(temperature <= 3.0e38f) || !uniforms || (k > 0 && !draft_probs))
+        return SPEC_EINVAL;
+    if (!aligned(uniforms, 4) || (draft_probs && !aligned(draft_probs, 4)) ||
+        (out_residual && !aligned(out_residual, 4)) || (flags && !aligned(flags, 4)))
+        return SPEC_EALIGN;
+    rc = check_workspace(workspace, workspace_bytes, spec_workspace_bytes(B, k, V));
+    if (rc != SPEC_OK)
+        return rc;
+    VerifyArgs a{};
+    a.logits = target_logits;
+    a.B = B;
+    a.k = k;
+    a.V = V;
+    a.C = verify_chunks(V);
+    a.draft = draft_tokens;
+    a.draft_len = draft_len;
+    a.eos = eos_id;
+    a.remaining = remaining;
+    a.out_tokens = out_tokens;
+    a.n_accept = n_accept;
+    a.n_emit = n_emit;
+    a.ws = workspace;
+    a.inv_temp = 1.0f / temperature;
+    a.unit_temp = temperature == 1.0f ? 1 : 0;
+    a.q = draft_probs;
+    a.u = uniforms;
+    a.out_residual = out_residual;
+    a.flags = flags;
+    return launched(launch_verify_sample(a, dt, (cudaStream_t)cuda_stream));
+}
+
+int spec_realign_kv(void *kv, spec_dtype dt, int L, int B, int H, int S, int D, const int32_t *len,
+                    const int32_t *pad, const int32_t *n_emit, int32_t *len_new, int32_t *pad_new,
+                    int32_t *width_new, int32_t *err, void *workspace, size_t workspace_bytes, void *cuda_stream)
+{
+    if (B < 0 || L < 1 || H < 1 || S < 1 || D < 1)
+        return SPEC_EINVAL;
+    if (!dtype_ok(dt))
+        return SPEC_EDTYPE;
+    if (B == 0)
+        return SPEC_OK;
+    if (!kv || !len || !pad || !n_emit || !len_new || !pad_new || !width_new || !err)
+        return SPEC_EINVAL;
+    if ((long long)B * L * 2 * H > INT_MAX)
+        return SPEC_EINVAL;
+    if (!aligned(kv, dtype_bytes(dt)) || !aligned(len, 4) || !aligned(pad, 4) || !aligned(n_emit, 4) ||
+        !aligned(len_new, 4) || !aligned(pad_new, 4) || !aligned(width_new, 4) || !aligned(err, 4))
+        return SPEC_EALIGN;
+    const int rc = check_workspace(workspace, workspace_bytes, spec_workspace_bytes(B, 0, 1));
+    if (rc != SPEC_OK)
+        return rc;
+    RealignArgs a{};
+    a.kv = kv;
+    a.elt_bytes = dtype_bytes(dt);
+    a.L = L;
+    a.B = B;
+    a.H = H;
+    a.S = S;
+    a.D = D;
+    a.len = len;
+    a.pad = pad;
+    a.n_emit = n_emit;
+    a.len_new = len_new;
+    a.pad_new = pad_new;
+    a.width_new = width_new;
+    a.err = err;
+    a.ws = workspace;
+    return launched(launch_realign(a, (cudaStream_t)cuda_stream));
+}
+
+int spec_rebuild_pos_mask(int B, int S, const int32_t *pad_old, const int32_t *pad_new, int32_t *pos,
+                          uint8_t *mask, void *cuda_stream)
+{
+    if (B < 0 || S < 0 || B > 65535)
+        return SPEC_EINVAL;
+    if (B == 0 || S == 0)
+        return SPEC_OK;
+    if (!pad_new || !pos || !mask || (pad_old && pad_old == pad_new))
+        return SPEC_EINVAL;
+    if (!aligned(pad_new, 4) || !aligned(pos, 4) || (pad_old && !aligned(pad_old, 4)))
+        return SPEC_EALIGN;
+    return launched(launch_pos_mask(B, S, pad_old, pad_new, pos, mask, (cudaStream_t)cuda_stream));
+}
+
+int spec_group_by_length(int N, const int32_t *len, const uint8_t *active, int B, int32_t *out_idx,
+                         int32_t *out_count_equal, int32_t *out_group_len, void *cuda_stream)
+{
+    if (N < 0 || N > SPEC_MAX_GROUP_N || B < 0)
+        return SPEC_EINVAL;
+    if ((N > 0 && !len) || (B > 0 && !out_idx) || !out_count_equal || !out_group_len)
+        return SPEC_EINVAL;
+    if ((len && !aligned(len, 4)) || (out_idx && !aligned(out_idx, 4)) || !aligned(out_count_equal, 4) ||
+        !aligned(out_group_len, 4))
+        return SPEC_EALIGN;
+    return launched(
+        launch_group(N, len, active, B, out_idx, out_count_equal, out_group_len, (cudaStream_t)cuda_stream));
+}
+
+}  // extern "C"

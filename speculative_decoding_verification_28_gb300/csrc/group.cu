@@ -1,0 +1,135 @@
+// group.cu -- same-length grouping over a pool of ragged sequences (EXSPEC,
+// "Correctness Forensics for Batch Speculative Decoding", §3.2: keep
+// sequences ragged and batch sequences of identical current length so that
+// realignment is bypassed).  The pages give no algorithm; the policy is this
+// library's: L* = most frequent active length (ties to the smaller), members of
+// length L* by ascending index (at most B), then other active sequences by
+// ascending (|len - L*|, index); -1 beyond the active count.
+// One CTA: bitonic sort of (length, index) keys in shared memory, run lengths
+// by binary search, best run by a max-reduction, second sort for the fill.
+#include "spec_common.cuh"
+#include "spec_launch.h"
+
+namespace spec {
+
+constexpr int kGroupThreads = 1024;
+
+__device__ void bitonic_sort_asc(uint64_t *k, int P)
+{
+    for (int size = 2; size <= P; size <<= 1)
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < P; i += kGroupThreads) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const bool asc = (i & size) == 0;
+                    const uint64_t x = k[i], y = k[j];
+                    if (asc ? (x > y) : (x < y)) {
+                        k[i] = y;
+                        k[j] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+}
+
+__global__ void __launch_bounds__(kGroupThreads)
+    group_kernel(int N, const int32_t *len, const uint8_t *active, int B, int32_t *out_idx,
+                 int32_t *out_count_equal, int32_t *out_group_len)
+{
+    __shared__ uint64_t key[SPEC_MAX_GROUP_N];
+    __shared__ unsigned long long s_best;
+    __shared__ int s_nact;
+    const uint64_t NONE = ~0ull;
+    int P = 1;
+    while (P < N)
+        P <<= 1;
+    if (threadIdx.x == 0) {
+        s_best = 0;
+        s_nact = 0;
+    }
+    // (length ^ sign bit, index): unsigned order of the key = signed order of length
+    for (int i = threadIdx.x; i < P; i += kGroupThreads) {
+        uint64_t kk = NONE;
+        if (i < N && (!active || active[i]))
+            kk = ((uint64_t)((uint32_t)len[i] ^ 0x80000000u) << 32) | (uint32_t)i;
+        key[i] = kk;
+    }
+    __syncthreads();
+    bitonic_sort_asc(key, P);
+    // active count = first NONE position
+    for (int i = threadIdx.x; i < P; i += kGroupThreads)
+        if (key[i] != NONE && (i + 1 == P || key[i + 1] == NONE))
+            s_nact = i + 1;
+    __syncthreads();
+    const int nact = s_nact;
+    // each run start: its length by binary search for the first larger length
+    for (int i = threadIdx.x; i < nact; i += kGroupThreads) {
+        const uint32_t li = (uint32_t)(key[i] >> 32);
+        if (i > 0 && (uint32_t)(key[i - 1] >> 32) == li)
+            continue;
+        int lo = i, hi = nact;  // first index with length > li
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if ((uint32_t)(key[mid] >> 32) > li)
+                hi = mid;
+            else
+                lo = mid + 1;
+        }
+        const unsigned long long cand =
+            ((unsigned long long)(lo - i) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)i);
+        atomicMax(&s_best, cand);
+    }
+    __syncthreads();
+    const unsigned long long best = s_best;
+    const int start = nact > 0 ? (int)(0xFFFFFFFFu - (uint32_t)best) : 0;
+    const int cnt = nact > 0 ? (int)(best >> 32) : 0;
+    const int ce = cnt < B ? cnt : B;
+    const uint32_t lstar_u = nact > 0 ? (uint32_t)(key[start] >> 32) : 0u;
+    const int lstar = (int)(lstar_u ^ 0x80000000u);
+    for (int s = threadIdx.x; s < ce; s += kGroupThreads)
+        out_idx[s] = (int)(uint32_t)key[start + s];
+    __syncthreads();
+    // fill: other active sequences by (|len - L*|, index); new keys are built
+    // in registers, then written after every thread has read the old ones
+    constexpr int kPer = SPEC_MAX_GROUP_N / kGroupThreads;
+    uint64_t nk[kPer];
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+        const int i = threadIdx.x + r * kGroupThreads;
+        uint64_t kk = NONE;
+        if (i < nact && !(i >= start && i < start + ce)) {
+            const int li = (int)((uint32_t)(key[i] >> 32) ^ 0x80000000u);
+            const long long dist = (long long)li - lstar;
+            const uint32_t ad = (uint32_t)(dist < 0 ? -dist : dist);
+            kk = ((uint64_t)ad << 32) | (uint32_t)key[i];
+        }
+        nk[r] = kk;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+        const int i = threadIdx.x + r * kGroupThreads;
+        if (i < P)
+            key[i] = nk[r];
+    }
+    __syncthreads();
+    bitonic_sort_asc(key, P);
+    for (int s = ce + threadIdx.x; s < B; s += kGroupThreads) {
+        const int r = s - ce;
+        out_idx[s] = (r < P && key[r] != NONE) ? (int)(uint32_t)key[r] : -1;
+    }
+    if (threadIdx.x == 0) {
+        *out_count_equal = ce;
+        *out_group_len = nact > 0 ? lstar : -1;
+    }
+}
+
+cudaError_t launch_group(int N, const int32_t *len, const uint8_t *active, int B, int32_t *out_idx,
+                         int32_t *out_count_equal, int32_t *out_group_len, cudaStream_t st)
+{
+    group_kernel<<<1, kGroupThreads, 0, st>>>(N, len, active, B, out_idx, out_count_equal, out_group_len);
+    return cudaGetLastError();
+}
+
+}  // namespace spec

@@ -1,0 +1,62 @@
+// posmask.cu -- position IDs and attention mask recomputed from the new
+// padding after realignment, in one pass ("Correctness Forensics for Batch
+// Speculative Decoding", App. B: position IDs are restored by recomputing them
+// from the attention mask after repadding).
+//   mask[b, s] = s >= pad'_b;   pos[b, s] = s - pad'_b there, 0 in the padding
+// (cumsum(mask) - 1 clamped at 0).  Rows whose padding did not change are
+// skipped.  Roofline: write-only, 5 bytes per slot of a changed row.
+#include "spec_common.cuh"
+#include "spec_launch.h"
+
+namespace spec {
+
+constexpr int kPmThreads = 256;
+constexpr int kPmSlots = 8;  // slots per thread on the vector path
+
+__global__ void __launch_bounds__(kPmThreads)
+    pos_mask_kernel(int B, int S, const int32_t *pad_old, const int32_t *pad_new, int32_t *pos, uint8_t *mask,
+                    int vec)
+{
+    const int b = blockIdx.y;
+    const int pn = pad_new[b];
+    if (pad_old && pad_old[b] == pn)
+        return;
+    int32_t *prow = pos + (size_t)b * S;
+    uint8_t *mrow = mask + (size_t)b * S;
+    if (vec) {
+        const int s0 = (blockIdx.x * kPmThreads + threadIdx.x) * kPmSlots;
+        if (s0 >= S)
+            return;
+        int p[kPmSlots];
+        uint32_t m[2] = {0, 0};
+#pragma unroll
+        for (int e = 0; e < kPmSlots; ++e) {
+            const int s = s0 + e;
+            const bool in = s >= pn;
+            p[e] = in ? s - pn : 0;
+            m[e >> 2] |= (in ? 1u : 0u) << (8 * (e & 3));
+        }
+        *reinterpret_cast<int4 *>(prow + s0) = make_int4(p[0], p[1], p[2], p[3]);
+        *reinterpret_cast<int4 *>(prow + s0 + 4) = make_int4(p[4], p[5], p[6], p[7]);
+        *reinterpret_cast<uint2 *>(mrow + s0) = make_uint2(m[0], m[1]);
+    } else {
+        for (int s = blockIdx.x * kPmThreads + threadIdx.x; s < S; s += gridDim.x * kPmThreads) {
+            const bool in = s >= pn;
+            prow[s] = in ? s - pn : 0;
+            mrow[s] = in ? 1 : 0;
+        }
+    }
+}
+
+cudaError_t launch_pos_mask(int B, int S, const int32_t *pad_old, const int32_t *pad_new, int32_t *pos,
+                            uint8_t *mask, cudaStream_t st)
+{
+    const bool vec = (S % kPmSlots == 0) && (reinterpret_cast<uintptr_t>(pos) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(mask) % 8 == 0);
+    const int per_block = vec ? kPmThreads * kPmSlots : kPmThreads * 4;
+    dim3 grid((unsigned)((S + per_block - 1) / per_block), (unsigned)B);
+    pos_mask_kernel<<<grid, kPmThreads, 0, st>>>(B, S, pad_old, pad_new, pos, mask, vec ? 1 : 0);
+    return cudaGetLastError();
+}
+
+}  // namespace spec

@@ -1,0 +1,392 @@
+// realign.cu -- ragged-to-rectangular realignment of a contiguous
+// left-padded KV cache after a speculative round ("unpad-append-repad",
+// "Correctness Forensics for Batch Speculative Decoding", §3.2 and App. B:
+// relocate retained entries, drop rejected ones, keep the target-computed
+// entries of accepted tokens, repad).
+//
+// plan  (1 CTA): checks rectangular alignment of the input, computes
+//       len' = len + n, W' = max len', pad' = W' - len', the shift
+//       delta = pad' - pad and the run of len' - 1 rows to move, and lists the
+//       sequences that move, longest run first (so the long slabs start early
+//       and the tail of the shift is short).
+// shift (persistent, one thread per CTA drives the bulk-copy engine): each
+//       (layer, K/V, sequence, head) slab of a moving sequence is an in-place
+//       memmove of run * D * elt contiguous bytes by delta rows.  Tiles are
+//       staged global -> shared -> global with cp.async.bulk; they are taken
+//       from the end the run moves towards (descending for delta > 0), so a
+//       tile's destination overlaps only its own source and sources already
+//       loaded.  Loads run up to kStages - 1 tiles ahead of the stores; the
+//       stores are issued strictly in tile order after each tile's load has
+//       completed on its mbarrier.
+// Roofline: HBM-bound, 2 * run * D * elt bytes per moving slab.
+#include "spec_common.cuh"
+#include "spec_launch.h"
+
+namespace spec {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kSortMax = 2048;  // longest-first ordering up to this batch size
+
+struct PlanView {
+    int *order, *delta, *src_pad, *run, *misc;
+};
+
+__device__ __forceinline__ PlanView plan_view(void *ws, int B)
+{
+    const Layout lay = make_layout(B, 0, 1);
+    return PlanView{ws_at<int>(ws, lay.order), ws_at<int>(ws, lay.delta), ws_at<int>(ws, lay.src_pad),
+                    ws_at<int>(ws, lay.run), ws_at<int>(ws, lay.misc)};
+}
+
+__global__ void __launch_bounds__(kPlanThreads) realign_plan_kernel(RealignArgs a)
+{
+    __shared__ uint64_t s_key[kSortMax];
+    __shared__ int s_bad2, s_bad3, s_minpad, s_maxlen, s_count, s_rows;
+    const PlanView pv = plan_view(a.ws, a.B);
+    const int t = threadIdx.x;
+    if (t == 0) {
+        s_bad2 = 0;
+        s_bad3 = 0;
+        s_minpad = 0x7FFFFFFF;
+        s_maxlen = 0;
+        s_count = 0;
+        s_rows = 0;
+    }
+    __syncthreads();
+    const int W = a.pad[0] + a.len[0];
+    int bad2 = 0, bad3 = 0, minpad = 0x7FFFFFFF, maxlen = 0;
+    for (int b = t; b < a.B; b += kPlanThreads) {
+        const int l = a.len[b], p = a.pad[b], n = a.n_emit[b];
+        if (l < 1 || p < 0 || p + l != W)
+            bad2 = 1;
+        if (n < 0 || (long long)W + n - 1 > a.S)
+            bad3 = 1;
+        minpad = min(minpad, p);
+        if (n >= 0)
+            maxlen = max(maxlen, l + n);
+    }
+    if (bad2)
+        atomicOr(&s_bad2, 1);
+    if (bad3)
+        atomicOr(&s_bad3, 1);
+    atomicMin(&s_minpad, minpad);
+    atomicMax(&s_maxlen, maxlen);
+    __syncthreads();
+    int err = SPEC_REALIGN_OK;
+    if (s_bad2 || s_minpad != 0)
+        err = SPEC_REALIGN_LAYOUT;
+    else if (s_bad3)
+        err = SPEC_REALIGN_EMIT;
+    else if (s_maxlen > a.S)
+        err = SPEC_REALIGN_CAPACITY;
+    const int Wn = s_maxlen;
+    if (err != SPEC_REALIGN_OK) {
+        if (t == 0) {
+            pv.misc[MISC_NMOVING] = 0;
+            pv.misc[MISC_ERR] = err;
+            *a.err = err;
+        }
+        return;
+    }
+    // per-sequence shift; inputs are read before any output is written
+    // (len_new / pad_new may alias len / pad)
+    int rows = 0;
+    for (int b = t; b < a.B; b += kPlanThreads) {
+        const int l = a.len[b], p = a.pad[b], n = a.n_emit[b];
+        const int ln = l + n, pn = Wn - ln;
+        const int d = pn - p;
+        const int run = (d != 0 && ln - 1 > 0) ? ln - 1 : 0;
+        pv.delta[b] = d;
+        pv.src_pad[b] = p;
+        pv.run[b] = run;
+        rows += run;
+    }
+    atomicAdd(&s_rows, rows);
+    __syncthreads();
+    for (int b = t; b < a.B; b += kPlanThreads) {
+        const int pn = pv.src_pad[b] + pv.delta[b];
+        a.pad_new[b] = pn;
+        a.len_new[b] = Wn - pn;
+    }
+    // moving sequences, longest run first (ties: lower index first)
+    if (a.B <= kSortMax) {
+        int P = 1;
+        while (P < a.B)
+            P <<= 1;
+        for (int i = t; i < P; i += kPlanThreads) {
+            uint64_t key = 0;
+            if (i < a.B && pv.run[i] > 0)
+                key = ((uint64_t)pv.run[i] << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)i);
+            s_key[i] = key;
+        }
+        __syncthreads();
+        for (int size = 2; size <= P; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int i = t; i < P; i += kPlanThreads) {
+                    const int jx = i ^ stride;
+                    if (jx > i) {
+                        const bool desc = (i & size) == 0;
+                        const uint64_t x = s_key[i], y = s_key[jx];
+                        if (desc ? (x < y) : (x > y)) {
+                            s_key[i] = y;
+                            s_key[jx] = x;
+                        }
+                    }
+                }
+                __syncthreads();
+            }
+        }
+        for (int i = t; i < a.B; i += kPlanThreads) {
+            const uint64_t key = s_key[i];
+            if (key != 0) {
+                pv.order[i] = (int)(0xFFFFFFFFu - (uint32_t)key);
+                atomicAdd(&s_count, 1);
+            }
+        }
+    } else {
+        // large batches: stable compaction in index order
+        if (t == 0) {
+            int c = 0;
+            for (int b = 0; b < a.B; ++b)
+                if (pv.run[b] > 0)
+                    pv.order[c++] = b;
+            s_count = c;
+        }
+    }
+    __syncthreads();
+    if (t == 0) {
+        pv.misc[MISC_NMOVING] = s_count;
+        pv.misc[MISC_WORK] = 0;
+        pv.misc[MISC_WIDTH] = Wn;
+        pv.misc[MISC_ERR] = 0;
+        pv.misc[MISC_TOTAL_ROWS] = s_rows;
+        *a.width_new = Wn;
+        *a.err = SPEC_REALIGN_OK;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// bulk-copy shift
+// ---------------------------------------------------------------------------
+constexpr int kStages = 4;
+constexpr int kTile = 48 * 1024;  // bytes per stage
+constexpr int kShiftSmem = kStages * kTile;
+constexpr int kWaitLimit = 4000;  // probes of up to ~1 ms each before giving up
+
+struct TileGen {
+    char *slab;
+    long long src, dst, nbytes, done;  // byte offsets within the slab
+    int desc;                          // 1: tiles from the top of the run down
+};
+
+__device__ __forceinline__ bool tile_next(TileGen &g, const char *&src, char *&dst, uint32_t &bytes)
+{
+    if (g.done >= g.nbytes)
+        return false;
+    long long take = g.nbytes - g.done;
+    if (take > kTile)
+        take = kTile;
+    const long long lo = g.desc ? g.nbytes - g.done - take : g.done;
+    src = g.slab + g.src + lo;
+    dst = g.slab + g.dst + lo;
+    bytes = (uint32_t)take;
+    g.done += take;
+    return true;
+}
+
+template <int N>
+__device__ __forceinline__ void wait_read_upto(int newer)
+{
+    if constexpr (N > 0) {
+        if (newer >= N) {
+            bulk_wait_read<N>();
+            return;
+        }
+        wait_read_upto<N - 1>(newer);
+    } else {
+        bulk_wait_read<0>();
+    }
+}
+
+__global__ void __launch_bounds__(32) kv_shift_bulk_kernel(RealignArgs a)
+{
+    extern __shared__ __align__(128) unsigned char stage_mem[];
+    __shared__ __align__(8) uint64_t full[kStages];
+    if (threadIdx.x != 0)
+        return;
+    const PlanView pv = plan_view(a.ws, a.B);
+    const int n_moving = pv.misc[MISC_NMOVING];
+    if (n_moving <= 0)
+        return;
+    const int sps = a.L * 2 * a.H;  // slabs per sequence
+    const long long n_items = (long long)n_moving * sps;
+    const long long row_bytes = (long long)a.D * a.elt_bytes;
+    const long long slab_bytes = row_bytes * a.S;
+
+    for (int s = 0; s < kStages; ++s)
+        mbar_init(&full[s], 1);
+    fence_mbar_init();
+
+    // work items: (rank in the longest-first list, slab within the sequence)
+    long long item = atomicAdd(pv.misc + MISC_WORK, 1);
+    TileGen g{nullptr, 0, 0, 0, 0, 0};
+    auto open_item = [&](long long it) -> bool {
+        if (it >= n_items)
+            return false;
+        const int r = (int)(it / sps), within = (int)(it % sps);
+        const int b = pv.order[r];
+        const int h = within % a.H, lc = within / a.H;  // lc = l * 2 + c
+        const long long slab = ((long long)lc * a.B + b) * a.H + h;
+        const int d = pv.delta[b];
+        g.slab = reinterpret_cast<char *>(a.kv) + slab * slab_bytes;
+        g.src = (long long)pv.src_pad[b] * row_bytes;
+        g.dst = (long long)(pv.src_pad[b] + d) * row_bytes;
+        g.nbytes = (long long)pv.run[b] * row_bytes;
+        g.done = 0;
+        g.desc = d > 0;
+        return true;
+    };
+    bool more = open_item(item);
+    if (more)
+        item = atomicAdd(pv.misc + MISC_WORK, 1);  // prefetch the next item
+
+    char *dst_of[kStages];
+    uint32_t bytes_of[kStages];
+    uint32_t parity = 0;
+    long long issued = 0, done = 0;
+    bool failed = false;
+    while (true) {
+        while (more && issued - done < kStages - 1) {
+            const char *src;
+            char *dst;
+            uint32_t bytes;
+            if (!tile_next(g, src, dst, bytes)) {
+                more = open_item(item);
+                if (more)
+                    item = atomicAdd(pv.misc + MISC_WORK, 1);
+                continue;
+            }
+            const int s = (int)(issued % kStages);
+            if (issued >= kStages)
+                wait_read_upto<kStages - 1>((int)(done - 1 - (issued - kStages)));
+            mbar_arrive_expect_tx(&full[s], bytes);
+            bulk_g2s(stage_mem + (size_t)s * kTile, src, bytes, &full[s]);
+            dst_of[s] = dst;
+            bytes_of[s] = bytes;
+            ++issued;
+        }
+        if (done == issued)
+            break;
+        const int s = (int)(done % kStages);
+        const uint32_t par = (parity >> s) & 1u;
+        int probes = 0;
+        while (!mbar_try_wait(&full[s], par)) {
+            if (++probes >= kWaitLimit) {
+                failed = true;
+                break;
+            }
+        }
+        if (failed)
+            break;
+        parity ^= 1u << s;
+        bulk_s2g(dst_of[s], stage_mem + (size_t)s * kTile, bytes_of[s]);
+        bulk_commit();
+        ++done;
+    }
+    if (failed) {
+        // record the error, then wait (bounded) for the loads still in flight
+        *a.err = SPEC_REALIGN_TIMEOUT;
+        for (long long i = done; i < issued; ++i) {
+            const int s = (int)(i % kStages);
+            const uint32_t par = (parity >> s) & 1u;
+            for (int p = 0; p < kWaitLimit && !mbar_try_wait(&full[s], par); ++p) {
+            }
+            parity ^= 1u << s;
+        }
+    }
+    bulk_wait_all();
+}
+
+// Plain path for rows that are not a multiple of 16 bytes (or an unaligned
+// cache): one CTA per slab, tiles staged in registers, element granularity.
+template <typename E>
+__global__ void __launch_bounds__(256) kv_shift_plain_kernel(RealignArgs a)
+{
+    const PlanView pv = plan_view(a.ws, a.B);
+    const int n_moving = pv.misc[MISC_NMOVING];
+    const int sps = a.L * 2 * a.H;
+    const long long it = blockIdx.x;
+    if (it >= (long long)n_moving * sps)
+        return;
+    const int r = (int)(it / sps), within = (int)(it % sps);
+    const int b = pv.order[r];
+    const int h = within % a.H, lc = within / a.H;
+    const long long slab = ((long long)lc * a.B + b) * a.H + h;
+    E *base = reinterpret_cast<E *>(a.kv) + slab * (long long)a.S * a.D;
+    const int d = pv.delta[b];
+    const long long n = (long long)pv.run[b] * a.D;
+    E *src = base + (long long)pv.src_pad[b] * a.D;
+    E *dst = src + (long long)d * a.D;
+    constexpr int kPer = 4, kT = 256 * kPer;
+    for (long long done = 0; done < n; done += kT) {
+        const long long take = (n - done) < kT ? (n - done) : kT;
+        const long long lo = d > 0 ? n - done - take : done;
+        E v[kPer];
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+            const long long i = lo + threadIdx.x + e * 256;
+            if (i < lo + take)
+                v[e] = src[i];
+        }
+        __syncthreads();  // the whole tile is read before any of it is written
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+            const long long i = lo + threadIdx.x + e * 256;
+            if (i < lo + take)
+                dst[i] = v[e];
+        }
+        __syncthreads();
+    }
+}
+
+static int g_sm_count[64];
+static bool g_smem_set[64];
+
+cudaError_t launch_realign(const RealignArgs &a, cudaStream_t st)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const int slot = dev & 63;
+    if (g_sm_count[slot] == 0) {
+        e = cudaDeviceGetAttribute(&g_sm_count[slot], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return e;
+    }
+    realign_plan_kernel<<<1, kPlanThreads, 0, st>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    const long long row_bytes = (long long)a.D * a.elt_bytes;
+    const bool bulk = (row_bytes % 16 == 0) && (reinterpret_cast<uintptr_t>(a.kv) % 16 == 0);
+    if (bulk) {
+        if (!g_smem_set[slot]) {
+            e = cudaFuncSetAttribute(kv_shift_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kShiftSmem);
+            if (e != cudaSuccess)
+                return e;
+            g_smem_set[slot] = true;
+        }
+        kv_shift_bulk_kernel<<<g_sm_count[slot], 32, kShiftSmem, st>>>(a);
+    } else {
+        const long long blocks = (long long)a.B * a.L * 2 * a.H;
+        if (a.elt_bytes == 4)
+            kv_shift_plain_kernel<uint32_t><<<(unsigned)blocks, 256, 0, st>>>(a);
+        else
+            kv_shift_plain_kernel<uint16_t><<<(unsigned)blocks, 256, 0, st>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace spec

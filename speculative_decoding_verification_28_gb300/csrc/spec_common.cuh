@@ -1,0 +1,245 @@
+// spec_common.cuh -- device helpers shared by the library's kernels:
+// workspace layout, storage-type loads, the argmax ordering key, and inline
+// PTX for mbarriers and 1-D bulk (TMA) copies on sm_103a.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "specverify.h"
+
+namespace spec {
+
+// ---------------------------------------------------------------------------
+// sizes
+// ---------------------------------------------------------------------------
+constexpr int kThreads = 256;          // threads of the row-streaming kernels
+constexpr int kChunk = 8192;           // vocabulary elements per CTA work unit
+constexpr int kMaxRows = SPEC_MAX_K + 1;
+constexpr int kStopBase = 1024;        // stop row j is stored as kStopBase - j
+
+__host__ __device__ inline int verify_chunks(int V) { return (V + kChunk - 1) / kChunk; }
+
+// ---------------------------------------------------------------------------
+// workspace layout (byte offsets; every array 256-byte aligned)
+//   [realign region: depends on B]
+//   [counter region: depends on B; zero between calls]
+//   [verify scratch: depends on B, k, V]
+// ---------------------------------------------------------------------------
+struct Layout {
+    // realignment plan
+    size_t order, delta, src_pad, run, misc;
+    // counters that every verify call leaves at zero
+    size_t zero_begin, seq_cnt, stop_enc, res_cnt, row_cnt, zero_end;
+    // verify scratch
+    size_t row_tok, row_ms, row_flag, part, draw_row, rpart, rtot;
+    size_t total;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+__host__ __device__ inline Layout make_layout(int B, int k, int V)
+{
+    Layout L{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o = align256(o + bytes);
+        return at;
+    };
+    const size_t b = (size_t)(B > 0 ? B : 0);
+    const size_t rows = b * (size_t)(k + 1);
+    const size_t C = (size_t)verify_chunks(V > 0 ? V : 1);
+    L.order = take(b * 4);
+    L.delta = take(b * 4);
+    L.src_pad = take(b * 4);
+    L.run = take(b * 4);
+    L.misc = take(64);
+    L.zero_begin = o;
+    L.seq_cnt = take(b * 4);
+    L.stop_enc = take(b * 4);
+    L.res_cnt = take(b * 4);
+    L.row_cnt = take(b * kMaxRows * 4);  // sized for the largest k
+    L.zero_end = o;
+    L.row_tok = take(rows * 4);
+    L.row_ms = take(rows * 8);
+    L.row_flag = take(rows * 4);
+    L.part = take(rows * C * 16);
+    L.draw_row = take(b * 4);
+    L.rpart = take(b * C * 8);
+    L.rtot = take(b * 8);
+    L.total = o;
+    return L;
+}
+
+// misc slots of the realignment plan
+enum { MISC_NMOVING = 0, MISC_WORK = 1, MISC_WIDTH = 2, MISC_ERR = 3, MISC_TOTAL_ROWS = 4 };
+
+template <typename T>
+__host__ __device__ inline T *ws_at(void *ws, size_t off)
+{
+    return reinterpret_cast<T *>(reinterpret_cast<char *>(ws) + off);
+}
+
+// ---------------------------------------------------------------------------
+// storage types
+// ---------------------------------------------------------------------------
+template <typename T>
+struct Storage;
+template <>
+struct Storage<float> {
+    static constexpr int kVec = 4;  // elements per 16-byte vector
+    __device__ static float at(const float *p, int64_t i) { return __ldg(p + i); }
+    __device__ static void unpack(const uint4 &u, float (&f)[4])
+    {
+        f[0] = __uint_as_float(u.x);
+        f[1] = __uint_as_float(u.y);
+        f[2] = __uint_as_float(u.z);
+        f[3] = __uint_as_float(u.w);
+    }
+};
+template <>
+struct Storage<__nv_bfloat16> {
+    static constexpr int kVec = 8;
+    __device__ static float at(const __nv_bfloat16 *p, int64_t i)
+    {
+        const unsigned short h = __ldg(reinterpret_cast<const unsigned short *>(p) + i);
+        return __uint_as_float((uint32_t)h << 16);
+    }
+    __device__ static void unpack(const uint4 &u, float (&f)[8])
+    {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+};
+template <>
+struct Storage<__half> {
+    static constexpr int kVec = 8;
+    __device__ static float at(const __half *p, int64_t i) { return __half2float(__ldg(p + i)); }
+    __device__ static void unpack(const uint4 &u, float (&f)[8])
+    {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h;
+            memcpy(&h, &w[i], 4);
+            const float2 t = __half22float2(h);
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        }
+    }
+};
+
+// 16-byte streaming load that does not allocate in L1 (each logit is read once)
+__device__ __forceinline__ uint4 ld_stream16(const void *p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ int ld_relaxed(const int *p)
+{
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Ordering key for "largest value, lowest index on ties, NaN above all":
+// a larger key is a better candidate.  +0 and -0 compare equal.
+__device__ __forceinline__ uint64_t argmax_key(float v, uint32_t idx)
+{
+    uint32_t ord;
+    if (v != v) {
+        ord = 0xFFFFFFFFu;
+    } else {
+        uint32_t b = (v == 0.0f) ? 0u : __float_as_uint(v);
+        ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    }
+    return ((uint64_t)ord << 32) | (uint64_t)(0xFFFFFFFFu - idx);
+}
+__device__ __forceinline__ uint32_t key_index(uint64_t key) { return 0xFFFFFFFFu - (uint32_t)key; }
+
+__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m)
+{
+    uint32_t lo = (uint32_t)v, hi = (uint32_t)(v >> 32);
+    lo = __shfl_xor_sync(0xFFFFFFFFu, lo, m);
+    hi = __shfl_xor_sync(0xFFFFFFFFu, hi, m);
+    return ((uint64_t)hi << 32) | lo;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier + 1-D bulk copy (cp.async.bulk) wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// one bounded probe of the barrier phase; true once phase `parity` completed
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// global -> shared bulk copy completing on an mbarrier
+__device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst_smem)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// shared -> global bulk copy tracked by bulk async-groups
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src_smem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_addr(src_smem)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+}  // namespace spec

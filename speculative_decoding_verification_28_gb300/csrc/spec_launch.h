@@ -1,0 +1,50 @@
+// spec_launch.h -- host-side launchers of the library's kernels (internal;
+// the public ABI is include/specverify.h, implemented in api.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "specverify.h"
+
+namespace spec {
+
+struct VerifyArgs {
+    const void *logits;
+    int B, k, V, C;
+    const int32_t *draft;
+    const int32_t *draft_len;
+    int32_t eos;
+    const int32_t *remaining;
+    int32_t *out_tokens;
+    int32_t *n_accept;
+    int32_t *n_emit;
+    void *ws;
+    // stochastic verification only
+    float inv_temp;
+    int unit_temp;
+    const float *q;
+    const float *u;
+    float *out_residual;
+    uint32_t *flags;
+};
+
+cudaError_t launch_verify_greedy(const VerifyArgs &a, spec_dtype dt, cudaStream_t st);
+cudaError_t launch_verify_sample(const VerifyArgs &a, spec_dtype dt, cudaStream_t st);
+
+struct RealignArgs {
+    void *kv;
+    int elt_bytes, L, B, H, S, D;
+    const int32_t *len, *pad, *n_emit;
+    int32_t *len_new, *pad_new, *width_new, *err;
+    void *ws;
+};
+cudaError_t launch_realign(const RealignArgs &a, cudaStream_t st);
+
+cudaError_t launch_pos_mask(int B, int S, const int32_t *pad_old, const int32_t *pad_new, int32_t *pos,
+                            uint8_t *mask, cudaStream_t st);
+
+cudaError_t launch_group(int N, const int32_t *len, const uint8_t *active, int B, int32_t *out_idx,
+                         int32_t *out_count_equal, int32_t *out_group_len, cudaStream_t st);
+
+}  // namespace spec

@@ -1,0 +1,142 @@
+"""The C ABI boundary, checked on the host (no GPU needed).
+
+The library must load and export every entry point include/specverify.h
+declares; argument errors must be reported before anything is launched (these
+calls return before any CUDA runtime call, so they run on a CPU-only box).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "specverify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_28_gb300 import _lib
+    from speculative_decoding_verification_28_gb300 import build as libbuild
+
+    libbuild.build()
+    return _lib.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert {"spec_verify_greedy", "spec_verify_sample", "spec_realign_kv", "spec_rebuild_pos_mask",
+            "spec_group_by_length", "spec_workspace_bytes"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    from speculative_decoding_verification_28_gb300._lib import SIGNATURES
+
+    assert set(SIGNATURES) == set(names)
+
+
+def test_workspace_sizes(lib):
+    assert lib.spec_workspace_bytes(0, 4, 100) == 0
+    a = lib.spec_workspace_bytes(8, 5, 32000)
+    b = lib.spec_workspace_bytes(8, 5, 64000)
+    c = lib.spec_workspace_bytes(16, 5, 32000)
+    assert 0 < a < b and a < c and a % 256 == 0
+    # the realignment needs only the batch-dependent part
+    assert lib.spec_workspace_bytes(8, 0, 1) <= a
+
+
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: every call below returns first
+FAKE_ODD = ctypes.c_void_p(0x10001)
+
+
+def greedy(lib, logits=FAKE, dt=1, B=2, k=3, V=100, draft=FAKE, out=FAKE, ws=FAKE, wsb=1 << 30):
+    return lib.spec_verify_greedy(logits, dt, B, k, V, draft, None, -1, None, out, FAKE, FAKE, ws, wsb, None)
+
+
+def test_greedy_argument_errors(lib):
+    assert greedy(lib, B=-1) == -1
+    assert greedy(lib, k=-1) == -1
+    assert greedy(lib, k=32) == -1  # above SPEC_MAX_K
+    assert greedy(lib, V=0) == -1
+    assert greedy(lib, dt=7) == -2
+    assert greedy(lib, logits=None) == -1
+    assert greedy(lib, draft=None) == -1
+    assert greedy(lib, out=None) == -1
+    assert greedy(lib, ws=None) == -3
+    assert greedy(lib, wsb=16) == -3
+    assert greedy(lib, ws=FAKE_ODD) == -3
+    assert greedy(lib, logits=FAKE_ODD) == -5
+    assert greedy(lib, B=0) == 0  # empty batch: valid no-op, nothing launched
+
+
+def test_sample_argument_errors(lib):
+    def sample(temp=1.0, u=FAKE, q=FAKE, k=2):
+        return lib.spec_verify_sample(FAKE, 0, temp, q, FAKE, u, 2, k, 50, None, -1, None, FAKE, FAKE, FAKE, None,
+                                      None, FAKE, 1 << 30, None)
+
+    assert sample(temp=0.0) == -1
+    assert sample(temp=-1.0) == -1
+    assert sample(temp=float("nan")) == -1
+    assert sample(temp=float("inf")) == -1
+    assert sample(u=None) == -1
+    assert sample(q=None) == -1
+    assert sample(u=FAKE_ODD) == -5
+
+
+def test_realign_argument_errors(lib):
+    def realign(kv=FAKE, dt=1, L=2, B=3, H=2, S=64, D=8, ws=FAKE, wsb=1 << 20, err=FAKE):
+        return lib.spec_realign_kv(kv, dt, L, B, H, S, D, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, err, ws, wsb, None)
+
+    assert realign(L=0) == -1
+    assert realign(S=0) == -1
+    assert realign(B=-2) == -1
+    assert realign(B=0) == 0
+    assert realign(dt=5) == -2
+    assert realign(kv=None) == -1
+    assert realign(err=None) == -1
+    assert realign(ws=None) == -3
+    assert realign(wsb=8) == -3
+    assert realign(kv=FAKE_ODD) == -5
+
+
+def test_posmask_and_group_argument_errors(lib):
+    assert lib.spec_rebuild_pos_mask(-1, 8, None, FAKE, FAKE, FAKE, None) == -1
+    assert lib.spec_rebuild_pos_mask(0, 8, None, FAKE, FAKE, FAKE, None) == 0
+    assert lib.spec_rebuild_pos_mask(2, 0, None, FAKE, FAKE, FAKE, None) == 0
+    assert lib.spec_rebuild_pos_mask(2, 8, FAKE, FAKE, FAKE, FAKE, None) == -1  # pad_old aliases pad_new
+    assert lib.spec_rebuild_pos_mask(2, 8, None, None, FAKE, FAKE, None) == -1
+    assert lib.spec_group_by_length(-1, FAKE, None, 4, FAKE, FAKE, FAKE, None) == -1
+    assert lib.spec_group_by_length(4097, FAKE, None, 4, FAKE, FAKE, FAKE, None) == -1
+    assert lib.spec_group_by_length(8, None, None, 4, FAKE, FAKE, FAKE, None) == -1
+    assert lib.spec_group_by_length(8, FAKE, None, -1, FAKE, FAKE, FAKE, None) == -1
+
+
+def test_status_strings(lib):
+    for rc in (0, -1, -2, -3, -4, -5):
+        assert lib.spec_status_str(rc)
+    assert lib.spec_status_str(0) == b"ok"
+
+
+def test_product_path_has_no_fallback():
+    """The binding never imports the oracle and fails loudly without its library."""
+    pkg = os.path.join(ROOT, "speculative_decoding_verification_28_gb300")
+    for fn in os.listdir(pkg):
+        if fn.endswith(".py"):
+            src = open(os.path.join(pkg, fn)).read()
+            assert "oracle" not in src, fn
+            assert "specgen" not in src, fn
+    from speculative_decoding_verification_28_gb300 import _lib
+
+    saved = _lib.LIB_PATH, _lib._lib
+    try:
+        _lib.LIB_PATH, _lib._lib = "/nonexistent/libspecverify.so", None
+        with pytest.raises(ImportError):
+            _lib.load()
+    finally:
+        _lib.LIB_PATH, _lib._lib = saved

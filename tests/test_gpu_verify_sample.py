@@ -1,0 +1,168 @@
+"""Stochastic verification: CUDA path (fp32 arithmetic) vs the CPU oracle
+(fp64 probabilities).
+
+Acceptance criteria: tokens, accepted and committed counts equal the oracle's
+except where the oracle's own decision sits on a boundary --
+  * a ratio test with |u - p/q| <= 1e-5 * p/q, or
+  * a draw whose uniform lies within 1e-5 * u of every oracle CDF boundary
+    C_i / sum(w) between the two chosen indices;
+such cases are counted and their rate must stay below 1e-4 of all decisions.
+Normalised residual / draw distributions must match within 1e-6 absolute.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_verification_28_gb300 as sv
+from gpu_util import DT_OF, dev, logits_to_dev, storage_of, to_dev
+from specgen import CONFIGS, sample_round_inputs
+from specgen import torch_gen
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-5
+STATS = {"decisions": 0, "boundary": 0}
+
+
+def _boundary_explains(x, dt, q, d, u, T, b, o_out, o_na, o_ne, o_res, g_out, g_na, g_ne, kb):
+    """True when the first difference between the two results of sequence b
+    is a decision on a boundary of the oracle's arithmetic."""
+    k = d.shape[1]
+    # first ratio test where the two sides decided differently
+    j = 0
+    while j < kb and j < min(o_na, g_na) + 1:
+        if j >= o_ne or j >= g_ne:
+            break
+        if (j < o_na) != (j < g_na):
+            p, _ = oracle.softmax_row(x.reshape(-1, x.shape[-1]), dt, b * (k + 1) + j, T)
+            y = int(d[b, j])
+            r = p[y] / float(q[b, j, y])
+            return abs(float(u[b, j]) - r) <= TOL * r
+        j += 1
+    if o_na != g_na:
+        return False
+    # same accepted prefix: the draw differs
+    if o_res is None:
+        return False
+    g_tok, o_tok = int(g_out[b, o_na]), int(o_out[b, o_na])
+    if g_tok == o_tok:
+        return False
+    c = np.cumsum(o_res[b])
+    uu = float(u[b, k])
+    lo, hi = min(g_tok, o_tok), max(g_tok, o_tok)
+    return bool(np.all(np.abs(c[lo:hi] - uu) <= TOL * uu))
+
+
+def check(x, dt, q, d, u, T=1.0, draft_len=None, eos=-1, remaining=None, residual=True):
+    g = sv.spec_verify_sample(logits_to_dev(x, dt), to_dev(q), to_dev(d), to_dev(u), temperature=T,
+                              draft_len=None if draft_len is None else to_dev(draft_len), eos_id=eos,
+                              remaining=None if remaining is None else to_dev(remaining), want_residual=residual)
+    g_out, g_na, g_ne, g_fl = (t.cpu().numpy() for t in g[:4])
+    g_res = g[4].cpu().numpy() if residual else None
+    o_out, o_na, o_ne, o_fl, o_res = oracle.verify_sample(x, dt, q, d, u, T, draft_len, eos, remaining,
+                                                          want_residual=True)
+    B, k1 = o_out.shape
+    kbs = np.full(B, k1 - 1) if draft_len is None else draft_len
+    for b in range(B):
+        STATS["decisions"] += int(o_ne[b]) + 1
+        if o_fl[b] & 4:  # non-finite rows: only the flag is specified
+            assert g_fl[b] & 4
+            continue
+        same = (np.array_equal(g_out[b], o_out[b]) and g_na[b] == o_na[b] and g_ne[b] == o_ne[b])
+        if not same:
+            assert _boundary_explains(x, dt, q, d, u, T, b, o_out, o_na[b], o_ne[b], o_res, g_out, g_na[b],
+                                      g_ne[b], int(kbs[b])), (b, g_out[b], o_out[b], g_na[b], o_na[b])
+            STATS["boundary"] += 1
+            continue
+        assert (g_fl[b] & ~4) == (o_fl[b] & ~4), (b, g_fl[b], o_fl[b])
+        if residual and not np.isnan(o_res[b]).all():
+            err = np.abs(g_res[b].astype(np.float64) - o_res[b]).max()
+            assert err <= 1e-6, (b, err)
+    return g, (o_out, o_na, o_ne, o_fl, o_res)
+
+
+def test_config3_rounds():
+    """B=32, k=4, V=128256 fp32 target, draft = target + N(0, 0.5), 20 rounds."""
+    c = CONFIGS["c3"]
+    g = torch.Generator(device=dev()).manual_seed(1003)
+    acc = 0
+    for r in range(c["rounds"]):
+        xt, qt, dt_, ut = torch_gen.sample_round_inputs(c["B"], c["k"], c["V"], c["noise"], g, torch.float32, dev())
+        _, o = check(xt.cpu().numpy(), oracle.DT_F32, qt.cpu().numpy(), dt_.cpu().numpy(), ut.cpu().numpy())
+        acc += o[1].sum()
+    # acceptance rate ~ sum min(p, q) for this construction (about 0.8)
+    assert 0.6 < acc / (c["rounds"] * c["B"] * c["k"]) < 0.95
+
+
+def test_config5_stochastic_full_size():
+    """B=256, k=8, V=128256 bf16 target; 1 GB of draft probabilities."""
+    c = CONFIGS["c5"]
+    g = torch.Generator(device=dev()).manual_seed(1005)
+    for r in range(2):
+        xt, qt, dt_, ut = torch_gen.sample_round_inputs(c["B"], c["k"], c["V"], c["noise"], g, torch.bfloat16,
+                                                        dev())
+        check(storage_of(xt), oracle.DT_BF16, qt.cpu().numpy(), dt_.cpu().numpy(), ut.cpu().numpy(),
+              residual=(r == 0))
+
+
+@pytest.mark.parametrize("V", [2, 3, 8, 100, 8193, 20000])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_small_vocabularies_many_draws(V, dtype):
+    B = 4096 if V <= 100 else 64
+    x, q, d, u = sample_round_inputs(B, 3, V, 0.8, seed=V, dtype=dtype)
+    check(x, DT_OF[dtype], q, d, u)
+
+
+@pytest.mark.parametrize("T", [0.5, 0.7, 1.5, 3.0])
+def test_temperature(T):
+    x, q, d, u = sample_round_inputs(256, 4, 5000, 0.5, seed=int(T * 10), dtype="f32")
+    check(x, oracle.DT_F32, q, d, u, T=T)
+
+
+def test_stop_rules_and_per_sequence_arguments():
+    rng = np.random.default_rng(11)
+    B, k, V = 512, 6, 50
+    for trial in range(6):
+        x, q, d, u = sample_round_inputs(B, k, V, 0.3, seed=trial, dtype="bf16")
+        dl = rng.integers(0, k + 1, size=B).astype(np.int32)
+        rem = rng.integers(-1, k + 3, size=B).astype(np.int32)
+        eos = int(rng.integers(0, V))
+        check(x, oracle.DT_BF16, q, d, u, draft_len=dl, eos=eos, remaining=rem)
+
+
+def test_flags_and_degenerate_rows():
+    V, k, B = 16, 2, 6
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((B, k + 1, V)).astype(np.float32)
+    q = np.full((B, k, V), 1.0 / V, np.float32)
+    d = rng.integers(0, V, size=(B, k)).astype(np.int32)
+    u = rng.random((B, k + 1), dtype=np.float32)
+    q[0, 0, d[0, 0]] = 0.0  # flag 1
+    q[1, 0] = 1.5 * np.exp(x[1, 0]) / np.exp(x[1, 0]).sum()  # q > p everywhere: zero residual
+    u[1, 0] = 0.9
+    x[2, 0, 3] = np.inf  # flag 4
+    x[3, 0, 5] = np.nan  # flag 4
+    d[4, 0] = -3  # flag 8
+    d[5, 1] = V + 2
+    check(x, oracle.DT_F32, q, d, u)
+
+
+def test_workspace_reuse_across_kinds():
+    """Greedy and stochastic calls alternate on one workspace."""
+    B = 64
+    ws = sv.Workspace(B, sv.MAX_K, 20000, dev())
+    for trial in range(4):
+        x, q, d, u = sample_round_inputs(B, 4, 20000, 0.5, seed=100 + trial, dtype="f32")
+        g = sv.spec_verify_sample(to_dev(x), to_dev(q), to_dev(d), to_dev(u), workspace=ws)
+        o = oracle.verify_sample(x, oracle.DT_F32, q, d, u)
+        assert np.array_equal(g[2].cpu().numpy(), o[2])
+        gg = sv.spec_verify_greedy(to_dev(x), to_dev(d), workspace=ws)
+        og = oracle.verify_greedy(x, oracle.DT_F32, d)
+        assert np.array_equal(gg[0].cpu().numpy(), og[0])
+
+
+def test_zz_boundary_rate():
+    """All files above: boundary cases stay below 1e-4 of the decisions."""
+    assert STATS["decisions"] > 50_000
+    assert STATS["boundary"] < 1e-4 * STATS["decisions"], STATS
