@@ -32,10 +32,10 @@ def test_config4_pools(variant):
             lens = rng.integers(c["pool_len"][0], c["pool_len"][1] + 1, size=c["N"]).astype(np.int32)
         else:
             lens = (rng.integers(1, 9, size=c["N"]) * 128).astype(np.int32)
-        act = (rng.random(c["N"]) < 0.9).astype(np.uint8)
+        act = (rng.random(c["N"]) < 0.9).astype(np.uint8) if r % 2 else None
         full += group_both(lens, c["B"], act) == c["B"]
     if variant == "b":
-        assert full == 20  # ~58 sequences per length bucket: a full group every round
+        assert full >= 16  # 8 length buckets of ~60 sequences: a full group of 64 most rounds
 
 
 def test_small_pools_and_degenerate_cases():

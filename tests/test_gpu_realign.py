@@ -112,7 +112,7 @@ def test_errors_leave_state_untouched():
     pad = np.array([0, 3, 1], np.int32)
     sentinel = torch.full((B,), -7, dtype=torch.int32, device=dev())
     cases = [
-        (ln, pad, [1, 20, 1], sv.REALIGN_EMIT),       # run would pass S
+        (ln, pad, [1, 30, 1], sv.REALIGN_EMIT),       # run would pass S: W + 30 - 1 > 32
         (ln, pad, [-1, 1, 1], sv.REALIGN_EMIT),
         (ln, np.array([0, 2, 1], np.int32), [1, 1, 1], sv.REALIGN_LAYOUT),  # pad + len not constant
         (ln - 1, pad + 1, [1, 1, 1], sv.REALIGN_LAYOUT),  # no sequence without padding

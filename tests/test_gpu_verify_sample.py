@@ -22,7 +22,26 @@ from specgen import torch_gen
 pytestmark = pytest.mark.gpu
 
 TOL = 1e-5
-STATS = {"decisions": 0, "boundary": 0}
+RES_TOL = 1e-6
+STATS = {"decisions": 0, "boundary": 0, "residual_rows": 0, "widened_rows": 0}
+
+
+def residual_tolerance(x, dt, q, T, b, k, row, bonus, r_o):
+    """Per-element tolerance of the normalised draw distribution.
+
+    1e-6 absolute, widened only where fp32 arithmetic cannot reach it:
+    r_v = w_v / W with w_v = max(0, p_v - q_v) inherits p_v's fp32 relative
+    error (expf <= 2 ulp, the division and the row sum: ~5 * 2^-24 ~ 3e-7)
+    amplified by p_v / W, and the error of W itself.  The bound used,
+    1e-6 * (1 + (p_v + r_v * sum_{w>0} p) / W), is that estimate with a 3x
+    margin; with large vocabularies (p_v << W) it is the plain 1e-6."""
+    p, _ = oracle.softmax_row(x.reshape(-1, x.shape[-1]), dt, b * (k + 1) + row, T)
+    w = p if bonus else np.maximum(p - q[b, row].astype(np.float64), 0.0)
+    if not bonus and not (w.sum() > 0):
+        w = p
+    W = w.sum()
+    ppos = p[w > 0].sum()
+    return RES_TOL * (1.0 + (p + r_o * ppos) / W)
 
 
 def _boundary_explains(x, dt, q, d, u, T, b, o_out, o_na, o_ne, o_res, g_out, g_na, g_ne, kb):
@@ -67,7 +86,7 @@ def check(x, dt, q, d, u, T=1.0, draft_len=None, eos=-1, remaining=None, residua
     for b in range(B):
         STATS["decisions"] += int(o_ne[b]) + 1
         if o_fl[b] & 4:  # non-finite rows: only the flag is specified
-            assert g_fl[b] & 4
+            assert int(g_fl[b]) & 4
             continue
         same = (np.array_equal(g_out[b], o_out[b]) and g_na[b] == o_na[b] and g_ne[b] == o_ne[b])
         if not same:
@@ -75,10 +94,16 @@ def check(x, dt, q, d, u, T=1.0, draft_len=None, eos=-1, remaining=None, residua
                                       g_ne[b], int(kbs[b])), (b, g_out[b], o_out[b], g_na[b], o_na[b])
             STATS["boundary"] += 1
             continue
-        assert (g_fl[b] & ~4) == (o_fl[b] & ~4), (b, g_fl[b], o_fl[b])
+        assert (int(g_fl[b]) & ~4) == (int(o_fl[b]) & ~4), (b, g_fl[b], o_fl[b])
         if residual and not np.isnan(o_res[b]).all():
-            err = np.abs(g_res[b].astype(np.float64) - o_res[b]).max()
-            assert err <= 1e-6, (b, err)
+            err = np.abs(g_res[b].astype(np.float64) - o_res[b])
+            STATS["residual_rows"] += 1
+            if err.max() > RES_TOL:
+                row = int(o_na[b])
+                kb = int(kbs[b])
+                tol = residual_tolerance(x, dt, q, T, b, k1 - 1, row, row == kb, o_res[b])
+                assert (err <= tol).all(), (b, err.max(), tol[np.argmax(err - tol)])
+                STATS["widened_rows"] += 1
     return g, (o_out, o_na, o_ne, o_fl, o_res)
 
 
@@ -86,13 +111,16 @@ def test_config3_rounds():
     """B=32, k=4, V=128256 fp32 target, draft = target + N(0, 0.5), 20 rounds."""
     c = CONFIGS["c3"]
     g = torch.Generator(device=dev()).manual_seed(1003)
-    acc = 0
+    acc = tested = 0
+    widened = STATS["widened_rows"]
     for r in range(c["rounds"]):
         xt, qt, dt_, ut = torch_gen.sample_round_inputs(c["B"], c["k"], c["V"], c["noise"], g, torch.float32, dev())
         _, o = check(xt.cpu().numpy(), oracle.DT_F32, qt.cpu().numpy(), dt_.cpu().numpy(), ut.cpu().numpy())
         acc += o[1].sum()
-    # acceptance rate ~ sum min(p, q) for this construction (about 0.8)
-    assert 0.6 < acc / (c["rounds"] * c["B"] * c["k"]) < 0.95
+        tested += o[1].sum() + (o[1] < c["k"]).sum()  # ratio tests actually performed
+    # acceptance rate per ratio test ~ sum min(p, q) (about 0.8 for this construction)
+    assert 0.7 < acc / tested < 0.9
+    assert STATS["widened_rows"] == widened  # large vocabulary: the plain 1e-6 holds
 
 
 def test_config5_stochastic_full_size():
@@ -102,8 +130,10 @@ def test_config5_stochastic_full_size():
     for r in range(2):
         xt, qt, dt_, ut = torch_gen.sample_round_inputs(c["B"], c["k"], c["V"], c["noise"], g, torch.bfloat16,
                                                         dev())
+        widened = STATS["widened_rows"]
         check(storage_of(xt), oracle.DT_BF16, qt.cpu().numpy(), dt_.cpu().numpy(), ut.cpu().numpy(),
               residual=(r == 0))
+        assert STATS["widened_rows"] == widened
 
 
 @pytest.mark.parametrize("V", [2, 3, 8, 100, 8193, 20000])
@@ -166,3 +196,4 @@ def test_zz_boundary_rate():
     """All files above: boundary cases stay below 1e-4 of the decisions."""
     assert STATS["decisions"] > 50_000
     assert STATS["boundary"] < 1e-4 * STATS["decisions"], STATS
+    print("sampling parity statistics:", STATS)
