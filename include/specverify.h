@@ -57,7 +57,8 @@ enum {
     SPEC_EDTYPE = -2,     /* unknown spec_dtype */
     SPEC_EWORKSPACE = -3, /* workspace NULL, misaligned or too small */
     SPEC_ECUDA = -4,      /* a CUDA launch failed (see cudaGetLastError) */
-    SPEC_EALIGN = -5      /* a pointer lacks the alignment its type needs */
+    SPEC_EALIGN = -5,     /* a pointer lacks the alignment its type needs */
+    SPEC_ESCRATCH = -6    /* sizes need more than SPEC_STATIC_SCRATCH_BYTES */
 };
 
 /* Per-sequence flag bits of spec_verify_sample. */
@@ -197,6 +198,36 @@ SPEC_API int spec_rebuild_pos_mask(int B, int S, const int32_t *pad_old, const i
 SPEC_API int spec_group_by_length(int N, const int32_t *len, const uint8_t *active, int B,
                          int32_t *out_idx, int32_t *out_count_equal, int32_t *out_group_len,
                          void *cuda_stream);
+
+/* Size of the device scratch built into the library for
+ * spec_verify_greedy_static (held by every GPU that loads the library). */
+#define SPEC_STATIC_SCRATCH_BYTES (4u << 20)
+
+/*
+ * spec_verify_greedy_static -- spec_verify_greedy without a workspace
+ * argument.  The pages have no counterpart: this entry point exists for
+ * callers that cannot allocate device memory when they call in, for example
+ * a serving loop that allows no allocation after start-up so that its memory
+ * use stays fixed, or a plugin whose host framework hands it only its input
+ * and output buffers and no scratch.  It allocates nothing (no cudaMalloc,
+ * no cudaFree, no allocating library call): its scratch is a file-scope
+ * device array of SPEC_STATIC_SCRATCH_BYTES in the library itself.
+ *
+ * Same arguments, results and definition as spec_verify_greedy.  Sizes whose
+ * scratch (spec_workspace_bytes(B, k, V)) exceeds SPEC_STATIC_SCRATCH_BYTES
+ * are rejected with SPEC_ESCRATCH before anything is launched.
+ *
+ * The first call on each device looks up the device address of the array
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  Every call also clears the array's counters
+ * with an asynchronous memset on the caller's stream.  All calls on a device
+ * share the one array and it keeps the last call's contents, so calls that
+ * overlap on the GPU (different streams without ordering) race: order them.
+ */
+SPEC_API int spec_verify_greedy_static(const void *target_logits, spec_dtype dt, int B, int k, int V,
+                              const int32_t *draft_tokens, const int32_t *draft_len, int32_t eos_id,
+                              const int32_t *remaining, int32_t *out_tokens, int32_t *n_accept,
+                              int32_t *n_emit, void *cuda_stream);
 
 #ifdef __cplusplus
 }

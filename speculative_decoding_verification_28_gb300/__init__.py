@@ -24,6 +24,8 @@ from .api import (  # noqa: F401
     spec_realign_kv,
     spec_rebuild_pos_mask,
     spec_verify_greedy,
+    spec_verify_greedy_static,
+    STATIC_SCRATCH_BYTES,
     spec_verify_sample,
     spec_workspace_bytes,
 )

@@ -25,6 +25,8 @@ SIGNATURES = {
                         _i32),
     "spec_rebuild_pos_mask": ([_i32, _i32, _vp, _vp, _vp, _vp, _vp], _i32),
     "spec_group_by_length": ([_i32, _vp, _vp, _i32, _vp, _vp, _vp, _vp], _i32),
+    "spec_verify_greedy_static": ([_vp, _i32, _i32, _i32, _i32, _vp, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp],
+                                  _i32),
 }
 
 _lib = None

@@ -116,6 +116,42 @@ def spec_verify_greedy(target_logits, draft_tokens, draft_len=None, eos_id=-1, r
     return out_tokens, n_accept, n_emit
 
 
+STATIC_SCRATCH_BYTES = 4 << 20
+
+
+def spec_verify_greedy_static(target_logits, draft_tokens, draft_len=None, eos_id=-1, remaining=None,
+                              out_tokens=None, n_accept=None, n_emit=None, stream=None):
+    """spec_verify_greedy for callers that cannot allocate device memory at
+    call time (a serving loop that forbids allocation after start-up, or a
+    plugin given only its input and output buffers): the scratch is a device
+    array built into the library (STATIC_SCRATCH_BYTES per device), so no
+    workspace is passed.  Pass preallocated outputs to allocate nothing here
+    either.  Calls on one device share that array: calls that overlap on the
+    GPU race, so order them.  The first call on a device looks up the array's
+    address; make it before any stream capture."""
+    lib = _lib.load()
+    B, k1, V = target_logits.shape
+    k = k1 - 1
+    dev = target_logits.device
+    _need(target_logits, None, "target_logits", dev)
+    if target_logits.dtype not in _DT:
+        raise ValueError(f"unsupported logits dtype {target_logits.dtype}")
+    _need(draft_tokens, torch.int32, "draft_tokens", dev, (B, k))
+    _need(draft_len, torch.int32, "draft_len", dev, (B,))
+    _need(remaining, torch.int32, "remaining", dev, (B,))
+    out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev) if out_tokens is None else out_tokens
+    n_accept = torch.empty(B, dtype=torch.int32, device=dev) if n_accept is None else n_accept
+    n_emit = torch.empty(B, dtype=torch.int32, device=dev) if n_emit is None else n_emit
+    for t, nm, shp in ((out_tokens, "out_tokens", (B, k + 1)), (n_accept, "n_accept", (B,)),
+                       (n_emit, "n_emit", (B,))):
+        _need(t, torch.int32, nm, dev, shp)
+    st = _stream(stream, dev)
+    _check(lib.spec_verify_greedy_static(_p(target_logits), _DT[target_logits.dtype], B, k, V, _p(draft_tokens),
+                                         _p(draft_len), int(eos_id), _p(remaining), _p(out_tokens), _p(n_accept),
+                                         _p(n_emit), st))
+    return out_tokens, n_accept, n_emit
+
+
 def spec_verify_sample(target_logits, draft_probs, draft_tokens, uniforms, temperature=1.0, draft_len=None,
                        eos_id=-1, remaining=None, out_tokens=None, n_accept=None, n_emit=None,
                        out_residual=None, flags=None, want_residual=False, workspace=None, stream=None):

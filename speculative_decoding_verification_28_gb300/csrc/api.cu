@@ -81,6 +81,8 @@ const char *spec_status_str(int status)
         return "a CUDA launch failed";
     case SPEC_EALIGN:
         return "a pointer lacks the alignment of its element type";
+    case SPEC_ESCRATCH:
+        return "sizes need more scratch than the library's built-in SPEC_STATIC_SCRATCH_BYTES";
     default:
         return "unknown status";
     }

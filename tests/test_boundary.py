@@ -140,3 +140,19 @@ def test_product_path_has_no_fallback():
             _lib.load()
     finally:
         _lib.LIB_PATH, _lib._lib = saved
+
+
+def test_static_entry_point_rejects_oversized_batches_before_any_launch(lib):
+    """The allocation-free variant has a fixed scratch: sizes beyond it are a
+    clear error (-6) found on the host."""
+    from speculative_decoding_verification_28_gb300 import STATIC_SCRATCH_BYTES
+
+    B, k, V = 4096, 31, 151936
+    assert lib.spec_workspace_bytes(B, k, V) > STATIC_SCRATCH_BYTES
+    rc = lib.spec_verify_greedy_static(FAKE, 1, B, k, V, FAKE, None, -1, None, FAKE, FAKE, FAKE, None)
+    assert rc == -6 and b"SPEC_STATIC_SCRATCH_BYTES" in lib.spec_status_str(-6)
+    assert lib.spec_verify_greedy_static(FAKE, 1, -1, k, V, FAKE, None, -1, None, FAKE, FAKE, FAKE, None) == -1
+    assert lib.spec_verify_greedy_static(FAKE, 9, 2, k, V, FAKE, None, -1, None, FAKE, FAKE, FAKE, None) == -2
+    assert lib.spec_verify_greedy_static(FAKE, 1, 0, k, V, FAKE, None, -1, None, FAKE, FAKE, FAKE, None) == 0
+    # the benchmark's largest workload fits
+    assert lib.spec_workspace_bytes(256, 8, 128256) <= STATIC_SCRATCH_BYTES
