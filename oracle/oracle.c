@@ -180,7 +180,8 @@ void oracle_verify_greedy(const void *logits, int dtype, int B, int k, int V,
 /* ------------------------------------------------------------------ */
 
 /* p = softmax(x / T) of one row in fp64: m = max z, p_v = e^(z_v - m) / sum.
-   Returns 1 when the row holds a non-finite logit or the sum is not finite. */
+   A -inf logit is a masked token with probability 0.  Returns 1 when the
+   distribution is undefined: a NaN or +inf logit, or no finite logit at all. */
 static int softmax_row(const void *x, int dtype, int64_t off, int V, double T, double *p)
 {
     int bad = 0;
@@ -188,7 +189,7 @@ static int softmax_row(const void *x, int dtype, int64_t off, int V, double T, d
     for (int v = 0; v < V; ++v) {
         double z = logit_at(x, dtype, off + v) / T;
         p[v] = z;
-        if (!isfinite(z))
+        if (isnan(z) || z == INFINITY)
             bad = 1;
         if (z > m)
             m = z;
@@ -247,8 +248,10 @@ static int inverse_cdf(const double *w, int V, double u)
  *   - EOS and the output budget stop the round as in greedy commitment.
  * Flags per sequence: 1 = a tested proposal had q(y) = 0 (the page says such a
  * symbol cannot be proposed; IEEE then gives +inf -> accept when p > 0, or
- * NaN -> reject when p = 0), 2 = zero residual mass, 4 = a non-finite logit in
- * a row that was used, 8 = a proposal outside [0, V) (rejected).
+ * NaN -> reject when p = 0), 2 = zero residual mass, 4 = a used row whose
+ * softmax is undefined (a NaN or +inf logit, or every logit -inf; a -inf
+ * logit alone is a masked token of probability 0), 8 = a proposal outside
+ * [0, V) (rejected).
  *
  * out_residual [B, V] (or NULL): the normalised distribution the final draw
  * came from (residual, or p on zero residual, or the bonus row's p); rows of

@@ -229,3 +229,23 @@ def test_out_of_vocabulary_proposal_is_rejected_and_flagged():
         assert fl[0] & 8 and na[0] == 0 and ne[0] == 1
         # drawn from the residual max(0, p - q) = [0, 0, 0.05, 0.15]
         assert np.allclose(res[0], [0, 0, 0.25, 0.75], atol=1e-6)
+
+
+def test_negative_infinity_is_a_masked_token():
+    """-inf logits (masked tokens, e.g. after top-k filtering) get probability
+    0 and do not make the distribution undefined; NaN, +inf or an all -inf
+    row do (flag 4)."""
+    V = 5
+    x = np.zeros((1, 2, V), np.float32)
+    x[0, :, 1] = -np.inf
+    x[0, :, 3] = -np.inf
+    q = np.full((1, 1, V), 0.2, np.float32)
+    out, na, ne, fl, res = oracle.verify_sample(x, DT_F32, q, np.array([[1]], np.int32),
+                                                np.array([[0.0, 0.5]], np.float32), want_residual=True)
+    assert fl[0] == 0 and na[0] == 0  # p(1) = 0: the masked proposal is rejected
+    assert res[0, 1] == 0 and res[0, 3] == 0 and out[0, 0] in (0, 2, 4)
+    p, bad = oracle.softmax_row(x[0], DT_F32, 0)
+    assert not bad and p[1] == 0 and np.isclose(p.sum(), 1.0)
+    x[0, 0, :] = -np.inf
+    _, bad = oracle.softmax_row(x[0], DT_F32, 0)
+    assert bad
