@@ -182,7 +182,7 @@ def kernel_source_digest():
     import hashlib
 
     h = hashlib.sha256()
-    for fn in ("realign.cu", "spec_common.cuh"):
+    for fn in ("realign.cu", "bulk_copy.cuh"):
         h.update(open(os.path.join(ROOT, "speculative_decoding_verification_28_gb300", "csrc", fn), "rb").read())
     return h.hexdigest()[:16]
 
@@ -267,8 +267,22 @@ class Round:
 
     def verify(self):
         if self.c["mode"] == "greedy":
-            return self.sv.spec_verify_greedy(self.x, self.d, workspace=self.ws)[2]
-        return self.sv.spec_verify_sample(self.x, self.q, self.d, self.u, workspace=self.ws)[2]
+            _, self.na, ne = self.sv.spec_verify_greedy(self.x, self.d, workspace=self.ws)
+        else:
+            _, self.na, ne, _, _ = self.sv.spec_verify_sample(self.x, self.q, self.d, self.u, workspace=self.ws)
+        return ne
+
+    def verify_alg_bytes(self, ne):
+        """Bytes verification must read: every row up to each sequence's first
+        stop (n_emit rows), plus the draft row of a residual draw."""
+        c = self.c
+        elt = 2 if c["logit_dtype"] == "bf16" else 4
+        n = ne.cpu().numpy().astype(np.int64)
+        b = int(n.sum()) * c["V"] * elt
+        if c["mode"] == "sample":
+            na = self.na.cpu().numpy()
+            b += int(((n == na + 1) & (na < c["k"])).sum()) * c["V"] * 4
+        return b
 
     def realign(self, ne):
         return self.sv.spec_realign_kv(self.kv, self.ln, self.pad, ne, workspace=self.ws)
@@ -302,7 +316,10 @@ def run_ours(args, c, rank, local_rank, world):
     st = torch.cuda.current_stream(dev)
     R = Round(c, rank_seed(args.seed, rank), dev)
 
-    def one_step(timed):
+    def one_step(timed, breakdown=False):
+        """One round; returns [step, verify, realign + pos/mask] device ms (or,
+        with breakdown, [verify, realign, pos/mask] with an event between
+        every call, which keeps pos/mask from overlapping the shift)."""
         R.prepare()
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         # untimed gate: the GPU spins ~0.5 ms while the host enqueues the
@@ -312,17 +329,22 @@ def run_ours(args, c, rank, local_rank, world):
         ne = R.verify()
         ev[1].record(st)
         ln_new, pad_new, width, err = R.realign(ne)
-        ev[2].record(st)
+        if breakdown:
+            ev[2].record(st)
         R.posmask(pad_new)
         ev[3].record(st)
         torch.cuda.synchronize(dev)
         assert int(err.item()) == 0, "realign error"
+        vbytes = R.verify_alg_bytes(ne)
         moved, emitted, _ = R.advance(ne, ln_new, pad_new, width)
-        times = [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
+        if breakdown:
+            times = [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
+        else:
+            times = [ev[0].elapsed_time(ev[3]), ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[3])]
         if dump is not None:
             dump.write(json.dumps({"timed": timed, "realign_alg_bytes": moved * R.row_bytes_all_slabs() * 2,
-                                   "emitted": emitted, "call_ms": times}) + "\n")
-        return times, moved, emitted
+                                   "verify_alg_bytes": vbytes, "emitted": emitted, "call_ms": times}) + "\n")
+        return times, moved, emitted, vbytes
 
     dump = open(args.dump_steps, "w") if args.dump_steps else None
 
@@ -333,31 +355,39 @@ def run_ours(args, c, rank, local_rank, world):
     torch.cuda.synchronize(dev)
     per = []
     moved_rows = []
+    verify_bytes = []
     emitted = 0
     with ClockSampler(local_rank) as clk:
         for _ in range(args.steps):
-            t, m, e = one_step(True)
+            t, m, e, vb = one_step(True)
             per.append(t)
             moved_rows.append(m)
+            verify_bytes.append(vb)
             emitted += e
     torch.cuda.synchronize(dev)
     if pg:
         dist.barrier()
-    per = np.array(per)  # ms [steps, 3]
-    total_s = per.sum() / 1e3
+    per = np.array(per)  # ms [steps, 3]: step, verify, realign + pos/mask
+    total_s = per[:, 0].sum() / 1e3
     total_s = max_over_ranks(total_s, pg, dev)
     value = aggregate(args.steps, total_s, world)
+    # untimed breakdown steps: an event between every call
+    brk_steps = [one_step(False, breakdown=True) for _ in range(min(10, max(3, args.steps // 5)))]
+    brk = np.array([b[0] for b in brk_steps])
+    brk_bytes = np.array([b[1] for b in brk_steps], dtype=np.float64) * R.row_bytes_all_slabs() * 2
 
-    # roofline of the dominant kernel: the KV shift (timed together with its
-    # one-CTA plan kernel, so the achieved figure is a lower bound)
+    # roofline of the dominant kernel: the KV shift, timed over the realign
+    # call and the position/mask rebuild that may overlap it (plan kernel and
+    # rebuild included, so the achieved figure is a lower bound)
     row_all = R.row_bytes_all_slabs()
     alg_bytes = np.array(moved_rows, dtype=np.float64) * row_all * 2  # read + write
-    realign_ms = per[:, 1]
+    realign_ms = per[:, 2]
     mean_alg = float(alg_bytes.mean())
     achieved = float(alg_bytes.sum() / (realign_ms.sum() / 1e3) / 1e9)
     peak, peak_src = hbm_peak()
     ratio = ncu_traffic_ratio(args.workload)
-    roofline = {"bound": "hbm", "kernel": "kv_shift_bulk_kernel (+ realign_plan_kernel in the same timing)",
+    roofline = {"bound": "hbm",
+                "kernel": "kv_shift_bulk_kernel (timed with realign_plan_kernel and pos_mask_kernel: lower bound)",
                 "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
                 "traffic": None if ratio is None else round(ratio * mean_alg),
@@ -365,7 +395,7 @@ def run_ours(args, c, rank, local_rank, world):
 
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "rounds/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(float(per.sum(1).mean()), 4), "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": round(float(per[:, 0].mean()), 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": c["logit_dtype"] if c["mode"] == "greedy" else "f32 arithmetic on " + c["logit_dtype"] + " logits",
         "data": "synthetic (seeded; stands in for SpecBench/Multi30k-shaped rounds)",
@@ -375,9 +405,18 @@ def run_ours(args, c, rank, local_rank, world):
                    "the harness target forward runs between steps",
                    "parallelism": f"independent batch per GPU x{world}"},
         "roofline": roofline,
-        "per_call_us": {"verify": round(float(per[:, 0].mean()) * 1e3, 2),
-                        "realign": round(float(per[:, 1].mean()) * 1e3, 2),
-                        "pos_mask": round(float(per[:, 2].mean()) * 1e3, 2)},
+        "verify_roofline": {"bound": "hbm", "kernels": ("verify_greedy_kernel" if c["mode"] == "greedy" else
+                                                        "verify_stats_kernel + verify_draw_kernel"),
+                            "achieved": round(float(np.sum(verify_bytes) / (per[:, 1].sum() / 1e3) / 1e9), 1),
+                            "peak": peak, "unit": "GB/s",
+                            "frac": round(float(np.sum(verify_bytes) / (per[:, 1].sum() / 1e3) / 1e9) / peak, 4),
+                            "algorithmic_bytes_per_launch": round(float(np.mean(verify_bytes)))},
+        "per_call_us": {"verify": round(float(per[:, 1].mean()) * 1e3, 2),
+                        "realign_and_pos_mask": round(float(per[:, 2].mean()) * 1e3, 2),
+                        "breakdown_steps": {"verify": round(float(brk[:, 0].mean()) * 1e3, 2),
+                                            "realign_alone_gbs": round(float(brk_bytes.sum() / (brk[:, 1].sum() / 1e3)
+                                                                             / 1e9), 1),
+                                            "pos_mask": round(float(brk[:, 2].mean()) * 1e3, 2)}},
         "tokens_per_round": round(emitted / args.steps / c["B"], 4),
         "gpu_launches": args.steps * (4 if c["mode"] == "greedy" else 5),
         "clocks": clk.summary(),
@@ -394,32 +433,50 @@ def run_ours(args, c, rank, local_rank, world):
 def run_e2e(args, R, st, dev, pg, world):
     """Same rounds through the public API with HOST inputs and outputs: the
     timed region of every step includes the pinned host->device copy of the
-    round's logits and proposals and the device->host copy of its results."""
+    round's logits and proposals, the library calls, and one device->host
+    copy of the round's results (committed tokens, counts, new lengths and
+    paddings, width, error word), which the calls write into one block."""
     import torch
 
     c = R.c
+    B, k = c["B"], c["k"]
     steps = max(1, args.steps)
     hx = torch.empty(tuple(R.x.shape), dtype=R.x.dtype).pin_memory()
     hd = torch.empty(tuple(R.d.shape), dtype=torch.int32).pin_memory()
     extra = []
     if c["mode"] == "sample":
-        hq = torch.empty(tuple(R.q.shape), dtype=torch.float32).pin_memory()
-        hu = torch.empty(tuple(R.u.shape), dtype=torch.float32).pin_memory()
-        extra = [hq, hu]
-    B = c["B"]
-    h_out = torch.empty((B, c["k"] + 1), dtype=torch.int32).pin_memory()
-    h_small = torch.empty((4, B), dtype=torch.int32).pin_memory()
-    h_w = torch.empty(2, dtype=torch.int32).pin_memory()
+        extra = [torch.empty(tuple(R.q.shape), dtype=torch.float32).pin_memory(),
+                 torch.empty(tuple(R.u.shape), dtype=torch.float32).pin_memory()]
+    n_out = B * (k + 1) + 4 * B + 2
+    blocks = [torch.empty(n_out, dtype=torch.int32, device=dev) for _ in range(2)]
+    h_res = torch.empty(n_out, dtype=torch.int32).pin_memory()
+
+    def views(blk):
+        o = 0
+        out = blk[o:o + B * (k + 1)].view(B, k + 1)
+        o += B * (k + 1)
+        na, ne, ln, pad = (blk[o + i * B:o + (i + 1) * B] for i in range(4))
+        o += 4 * B
+        return out, na, ne, ln, pad, blk[o:o + 1], blk[o + 1:o + 2]
+
+    views(blocks[0])[3].copy_(R.ln)
+    views(blocks[0])[4].copy_(R.pad)
+    cur = 0
     total = 0.0
-    h2d = d2h = 0
     for _ in range(steps):
+        R.ln, R.pad = views(blocks[cur])[3], views(blocks[cur])[4]
         R.prepare()
+        if views(blocks[cur])[3].data_ptr() != R.ln.data_ptr():  # prepare() reset the state
+            views(blocks[cur])[3].copy_(R.ln)
+            views(blocks[cur])[4].copy_(R.pad)
+            R.ln, R.pad = views(blocks[cur])[3], views(blocks[cur])[4]
         hx.copy_(R.x)
         hd.copy_(R.d)
         if extra:
             extra[0].copy_(R.q)
             extra[1].copy_(R.u)
         torch.cuda.synchronize(dev)
+        out, na, ne, ln_new, pad_new, width, err = views(blocks[1 - cur])
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(st)
         R.x.copy_(hx, non_blocking=True)
@@ -428,28 +485,24 @@ def run_e2e(args, R, st, dev, pg, world):
             R.q.copy_(extra[0], non_blocking=True)
             R.u.copy_(extra[1], non_blocking=True)
         if c["mode"] == "greedy":
-            out, na, ne = R.sv.spec_verify_greedy(R.x, R.d, workspace=R.ws)
+            R.sv.spec_verify_greedy(R.x, R.d, out_tokens=out, n_accept=na, n_emit=ne, workspace=R.ws)
         else:
-            out, na, ne, _, _ = R.sv.spec_verify_sample(R.x, R.q, R.d, R.u, workspace=R.ws)
-        ln_new, pad_new, width, err = R.realign(ne)
-        R.posmask(pad_new)
-        h_out.copy_(out, non_blocking=True)
-        h_small[0].copy_(na, non_blocking=True)
-        h_small[1].copy_(ne, non_blocking=True)
-        h_small[2].copy_(ln_new, non_blocking=True)
-        h_small[3].copy_(pad_new, non_blocking=True)
-        h_w[0].copy_(width[0], non_blocking=True)
-        h_w[1].copy_(err[0], non_blocking=True)
+            R.sv.spec_verify_sample(R.x, R.q, R.d, R.u, out_tokens=out, n_accept=na, n_emit=ne, workspace=R.ws)
+        R.sv.spec_realign_kv(R.kv, R.ln, R.pad, ne, len_new=ln_new, pad_new=pad_new, width_new=width, err=err,
+                             workspace=R.ws)
+        R.sv.spec_rebuild_pos_mask(pad_new, R.pos, R.mask, pad_old=R.pad)
+        h_res.copy_(blocks[1 - cur], non_blocking=True)
         e1.record(st)
         torch.cuda.synchronize(dev)
         total += e0.elapsed_time(e1) / 1e3
-        assert int(h_w[1]) == 0
-        R.advance(ne, ln_new, pad_new, width)
-        h2d = hx.numel() * hx.element_size() + hd.numel() * 4 + sum(t.numel() * 4 for t in extra)
-        d2h = h_out.numel() * 4 + h_small.numel() * 4 + h_w.numel() * 4
+        assert int(h_res[-1]) == 0
+        R.W = int(h_res[-2])
+        cur = 1 - cur
+    R.ln, R.pad = views(blocks[cur])[3].clone(), views(blocks[cur])[4].clone()
     total = max_over_ranks(total, pg, dev)
+    h2d = hx.numel() * hx.element_size() + hd.numel() * 4 + sum(t.numel() * 4 for t in extra)
     return {"value": round(aggregate(steps, total, world), 3), "unit": "rounds/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps}
+            "d2h_bytes_per_step": n_out * 4, "steps": steps}
 
 
 # ---------------------------------------------------------------------------

@@ -35,7 +35,7 @@ int check_verify_common(const void *logits, int dt, int B, int k, int V, const i
         return SPEC_OK;
     if (!logits || (k > 0 && !draft) || !out_tokens || !n_accept || !n_emit)
         return SPEC_EINVAL;
-    const long long units = (long long)B * (k + 1) * verify_chunks(V);
+    const long long units = (long long)B * (k + 1) * verify_chunks(B, k, V);
     if (units > INT_MAX)
         return SPEC_EINVAL;
     if (!aligned(logits, dtype_bytes(dt)) || !aligned(out_tokens, 4) || !aligned(n_accept, 4) ||
@@ -104,7 +104,6 @@ int spec_verify_greedy(const void *target_logits, spec_dtype dt, int B, int k, i
     a.B = B;
     a.k = k;
     a.V = V;
-    a.C = verify_chunks(V);
     a.draft = draft_tokens;
     a.draft_len = draft_len;
     a.eos = eos_id;
@@ -138,7 +137,6 @@ int spec_verify_sample(const void *target_logits, spec_dtype dt, float temperatu
     a.B = B;
     a.k = k;
     a.V = V;
-    a.C = verify_chunks(V);
     a.draft = draft_tokens;
     a.draft_len = draft_len;
     a.eos = eos_id;

@@ -54,9 +54,22 @@ cudaError_t launch_pos_mask(int B, int S, const int32_t *pad_old, const int32_t 
     const bool vec = (S % kPmSlots == 0) && (reinterpret_cast<uintptr_t>(pos) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(mask) % 8 == 0);
     const int per_block = vec ? kPmThreads * kPmSlots : kPmThreads * 4;
-    dim3 grid((unsigned)((S + per_block - 1) / per_block), (unsigned)B);
-    pos_mask_kernel<<<grid, kPmThreads, 0, st>>>(B, S, pad_old, pad_new, pos, mask, vec ? 1 : 0);
-    return cudaGetLastError();
+    // Launched programmatically: it may start while the previous kernel on
+    // the stream finishes, once that kernel allows it.  The library's KV shift
+    // allows it only after the plan that wrote pad_new is complete, and it
+    // never touches pos or mask; a kernel that does not release dependents
+    // early (any other kernel) completes first, as in an ordinary launch.
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((S + per_block - 1) / per_block), (unsigned)B);
+    cfg.blockDim = dim3(kPmThreads);
+    cfg.stream = st;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, pos_mask_kernel, B, S, pad_old, pad_new, pos, mask, vec ? 1 : 0);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace spec

@@ -19,6 +19,7 @@
 //       stores are issued strictly in tile order after each tile's load has
 //       completed on its mbarrier.
 // Roofline: HBM-bound, 2 * run * D * elt bytes per moving slab.
+#include "bulk_copy.cuh"
 #include "spec_common.cuh"
 #include "spec_launch.h"
 
@@ -42,8 +43,11 @@ __global__ void __launch_bounds__(kPlanThreads) realign_plan_kernel(RealignArgs 
 {
     __shared__ uint64_t s_key[kSortMax];
     __shared__ int s_bad2, s_bad3, s_minpad, s_maxlen, s_count, s_rows;
+    // the shift kernel may be scheduled now; it waits for this grid's results
+    dep_release();
     const PlanView pv = plan_view(a.ws, a.B);
     const int t = threadIdx.x;
+    const int nt = blockDim.x;
     if (t == 0) {
         s_bad2 = 0;
         s_bad3 = 0;
@@ -55,7 +59,7 @@ __global__ void __launch_bounds__(kPlanThreads) realign_plan_kernel(RealignArgs 
     __syncthreads();
     const int W = a.pad[0] + a.len[0];
     int bad2 = 0, bad3 = 0, minpad = 0x7FFFFFFF, maxlen = 0;
-    for (int b = t; b < a.B; b += kPlanThreads) {
+    for (int b = t; b < a.B; b += nt) {
         const int l = a.len[b], p = a.pad[b], n = a.n_emit[b];
         if (l < 1 || p < 0 || p + l != W)
             bad2 = 1;
@@ -91,7 +95,7 @@ __global__ void __launch_bounds__(kPlanThreads) realign_plan_kernel(RealignArgs 
     // per-sequence shift; inputs are read before any output is written
     // (len_new / pad_new may alias len / pad)
     int rows = 0;
-    for (int b = t; b < a.B; b += kPlanThreads) {
+    for (int b = t; b < a.B; b += nt) {
         const int l = a.len[b], p = a.pad[b], n = a.n_emit[b];
         const int ln = l + n, pn = Wn - ln;
         const int d = pn - p;
@@ -103,7 +107,7 @@ __global__ void __launch_bounds__(kPlanThreads) realign_plan_kernel(RealignArgs 
     }
     atomicAdd(&s_rows, rows);
     __syncthreads();
-    for (int b = t; b < a.B; b += kPlanThreads) {
+    for (int b = t; b < a.B; b += nt) {
         const int pn = pv.src_pad[b] + pv.delta[b];
         a.pad_new[b] = pn;
         a.len_new[b] = Wn - pn;
@@ -113,7 +117,7 @@ __global__ void __launch_bounds__(kPlanThreads) realign_plan_kernel(RealignArgs 
         int P = 1;
         while (P < a.B)
             P <<= 1;
-        for (int i = t; i < P; i += kPlanThreads) {
+        for (int i = t; i < P; i += nt) {
             uint64_t key = 0;
             if (i < a.B && pv.run[i] > 0)
                 key = ((uint64_t)pv.run[i] << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)i);
@@ -122,7 +126,7 @@ __global__ void __launch_bounds__(kPlanThreads) realign_plan_kernel(RealignArgs 
         __syncthreads();
         for (int size = 2; size <= P; size <<= 1) {
             for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                for (int i = t; i < P; i += kPlanThreads) {
+                for (int i = t; i < P; i += nt) {
                     const int jx = i ^ stride;
                     if (jx > i) {
                         const bool desc = (i & size) == 0;
@@ -136,7 +140,7 @@ __global__ void __launch_bounds__(kPlanThreads) realign_plan_kernel(RealignArgs 
                 __syncthreads();
             }
         }
-        for (int i = t; i < a.B; i += kPlanThreads) {
+        for (int i = t; i < a.B; i += nt) {
             const uint64_t key = s_key[i];
             if (key != 0) {
                 pv.order[i] = (int)(0xFFFFFFFFu - (uint32_t)key);
@@ -214,6 +218,8 @@ __global__ void __launch_bounds__(32) kv_shift_bulk_kernel(RealignArgs a)
     __shared__ __align__(8) uint64_t full[kStages];
     if (threadIdx.x != 0)
         return;
+    dep_wait();     // the plan kernel's results are complete and visible
+    dep_release();  // a following position/mask rebuild may run alongside
     const PlanView pv = plan_view(a.ws, a.B);
     const int n_moving = pv.misc[MISC_NMOVING];
     if (n_moving <= 0)
@@ -312,6 +318,8 @@ __global__ void __launch_bounds__(32) kv_shift_bulk_kernel(RealignArgs a)
 template <typename E>
 __global__ void __launch_bounds__(256) kv_shift_plain_kernel(RealignArgs a)
 {
+    dep_wait();
+    dep_release();
     const PlanView pv = plan_view(a.ws, a.B);
     const int n_moving = pv.misc[MISC_NMOVING];
     const int sps = a.L * 2 * a.H;
@@ -364,10 +372,21 @@ cudaError_t launch_realign(const RealignArgs &a, cudaStream_t st)
         if (e != cudaSuccess)
             return e;
     }
-    realign_plan_kernel<<<1, kPlanThreads, 0, st>>>(a);
+    int plan_threads = ((a.B + 31) / 32) * 32;
+    plan_threads = plan_threads < 32 ? 32 : (plan_threads > kPlanThreads ? kPlanThreads : plan_threads);
+    realign_plan_kernel<<<1, plan_threads, 0, st>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
+    // the shift is launched programmatically: it becomes resident while the
+    // plan runs and waits for it on the device
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = st;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
     const long long row_bytes = (long long)a.D * a.elt_bytes;
     const bool bulk = (row_bytes % 16 == 0) && (reinterpret_cast<uintptr_t>(a.kv) % 16 == 0);
     if (bulk) {
@@ -378,15 +397,21 @@ cudaError_t launch_realign(const RealignArgs &a, cudaStream_t st)
                 return e;
             g_smem_set[slot] = true;
         }
-        kv_shift_bulk_kernel<<<g_sm_count[slot], 32, kShiftSmem, st>>>(a);
+        cfg.gridDim = dim3(g_sm_count[slot]);
+        cfg.blockDim = dim3(32);
+        cfg.dynamicSmemBytes = kShiftSmem;
+        e = cudaLaunchKernelEx(&cfg, kv_shift_bulk_kernel, a);
     } else {
         const long long blocks = (long long)a.B * a.L * 2 * a.H;
+        cfg.gridDim = dim3((unsigned)blocks);
+        cfg.blockDim = dim3(256);
+        cfg.dynamicSmemBytes = 0;
         if (a.elt_bytes == 4)
-            kv_shift_plain_kernel<uint32_t><<<(unsigned)blocks, 256, 0, st>>>(a);
+            e = cudaLaunchKernelEx(&cfg, kv_shift_plain_kernel<uint32_t>, a);
         else
-            kv_shift_plain_kernel<uint16_t><<<(unsigned)blocks, 256, 0, st>>>(a);
+            e = cudaLaunchKernelEx(&cfg, kv_shift_plain_kernel<uint16_t>, a);
     }
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace spec

@@ -16,11 +16,42 @@ namespace spec {
 // sizes
 // ---------------------------------------------------------------------------
 constexpr int kThreads = 256;          // threads of the row-streaming kernels
-constexpr int kChunk = 8192;           // vocabulary elements per CTA work unit
+constexpr int kMinChunk = 4096;        // smallest vocabulary chunk of a verify work unit
+#ifndef SPEC_TARGET_UNITS
+#define SPEC_TARGET_UNITS 2432
+#endif
+constexpr int kTargetUnits = SPEC_TARGET_UNITS;  // ~two waves of 8 CTAs on 152 SMs
+constexpr int kDrawChunk = 8192;       // elements per CTA in the draw kernel (its scan stages one in smem)
 constexpr int kMaxRows = SPEC_MAX_K + 1;
 constexpr int kStopBase = 1024;        // stop row j is stored as kStopBase - j
 
-__host__ __device__ inline int verify_chunks(int V) { return (V + kChunk - 1) / kChunk; }
+// Split of each logits row into work units: enough units for about two waves
+// over the whole batch, each at least kMinChunk elements, lengths a multiple of
+// 64 elements (16-byte aligned starts whenever the row start is).
+struct Split {
+    int C;    // chunks per row
+    int len;  // elements per chunk (the last one may be shorter)
+};
+__host__ __device__ inline Split verify_split(int B, int k, int V)
+{
+    const long long rows = (long long)(B > 0 ? B : 1) * (k + 1);
+    long long c = (kTargetUnits + rows - 1) / rows;
+    long long cmax = V / kMinChunk;
+    if (cmax < 1)
+        cmax = 1;
+    if (c > cmax)
+        c = cmax;
+    if (c < 1)
+        c = 1;
+    int len = (int)((V + c - 1) / c);
+    len = (len + 63) & ~63;
+    Split sp;
+    sp.len = len;
+    sp.C = (V + len - 1) / len;
+    return sp;
+}
+__host__ __device__ inline int verify_chunks(int B, int k, int V) { return verify_split(B, k, V).C; }
+__host__ __device__ inline int draw_chunks(int V) { return (V + kDrawChunk - 1) / kDrawChunk; }
 
 // ---------------------------------------------------------------------------
 // workspace layout (byte offsets; every array 256-byte aligned)
@@ -51,7 +82,7 @@ __host__ __device__ inline Layout make_layout(int B, int k, int V)
     };
     const size_t b = (size_t)(B > 0 ? B : 0);
     const size_t rows = b * (size_t)(k + 1);
-    const size_t C = (size_t)verify_chunks(V > 0 ? V : 1);
+    const size_t C = (size_t)verify_chunks(B, k, V > 0 ? V : 1);
     L.order = take(b * 4);
     L.delta = take(b * 4);
     L.src_pad = take(b * 4);
@@ -68,7 +99,7 @@ __host__ __device__ inline Layout make_layout(int B, int k, int V)
     L.row_flag = take(rows * 4);
     L.part = take(rows * C * 16);
     L.draw_row = take(b * 4);
-    L.rpart = take(b * C * 8);
+    L.rpart = take(b * (size_t)draw_chunks(V > 0 ? V : 1) * 8);
     L.rtot = take(b * 8);
     L.total = o;
     return L;
@@ -175,71 +206,5 @@ __device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m)
     hi = __shfl_xor_sync(0xFFFFFFFFu, hi, m);
     return ((uint64_t)hi << 32) | lo;
 }
-
-// ---------------------------------------------------------------------------
-// mbarrier + 1-D bulk copy (cp.async.bulk) wrappers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_addr(const void *p)
-{
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void fence_mbar_init()
-{
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-                 : "memory");
-}
-
-// one bounded probe of the barrier phase; true once phase `parity` completed
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// global -> shared bulk copy completing on an mbarrier
-__device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(dst_smem)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
-}
-
-// shared -> global bulk copy tracked by bulk async-groups
-__device__ __forceinline__ void bulk_s2g(void *dst, const void *src_smem, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-                 "r"(smem_addr(src_smem)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-template <int N>
-__device__ __forceinline__ void bulk_wait_read()
-{
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 }  // namespace spec

@@ -12,6 +12,7 @@ namespace spec {
 struct VerifyArgs {
     const void *logits;
     int B, k, V, C;
+    int chunk;  // elements per work unit (set by the launcher)
     const int32_t *draft;
     const int32_t *draft_len;
     int32_t eos;
@@ -20,6 +21,13 @@ struct VerifyArgs {
     int32_t *n_accept;
     int32_t *n_emit;
     void *ws;
+    // workspace arrays, resolved on the host by the launcher from ws
+    int *stop_enc, *row_cnt, *seq_cnt, *res_cnt, *row_tok, *draw_row;
+    float2 *row_ms;
+    uint32_t *row_flag;
+    void *part;
+    float *rpart;
+    double *rtot;
     // stochastic verification only
     float inv_temp;
     int unit_temp;
@@ -29,6 +37,8 @@ struct VerifyArgs {
     uint32_t *flags;
 };
 
+// fills C, chunk and the workspace pointers of `a` from B, k, V and ws
+void resolve_verify_args(VerifyArgs &a);
 cudaError_t launch_verify_greedy(const VerifyArgs &a, spec_dtype dt, cudaStream_t st);
 cudaError_t launch_verify_sample(const VerifyArgs &a, spec_dtype dt, cudaStream_t st);
 

@@ -36,8 +36,8 @@ __device__ __forceinline__ Unit decode_unit(const VerifyArgs &a)
 {
     Unit u;
     const int bid = blockIdx.x;
-    u.c = bid % a.C;
     const int jb = bid / a.C;
+    u.c = bid - jb * a.C;
     u.b = jb % a.B;
     u.j = jb / a.B;
     u.row = u.b * (a.k + 1) + u.j;
@@ -54,6 +54,81 @@ __device__ __forceinline__ bool stopped_before(const int *stop_enc, int b, int j
     const int enc = ld_relaxed(stop_enc + b);
     return enc > 0 && (kStopBase - enc) < j;
 }
+
+// 2^x by the SFU instruction ex2.approx.ftz.f32 (relative error about
+// 2^-22; results below 2^-126 flush to zero, negligible in a softmax sum).
+// e^x is computed as 2^(x log2 e) with the scale folded into one FFMA.
+__device__ __forceinline__ float exp2_sfu(float x)
+{
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// Maxima that propagate NaN (PTX max.NaN): a vector's maximum is NaN when
+// any element is NaN, so one comparison per 16-byte vector finds both a new
+// largest value and a NaN.
+__device__ __forceinline__ float max_nan(float a, float b)
+{
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t max_nan_f16x2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.NaN.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// maximum (NaN-propagating) of the elements of one 16-byte vector, as fp32
+template <typename T>
+__device__ __forceinline__ float vec_max(const uint4 &u);
+template <>
+__device__ __forceinline__ float vec_max<float>(const uint4 &u)
+{
+    return max_nan(max_nan(__uint_as_float(u.x), __uint_as_float(u.y)),
+                   max_nan(__uint_as_float(u.z), __uint_as_float(u.w)));
+}
+template <>
+__device__ __forceinline__ float vec_max<__nv_bfloat16>(const uint4 &u)
+{
+    const uint32_t m = max_nan_bf16x2(max_nan_bf16x2(u.x, u.y), max_nan_bf16x2(u.z, u.w));
+    return max_nan(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+}
+template <>
+__device__ __forceinline__ float vec_max<__half>(const uint4 &u)
+{
+    const uint32_t m = max_nan_f16x2(max_nan_f16x2(u.x, u.y), max_nan_f16x2(u.z, u.w));
+    __half2 h;
+    memcpy(&h, &m, 4);
+    const float2 f = __half22float2(h);
+    return max_nan(f.x, f.y);
+}
+
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e): e^x = 2^(x log2 e)
+
+// Per-warp re-check, between load batches, that the unit's row is still
+// needed: once a stop before row j is recorded for the sequence, the row will
+// never be evaluated (the record only moves earlier), so the warp can drop
+// the rest of its chunk.  Lane 0 reads the word; the decision is warp-uniform.
+struct StopProbe {
+    const int *stop_enc;
+    int b, j;
+    __device__ __forceinline__ bool dropped() const
+    {
+        int s = 0;
+        if ((threadIdx.x & 31) == 0)
+            s = stopped_before(stop_enc, b, j) ? 1 : 0;
+        return __shfl_sync(0xFFFFFFFFu, s, 0) != 0;
+    }
+};
 
 // Block-wide max of a u64 key (all threads get the result).
 __device__ __forceinline__ uint64_t block_max_u64(uint64_t key, uint64_t *s_red)

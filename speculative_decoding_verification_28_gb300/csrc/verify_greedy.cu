@@ -14,12 +14,16 @@
 
 namespace spec {
 
-// Argmax key of chunk [lo, hi) of one row: fast float compare per element,
-// exact key recomputation for the (rare) chunk that holds a NaN.
+// Argmax key of chunk [lo, hi) of one row.  Per 16-byte vector: its
+// NaN-propagating maximum (3 packed max instructions for 8 bf16 values); the
+// elements are looked at one by one only when that maximum beats the running
+// best, which happens O(log n) times per thread.  A chunk holding a NaN is
+// recomputed exactly (NaN counts as larger than every number; first NaN wins).
 template <typename T>
-__device__ uint64_t chunk_argmax(const T *row, int lo, int hi, uint64_t *s_red)
+__device__ uint64_t chunk_argmax(const T *row, int lo, int hi, uint64_t *s_red, const StopProbe &probe)
 {
     constexpr int VEC = Storage<T>::kVec;
+    constexpr int UNROLL = 4;
     const ChunkSplit<T> cs(row, lo, hi);
     float best = -INFINITY;
     uint32_t bidx = 0xFFFFFFFFu;
@@ -28,9 +32,10 @@ __device__ uint64_t chunk_argmax(const T *row, int lo, int hi, uint64_t *s_red)
 
     auto see = [&](float x, uint32_t i) {
         first = first == 0xFFFFFFFFu ? i : first;
-        const bool gt = x > best;
-        best = gt ? x : best;
-        bidx = gt ? i : bidx;
+        if (x > best) {
+            best = x;
+            bidx = i;
+        }
         nan |= (x != x);
     };
 
@@ -38,24 +43,35 @@ __device__ uint64_t chunk_argmax(const T *row, int lo, int hi, uint64_t *s_red)
     if (lo + t < cs.head_end)
         see(Storage<T>::at(row, lo + t), lo + t);
     const T *body = row + cs.head_end;
-    for (int i = t; i < cs.nvec; i += 4 * kThreads) {
-        uint4 r[4];
+    if (t < cs.nvec)
+        first = first == 0xFFFFFFFFu ? (uint32_t)(cs.head_end + t * VEC) : first;
+    for (int base = 0; base < cs.nvec; base += UNROLL * kThreads) {  // warp-uniform trip count
+        if (base > 0 && probe.dropped())
+            break;
+        const int i = base + t;
+        uint4 r[UNROLL];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < UNROLL; ++u) {
             const int vi = i + u * kThreads;
             if (vi < cs.nvec)
                 r[u] = ld_stream16(body + (size_t)vi * VEC);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < UNROLL; ++u) {
             const int vi = i + u * kThreads;
             if (vi < cs.nvec) {
-                float f[VEC];
-                Storage<T>::unpack(r[u], f);
-                const uint32_t i0 = (uint32_t)(cs.head_end + vi * VEC);
+                const float vm = vec_max<T>(r[u]);
+                nan |= (vm != vm);
+                if (vm > best) {  // a new maximum: its first position in the vector
+                    float f[VEC];
+                    Storage<T>::unpack(r[u], f);
+                    int e = 0;
 #pragma unroll
-                for (int e = 0; e < VEC; ++e)
-                    see(f[e], i0 + e);
+                    for (int q = VEC - 1; q >= 0; --q)
+                        e = (f[q] == vm) ? q : e;
+                    best = vm;
+                    bidx = (uint32_t)(cs.head_end + vi * VEC + e);
+                }
             }
         }
     }
@@ -66,7 +82,6 @@ __device__ uint64_t chunk_argmax(const T *row, int lo, int hi, uint64_t *s_red)
     if (first != 0xFFFFFFFFu)
         key = bidx != 0xFFFFFFFFu ? argmax_key(best, bidx) : argmax_key(-INFINITY, first);
     if (__syncthreads_or(nan)) {
-        // exact path: NaN counts as larger than every number, first NaN wins
         key = 0;
         for (int i = lo + t; i < hi; i += kThreads) {
             const uint64_t kk = argmax_key(Storage<T>::at(row, i), (uint32_t)i);
@@ -81,12 +96,8 @@ __global__ void __launch_bounds__(kThreads) verify_greedy_kernel(VerifyArgs a)
 {
     __shared__ uint64_t s_red[kThreads / 32];
     __shared__ int s_flag;
-    const Layout lay = make_layout(a.B, a.k, a.V);
-    int *stop_enc = ws_at<int>(a.ws, lay.stop_enc);
-    int *row_cnt = ws_at<int>(a.ws, lay.row_cnt);
-    int *seq_cnt = ws_at<int>(a.ws, lay.seq_cnt);
-    int *row_tok = ws_at<int>(a.ws, lay.row_tok);
-    uint64_t *part = ws_at<uint64_t>(a.ws, lay.part);
+    int *stop_enc = a.stop_enc, *row_cnt = a.row_cnt, *seq_cnt = a.seq_cnt, *row_tok = a.row_tok;
+    uint64_t *part = static_cast<uint64_t *>(a.part);
 
     const Unit u = decode_unit(a);
     if (threadIdx.x == 0)
@@ -94,16 +105,20 @@ __global__ void __launch_bounds__(kThreads) verify_greedy_kernel(VerifyArgs a)
     __syncthreads();
     if (!s_flag) {
         const T *row = reinterpret_cast<const T *>(a.logits) + (size_t)u.row * a.V;
-        const int lo = u.c * kChunk;
-        const int hi = min(a.V, lo + kChunk);
-        const uint64_t key = chunk_argmax<T>(row, lo, hi, s_red);
+        const int lo = u.c * a.chunk;
+        const int hi = min(a.V, lo + a.chunk);
+        const uint64_t key = chunk_argmax<T>(row, lo, hi, s_red, StopProbe{stop_enc, u.b, u.j});
         if (threadIdx.x == 0)
             part[((size_t)u.row * a.C + u.c) * 2] = key;
     }
     // arrival on the row counter; the last CTA of the row finalises it
     if (threadIdx.x == 0) {
-        __threadfence();
-        s_flag = (atomicAdd(row_cnt + u.row, 1) == a.C - 1) ? 1 : 0;
+        if (a.C > 1) {
+            __threadfence();
+            s_flag = (atomicAdd(row_cnt + u.row, 1) == a.C - 1) ? 1 : 0;
+        } else {
+            s_flag = 1;  // a single-chunk row is finalised by its only CTA
+        }
     }
     __syncthreads();
     if (!s_flag || threadIdx.x >= 32)
@@ -178,8 +193,29 @@ __global__ void __launch_bounds__(kThreads) verify_greedy_kernel(VerifyArgs a)
     }
 }
 
-cudaError_t launch_verify_greedy(const VerifyArgs &a, spec_dtype dt, cudaStream_t st)
+void resolve_verify_args(VerifyArgs &a)
 {
+    const Split sp = verify_split(a.B, a.k, a.V);
+    a.C = sp.C;
+    a.chunk = sp.len;
+    const Layout lay = make_layout(a.B, a.k, a.V);
+    a.stop_enc = ws_at<int>(a.ws, lay.stop_enc);
+    a.row_cnt = ws_at<int>(a.ws, lay.row_cnt);
+    a.seq_cnt = ws_at<int>(a.ws, lay.seq_cnt);
+    a.res_cnt = ws_at<int>(a.ws, lay.res_cnt);
+    a.row_tok = ws_at<int>(a.ws, lay.row_tok);
+    a.draw_row = ws_at<int>(a.ws, lay.draw_row);
+    a.row_ms = ws_at<float2>(a.ws, lay.row_ms);
+    a.row_flag = ws_at<uint32_t>(a.ws, lay.row_flag);
+    a.part = ws_at<void>(a.ws, lay.part);
+    a.rpart = ws_at<float>(a.ws, lay.rpart);
+    a.rtot = ws_at<double>(a.ws, lay.rtot);
+}
+
+cudaError_t launch_verify_greedy(const VerifyArgs &args, spec_dtype dt, cudaStream_t st)
+{
+    VerifyArgs a = args;
+    resolve_verify_args(a);
     const unsigned grid = (unsigned)(a.B * (a.k + 1) * a.C);
     switch (dt) {
     case SPEC_F32:

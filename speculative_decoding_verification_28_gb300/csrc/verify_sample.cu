@@ -7,15 +7,21 @@
 //   first rejection -> correction drawn from normalised max(0, p_j - q_j);
 //   full acceptance -> bonus drawn from p_{k_b} (the target).
 //
+// Arithmetic: p_v = 2^(x_v * c - m) / s with c = log2(e) / T, m the row
+// maximum of x * c and s = sum of 2^(x * c - m) -- the same softmax in base
+// 2, so each element costs one FFMA and one ex2.approx.  A -inf logit is a masked
+// token (probability 0); NaN / +inf, or a row without a finite logit, flags
+// the row as undefined.
+//
 // Three kernels, stream-ordered:
-//   stats  : per (b, j, chunk) online max / sum-of-exp of x/T (lazy rows, as
-//            in the greedy kernel); the row's last CTA gathers x[y] and q[y],
-//            runs the ratio test; the sequence's last row runs the first-stop
-//            ballot scan and decides which row (if any) is drawn from;
-//   draw   : per (b, chunk) of the drawn row, one pass over p (and q) that
-//            sums the residual and p; the row's last CTA picks the mode,
-//            finds the chunk holding u * total from the chunk prefix sums and
-//            scans that one chunk (now in L2) for the inverse-CDF index;
+//   stats  : per (b, j, chunk) online max / sum of 2^(x c - m) (lazy rows, as
+//            in the greedy kernel); the row's last CTA gathers x[y] and q[y]
+//            and runs the ratio test; the sequence's last row runs the
+//            first-stop ballot and decides which row (if any) is drawn from;
+//   draw   : per (b, chunk) of the drawn row, one vectorised pass summing the
+//            residual and p; the row's last CTA picks the mode, finds the chunk
+//            holding u * total from the chunk sums, stages that chunk's weights
+//            in shared memory and scans them for the inverse-CDF index;
 //   resid  : optional, writes the normalised distribution of the draw.
 // Roofline: HBM-bound; stats reads V * sizeof(T) per needed row; draw reads
 // V * (sizeof(T) + 4) for one row per drawing sequence.
@@ -26,69 +32,71 @@
 namespace spec {
 
 struct RowStats {
-    float m, s;
+    float m, s;  // base-2 row maximum of x * c and sum of 2^(x c - m)
 };
+
+__device__ __forceinline__ float scale_of(const VerifyArgs &a) { return a.unit_temp ? kLog2e : a.inv_temp * kLog2e; }
 
 // ---------------------------------------------------------------------------
 // stats kernel
 // ---------------------------------------------------------------------------
 template <typename T>
-__device__ void chunk_softmax_stats(const T *row, int lo, int hi, float inv_temp, bool unit, float &m_out,
-                                    float &s_out, bool &bad_out, float *s_f, int *s_i)
+__device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float &m_out, float &s_out,
+                                    bool &bad_out, float *s_f, const StopProbe &probe)
 {
     constexpr int VEC = Storage<T>::kVec;
+    constexpr int UNROLL = 4;
     const ChunkSplit<T> cs(row, lo, hi);
     float m = -INFINITY, s = 0.0f;
     bool bad = false;
-    auto add_vec = [&](const float *z, int n) {
-        float vmax = -INFINITY;
-        for (int e = 0; e < n; ++e) {
-            vmax = fmaxf(vmax, z[e]);
-            bad |= !(fabsf(z[e]) <= FLT_MAX);
-        }
-        if (vmax > m) {
-            s = (m > -INFINITY) ? s * expf(m - vmax) : 0.0f;
-            m = vmax;
+    // one element (head / tail)
+    auto add1 = [&](float x) {
+        const float z = x * c;
+        bad |= !(z < INFINITY);  // NaN or +inf; -inf is a masked token
+        if (z > m) {
+            s = (m > -INFINITY) ? s * exp2f(m - z) : 0.0f;
+            m = z;
         }
         if (m > -INFINITY)
-            for (int e = 0; e < n; ++e)
-                s += expf(z[e] - m);
+            s += exp2_sfu(fmaf(x, c, -m));
     };
     const int t = threadIdx.x;
-    if (lo + t < cs.head_end) {
-        float z = Storage<T>::at(row, lo + t);
-        z = unit ? z : z * inv_temp;
-        add_vec(&z, 1);
-    }
+    if (lo + t < cs.head_end)
+        add1(Storage<T>::at(row, lo + t));
     const T *body = row + cs.head_end;
-    for (int i = t; i < cs.nvec; i += 4 * kThreads) {
-        uint4 r[4];
+    for (int base = 0; base < cs.nvec; base += UNROLL * kThreads) {  // warp-uniform trip count
+        if (base > 0 && probe.dropped())
+            break;
+        const int i = base + t;
+        uint4 r[UNROLL];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < UNROLL; ++u) {
             const int vi = i + u * kThreads;
             if (vi < cs.nvec)
                 r[u] = ld_stream16(body + (size_t)vi * VEC);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < UNROLL; ++u) {
             const int vi = i + u * kThreads;
             if (vi < cs.nvec) {
-                float f[VEC];
-                Storage<T>::unpack(r[u], f);
-                if (!unit) {
+                const float vm = vec_max<T>(r[u]) * c;  // c > 0: the maximum commutes with the scale
+                bad |= !(vm < INFINITY);                // NaN or +inf in the vector
+                if (vm > m) {
+                    s = (m > -INFINITY) ? s * exp2f(m - vm) : 0.0f;
+                    m = vm;
+                }
+                if (m > -INFINITY) {
+                    float f[VEC];
+                    Storage<T>::unpack(r[u], f);
 #pragma unroll
                     for (int e = 0; e < VEC; ++e)
-                        f[e] *= inv_temp;
+                        s += exp2_sfu(fmaf(f[e], c, -m));
                 }
-                add_vec(f, VEC);
             }
         }
     }
-    if (cs.tail_beg + t < hi) {
-        float z = Storage<T>::at(row, cs.tail_beg + t);
-        z = unit ? z : z * inv_temp;
-        add_vec(&z, 1);
-    }
+    if (cs.tail_beg + t < hi)
+        add1(Storage<T>::at(row, cs.tail_beg + t));
     // block combine: max, then rescaled sum
     const int w = t >> 5, l = t & 31;
     float mm = m;
@@ -101,7 +109,7 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float inv_temp
     float mb = -INFINITY;
     for (int i = 0; i < kThreads / 32; ++i)
         mb = fmaxf(mb, s_f[i]);
-    float ss = (m > -INFINITY) ? s * expf(m - mb) : 0.0f;
+    float ss = (m > -INFINITY) ? s * exp2f(m - mb) : 0.0f;
 #pragma unroll
     for (int k = 16; k > 0; k >>= 1)
         ss += __shfl_xor_sync(0xFFFFFFFFu, ss, k);
@@ -115,7 +123,6 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float inv_temp
     m_out = mb;
     s_out = sb;
     bad_out = any_bad != 0;
-    (void)s_i;
 }
 
 template <typename T>
@@ -123,15 +130,12 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(VerifyArgs a)
 {
     __shared__ float s_f[2 * kThreads / 32];
     __shared__ int s_flag;
-    const Layout lay = make_layout(a.B, a.k, a.V);
-    int *stop_enc = ws_at<int>(a.ws, lay.stop_enc);
-    int *row_cnt = ws_at<int>(a.ws, lay.row_cnt);
-    int *seq_cnt = ws_at<int>(a.ws, lay.seq_cnt);
-    int *row_acc = ws_at<int>(a.ws, lay.row_tok);
-    RowStats *row_ms = ws_at<RowStats>(a.ws, lay.row_ms);
-    uint32_t *row_flag = ws_at<uint32_t>(a.ws, lay.row_flag);
-    float4 *part = ws_at<float4>(a.ws, lay.part);
-    int *draw_row = ws_at<int>(a.ws, lay.draw_row);
+    int *stop_enc = a.stop_enc, *row_cnt = a.row_cnt, *seq_cnt = a.seq_cnt, *row_acc = a.row_tok;
+    RowStats *row_ms = reinterpret_cast<RowStats *>(a.row_ms);
+    uint32_t *row_flag = a.row_flag;
+    float4 *part = static_cast<float4 *>(a.part);
+    int *draw_row = a.draw_row;
+    const float c = scale_of(a);
 
     const Unit u = decode_unit(a);
     const T *row = reinterpret_cast<const T *>(a.logits) + (size_t)u.row * a.V;
@@ -139,17 +143,21 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(VerifyArgs a)
         s_flag = (!u.needed || stopped_before(stop_enc, u.b, u.j)) ? 1 : 0;
     __syncthreads();
     if (!s_flag) {
-        const int lo = u.c * kChunk;
-        const int hi = min(a.V, lo + kChunk);
+        const int lo = u.c * a.chunk;
+        const int hi = min(a.V, lo + a.chunk);
         float m, s;
         bool bad;
-        chunk_softmax_stats<T>(row, lo, hi, a.inv_temp, a.unit_temp != 0, m, s, bad, s_f, nullptr);
+        chunk_softmax_stats<T>(row, lo, hi, c, m, s, bad, s_f, StopProbe{stop_enc, u.b, u.j});
         if (threadIdx.x == 0)
             part[(size_t)u.row * a.C + u.c] = make_float4(m, s, bad ? 1.0f : 0.0f, 0.0f);
     }
     if (threadIdx.x == 0) {
-        __threadfence();
-        s_flag = (atomicAdd(row_cnt + u.row, 1) == a.C - 1) ? 1 : 0;
+        if (a.C > 1) {
+            __threadfence();
+            s_flag = (atomicAdd(row_cnt + u.row, 1) == a.C - 1) ? 1 : 0;
+        } else {
+            s_flag = 1;  // a single-chunk row is finalised by its only CTA
+        }
     }
     __syncthreads();
     if (!s_flag || threadIdx.x >= 32)
@@ -163,16 +171,16 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(VerifyArgs a)
     if (eval) {
         // merge the chunk statistics of the row
         float m = -INFINITY;
-        for (int c = lane; c < a.C; c += 32)
-            m = fmaxf(m, part[(size_t)u.row * a.C + c].x);
+        for (int cc = lane; cc < a.C; cc += 32)
+            m = fmaxf(m, part[(size_t)u.row * a.C + cc].x);
 #pragma unroll
         for (int k = 16; k > 0; k >>= 1)
             m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, k));
         float s = 0.0f, bad = 0.0f;
-        for (int c = lane; c < a.C; c += 32) {
-            const float4 p = part[(size_t)u.row * a.C + c];
+        for (int cc = lane; cc < a.C; cc += 32) {
+            const float4 p = part[(size_t)u.row * a.C + cc];
             if (p.x > -INFINITY)
-                s += p.y * expf(p.x - m);
+                s += p.y * exp2f(p.x - m);
             bad = fmaxf(bad, p.z);
         }
 #pragma unroll
@@ -189,15 +197,11 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(VerifyArgs a)
                 if (y < 0 || y >= a.V) {
                     fl |= SPEC_FLAG_BAD_TOKEN;
                 } else {
-                    float zy = Storage<T>::at(row, y);
-                    zy = a.unit_temp ? zy : zy * a.inv_temp;
-                    const float py = expf(zy - m) / s;
+                    const float py = exp2f(fmaf(Storage<T>::at(row, y), c, -m)) / s;
                     const float qy = a.q[((size_t)u.b * a.k + u.j) * a.V + y];
                     if (qy == 0.0f)
                         fl |= SPEC_FLAG_Q_ZERO;
-                    const float ratio = py / qy;
-                    acc = (a.u[(size_t)u.b * (a.k + 1) + u.j] < ratio) ? 1 : 0;
-                    stop = false;
+                    acc = (a.u[(size_t)u.b * (a.k + 1) + u.j] < py / qy) ? 1 : 0;
                 }
                 stop = !acc || (a.eos >= 0 && y == a.eos) || (u.j + 1 == u.rem);
             } else {
@@ -267,36 +271,29 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(VerifyArgs a)
 // ---------------------------------------------------------------------------
 template <typename T>
 struct DrawRow {
-    const T *x;       // target logits row
-    const float *q;   // draft row (residual mode) or nullptr
-    float m, s, it;   // row max / sum of the scaled logits, 1/T
-    bool unit;
-    __device__ float p(int v) const
-    {
-        float z = Storage<T>::at(x, v);
-        z = unit ? z : z * it;
-        return expf(z - m) / s;
-    }
+    const T *x;      // target logits row
+    const float *q;  // draft row (residual mode) or nullptr
+    float m, inv_s, c;  // base-2 row maximum, 1 / sum, scale log2(e)/T
+    __device__ float p(float x_v) const { return exp2_sfu(fmaf(x_v, c, -m)) * inv_s; }
+    __device__ float pv(int v) const { return p(Storage<T>::at(x, v)); }
     // weight of index v; residual mode needs q
     __device__ float w(int v, bool residual) const
     {
-        const float pv = p(v);
-        return residual ? fmaxf(pv - __ldg(q + v), 0.0f) : pv;
+        const float p_v = pv(v);
+        return residual ? fmaxf(p_v - __ldg(q + v), 0.0f) : p_v;
     }
 };
 
 template <typename T>
 __device__ DrawRow<T> draw_row_of(const VerifyArgs &a, int b, int r, int kb)
 {
-    const Layout lay = make_layout(a.B, a.k, a.V);
-    const RowStats ms = ws_at<RowStats>(a.ws, lay.row_ms)[b * (a.k + 1) + r];
+    const RowStats ms = reinterpret_cast<const RowStats *>(a.row_ms)[b * (a.k + 1) + r];
     DrawRow<T> d;
     d.x = reinterpret_cast<const T *>(a.logits) + ((size_t)b * (a.k + 1) + r) * a.V;
     d.q = (r < kb) ? a.q + ((size_t)b * a.k + r) * a.V : nullptr;
     d.m = ms.m;
-    d.s = ms.s;
-    d.it = a.inv_temp;
-    d.unit = a.unit_temp != 0;
+    d.inv_s = 1.0f / ms.s;
+    d.c = scale_of(a);
     return d;
 }
 
@@ -316,43 +313,97 @@ __device__ __forceinline__ float block_sum(float v, float *s_f)
     return t;
 }
 
+// sums of max(0, p - q) and of p over elements [lo, hi) of the drawn row:
+// 16-byte loads of the logits and of q where both rows allow it
+template <typename T>
+__device__ void draw_chunk_sums(const DrawRow<T> &dr, bool residual, int lo, int hi, float &sr, float &sp)
+{
+    constexpr int VEC = Storage<T>::kVec;
+    const bool vec_ok = ((reinterpret_cast<uintptr_t>(dr.x + lo) & 15) == 0) &&
+                        (!residual || (reinterpret_cast<uintptr_t>(dr.q + lo) & 15) == 0);
+    int v0 = lo;
+    if (vec_ok) {
+        constexpr int UNROLL = 4;
+        constexpr int QV = VEC / 4;  // 16-byte q vectors per logits vector
+        const int nvec = (hi - lo) / VEC;
+        for (int i = threadIdx.x; i < nvec; i += UNROLL * kThreads) {
+            uint4 r[UNROLL], qq[UNROLL][QV];
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int vi = i + u * kThreads;
+                if (vi < nvec) {
+                    r[u] = ld_stream16(dr.x + lo + (size_t)vi * VEC);
+                    if (residual) {
+#pragma unroll
+                        for (int h = 0; h < QV; ++h)
+                            qq[u][h] = ld_stream16(dr.q + lo + (size_t)vi * VEC + 4 * h);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int vi = i + u * kThreads;
+                if (vi < nvec) {
+                    float f[VEC];
+                    Storage<T>::unpack(r[u], f);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        const float p = dr.p(f[e]);
+                        sp += p;
+                        if (residual) {
+                            const uint4 &w4 = qq[u][e / 4];
+                            const uint32_t qb = (e & 3) == 0 ? w4.x : (e & 3) == 1 ? w4.y : (e & 3) == 2 ? w4.z : w4.w;
+                            sr += fmaxf(p - __uint_as_float(qb), 0.0f);
+                        }
+                    }
+                }
+            }
+        }
+        v0 = lo + nvec * VEC;
+    }
+    for (int v = v0 + threadIdx.x; v < hi; v += kThreads) {
+        const float p = dr.pv(v);
+        sp += p;
+        if (residual)
+            sr += fmaxf(p - __ldg(dr.q + v), 0.0f);
+    }
+}
+
+constexpr int kSeg = kDrawChunk / kThreads;  // contiguous elements per thread in the final scan
+constexpr int kPadded = kDrawChunk + kDrawChunk / 32;
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) verify_draw_kernel(VerifyArgs a)
 {
+    __shared__ float s_w[kPadded];  // weights of the chosen chunk, one pad word per 32
     __shared__ float s_f[kThreads / 32];
     __shared__ double s_d[kThreads / 32];
-    __shared__ int s_flag, s_pick, s_lastpos;
-    __shared__ double s_base;
-    __shared__ int s_chunk;
-    const Layout lay = make_layout(a.B, a.k, a.V);
-    const int b = blockIdx.x / a.C, c = blockIdx.x % a.C;
-    const int r = ws_at<int>(a.ws, lay.draw_row)[b];
+    __shared__ int s_flag, s_pick, s_lastpos, s_chunk, s_use_res;
+    __shared__ double s_base, s_target;
+    const int Cd = draw_chunks(a.V);
+    const int b = blockIdx.x / Cd, c = blockIdx.x % Cd;
+    const int r = a.draw_row[b];
     if (r < 0)
         return;
     int kb = a.draft_len ? a.draft_len[b] : a.k;
     kb = kb < 0 ? 0 : (kb > a.k ? a.k : kb);
     const bool residual = r < kb;
     const DrawRow<T> dr = draw_row_of<T>(a, b, r, kb);
-    float *rpart = ws_at<float>(a.ws, lay.rpart);
-    int *res_cnt = ws_at<int>(a.ws, lay.res_cnt);
-    double *rtot = ws_at<double>(a.ws, lay.rtot);
+    float *rpart = a.rpart;
+    int *res_cnt = a.res_cnt;
+    double *rtot = a.rtot;
 
-    // pass over this chunk: sum of the residual and sum of p
-    const int lo = c * kChunk, hi = min(a.V, lo + kChunk);
+    // one pass over this chunk: sum of the residual and sum of p
+    const int lo = c * kDrawChunk, hi = min(a.V, lo + kDrawChunk);
     float sr = 0.0f, sp = 0.0f;
-    for (int v = lo + threadIdx.x; v < hi; v += kThreads) {
-        const float pv = dr.p(v);
-        sp += pv;
-        if (residual)
-            sr += fmaxf(pv - __ldg(dr.q + v), 0.0f);
-    }
+    draw_chunk_sums<T>(dr, residual, lo, hi, sr, sp);
     sr = block_sum(sr, s_f);
     sp = block_sum(sp, s_f);
     if (threadIdx.x == 0) {
-        rpart[((size_t)b * a.C + c) * 2 + 0] = sr;
-        rpart[((size_t)b * a.C + c) * 2 + 1] = sp;
+        rpart[((size_t)b * Cd + c) * 2 + 0] = sr;
+        rpart[((size_t)b * Cd + c) * 2 + 1] = sp;
         __threadfence();
-        s_flag = (atomicAdd(res_cnt + b, 1) == a.C - 1) ? 1 : 0;
+        s_flag = (atomicAdd(res_cnt + b, 1) == Cd - 1) ? 1 : 0;
     }
     __syncthreads();
     if (!s_flag)
@@ -360,21 +411,20 @@ __global__ void __launch_bounds__(kThreads) verify_draw_kernel(VerifyArgs a)
     __threadfence();
 
     // last CTA of the row: choose the weights, find the chunk, scan it
-    bool use_res = false;
     if (threadIdx.x == 0) {
         double R = 0.0, P = 0.0;
-        for (int i = 0; i < a.C; ++i) {
-            R += (double)rpart[((size_t)b * a.C + i) * 2 + 0];
-            P += (double)rpart[((size_t)b * a.C + i) * 2 + 1];
+        for (int i = 0; i < Cd; ++i) {
+            R += (double)rpart[((size_t)b * Cd + i) * 2 + 0];
+            P += (double)rpart[((size_t)b * Cd + i) * 2 + 1];
         }
-        use_res = residual && R > 0.0;
+        const bool use_res = residual && R > 0.0;
         const int sel = use_res ? 0 : 1;
         const double W = use_res ? R : P;
         const double target = (double)a.u[(size_t)b * (a.k + 1) + a.k] * W;
         double acc = 0.0;
         int cs = -1, lastpos = -1;
-        for (int i = 0; i < a.C; ++i) {
-            const double pc = (double)rpart[((size_t)b * a.C + i) * 2 + sel];
+        for (int i = 0; i < Cd; ++i) {
+            const double pc = (double)rpart[((size_t)b * Cd + i) * 2 + sel];
             if (pc > 0.0)
                 lastpos = i;
             if (cs < 0 && acc + pc > target) {
@@ -384,35 +434,54 @@ __global__ void __launch_bounds__(kThreads) verify_draw_kernel(VerifyArgs a)
             acc += pc;
         }
         if (cs < 0) {  // rounding left u * W at or past the total: last positive chunk
-            cs = lastpos >= 0 ? lastpos : a.C - 1;
+            cs = lastpos >= 0 ? lastpos : Cd - 1;
             s_base = -1.0;  // take the last positive index of that chunk
         }
         s_chunk = cs;
+        s_use_res = use_res ? 1 : 0;
+        s_target = target;
         s_pick = 0x7FFFFFFF;
         s_lastpos = -1;
         rtot[b] = use_res ? W : -W;  // sign records the mode for the residual writer
         if (residual && !use_res && a.flags)
             a.flags[b] |= SPEC_FLAG_ZERO_RESIDUAL;
         res_cnt[b] = 0;
-        s_d[0] = target;
     }
     __syncthreads();
-    use_res = rtot[b] > 0.0;
-    const double target = s_d[0];
-    const double base = s_base;
-    const int cs = s_chunk;
+    const bool use_res = s_use_res != 0;
+    const double target = s_target, base = s_base;
+    const int clo = s_chunk * kDrawChunk, n = min(a.V, clo + kDrawChunk) - clo;
+    // stage the chunk's weights (coalesced, all of a thread's loads issued
+    // before any is used), then scan contiguous segments
+    {
+        constexpr int kPer = kDrawChunk / kThreads;
+        float xv[kPer], qv[kPer];
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+            const int i = threadIdx.x + e * kThreads;
+            if (i < n) {
+                xv[e] = Storage<T>::at(dr.x, clo + i);
+                qv[e] = use_res ? __ldg(dr.q + clo + i) : 0.0f;
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+            const int i = threadIdx.x + e * kThreads;
+            if (i < n) {
+                const float p = dr.p(xv[e]);
+                s_w[i + (i >> 5)] = use_res ? fmaxf(p - qv[e], 0.0f) : p;
+            }
+        }
+    }
     __syncthreads();
-    // each thread owns a contiguous segment of the chunk
-    const int clo = cs * kChunk, chi = min(a.V, clo + kChunk);
-    const int per = (chi - clo + kThreads - 1) / kThreads;
-    const int slo = clo + threadIdx.x * per, shi = min(chi, slo + per);
+    const int slo = threadIdx.x * kSeg, shi = min(n, slo + kSeg);
     float seg = 0.0f;
     int seg_last = -1;
-    for (int v = slo; v < shi; ++v) {
-        const float wv = dr.w(v, use_res);
+    for (int i = slo; i < shi; ++i) {
+        const float wv = s_w[i + (i >> 5)];
         seg += wv;
         if (wv > 0.0f)
-            seg_last = v;
+            seg_last = clo + i;
     }
     // exclusive scan of the segment sums (fp64)
     double incl = (double)seg;
@@ -431,10 +500,10 @@ __global__ void __launch_bounds__(kThreads) verify_draw_kernel(VerifyArgs a)
         warp_off += s_d[i];
     double run = base + warp_off + incl - (double)seg;
     if (base >= 0.0) {
-        for (int v = slo; v < shi; ++v) {
-            run += (double)dr.w(v, use_res);
+        for (int i = slo; i < shi; ++i) {
+            run += (double)s_w[i + (i >> 5)];
             if (run > target) {
-                atomicMin(&s_pick, v);
+                atomicMin(&s_pick, clo + i);
                 break;
             }
         }
@@ -445,7 +514,7 @@ __global__ void __launch_bounds__(kThreads) verify_draw_kernel(VerifyArgs a)
     if (threadIdx.x == 0) {
         int tok = s_pick;
         if (tok == 0x7FFFFFFF)
-            tok = s_lastpos >= 0 ? s_lastpos : chi - 1;
+            tok = s_lastpos >= 0 ? s_lastpos : clo + n - 1;
         a.out_tokens[(size_t)b * (a.k + 1) + r] = tok;
     }
 }
@@ -454,28 +523,30 @@ __global__ void __launch_bounds__(kThreads) verify_draw_kernel(VerifyArgs a)
 template <typename T>
 __global__ void __launch_bounds__(kThreads) verify_residual_kernel(VerifyArgs a)
 {
-    const Layout lay = make_layout(a.B, a.k, a.V);
-    const int b = blockIdx.x / a.C, c = blockIdx.x % a.C;
-    const int r = ws_at<int>(a.ws, lay.draw_row)[b];
+    const int Cd = draw_chunks(a.V);
+    const int b = blockIdx.x / Cd, c = blockIdx.x % Cd;
+    const int r = a.draw_row[b];
     if (r < 0)
         return;
     int kb = a.draft_len ? a.draft_len[b] : a.k;
     kb = kb < 0 ? 0 : (kb > a.k ? a.k : kb);
     const DrawRow<T> dr = draw_row_of<T>(a, b, r, kb);
-    const double W = ws_at<double>(a.ws, lay.rtot)[b];
+    const double W = a.rtot[b];
     const bool use_res = W > 0.0;
     const float inv = (float)(1.0 / (use_res ? W : -W));
-    const int lo = c * kChunk, hi = min(a.V, lo + kChunk);
+    const int lo = c * kDrawChunk, hi = min(a.V, lo + kDrawChunk);
     float *out = a.out_residual + (size_t)b * a.V;
     for (int v = lo + threadIdx.x; v < hi; v += kThreads)
         out[v] = dr.w(v, use_res) * inv;
 }
 
 template <typename T>
-static cudaError_t launch_sample_t(const VerifyArgs &a, cudaStream_t st)
+static cudaError_t launch_sample_t(const VerifyArgs &args, cudaStream_t st)
 {
+    VerifyArgs a = args;
+    resolve_verify_args(a);
     const unsigned g1 = (unsigned)(a.B * (a.k + 1) * a.C);
-    const unsigned g2 = (unsigned)(a.B * a.C);
+    const unsigned g2 = (unsigned)(a.B * draw_chunks(a.V));
     verify_stats_kernel<T><<<g1, kThreads, 0, st>>>(a);
     verify_draw_kernel<T><<<g2, kThreads, 0, st>>>(a);
     if (a.out_residual)

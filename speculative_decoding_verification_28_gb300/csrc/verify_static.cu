@@ -57,7 +57,7 @@ extern "C" int spec_verify_greedy_static(const void *target_logits, spec_dtype d
         return SPEC_OK;
     if (!target_logits || (k > 0 && !draft_tokens) || !out_tokens || !n_accept || !n_emit)
         return SPEC_EINVAL;
-    if ((long long)B * (k + 1) * verify_chunks(V) > 0x7FFFFFFFLL)
+    if ((long long)B * (k + 1) * verify_chunks(B, k, V) > 0x7FFFFFFFLL)
         return SPEC_EINVAL;
     if (!aligned_to(target_logits, dt == SPEC_F32 ? 4 : 2) || !aligned_to(out_tokens, 4) ||
         !aligned_to(n_accept, 4) || !aligned_to(n_emit, 4) || (draft_tokens && !aligned_to(draft_tokens, 4)))
@@ -78,7 +78,6 @@ extern "C" int spec_verify_greedy_static(const void *target_logits, spec_dtype d
     a.B = B;
     a.k = k;
     a.V = V;
-    a.C = verify_chunks(V);
     a.draft = draft_tokens;
     a.draft_len = draft_len;
     a.eos = eos_id;

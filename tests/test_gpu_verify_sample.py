@@ -197,3 +197,18 @@ def test_zz_boundary_rate():
     assert STATS["decisions"] > 50_000
     assert STATS["boundary"] < 1e-4 * STATS["decisions"], STATS
     print("sampling parity statistics:", STATS)
+
+
+def test_masked_vocabulary_rows():
+    """Rows with -inf logits (masked tokens, e.g. after top-k filtering) are
+    ordinary distributions: masked tokens have probability 0."""
+    rng = np.random.default_rng(21)
+    B, k, V = 256, 3, 3000
+    x, q, d, u = sample_round_inputs(B, k, V, 0.5, seed=21, dtype="f32")
+    keep = rng.random((B, k + 1, V)) < 0.2
+    keep[np.arange(B)[:, None], np.arange(k)[None, :], d] = True  # proposals stay unmasked
+    x = np.where(keep, x, -np.inf).astype(np.float32)
+    x[::17] = -np.inf  # a few sequences with every logit masked: undefined, flagged
+    check(x, oracle.DT_F32, q, d, u)
+    xb = (x.view(np.uint32) >> 16).astype(np.uint16)  # -inf survives bf16 truncation
+    check(xb, oracle.DT_BF16, q, d, u)
