@@ -130,6 +130,31 @@ struct StopProbe {
     }
 };
 
+// Block-wide max of a u64 key for thread 0 only: warp shuffles, one
+// shared-memory exchange, one barrier (the other threads' results are
+// meaningless).
+__device__ __forceinline__ uint64_t block_max_u64_to0(uint64_t key, uint64_t *s_red)
+{
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) {
+        const uint64_t o = shfl_xor_u64(key, m);
+        key = o > key ? o : key;
+    }
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0)
+        s_red[w] = key;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        key = (l < (int)(blockDim.x >> 5)) ? s_red[l] : 0;
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) {
+            const uint64_t o = shfl_xor_u64(key, m);
+            key = o > key ? o : key;
+        }
+    }
+    return key;
+}
+
 // Block-wide max of a u64 key (all threads get the result).
 __device__ __forceinline__ uint64_t block_max_u64(uint64_t key, uint64_t *s_red)
 {

@@ -81,29 +81,29 @@ __device__ uint64_t chunk_argmax(const T *row, int lo, int hi, uint64_t *s_red, 
     uint64_t key = 0;
     if (first != 0xFFFFFFFFu)
         key = bidx != 0xFFFFFFFFu ? argmax_key(best, bidx) : argmax_key(-INFINITY, first);
-    if (__syncthreads_or(nan)) {
+    if (__syncthreads_or(nan)) {  // rare: a NaN somewhere in the chunk
         key = 0;
         for (int i = lo + t; i < hi; i += kThreads) {
             const uint64_t kk = argmax_key(Storage<T>::at(row, i), (uint32_t)i);
             key = kk > key ? kk : key;
         }
     }
-    return block_max_u64(key, s_red);
+    return block_max_u64_to0(key, s_red);  // meaningful in thread 0
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) verify_greedy_kernel(VerifyArgs a)
 {
     __shared__ uint64_t s_red[kThreads / 32];
-    __shared__ int s_flag;
+    __shared__ int s_skip, s_last;  // written once each: no read/write race between them
     int *stop_enc = a.stop_enc, *row_cnt = a.row_cnt, *seq_cnt = a.seq_cnt, *row_tok = a.row_tok;
     uint64_t *part = static_cast<uint64_t *>(a.part);
 
     const Unit u = decode_unit(a);
     if (threadIdx.x == 0)
-        s_flag = (!u.needed || stopped_before(stop_enc, u.b, u.j)) ? 1 : 0;
+        s_skip = (!u.needed || stopped_before(stop_enc, u.b, u.j)) ? 1 : 0;
     __syncthreads();
-    if (!s_flag) {
+    if (!s_skip) {
         const T *row = reinterpret_cast<const T *>(a.logits) + (size_t)u.row * a.V;
         const int lo = u.c * a.chunk;
         const int hi = min(a.V, lo + a.chunk);
@@ -115,13 +115,13 @@ __global__ void __launch_bounds__(kThreads) verify_greedy_kernel(VerifyArgs a)
     if (threadIdx.x == 0) {
         if (a.C > 1) {
             __threadfence();
-            s_flag = (atomicAdd(row_cnt + u.row, 1) == a.C - 1) ? 1 : 0;
+            s_last = (atomicAdd(row_cnt + u.row, 1) == a.C - 1) ? 1 : 0;
         } else {
-            s_flag = 1;  // a single-chunk row is finalised by its only CTA
+            s_last = 1;  // a single-chunk row is finalised by its only CTA
         }
     }
     __syncthreads();
-    if (!s_flag || threadIdx.x >= 32)
+    if (!s_last || threadIdx.x >= 32)
         return;
     __threadfence();
     const int lane = threadIdx.x;

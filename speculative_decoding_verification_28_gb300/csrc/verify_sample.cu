@@ -27,6 +27,7 @@
 // V * (sizeof(T) + 4) for one row per drawing sequence.
 #include <float.h>
 
+#include "bulk_copy.cuh"
 #include "verify_common.cuh"
 
 namespace spec {
@@ -97,39 +98,44 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
     }
     if (cs.tail_beg + t < hi)
         add1(Storage<T>::at(row, cs.tail_beg + t));
-    // block combine: max, then rescaled sum
+    // combine for thread 0: (max, rescaled sum) merged within each warp by
+    // shuffles, then across warps by warp 0 after one barrier
     const int w = t >> 5, l = t & 31;
-    float mm = m;
+    auto merge = [](float &ma, float &sa, float mb, float sb) {
+        const float mx = fmaxf(ma, mb);
+        const float a = (ma > -INFINITY) ? sa * exp2f(ma - mx) : 0.0f;
+        const float b = (mb > -INFINITY) ? sb * exp2f(mb - mx) : 0.0f;
+        ma = mx;
+        sa = a + b;
+    };
 #pragma unroll
     for (int k = 16; k > 0; k >>= 1)
-        mm = fmaxf(mm, __shfl_xor_sync(0xFFFFFFFFu, mm, k));
-    if (l == 0)
-        s_f[w] = mm;
+        merge(m, s, __shfl_xor_sync(0xFFFFFFFFu, m, k), __shfl_xor_sync(0xFFFFFFFFu, s, k));
+    const bool wbad = __any_sync(0xFFFFFFFFu, bad);
+    if (l == 0) {
+        s_f[w] = m;
+        s_f[kThreads / 32 + w] = wbad ? -s : s;  // the sign carries the warp's flag (s >= 0)
+        s_f[2 * (kThreads / 32) + w] = wbad ? 1.0f : 0.0f;
+    }
     __syncthreads();
-    float mb = -INFINITY;
-    for (int i = 0; i < kThreads / 32; ++i)
-        mb = fmaxf(mb, s_f[i]);
-    float ss = (m > -INFINITY) ? s * exp2f(m - mb) : 0.0f;
+    if (t < 32) {
+        float mm = (l < kThreads / 32) ? s_f[l] : -INFINITY;
+        float ss = (l < kThreads / 32) ? fabsf(s_f[kThreads / 32 + l]) : 0.0f;
+        const bool bb = (l < kThreads / 32) && s_f[2 * (kThreads / 32) + l] > 0.0f;
 #pragma unroll
-    for (int k = 16; k > 0; k >>= 1)
-        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, k);
-    const int any_bad = __syncthreads_or(bad);
-    if (l == 0)
-        s_f[kThreads / 32 + w] = ss;
-    __syncthreads();
-    float sb = 0.0f;
-    for (int i = 0; i < kThreads / 32; ++i)
-        sb += s_f[kThreads / 32 + i];
-    m_out = mb;
-    s_out = sb;
-    bad_out = any_bad != 0;
+        for (int k = 16; k > 0; k >>= 1)
+            merge(mm, ss, __shfl_xor_sync(0xFFFFFFFFu, mm, k), __shfl_xor_sync(0xFFFFFFFFu, ss, k));
+        m_out = mm;
+        s_out = ss;
+        bad_out = __any_sync(0xFFFFFFFFu, bb);
+    }
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) verify_stats_kernel(VerifyArgs a)
 {
-    __shared__ float s_f[2 * kThreads / 32];
-    __shared__ int s_flag;
+    __shared__ float s_f[3 * kThreads / 32];
+    __shared__ int s_skip, s_last;  // written once each: no read/write race between them
     int *stop_enc = a.stop_enc, *row_cnt = a.row_cnt, *seq_cnt = a.seq_cnt, *row_acc = a.row_tok;
     RowStats *row_ms = reinterpret_cast<RowStats *>(a.row_ms);
     uint32_t *row_flag = a.row_flag;
@@ -140,9 +146,9 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(VerifyArgs a)
     const Unit u = decode_unit(a);
     const T *row = reinterpret_cast<const T *>(a.logits) + (size_t)u.row * a.V;
     if (threadIdx.x == 0)
-        s_flag = (!u.needed || stopped_before(stop_enc, u.b, u.j)) ? 1 : 0;
+        s_skip = (!u.needed || stopped_before(stop_enc, u.b, u.j)) ? 1 : 0;
     __syncthreads();
-    if (!s_flag) {
+    if (!s_skip) {
         const int lo = u.c * a.chunk;
         const int hi = min(a.V, lo + a.chunk);
         float m, s;
@@ -154,13 +160,13 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(VerifyArgs a)
     if (threadIdx.x == 0) {
         if (a.C > 1) {
             __threadfence();
-            s_flag = (atomicAdd(row_cnt + u.row, 1) == a.C - 1) ? 1 : 0;
+            s_last = (atomicAdd(row_cnt + u.row, 1) == a.C - 1) ? 1 : 0;
         } else {
-            s_flag = 1;  // a single-chunk row is finalised by its only CTA
+            s_last = 1;  // a single-chunk row is finalised by its only CTA
         }
     }
     __syncthreads();
-    if (!s_flag || threadIdx.x >= 32)
+    if (!s_last || threadIdx.x >= 32)
         return;
     __threadfence();
     const int lane = threadIdx.x;
@@ -297,6 +303,31 @@ __device__ DrawRow<T> draw_row_of(const VerifyArgs &a, int b, int r, int kb)
     return d;
 }
 
+// two block sums for thread 0: warp shuffles, one barrier, warp 0 finishes
+__device__ __forceinline__ void block_sum2_to0(float &a, float &b, float *s_f)
+{
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1) {
+        a += __shfl_xor_sync(0xFFFFFFFFu, a, k);
+        b += __shfl_xor_sync(0xFFFFFFFFu, b, k);
+    }
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) {
+        s_f[w] = a;
+        s_f[kThreads / 32 + w] = b;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        a = (l < kThreads / 32) ? s_f[l] : 0.0f;
+        b = (l < kThreads / 32) ? s_f[kThreads / 32 + l] : 0.0f;
+#pragma unroll
+        for (int k = 16; k > 0; k >>= 1) {
+            a += __shfl_xor_sync(0xFFFFFFFFu, a, k);
+            b += __shfl_xor_sync(0xFFFFFFFFu, b, k);
+        }
+    }
+}
+
 __device__ __forceinline__ float block_sum(float v, float *s_f)
 {
 #pragma unroll
@@ -376,10 +407,11 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) verify_draw_kernel(VerifyArgs a)
 {
     __shared__ float s_w[kPadded];  // weights of the chosen chunk, one pad word per 32
-    __shared__ float s_f[kThreads / 32];
+    __shared__ float s_f[2 * kThreads / 32];
     __shared__ double s_d[kThreads / 32];
     __shared__ int s_flag, s_pick, s_lastpos, s_chunk, s_use_res;
     __shared__ double s_base, s_target;
+    dep_wait();  // launched programmatically: the stats grid's results are complete
     const int Cd = draw_chunks(a.V);
     const int b = blockIdx.x / Cd, c = blockIdx.x % Cd;
     const int r = a.draw_row[b];
@@ -397,8 +429,7 @@ __global__ void __launch_bounds__(kThreads) verify_draw_kernel(VerifyArgs a)
     const int lo = c * kDrawChunk, hi = min(a.V, lo + kDrawChunk);
     float sr = 0.0f, sp = 0.0f;
     draw_chunk_sums<T>(dr, residual, lo, hi, sr, sp);
-    sr = block_sum(sr, s_f);
-    sp = block_sum(sp, s_f);
+    block_sum2_to0(sr, sp, s_f);
     if (threadIdx.x == 0) {
         rpart[((size_t)b * Cd + c) * 2 + 0] = sr;
         rpart[((size_t)b * Cd + c) * 2 + 1] = sp;
@@ -410,67 +441,116 @@ __global__ void __launch_bounds__(kThreads) verify_draw_kernel(VerifyArgs a)
         return;
     __threadfence();
 
-    // last CTA of the row: choose the weights, find the chunk, scan it
-    if (threadIdx.x == 0) {
+    // last CTA of the row: choose the weights, find the chunk, scan it.
+    // Warp 0 loads the chunk sums in parallel (32 chunks per pass) and scans
+    // them in fp64 with shuffles; a ballot finds the chunk holding u * total.
+    if (threadIdx.x < 32) {
+        const int l = threadIdx.x;
         double R = 0.0, P = 0.0;
-        for (int i = 0; i < Cd; ++i) {
-            R += (double)rpart[((size_t)b * Cd + i) * 2 + 0];
-            P += (double)rpart[((size_t)b * Cd + i) * 2 + 1];
+        for (int i0 = 0; i0 < Cd; i0 += 32) {
+            const int i = i0 + l;
+            if (i < Cd) {
+                R += (double)rpart[((size_t)b * Cd + i) * 2 + 0];
+                P += (double)rpart[((size_t)b * Cd + i) * 2 + 1];
+            }
+        }
+#pragma unroll
+        for (int k = 16; k > 0; k >>= 1) {
+            R += __shfl_xor_sync(0xFFFFFFFFu, R, k);
+            P += __shfl_xor_sync(0xFFFFFFFFu, P, k);
         }
         const bool use_res = residual && R > 0.0;
         const int sel = use_res ? 0 : 1;
         const double W = use_res ? R : P;
         const double target = (double)a.u[(size_t)b * (a.k + 1) + a.k] * W;
-        double acc = 0.0;
+        double before = 0.0;  // sum of the chunks of earlier passes
         int cs = -1, lastpos = -1;
-        for (int i = 0; i < Cd; ++i) {
-            const double pc = (double)rpart[((size_t)b * Cd + i) * 2 + sel];
-            if (pc > 0.0)
-                lastpos = i;
-            if (cs < 0 && acc + pc > target) {
-                cs = i;
-                s_base = acc;
+        double cs_base = 0.0;
+        for (int i0 = 0; i0 < Cd && cs < 0; i0 += 32) {
+            const int i = i0 + l;
+            const double pc = (i < Cd) ? (double)rpart[((size_t)b * Cd + i) * 2 + sel] : 0.0;
+            double incl = pc;
+#pragma unroll
+            for (int k = 1; k < 32; k <<= 1) {
+                const double o = __shfl_up_sync(0xFFFFFFFFu, incl, k);
+                if (l >= k)
+                    incl += o;
             }
-            acc += pc;
+            const unsigned pos = __ballot_sync(0xFFFFFFFFu, pc > 0.0);
+            if (pos)
+                lastpos = i0 + 31 - __clz((int)pos);
+            const unsigned hit = __ballot_sync(0xFFFFFFFFu, i < Cd && before + incl > target);
+            if (hit) {
+                const int f = __ffs(hit) - 1;
+                cs = i0 + f;
+                cs_base = before + __shfl_sync(0xFFFFFFFFu, incl - pc, f);
+            }
+            before += __shfl_sync(0xFFFFFFFFu, incl, 31);
         }
-        if (cs < 0) {  // rounding left u * W at or past the total: last positive chunk
-            cs = lastpos >= 0 ? lastpos : Cd - 1;
-            s_base = -1.0;  // take the last positive index of that chunk
+        if (l == 0) {
+            if (cs < 0) {  // rounding left u * W at or past the total: last positive chunk
+                cs = lastpos >= 0 ? lastpos : Cd - 1;
+                cs_base = -1.0;  // take the last positive index of that chunk
+            }
+            s_base = cs_base;
+            s_chunk = cs;
+            s_use_res = use_res ? 1 : 0;
+            s_target = target;
+            s_pick = 0x7FFFFFFF;
+            s_lastpos = -1;
+            rtot[b] = use_res ? W : -W;  // sign records the mode for the residual writer
+            if (residual && !use_res && a.flags)
+                a.flags[b] |= SPEC_FLAG_ZERO_RESIDUAL;
+            res_cnt[b] = 0;
         }
-        s_chunk = cs;
-        s_use_res = use_res ? 1 : 0;
-        s_target = target;
-        s_pick = 0x7FFFFFFF;
-        s_lastpos = -1;
-        rtot[b] = use_res ? W : -W;  // sign records the mode for the residual writer
-        if (residual && !use_res && a.flags)
-            a.flags[b] |= SPEC_FLAG_ZERO_RESIDUAL;
-        res_cnt[b] = 0;
     }
     __syncthreads();
     const bool use_res = s_use_res != 0;
     const double target = s_target, base = s_base;
     const int clo = s_chunk * kDrawChunk, n = min(a.V, clo + kDrawChunk) - clo;
-    // stage the chunk's weights (coalesced, all of a thread's loads issued
-    // before any is used), then scan contiguous segments
+    // stage the chunk's weights: every thread issues all of its 16-byte loads
+    // (logits and q) before using any, then writes weights to shared memory
     {
-        constexpr int kPer = kDrawChunk / kThreads;
-        float xv[kPer], qv[kPer];
+        constexpr int VEC = Storage<T>::kVec;
+        constexpr int NV = kDrawChunk / VEC / kThreads;  // vectors per thread
+        const bool vec_ok = (n == kDrawChunk) && ((reinterpret_cast<uintptr_t>(dr.x + clo) & 15) == 0) &&
+                            (!use_res || (reinterpret_cast<uintptr_t>(dr.q + clo) & 15) == 0);
+        if (vec_ok) {
+            constexpr int NH = NV / 2;  // two halves keep the register count down
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+            uint4 xr[NH], qr[NH][VEC / 4];
 #pragma unroll
-        for (int e = 0; e < kPer; ++e) {
-            const int i = threadIdx.x + e * kThreads;
-            if (i < n) {
-                xv[e] = Storage<T>::at(dr.x, clo + i);
-                qv[e] = use_res ? __ldg(dr.q + clo + i) : 0.0f;
-            }
-        }
+            for (int v = 0; v < NH; ++v) {
+                const int i = (threadIdx.x + (half * NH + v) * kThreads) * VEC;
+                xr[v] = ld_stream16(dr.x + clo + i);
+                if (use_res) {
 #pragma unroll
-        for (int e = 0; e < kPer; ++e) {
-            const int i = threadIdx.x + e * kThreads;
-            if (i < n) {
-                const float p = dr.p(xv[e]);
-                s_w[i + (i >> 5)] = use_res ? fmaxf(p - qv[e], 0.0f) : p;
+                    for (int h = 0; h < VEC / 4; ++h)
+                        qr[v][h] = ld_stream16(dr.q + clo + i + 4 * h);
+                }
             }
+#pragma unroll
+            for (int v = 0; v < NH; ++v) {
+                const int i = (threadIdx.x + (half * NH + v) * kThreads) * VEC;
+                float f[VEC];
+                Storage<T>::unpack(xr[v], f);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const float p = dr.p(f[e]);
+                    float wv = p;
+                    if (use_res) {
+                        const uint4 &w4 = qr[v][e / 4];
+                        const uint32_t qb = (e & 3) == 0 ? w4.x : (e & 3) == 1 ? w4.y : (e & 3) == 2 ? w4.z : w4.w;
+                        wv = fmaxf(p - __uint_as_float(qb), 0.0f);
+                    }
+                    s_w[(i + e) + ((i + e) >> 5)] = wv;
+                }
+            }
+            }
+        } else {
+            for (int i = threadIdx.x; i < n; i += kThreads)
+                s_w[i + (i >> 5)] = dr.w(clo + i, use_res);
         }
     }
     __syncthreads();
@@ -498,11 +578,15 @@ __global__ void __launch_bounds__(kThreads) verify_draw_kernel(VerifyArgs a)
     double warp_off = 0.0;
     for (int i = 0; i < wid; ++i)
         warp_off += s_d[i];
-    double run = base + warp_off + incl - (double)seg;
-    if (base >= 0.0) {
+    // the segment holding the target: its start offset in fp64, the walk
+    // within it in fp32 against the remaining distance
+    const double seg_start = base + warp_off + incl - (double)seg;
+    if (base >= 0.0 && seg_start + (double)seg > target) {
+        const float rem = (float)(target - seg_start);
+        float run = 0.0f;
         for (int i = slo; i < shi; ++i) {
-            run += (double)s_w[i + (i >> 5)];
-            if (run > target) {
+            run += s_w[i + (i >> 5)];
+            if (run > rem) {
                 atomicMin(&s_pick, clo + i);
                 break;
             }
@@ -548,7 +632,20 @@ static cudaError_t launch_sample_t(const VerifyArgs &args, cudaStream_t st)
     const unsigned g1 = (unsigned)(a.B * (a.k + 1) * a.C);
     const unsigned g2 = (unsigned)(a.B * draw_chunks(a.V));
     verify_stats_kernel<T><<<g1, kThreads, 0, st>>>(a);
-    verify_draw_kernel<T><<<g2, kThreads, 0, st>>>(a);
+    // the draw kernel becomes resident while the stats kernel drains and
+    // waits for it on the device (griddepcontrol.wait)
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(g2);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = st;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, verify_draw_kernel<T>, a);
+    if (e != cudaSuccess)
+        return e;
     if (a.out_residual)
         verify_residual_kernel<T><<<g2, kThreads, 0, st>>>(a);
     return cudaGetLastError();
