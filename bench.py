@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--seed", type=int, default=1002)
     ap.add_argument("--dump-steps", default=None,
                     help="write each step's algorithmic bytes and call times (JSON lines) to this file")
+    ap.add_argument("--draft-cache", default=None,
+                    help="L,H,D of a draft model's cache realigned with the target's in one call, "
+                         "e.g. 2,12,64 (a 68M-class drafter)")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the cache's layer count (small profiling captures only)")
     return ap.parse_args()
@@ -70,6 +73,7 @@ def workload_params(args):
         c["k"] = args.k
     if args.layers:
         c["L"] = args.layers
+    c["draft"] = tuple(int(x) for x in args.draft_cache.split(",")) if args.draft_cache else None
     if c["mode"] == "greedy":
         c["alpha"] = args.alpha if args.alpha is not None else max(c["alphas"])
     else:
@@ -79,6 +83,9 @@ def workload_params(args):
 
 def describe(c):
     kv = f"{c['L']}x2x{c['B']}x{c['H']}x{c['S']}x{c['D']} {c['kv_dtype']}"
+    if c.get("draft"):
+        Ld, Hd, Dd = c["draft"]
+        kv += f" + draft cache {Ld}x2x{c['B']}x{Hd}x{c['S']}x{Dd} bf16 (one multi-cache realignment)"
     s = f"{c['mode']} round: B={c['B']} k={c['k']} V={c['V']} {c['logit_dtype']} logits"
     s += f", alpha={c['alpha']}" if c["alpha"] is not None else f", draft=target+N(0,{c['noise']})"
     return s + f"; KV {kv}; prompts U{list(c['prompt'])}"
@@ -227,6 +234,10 @@ class Round:
         self.g = torch.Generator(device=device).manual_seed(seed)
         self.rng = np.random.default_rng(seed)
         self.kv = torch.empty((c["L"], 2, B, c["H"], S, c["D"]), dtype=self.kv_dt, device=device)
+        self.draft = None
+        if c.get("draft"):
+            Ld, Hd, Dd = c["draft"]
+            self.draft = torch.empty((Ld, 2, B, Hd, S, Dd), dtype=torch.bfloat16, device=device)
         self.pos = torch.empty((B, S), dtype=torch.int32, device=device)
         self.mask = torch.empty((B, S), dtype=torch.uint8, device=device)
         self.tokens = torch.randint(0, c["V"], (B, S), device=device, dtype=torch.int32, generator=self.g)
@@ -245,6 +256,8 @@ class Round:
         self.pad = torch.from_numpy((W - ln).astype(np.int32)).to(self.dev)
         self.W = W
         self.tg.kv_fill(self.kv, self.tokens, self.pad, self.ln - 1, junk=False)
+        if self.draft is not None:
+            self.tg.kv_fill(self.draft, self.tokens, self.pad, self.ln - 1, junk=False)
         self.sv.spec_rebuild_pos_mask(self.pad, self.pos, self.mask)
 
     def prepare(self):
@@ -262,7 +275,10 @@ class Round:
             self.x, self.q, self.d, self.u = self.tg.sample_round_inputs(B, k, V, c["noise"], self.g, self.lg_dt,
                                                                          self.dev)
         last = torch.gather(self.tokens, 1, (self.ln.long() - 1).unsqueeze(1))
-        self.tg.kv_write_query(self.kv, torch.cat([last, self.d], 1).contiguous(), self.pos, self.W)
+        qtok = torch.cat([last, self.d], 1).contiguous()
+        self.tg.kv_write_query(self.kv, qtok, self.pos, self.W)
+        if self.draft is not None:  # the drafter consumed the last token and proposals 0..k-2
+            self.tg.kv_write_query(self.draft, qtok[:, :-1].contiguous(), self.pos, self.W)
         self.flush.zero_()
 
     def verify(self):
@@ -285,6 +301,8 @@ class Round:
         return b
 
     def realign(self, ne):
+        if self.draft is not None:
+            return self.sv.spec_realign_kv_multi([self.kv, self.draft], self.ln, self.pad, ne, workspace=self.ws)
         return self.sv.spec_realign_kv(self.kv, self.ln, self.pad, ne, workspace=self.ws)
 
     def posmask(self, pad_new):
@@ -299,8 +317,13 @@ class Round:
         return moved_rows, int(n.sum()), (ln0, pad0, n)
 
     def row_bytes_all_slabs(self):
+        """Bytes of one token row over every slab of every realigned cache."""
         c = self.c
-        return c["L"] * 2 * c["H"] * c["D"] * (2 if c["kv_dtype"] == "bf16" else 4)
+        b = c["L"] * 2 * c["H"] * c["D"] * (2 if c["kv_dtype"] == "bf16" else 4)
+        if c.get("draft"):
+            Ld, Hd, Dd = c["draft"]
+            b += Ld * 2 * Hd * Dd * 2
+        return b
 
 
 def run_ours(args, c, rank, local_rank, world):
@@ -488,8 +511,12 @@ def run_e2e(args, R, st, dev, pg, world):
             R.sv.spec_verify_greedy(R.x, R.d, out_tokens=out, n_accept=na, n_emit=ne, workspace=R.ws)
         else:
             R.sv.spec_verify_sample(R.x, R.q, R.d, R.u, out_tokens=out, n_accept=na, n_emit=ne, workspace=R.ws)
-        R.sv.spec_realign_kv(R.kv, R.ln, R.pad, ne, len_new=ln_new, pad_new=pad_new, width_new=width, err=err,
-                             workspace=R.ws)
+        if R.draft is not None:
+            R.sv.spec_realign_kv_multi([R.kv, R.draft], R.ln, R.pad, ne, len_new=ln_new, pad_new=pad_new,
+                                       width_new=width, err=err, workspace=R.ws)
+        else:
+            R.sv.spec_realign_kv(R.kv, R.ln, R.pad, ne, len_new=ln_new, pad_new=pad_new, width_new=width, err=err,
+                                 workspace=R.ws)
         R.sv.spec_rebuild_pos_mask(pad_new, R.pos, R.mask, pad_old=R.pad)
         h_res.copy_(blocks[1 - cur], non_blocking=True)
         e1.record(st)

@@ -74,6 +74,9 @@ enum {
 #define SPEC_REALIGN_EMIT 3     /* a committed count would run past S       */
 #define SPEC_REALIGN_TIMEOUT 4  /* a bounded wait gave up (never expected)  */
 
+/* Most caches one spec_realign_kv_multi call moves. */
+#define SPEC_MAX_CACHES 4
+
 /* Largest k (proposals per sequence) accepted by the verify entry points. */
 #define SPEC_MAX_K 31
 /* Largest pool accepted by spec_group_by_length. */
@@ -168,6 +171,35 @@ SPEC_API int spec_realign_kv(void *kv, spec_dtype dt, int L, int B, int H, int S
                     const int32_t *len, const int32_t *pad, const int32_t *n_emit,
                     int32_t *len_new, int32_t *pad_new, int32_t *width_new, int32_t *err,
                     void *workspace, size_t workspace_bytes, void *cuda_stream);
+
+/* One contiguous left-padded KV cache [L, 2, B, H, S, D] of `dt` elements
+ * (B and S are given to the call; every cache of one call shares them). */
+typedef struct {
+    void *kv;
+    spec_dtype dt;
+    int L, H, D;
+} spec_kv_cache;
+
+/*
+ * The realignment of spec_realign_kv applied to several caches that share the
+ * batch and its slot geometry -- typically the target model's cache and the
+ * draft model's, which both must follow the accepted prefix ("Design Document
+ * -- speculative-decoding-real", "KV Cache Synchronization": the draft cache
+ * is re-synchronised to the accepted prefix by copying the accepted cache
+ * entries).  One plan is computed and one shift launch moves the slabs of
+ * every cache, balanced across them.
+ *
+ * caches [n_caches] (host array, 1 <= n_caches <= SPEC_MAX_CACHES); the other
+ * arguments as in spec_realign_kv.  A draft cache that holds KV for the last
+ * token and proposals 0..k-2 (the draft consumed them while proposing) lacks
+ * the row of proposal k-1; when a sequence accepts all k proposals that row
+ * is moved like the others but holds no computed KV -- the drafter must
+ * recompute it (it re-feeds that token) before reading it.
+ */
+SPEC_API int spec_realign_kv_multi(const spec_kv_cache *caches, int n_caches, int B, int S,
+                          const int32_t *len, const int32_t *pad, const int32_t *n_emit,
+                          int32_t *len_new, int32_t *pad_new, int32_t *width_new, int32_t *err,
+                          void *workspace, size_t workspace_bytes, void *cuda_stream);
 
 /*
  * Position IDs and attention mask recomputed from the new padding ([CF]

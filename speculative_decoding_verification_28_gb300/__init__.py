@@ -22,6 +22,8 @@ from .api import (  # noqa: F401
     Workspace,
     spec_group_by_length,
     spec_realign_kv,
+    spec_realign_kv_multi,
+    MAX_CACHES,
     spec_rebuild_pos_mask,
     spec_verify_greedy,
     spec_verify_greedy_static,

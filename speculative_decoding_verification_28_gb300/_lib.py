@@ -29,6 +29,15 @@ SIGNATURES = {
                                   _i32),
 }
 
+class KVCacheDesc(ctypes.Structure):
+    """spec_kv_cache of include/specverify.h."""
+    _fields_ = [("kv", ctypes.c_void_p), ("dt", ctypes.c_int), ("L", ctypes.c_int), ("H", ctypes.c_int),
+                ("D", ctypes.c_int)]
+
+
+SIGNATURES["spec_realign_kv_multi"] = ([_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
+                                       _i32)
+
 _lib = None
 
 

@@ -211,6 +211,42 @@ def spec_realign_kv(kv, length, pad, n_emit, len_new=None, pad_new=None, width_n
     return len_new, pad_new, width_new, err
 
 
+MAX_CACHES = 4
+
+
+def spec_realign_kv_multi(caches, length, pad, n_emit, len_new=None, pad_new=None, width_new=None, err=None,
+                          workspace=None, stream=None):
+    """Realign several caches [L_c, 2, B, H_c, S, D_c] (e.g. target and draft)
+    by one plan in one shift launch.
+    -> (len_new [B], pad_new [B], width_new [1], err [1]) int32 on the device."""
+    lib = _lib.load()
+    if not 1 <= len(caches) <= MAX_CACHES:
+        raise ValueError(f"1..{MAX_CACHES} caches")
+    dev = caches[0].device
+    B, S = caches[0].shape[2], caches[0].shape[4]
+    descs = (_lib.KVCacheDesc * len(caches))()
+    for i, kv in enumerate(caches):
+        L, two, Bc, H, Sc, D = kv.shape
+        if two != 2 or Bc != B or Sc != S:
+            raise ValueError("every cache must be [L, 2, B, H, S, D] with the same B and S")
+        _need(kv, None, f"caches[{i}]", dev)
+        if kv.dtype not in _DT:
+            raise ValueError(f"unsupported kv dtype {kv.dtype}")
+        descs[i] = _lib.KVCacheDesc(kv.data_ptr(), _DT[kv.dtype], L, H, D)
+    for t, nm in ((length, "len"), (pad, "pad"), (n_emit, "n_emit")):
+        _need(t, torch.int32, nm, dev, (B,))
+    len_new = torch.empty(B, dtype=torch.int32, device=dev) if len_new is None else len_new
+    pad_new = torch.empty(B, dtype=torch.int32, device=dev) if pad_new is None else pad_new
+    width_new = torch.empty(1, dtype=torch.int32, device=dev) if width_new is None else width_new
+    err = torch.empty(1, dtype=torch.int32, device=dev) if err is None else err
+    st = _stream(stream, dev)
+    ws = _workspace(workspace, B, 0, 1, dev, st)
+    _check(lib.spec_realign_kv_multi(ctypes.cast(descs, ctypes.c_void_p), len(caches), B, S, _p(length), _p(pad),
+                                     _p(n_emit), _p(len_new), _p(pad_new), _p(width_new), _p(err), ws.ptr(),
+                                     ws.nbytes, st))
+    return len_new, pad_new, width_new, err
+
+
 def spec_rebuild_pos_mask(pad_new, pos, mask, pad_old=None, stream=None):
     """pos [B, S] int32 and mask [B, S] uint8 rewritten in place from pad_new."""
     lib = _lib.load()

@@ -154,6 +154,55 @@ int spec_verify_sample(const void *target_logits, spec_dtype dt, float temperatu
     return launched(launch_verify_sample(a, dt, (cudaStream_t)cuda_stream));
 }
 
+int spec_realign_kv_multi(const spec_kv_cache *caches, int n_caches, int B, int S, const int32_t *len,
+                          const int32_t *pad, const int32_t *n_emit, int32_t *len_new, int32_t *pad_new,
+                          int32_t *width_new, int32_t *err, void *workspace, size_t workspace_bytes,
+                          void *cuda_stream)
+{
+    if (!caches || n_caches < 1 || n_caches > SPEC_MAX_CACHES || B < 0 || S < 1)
+        return SPEC_EINVAL;
+    for (int c = 0; c < n_caches; ++c) {
+        const spec_kv_cache &kc = caches[c];
+        if (kc.L < 1 || kc.H < 1 || kc.D < 1)
+            return SPEC_EINVAL;
+        if (!dtype_ok(kc.dt))
+            return SPEC_EDTYPE;
+        if ((long long)B * kc.L * 2 * kc.H > INT_MAX)
+            return SPEC_EINVAL;
+    }
+    if (B == 0)
+        return SPEC_OK;
+    if (!len || !pad || !n_emit || !len_new || !pad_new || !width_new || !err)
+        return SPEC_EINVAL;
+    for (int c = 0; c < n_caches; ++c)
+        if (!caches[c].kv)
+            return SPEC_EINVAL;
+    for (int c = 0; c < n_caches; ++c)
+        if (!aligned(caches[c].kv, dtype_bytes(caches[c].dt)))
+            return SPEC_EALIGN;
+    if (!aligned(len, 4) || !aligned(pad, 4) || !aligned(n_emit, 4) || !aligned(len_new, 4) || !aligned(pad_new, 4) ||
+        !aligned(width_new, 4) || !aligned(err, 4))
+        return SPEC_EALIGN;
+    const int rc = check_workspace(workspace, workspace_bytes, spec_workspace_bytes(B, 0, 1));
+    if (rc != SPEC_OK)
+        return rc;
+    RealignArgs a{};
+    for (int c = 0; c < n_caches; ++c)
+        a.cache[c] = CacheDesc{caches[c].kv, dtype_bytes(caches[c].dt), caches[c].L, caches[c].H, caches[c].D};
+    a.n_caches = n_caches;
+    a.B = B;
+    a.S = S;
+    a.len = len;
+    a.pad = pad;
+    a.n_emit = n_emit;
+    a.len_new = len_new;
+    a.pad_new = pad_new;
+    a.width_new = width_new;
+    a.err = err;
+    a.ws = workspace;
+    return launched(launch_realign(a, (cudaStream_t)cuda_stream));
+}
+
 int spec_realign_kv(void *kv, spec_dtype dt, int L, int B, int H, int S, int D, const int32_t *len,
                     const int32_t *pad, const int32_t *n_emit, int32_t *len_new, int32_t *pad_new,
                     int32_t *width_new, int32_t *err, void *workspace, size_t workspace_bytes, void *cuda_stream)
@@ -164,33 +213,11 @@ int spec_realign_kv(void *kv, spec_dtype dt, int L, int B, int H, int S, int D, 
         return SPEC_EDTYPE;
     if (B == 0)
         return SPEC_OK;
-    if (!kv || !len || !pad || !n_emit || !len_new || !pad_new || !width_new || !err)
+    if (!kv)
         return SPEC_EINVAL;
-    if ((long long)B * L * 2 * H > INT_MAX)
-        return SPEC_EINVAL;
-    if (!aligned(kv, dtype_bytes(dt)) || !aligned(len, 4) || !aligned(pad, 4) || !aligned(n_emit, 4) ||
-        !aligned(len_new, 4) || !aligned(pad_new, 4) || !aligned(width_new, 4) || !aligned(err, 4))
-        return SPEC_EALIGN;
-    const int rc = check_workspace(workspace, workspace_bytes, spec_workspace_bytes(B, 0, 1));
-    if (rc != SPEC_OK)
-        return rc;
-    RealignArgs a{};
-    a.kv = kv;
-    a.elt_bytes = dtype_bytes(dt);
-    a.L = L;
-    a.B = B;
-    a.H = H;
-    a.S = S;
-    a.D = D;
-    a.len = len;
-    a.pad = pad;
-    a.n_emit = n_emit;
-    a.len_new = len_new;
-    a.pad_new = pad_new;
-    a.width_new = width_new;
-    a.err = err;
-    a.ws = workspace;
-    return launched(launch_realign(a, (cudaStream_t)cuda_stream));
+    const spec_kv_cache one = {kv, dt, L, H, D};
+    return spec_realign_kv_multi(&one, 1, B, S, len, pad, n_emit, len_new, pad_new, width_new, err, workspace,
+                                 workspace_bytes, cuda_stream);
 }
 
 int spec_rebuild_pos_mask(int B, int S, const int32_t *pad_old, const int32_t *pad_new, int32_t *pos,

@@ -224,10 +224,11 @@ __global__ void __launch_bounds__(32) kv_shift_bulk_kernel(RealignArgs a)
     const int n_moving = pv.misc[MISC_NMOVING];
     if (n_moving <= 0)
         return;
-    const int sps = a.L * 2 * a.H;  // slabs per sequence
-    const long long n_items = (long long)n_moving * sps;
-    const long long row_bytes = (long long)a.D * a.elt_bytes;
-    const long long slab_bytes = row_bytes * a.S;
+    // work items: the moving slabs of every bulk cache, cache after cache
+    long long n_items = 0;
+    for (int c = 0; c < a.n_caches; ++c)
+        if (a.bulk_mask & (1u << c))
+            n_items += (long long)n_moving * a.cache[c].L * 2 * a.cache[c].H;
 
     for (int s = 0; s < kStages; ++s)
         mbar_init(&full[s], 1);
@@ -239,12 +240,25 @@ __global__ void __launch_bounds__(32) kv_shift_bulk_kernel(RealignArgs a)
     auto open_item = [&](long long it) -> bool {
         if (it >= n_items)
             return false;
+        int c = 0;
+        for (; c < a.n_caches; ++c) {
+            if (!(a.bulk_mask & (1u << c)))
+                continue;
+            const long long cnt = (long long)n_moving * a.cache[c].L * 2 * a.cache[c].H;
+            if (it < cnt)
+                break;
+            it -= cnt;
+        }
+        const CacheDesc &cd = a.cache[c];
+        const int sps = cd.L * 2 * cd.H;  // slabs per sequence
+        const long long row_bytes = (long long)cd.D * cd.elt_bytes;
+        const long long slab_bytes = row_bytes * a.S;
         const int r = (int)(it / sps), within = (int)(it % sps);
         const int b = pv.order[r];
-        const int h = within % a.H, lc = within / a.H;  // lc = l * 2 + c
-        const long long slab = ((long long)lc * a.B + b) * a.H + h;
+        const int h = within % cd.H, lc = within / cd.H;  // lc = l * 2 + k/v
+        const long long slab = ((long long)lc * a.B + b) * cd.H + h;
         const int d = pv.delta[b];
-        g.slab = reinterpret_cast<char *>(a.kv) + slab * slab_bytes;
+        g.slab = reinterpret_cast<char *>(cd.kv) + slab * slab_bytes;
         g.src = (long long)pv.src_pad[b] * row_bytes;
         g.dst = (long long)(pv.src_pad[b] + d) * row_bytes;
         g.nbytes = (long long)pv.run[b] * row_bytes;
@@ -322,19 +336,20 @@ __global__ void __launch_bounds__(256) kv_shift_plain_kernel(RealignArgs a)
     dep_release();
     const PlanView pv = plan_view(a.ws, a.B);
     const int n_moving = pv.misc[MISC_NMOVING];
-    const int sps = a.L * 2 * a.H;
+    const CacheDesc &cd = a.cache[a.plain_cache];
+    const int sps = cd.L * 2 * cd.H;
     const long long it = blockIdx.x;
     if (it >= (long long)n_moving * sps)
         return;
     const int r = (int)(it / sps), within = (int)(it % sps);
     const int b = pv.order[r];
-    const int h = within % a.H, lc = within / a.H;
-    const long long slab = ((long long)lc * a.B + b) * a.H + h;
-    E *base = reinterpret_cast<E *>(a.kv) + slab * (long long)a.S * a.D;
+    const int h = within % cd.H, lc = within / cd.H;
+    const long long slab = ((long long)lc * a.B + b) * cd.H + h;
+    E *base = reinterpret_cast<E *>(cd.kv) + slab * (long long)a.S * cd.D;
     const int d = pv.delta[b];
-    const long long n = (long long)pv.run[b] * a.D;
-    E *src = base + (long long)pv.src_pad[b] * a.D;
-    E *dst = src + (long long)d * a.D;
+    const long long n = (long long)pv.run[b] * cd.D;
+    E *src = base + (long long)pv.src_pad[b] * cd.D;
+    E *dst = src + (long long)d * cd.D;
     constexpr int kPer = 4, kT = 256 * kPer;
     for (long long done = 0; done < n; done += kT) {
         const long long take = (n - done) < kT ? (n - done) : kT;
@@ -387,9 +402,14 @@ cudaError_t launch_realign(const RealignArgs &a, cudaStream_t st)
     cfg.stream = st;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    const long long row_bytes = (long long)a.D * a.elt_bytes;
-    const bool bulk = (row_bytes % 16 == 0) && (reinterpret_cast<uintptr_t>(a.kv) % 16 == 0);
-    if (bulk) {
+    RealignArgs la = a;
+    la.bulk_mask = 0;
+    for (int c = 0; c < a.n_caches; ++c) {
+        const long long row_bytes = (long long)a.cache[c].D * a.cache[c].elt_bytes;
+        if (row_bytes % 16 == 0 && reinterpret_cast<uintptr_t>(a.cache[c].kv) % 16 == 0)
+            la.bulk_mask |= 1u << c;
+    }
+    if (la.bulk_mask) {
         if (!g_smem_set[slot]) {
             e = cudaFuncSetAttribute(kv_shift_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kShiftSmem);
@@ -400,16 +420,26 @@ cudaError_t launch_realign(const RealignArgs &a, cudaStream_t st)
         cfg.gridDim = dim3(g_sm_count[slot]);
         cfg.blockDim = dim3(32);
         cfg.dynamicSmemBytes = kShiftSmem;
-        e = cudaLaunchKernelEx(&cfg, kv_shift_bulk_kernel, a);
-    } else {
-        const long long blocks = (long long)a.B * a.L * 2 * a.H;
+        e = cudaLaunchKernelEx(&cfg, kv_shift_bulk_kernel, la);
+        if (e != cudaSuccess)
+            return e;
+    }
+    // caches whose rows are not 16-byte multiples (or that are unaligned)
+    for (int c = 0; c < a.n_caches; ++c) {
+        if (la.bulk_mask & (1u << c))
+            continue;
+        RealignArgs pa = la;
+        pa.plain_cache = c;
+        const long long blocks = (long long)a.B * a.cache[c].L * 2 * a.cache[c].H;
         cfg.gridDim = dim3((unsigned)blocks);
         cfg.blockDim = dim3(256);
         cfg.dynamicSmemBytes = 0;
-        if (a.elt_bytes == 4)
-            e = cudaLaunchKernelEx(&cfg, kv_shift_plain_kernel<uint32_t>, a);
+        if (a.cache[c].elt_bytes == 4)
+            e = cudaLaunchKernelEx(&cfg, kv_shift_plain_kernel<uint32_t>, pa);
         else
-            e = cudaLaunchKernelEx(&cfg, kv_shift_plain_kernel<uint16_t>, a);
+            e = cudaLaunchKernelEx(&cfg, kv_shift_plain_kernel<uint16_t>, pa);
+        if (e != cudaSuccess)
+            return e;
     }
     return e != cudaSuccess ? e : cudaGetLastError();
 }

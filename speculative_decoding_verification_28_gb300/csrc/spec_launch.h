@@ -42,12 +42,21 @@ void resolve_verify_args(VerifyArgs &a);
 cudaError_t launch_verify_greedy(const VerifyArgs &a, spec_dtype dt, cudaStream_t st);
 cudaError_t launch_verify_sample(const VerifyArgs &a, spec_dtype dt, cudaStream_t st);
 
-struct RealignArgs {
+// one KV cache [L, 2, B, H, S, D] moved by a realignment plan
+struct CacheDesc {
     void *kv;
-    int elt_bytes, L, B, H, S, D;
+    int elt_bytes, L, H, D;
+};
+
+struct RealignArgs {
+    CacheDesc cache[SPEC_MAX_CACHES];
+    int n_caches;
+    int B, S;
     const int32_t *len, *pad, *n_emit;
     int32_t *len_new, *pad_new, *width_new, *err;
     void *ws;
+    unsigned bulk_mask;  // caches moved by the bulk-copy kernel (set by the launcher)
+    int plain_cache;     // the cache a plain-path launch moves (set by the launcher)
 };
 cudaError_t launch_realign(const RealignArgs &a, cudaStream_t st);
 

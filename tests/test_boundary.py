@@ -156,3 +156,24 @@ def test_static_entry_point_rejects_oversized_batches_before_any_launch(lib):
     assert lib.spec_verify_greedy_static(FAKE, 1, 0, k, V, FAKE, None, -1, None, FAKE, FAKE, FAKE, None) == 0
     # the benchmark's largest workload fits
     assert lib.spec_workspace_bytes(256, 8, 128256) <= STATIC_SCRATCH_BYTES
+
+
+def test_multi_cache_argument_errors(lib):
+    from speculative_decoding_verification_28_gb300._lib import KVCacheDesc
+
+    def multi(descs, n=None, B=3, S=64, ws=FAKE):
+        arr = (KVCacheDesc * max(1, len(descs)))(*descs)
+        return lib.spec_realign_kv_multi(ctypes.cast(arr, ctypes.c_void_p), len(descs) if n is None else n, B, S,
+                                         FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, 1 << 20, None)
+
+    good = KVCacheDesc(0x10000, 1, 2, 4, 128)
+    assert multi([good], n=0) == -1
+    assert multi([good] * 5) == -1  # above SPEC_MAX_CACHES
+    assert multi([good, KVCacheDesc(0x10000, 9, 2, 4, 128)]) == -2
+    assert multi([good, KVCacheDesc(0x10000, 1, 0, 4, 128)]) == -1
+    assert multi([good, KVCacheDesc(None, 1, 2, 4, 128)]) == -1
+    assert multi([good, KVCacheDesc(0x10001, 1, 2, 4, 128)]) == -5
+    assert multi([good], B=0) == 0
+    assert multi([good], ws=None) == -3
+    assert lib.spec_realign_kv_multi(None, 1, 3, 64, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20,
+                                     None) == -1

@@ -232,3 +232,83 @@ def test_pos_mask(S, offset):
     mask.fill_(9)
     sv.spec_rebuild_pos_mask(to_dev(pad_new), pos, mask)
     assert np.array_equal(pos.cpu().numpy(), p1) and np.array_equal(mask.cpu().numpy(), m1)
+
+
+# -- several caches by one plan (target + draft) ----------------------------------
+
+def test_multi_cache_matches_oracle_per_cache():
+    """Target (bf16, 16-byte rows: bulk path), draft (fp16, 128-byte rows) and an
+    odd cache (fp32, 12-byte rows: plain path) moved by one plan, several
+    chained rounds; each buffer bit-exact against the oracle's realignment."""
+    rng = np.random.default_rng(31)
+    B, S, k = 6, 200, 5
+    shapes = [(2, 4, 128, np.float16), (1, 3, 64, np.float16), (2, 2, 3, np.float32)]
+    host = [rng.standard_normal((L, 2, B, H, S, D)).astype(dt) for L, H, D, dt in shapes]
+    dev_t = [torch.from_numpy(h.copy()).to(dev()) for h in host]
+    dev_t[0] = dev_t[0].view(torch.bfloat16)  # bf16 storage of the same bytes
+    ln, pad = random_state(B, S, k, 1, 60, seed=31)
+    for r in range(10):
+        W = int(ln[0] + pad[0])
+        if W + k + 2 > S:
+            break
+        n = rng.integers(0, k + 2, size=B).astype(np.int32)
+        ln2, pd2, w2, err = sv.spec_realign_kv_multi(dev_t, to_dev(ln), to_dev(pad), to_dev(n))
+        assert int(err.item()) == 0
+        for h in host:
+            st, o_ln, o_pd, o_w = oracle.realign_kv(h.view(np.uint16) if h.dtype == np.float16 else h, ln, pad, n)
+            assert st == 0
+        assert np.array_equal(ln2.cpu().numpy(), o_ln) and np.array_equal(pd2.cpu().numpy(), o_pd)
+        assert int(w2.item()) == o_w
+        assert np.array_equal(dev_t[0].view(torch.int16).cpu().numpy().view(np.float16), host[0])
+        assert np.array_equal(dev_t[1].cpu().numpy(), host[1])
+        assert np.array_equal(dev_t[2].cpu().numpy(), host[2])
+        ln, pad = o_ln, o_pd
+
+
+def test_draft_cache_follows_the_accepted_prefix():
+    """The draft cache holds KV for the last token and proposals 0..k-2 (what
+    the drafter consumed); after the shared realignment every position below
+    len' - 1 holds the draft's entry for the committed history, except the
+    row of proposal k-1 when all k proposals were accepted, which the drafter
+    never computed."""
+    from specgen import kv_row_values
+
+    rng = np.random.default_rng(5)
+    B, S, k, L, H, D = 5, 64, 4, 1, 2, 8
+    lens = np.array([9, 4, 12, 7, 12], np.int32)
+    W = int(lens.max())
+    pad = (W - lens).astype(np.int32)
+    toks = [list(rng.integers(0, 99, size=lens[b])) for b in range(B)]
+    props = rng.integers(0, 99, size=(B, k))
+    DRAFT = 1000  # the draft's KV values: f of a shifted sequence id
+    kv_t = np.zeros((L, 2, B, H, S, D), np.float32)
+    kv_d = np.full((L, 2, B, H, S, D), 7.0, np.float32)  # 7.0: never written by the drafter
+    for b in range(B):
+        for p in range(lens[b] - 1):
+            kv_t[:, :, b, :, pad[b] + p, :] = kv_row_values(b, toks[b][p], p, L, H, D)
+            kv_d[:, :, b, :, pad[b] + p, :] = kv_row_values(DRAFT + b, toks[b][p], p, L, H, D)
+        q = [toks[b][-1]] + list(props[b])
+        for j, t in enumerate(q):
+            kv_t[:, :, b, :, W - 1 + j, :] = kv_row_values(b, int(t), lens[b] - 1 + j, L, H, D)
+            if j < k:  # the drafter consumed the last token and proposals 0..k-2
+                kv_d[:, :, b, :, W - 1 + j, :] = kv_row_values(DRAFT + b, int(t), lens[b] - 1 + j, L, H, D)
+    n = np.array([k + 1, 1, 3, k + 1, 0], np.int32)
+    t_dev, d_dev = torch.from_numpy(kv_t).to(dev()), torch.from_numpy(kv_d).to(dev())
+    ln2, pd2, w2, err = sv.spec_realign_kv_multi([t_dev, d_dev], to_dev(lens), to_dev(pad), to_dev(n))
+    assert int(err.item()) == 0
+    ln2, pd2 = ln2.cpu().numpy(), pd2.cpu().numpy()
+    got_d = d_dev.cpu().numpy()
+    for b in range(B):
+        hist = list(toks[b]) + list(props[b][: max(n[b] - 1, 0)])
+        for p in range(ln2[b] - 1):
+            row = got_d[:, :, b, :, pd2[b] + p, :]
+            if n[b] == k + 1 and p == lens[b] - 1 + k:
+                assert (row == 7.0).all()  # proposal k-1: no draft KV yet
+            else:
+                assert np.array_equal(row, kv_row_values(DRAFT + b, int(hist[p]), p, L, H, D)), (b, p)
+    # and the target cache satisfies I2 everywhere
+    got_t = t_dev.cpu().numpy()
+    for b in range(B):
+        hist = list(toks[b]) + list(props[b][: max(n[b] - 1, 0)])
+        for p in range(ln2[b] - 1):
+            assert np.array_equal(got_t[:, :, b, :, pd2[b] + p, :], kv_row_values(b, int(hist[p]), p, L, H, D))
