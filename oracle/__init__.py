@@ -15,6 +15,9 @@ from .core import (  # noqa: F401
     DT_F32,
     MUTANTS,
     build,
+    commit_ragged,
+    repad_gather,
+    unpad_scatter,
     group_by_length,
     mutant,
     realign_kv,

@@ -68,6 +68,12 @@ def _load():
             lib.oracle_realign_kv.restype = i32
             lib.oracle_rebuild_pos_mask.argtypes = [i32, i32, vp, vp, vp]
             lib.oracle_group_by_length.argtypes = [i32, vp, vp, i32, vp, vp, vp]
+            lib.oracle_commit_ragged.argtypes = [i32, vp, i32, vp, vp, i32]
+            lib.oracle_commit_ragged.restype = i32
+            lib.oracle_repad_gather.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp]
+            lib.oracle_repad_gather.restype = i32
+            lib.oracle_unpad_scatter.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp]
+            lib.oracle_unpad_scatter.restype = i32
             _lib = lib
     return _lib
 
@@ -210,3 +216,38 @@ def group_by_length(length, B, active=None):
     gl = np.zeros(1, np.int32)
     lib.oracle_group_by_length(ln.shape[0], _ptr(ln), _ptr(act), B, _ptr(idx), _ptr(ce), _ptr(gl))
     return idx, int(ce[0]), int(gl[0])
+
+
+def commit_ragged(pool_len, idx, n_emit, S):
+    """In place on pool_len [N]; -> status."""
+    lib = _load()
+    assert pool_len.dtype == np.int32 and pool_len.flags.c_contiguous
+    ix, ne = _c(idx, np.int32), _c(n_emit, np.int32)
+    return lib.oracle_commit_ragged(pool_len.shape[0], _ptr(pool_len), ix.shape[0], _ptr(ix), _ptr(ne), int(S))
+
+
+def repad_gather(pool, batch, idx, pool_len):
+    """pool [L,2,N,H,S,D] -> batch [L,2,B,H,S,D] in place.
+    -> (status, len [B], pad [B], width)."""
+    lib = _load()
+    L, _, N, H, S, D = pool.shape
+    B = batch.shape[2]
+    assert batch.dtype.itemsize == pool.dtype.itemsize and batch.flags.c_contiguous
+    ix, pl = _c(idx, np.int32), _c(pool_len, np.int32)
+    ln = np.zeros(B, np.int32)
+    pd = np.zeros(B, np.int32)
+    w = np.zeros(1, np.int32)
+    st = lib.oracle_repad_gather(_ptr(pool), _ptr(batch), pool.dtype.itemsize, L, N, B, H, S, D, _ptr(ix), _ptr(pl),
+                                 _ptr(ln), _ptr(pd), _ptr(w))
+    return st, ln, pd, int(w[0])
+
+
+def unpad_scatter(batch, pool, idx, length, pad, pool_len):
+    """batch -> pool in place; pool_len [N] updated in place. -> status."""
+    lib = _load()
+    L, _, N, H, S, D = pool.shape
+    B = batch.shape[2]
+    assert pool.flags.c_contiguous and pool_len.dtype == np.int32
+    ix, ln, pd = _c(idx, np.int32), _c(length, np.int32), _c(pad, np.int32)
+    return lib.oracle_unpad_scatter(_ptr(batch), _ptr(pool), pool.dtype.itemsize, L, N, B, H, S, D, _ptr(ix),
+                                    _ptr(ln), _ptr(pd), _ptr(pool_len))

@@ -556,3 +556,107 @@ void oracle_group_by_length(int N, const int32_t *len, const uint8_t *active, in
     }
     free(taken);
 }
+
+/* ------------------------------------------------------------------ */
+/* O7  ragged pool (EXSPEC) -- repad, unpad, commit                        */
+/* ------------------------------------------------------------------ */
+
+/*
+ * EXSPEC keeps sequences ragged ([CF] §3.2): here a pool cache
+ * pool[L, 2, N, H, S, D] holds sequence n left-aligned at slot 0, positions
+ * 0 .. pool_len[n] - 2 with KV (the last token has none).  Position = slot, so
+ * rectangular alignment is never needed for a group of equal lengths, and a
+ * round's rejected proposals need no movement: their rows lie past the new
+ * length (the "rollback of rejected tokens" of variable-length layouts, [CF]
+ * §2, is the length update).  When no same-length group forms, EXSPEC falls
+ * back to unpad-append-repad ([CF] §3.2): the chosen sequences are repadded
+ * into a contiguous left-padded batch, realigned there round by round, and
+ * unpadded back into the pool.
+ */
+
+/* pool_len[idx[b]] += n_emit[b].  Returns 0, 2 for a bad or repeated index
+   (or a negative count), 1 when a length would exceed S; nothing changes
+   unless it returns 0. */
+int oracle_commit_ragged(int N, int32_t *pool_len, int B, const int32_t *idx, const int32_t *n_emit, int S)
+{
+    for (int b = 0; b < B; ++b) {
+        if (idx[b] < 0 || idx[b] >= N || n_emit[b] < 0)
+            return 2;
+        for (int c = 0; c < b; ++c)
+            if (idx[c] == idx[b])
+                return 2;
+    }
+    for (int b = 0; b < B; ++b)
+        if ((int64_t)pool_len[idx[b]] + n_emit[b] > S)
+            return 1;
+    for (int b = 0; b < B; ++b)
+        pool_len[idx[b]] += n_emit[b];
+    return 0;
+}
+
+/* Repad: batch slab (l, c, b, h) receives the pool slab (l, c, idx[b], h)'s
+   rows 0 .. pool_len[idx[b]] - 2 at slot pad_b = W - pool_len[idx[b]], with
+   W = max_b pool_len[idx[b]]; no other batch byte changes.  Outputs the
+   batch lengths, paddings and width.  Returns 0, or 2 for a bad or repeated
+   index or a length < 1 (nothing written). */
+int oracle_repad_gather(const void *pool, void *batch, int elt_bytes, int L, int N, int B, int H, int S, int D,
+                        const int32_t *idx, const int32_t *pool_len, int32_t *len_out, int32_t *pad_out,
+                        int32_t *width_out)
+{
+    int64_t W = 0;
+    for (int b = 0; b < B; ++b) {
+        if (idx[b] < 0 || idx[b] >= N || pool_len[idx[b]] < 1 || pool_len[idx[b]] > S)
+            return 2;
+        for (int c = 0; c < b; ++c)
+            if (idx[c] == idx[b])
+                return 2;
+        if (pool_len[idx[b]] > W)
+            W = pool_len[idx[b]];
+    }
+    const int64_t row = (int64_t)D * elt_bytes, slab = row * S;
+    for (int l = 0; l < L; ++l)
+        for (int c = 0; c < 2; ++c)
+            for (int b = 0; b < B; ++b)
+                for (int h = 0; h < H; ++h) {
+                    const int n = idx[b];
+                    const int64_t len = pool_len[n], pad = W - len;
+                    const uint8_t *src = (const uint8_t *)pool + ((((int64_t)l * 2 + c) * N + n) * H + h) * slab;
+                    uint8_t *dst = (uint8_t *)batch + ((((int64_t)l * 2 + c) * B + b) * H + h) * slab;
+                    memcpy(dst + pad * row, src, (size_t)((len - 1) * row));
+                }
+    for (int b = 0; b < B; ++b) {
+        len_out[b] = pool_len[idx[b]];
+        pad_out[b] = (int32_t)(W - pool_len[idx[b]]);
+    }
+    *width_out = (int32_t)W;
+    return 0;
+}
+
+/* Unpad: the batch slab (l, c, b, h)'s rows pad[b] .. pad[b] + len[b] - 2 go
+   back to slot 0 of the pool slab (l, c, idx[b], h), and pool_len[idx[b]] =
+   len[b]; no other pool byte changes.  Returns 0, or 2 for a bad or repeated
+   index, a length < 1 or a run past S (nothing written). */
+int oracle_unpad_scatter(const void *batch, void *pool, int elt_bytes, int L, int N, int B, int H, int S, int D,
+                         const int32_t *idx, const int32_t *len, const int32_t *pad, int32_t *pool_len)
+{
+    for (int b = 0; b < B; ++b) {
+        if (idx[b] < 0 || idx[b] >= N || len[b] < 1 || pad[b] < 0 || (int64_t)pad[b] + len[b] - 1 > S)
+            return 2;
+        for (int c = 0; c < b; ++c)
+            if (idx[c] == idx[b])
+                return 2;
+    }
+    const int64_t row = (int64_t)D * elt_bytes, slab = row * S;
+    for (int l = 0; l < L; ++l)
+        for (int c = 0; c < 2; ++c)
+            for (int b = 0; b < B; ++b)
+                for (int h = 0; h < H; ++h) {
+                    const int n = idx[b];
+                    const uint8_t *src = (const uint8_t *)batch + ((((int64_t)l * 2 + c) * B + b) * H + h) * slab;
+                    uint8_t *dst = (uint8_t *)pool + ((((int64_t)l * 2 + c) * N + n) * H + h) * slab;
+                    memcpy(dst, src + (int64_t)pad[b] * row, (size_t)(((int64_t)len[b] - 1) * row));
+                }
+    for (int b = 0; b < B; ++b)
+        pool_len[idx[b]] = len[b];
+    return 0;
+}

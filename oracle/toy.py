@@ -129,6 +129,10 @@ class ToyPair:
         """The forward's KV write for one query slot at that slot's position ID."""
         kv[:, :, b, :, slot, :] = self.kv_rows(b, int(tok), int(pos[b, slot]))
 
+    def write_query_kv_seq(self, kv, pos, b, seq, slot, tok):
+        """As write_query_kv for batch row b holding pool sequence `seq`."""
+        kv[:, :, b, :, slot, :] = self.kv_rows(seq, int(tok), int(pos[b, slot]))
+
     def batched_logits(self, kv, pos, mask, b, q_slot0, n_rows):
         """Logits of query slots q_slot0 .. q_slot0 + n_rows - 1 of sequence b,
         folding every visible slot of the cache in slot order."""
@@ -199,3 +203,94 @@ def run_batch_spec(pair: ToyPair, prompts, n_new, k, S, verify, realign, posmask
         posmask(S, pad2, pad, pos, mask)
         ln, pad = ln2.astype(np.int32), pad2.astype(np.int32)
     return gen
+
+
+def exspec_select(lens, active, window, B, group):
+    """The cross-batch selection: the first `window` active sequences in pool
+    order form the window; `group(window_lens, B)` returns (idx into the
+    window, count_equal, L*).  Returns pool indices (-1 dropped) and whether a
+    full same-length group formed.  (The pages give no algorithm for EXSPEC's
+    scheduler; this policy is this project's construction.)"""
+    win = [n for n in range(len(lens)) if active[n]][:window]
+    if not win:
+        return [], False
+    idx, ce, _ = group(np.array([lens[n] for n in win], np.int32), B)
+    picks = [win[i] for i in idx if i >= 0]
+    return picks, ce == B and len(picks) == B
+
+
+def run_exspec(pair: ToyPair, prompts, n_new, k, S, B, window, ops, eos_id=-1, max_rounds=2000):
+    """EXSPEC-style decoding of the toy pair over a ragged pool: each round the
+    window's largest same-length group is verified in place (grouped round, no
+    realignment: the commit is a length update); when no full group forms the
+    chosen sequences are repadded into a batch, verified and realigned there,
+    and unpadded back (fallback round).
+
+    ops: dict of callables
+      group(lens, B) -> (idx, count_equal, L*)
+      verify(logits, draft, remaining, eos) -> (out_tokens, n_accept, n_emit)
+      commit(pool_len, idx, n_emit, S) -> status            (pool_len in place)
+      repad(pool, batch, idx, pool_len) -> (status, len, pad, width)
+      realign(kv, len, pad, n_emit) -> (status, len_new, pad_new, width)
+      unpad(batch, pool, idx, len, pad, pool_len) -> status  (pool_len in place)
+    Returns (generated tokens per sequence, rounds, grouped rounds)."""
+    N = len(prompts)
+    L, H, D = pair.L, pair.H, pair.D
+    pool = np.zeros((L, 2, N, H, S, D), np.float32)
+    pool_len = np.array([len(p) for p in prompts], np.int32)
+    hist = [list(p) for p in prompts]
+    for n in range(N):
+        for p in range(len(prompts[n]) - 1):
+            pool[:, :, n, :, p, :] = pair.kv_rows(n, prompts[n][p], p)
+    pool_pos = np.broadcast_to(np.arange(S, dtype=np.int32), (N, S)).copy()
+    pool_mask = np.ones((N, S), np.uint8)
+    gen = [[] for _ in range(N)]
+    active = np.ones(N, bool)
+    rounds = grouped = 0
+    for _ in range(max_rounds):
+        if not active.any():
+            break
+        picks, full = exspec_select(pool_len, active, window, B, ops["group"])
+        Bb = len(picks)
+        rounds += 1
+        draft = np.zeros((Bb, k), np.int32)
+        logits = np.zeros((Bb, k + 1, pair.V), np.float32)
+        remaining = np.array([n_new - len(gen[n]) for n in picks], np.int32)
+        if full:
+            grouped += 1
+            for i, n in enumerate(picks):  # forward on the pool: position = slot
+                props = pair.propose(n, hist[n], k)
+                draft[i] = props
+                q0 = int(pool_len[n]) - 1
+                assert q0 + k < S, "toy pool too small"
+                for j, t in enumerate([hist[n][-1]] + props):
+                    pair.write_query_kv(pool, pool_pos, n, q0 + j, t)
+                logits[i] = pair.batched_logits(pool, pool_pos, pool_mask, n, q0, k + 1)
+            out, _, ne = ops["verify"](logits, draft, remaining, eos_id)
+            assert ops["commit"](pool_len, np.array(picks, np.int32), ne, S) == 0
+        else:
+            batch = np.zeros((L, 2, Bb, H, S, D), np.float32)
+            st, ln, pad, W = ops["repad"](pool, batch, np.array(picks, np.int32), pool_len)
+            assert st == 0 and W + k < S
+            pos = np.zeros((Bb, S), np.int32)
+            mask = np.zeros((Bb, S), np.uint8)
+            for i in range(Bb):
+                mask[i, pad[i]:] = 1
+                pos[i, pad[i]:] = np.arange(S - pad[i])
+            for i, n in enumerate(picks):
+                props = pair.propose(n, hist[n], k)
+                draft[i] = props
+                for j, t in enumerate([hist[n][-1]] + props):
+                    pair.write_query_kv_seq(batch, pos, i, n, W - 1 + j, t)
+                logits[i] = pair.batched_logits(batch, pos, mask, i, W - 1, k + 1)
+            out, _, ne = ops["verify"](logits, draft, remaining, eos_id)
+            st, ln2, pad2, _ = ops["realign"](batch, ln, pad, ne)
+            assert st == 0
+            assert ops["unpad"](batch, pool, np.array(picks, np.int32), ln2, pad2, pool_len) == 0
+        for i, n in enumerate(picks):
+            toks = [int(t) for t in out[i, : ne[i]]]
+            gen[n] += toks
+            hist[n] += toks
+            if len(gen[n]) >= n_new or (eos_id >= 0 and eos_id in toks):
+                active[n] = False
+    return gen, rounds, grouped
