@@ -35,6 +35,7 @@ WORKLOADS = {
     "c4": dict(cfg="c4", mode="greedy"),
     "c5": dict(cfg="c5", mode="greedy"),
     "c5s": dict(cfg="c5", mode="sample"),
+    "c4x": dict(cfg="c4", mode="exspec"),  # same-length grouping over the 512-sequence pool
 }
 
 
@@ -55,6 +56,9 @@ def parse():
     ap.add_argument("--draft-cache", default=None,
                     help="L,H,D of a draft model's cache realigned with the target's in one call, "
                          "e.g. 2,12,64 (a 68M-class drafter)")
+    ap.add_argument("--pool-lengths", choices=["a", "b"], default="a",
+                    help="c4x pool lengths: a = U[128,1024] (as configured), b = uniform over {128, 256, ..., 1024}")
+    ap.add_argument("--window", type=int, default=None, help="c4x: sliding window (default: the whole pool)")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the cache's layer count (small profiling captures only)")
     return ap.parse_args()
@@ -66,7 +70,7 @@ def workload_params(args):
     w = WORKLOADS[args.workload]
     c = dict(CONFIGS[w["cfg"]])
     c["mode"] = w["mode"]
-    if args.workload == "c4":
+    if args.workload in ("c4", "c4x"):
         c["k"] = args.k or 8
         c["prompt"] = c["pool_len"]
     if args.k:
@@ -74,7 +78,7 @@ def workload_params(args):
     if args.layers:
         c["L"] = args.layers
     c["draft"] = tuple(int(x) for x in args.draft_cache.split(",")) if args.draft_cache else None
-    if c["mode"] == "greedy":
+    if c["mode"] in ("greedy", "exspec"):
         c["alpha"] = args.alpha if args.alpha is not None else max(c["alphas"])
     else:
         c["alpha"] = None
@@ -611,12 +615,177 @@ def run_reference(args, c):
             "e2e": {"value": round(v, 4), "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_exspec_bench(args, c, rank, local_rank, world):
+    """EXSPEC rounds over a ragged pool: each round the largest same-length
+    group in the window is verified in place (grouped round: verify + commit,
+    no KV moves), or the chosen sequences take the unpad-append-repad
+    fallback (repad, verify, realign, pos/mask, unpad).  Timed: the library
+    calls only -- the selection, then the round -- with the synthetic target
+    forward between them untimed and an L2 flush before each timed part."""
+    import torch
+
+    import speculative_decoding_verification_28_gb300 as sv
+    from speculative_decoding_verification_28_gb300.exspec import ExspecScheduler
+    from specgen import torch_gen
+
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    pg = world > 1
+    if pg:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    st = torch.cuda.current_stream(dev)
+    seed = rank_seed(args.seed, rank)
+    g = torch.Generator(device=dev).manual_seed(seed)
+    rng = np.random.default_rng(seed)
+    N, B, k, V = c["N"], c["B"], c["k"], c["V"]
+    L, H, S, D = c["L"], c["H"], c["S"], c["D"]
+    lo, hi = c["pool_len"]
+    lens = (rng.integers(lo, hi + 1, size=N) if args.pool_lengths == "a"
+            else 128 * rng.integers(1, 9, size=N)).astype(np.int32)
+    pool = torch.empty((L, 2, N, H, S, D), dtype=torch.bfloat16, device=dev)
+    pool_len = torch.from_numpy(lens).to(dev)
+    tokens = torch.randint(0, V, (N, S), device=dev, dtype=torch.int32, generator=g)
+    torch_gen.kv_fill(pool, tokens, torch.zeros(N, dtype=torch.int32, device=dev), pool_len - 1, junk=False)
+    batch_flat = torch.empty(L * 2 * B * H * S * D, dtype=torch.bfloat16, device=dev)
+    pos_flat = torch.empty(B * S, dtype=torch.int32, device=dev)
+    mask_flat = torch.empty(B * S, dtype=torch.uint8, device=dev)
+    ws_by_rows = {}
+
+    def workspace(rows):  # one zero-initialised scratch per batch size (its layout depends on the size)
+        if rows not in ws_by_rows:
+            ws_by_rows[rows] = sv.Workspace(rows, k, V, dev)
+        return ws_by_rows[rows]
+    window = args.window or N
+    sched = ExspecScheduler(pool_len, B, window)
+    active = np.ones(N, bool)
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+    row_all = L * 2 * H * D * 2
+
+    def timed(fn):
+        torch.cuda._sleep(1_000_000)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        out = fn()
+        e1.record(st)
+        torch.cuda.synchronize(dev)
+        return out, e0.elapsed_time(e1) / 1e3
+
+    def one_round():
+        _, t_sel = timed(lambda: sched.select_async(active))
+        picks, full, _ = sched.selection()
+        Bb = len(picks)
+        if Bb == 0:
+            return None
+        ws = workspace(Bb)
+        idx = torch.from_numpy(picks.astype(np.int32)).to(dev)
+        plen = pool_len[idx.long()]
+        x, d = torch_gen.greedy_round_inputs(Bb, k, V, c["alpha"], c["sigma"], g, torch.bfloat16, dev)
+        last = tokens[idx.long(), (plen - 1).long()].unsqueeze(1)
+        qtok = torch.cat([last, d], 1).contiguous()
+        moved = 0
+        if full:  # grouped: the forward writes each member's own slots in the pool
+            torch_gen.kv_write_query_pool(pool, qtok, idx, (plen - 1).contiguous())
+            flush.zero_()
+
+            def grouped():
+                _, _, ne = sv.spec_verify_greedy(x, d, workspace=ws)
+                err = sv.spec_commit_ragged(pool_len, idx, ne, S)
+                return ne, err
+            (ne, err), t_round = timed(grouped)
+            t_parts = (t_sel, t_round, 0.0)
+        else:  # fallback: unpad-append-repad, on a batch of the Bb chosen rows
+            batch = batch_flat[: L * 2 * Bb * H * S * D].view(L, 2, Bb, H, S, D)
+            pos = pos_flat[: Bb * S].view(Bb, S)
+            mask = mask_flat[: Bb * S].view(Bb, S)
+            flush.zero_()
+
+            def repad():
+                return sv.spec_repad_gather(pool, batch, idx, pool_len, workspace=ws)
+            (ln, pd, w, err0), t_repad = timed(repad)
+            assert int(err0.item()) == 0
+            sv.spec_rebuild_pos_mask(pd, pos, mask)
+            W = int(w.item())
+            torch_gen.kv_write_query(batch, qtok, pos, W)
+            flush.zero_()
+            moved = int(((ln - 1).sum()).item())
+
+            def rest():
+                _, _, ne = sv.spec_verify_greedy(x, d, workspace=ws)
+                ln2, pd2, w2, err1 = sv.spec_realign_kv(batch, ln, pd, ne, workspace=ws)
+                sv.spec_rebuild_pos_mask(pd2, pos, mask, pad_old=pd)
+                err = sv.spec_unpad_scatter(batch, pool, idx, ln2, pd2, pool_len, workspace=ws)
+                return ne, err
+            (ne, err), t_round = timed(rest)
+            t_parts = (t_sel, t_repad, t_round)
+        assert int(err.item()) == 0
+        done = (pool_len >= S - (k + 2)).cpu().numpy()
+        active[done] = False
+        return full, t_parts, moved, int(ne.sum().item())
+
+    for _ in range(args.warmup):
+        one_round()
+    torch.cuda.synchronize(dev)
+    if pg:
+        dist.barrier()
+    rounds = []
+    with ClockSampler(local_rank) as clk:
+        for _ in range(args.steps):
+            r = one_round()
+            if r is not None:
+                rounds.append(r)
+    if pg:
+        dist.barrier()
+    total = sum(sum(r[1]) for r in rounds)
+    total = max_over_ranks(total, pg, dev)
+    n = len(rounds)
+    grouped = [r for r in rounds if r[0]]
+    fallback = [r for r in rounds if not r[0]]
+    peak, peak_src = hbm_peak()
+    copy_bytes = sum(r[2] for r in fallback) * row_all * 2  # repad: read + write of every gathered row
+    copy_time = sum(r[1][1] for r in fallback)
+    roof = None
+    if fallback and copy_time > 0:
+        ach = copy_bytes / copy_time / 1e9
+        roof = {"bound": "hbm", "kernel": "pool_copy_bulk_kernel (repad, timed with its plan kernel: lower bound)",
+                "achieved": round(ach, 1), "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)", "traffic": None,
+                "algorithmic_bytes_per_launch": round(copy_bytes / len(fallback))}
+    line = {
+        "metric": METRIC, "value": round(aggregate(n, total, world), 3), "unit": "rounds/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / max(n, 1) * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; stands in for Multi30k-shaped length mixes)",
+        "config": {"workload": f"c4x: EXSPEC rounds over a {N}-sequence ragged pool, lengths "
+                               + ("U[128,1024]" if args.pool_lengths == "a" else "uniform over {128,...,1024}")
+                               + f", B={B}, window={window}, k={k}, V={V} bf16, alpha={c['alpha']}; pool KV "
+                               f"{L}x2x{N}x{H}x{S}x{D} bf16",
+                   "l2": "flushed before every timed part (256 MiB write)",
+                   "timed": "selection, then the round's library calls; the target forward between them untimed",
+                   "parallelism": f"independent pool per GPU x{world}"},
+        "grouping_rate": round(len(grouped) / max(n, 1), 4),
+        "grouped_round_us": round(float(np.mean([sum(r[1]) for r in grouped])) * 1e6, 2) if grouped else None,
+        "fallback_round_us": round(float(np.mean([sum(r[1]) for r in fallback])) * 1e6, 2) if fallback else None,
+        "selection_us": round(float(np.mean([r[1][0] for r in rounds])) * 1e6, 2) if rounds else None,
+        "roofline": roof,
+        "tokens_per_round": round(sum(r[3] for r in rounds) / max(n, 1) / B, 4),
+        "gpu_launches": sum(3 if r[0] else 9 for r in rounds),
+        "clocks": clk.summary(),
+    }
+    if pg:
+        dist.destroy_process_group()
+    return line
+
+
 def main():
     args = parse()
     c = workload_params(args)
     rank, local_rank, world = dist_env()
     if args.impl == "reference":
         line = run_reference(args, c)
+    elif c["mode"] == "exspec":
+        line = run_exspec_bench(args, c, rank, local_rank, world)
     else:
         line = run_ours(args, c, rank, local_rank, world)
     if rank == 0 and line is not None:

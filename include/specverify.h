@@ -77,6 +77,9 @@ enum {
 /* Most caches one spec_realign_kv_multi call moves. */
 #define SPEC_MAX_CACHES 4
 
+/* Largest pool (sequences) of the ragged-pool entry points. */
+#define SPEC_MAX_POOL 65536
+
 /* Largest k (proposals per sequence) accepted by the verify entry points. */
 #define SPEC_MAX_K 31
 /* Largest pool accepted by spec_group_by_length. */
@@ -260,6 +263,48 @@ SPEC_API int spec_verify_greedy_static(const void *target_logits, spec_dtype dt,
                               const int32_t *draft_tokens, const int32_t *draft_len, int32_t eos_id,
                               const int32_t *remaining, int32_t *out_tokens, int32_t *n_accept,
                               int32_t *n_emit, void *cuda_stream);
+
+/*
+ * Ragged pool of EXSPEC ([CF] §3.2: keep sequences ragged and batch
+ * identical-length sequences so realignment is bypassed; when grouping fails,
+ * fall back to unpad-append-repad).  Pool cache pool[L, 2, N, H, S, D]:
+ * sequence n is left-aligned at slot 0, positions 0 .. pool_len[n] - 2 have
+ * KV (the last token has none), and a position ID is its slot index.  A group
+ * of equal lengths is rectangular as it is; after a round on it the commit
+ * below is the whole "rollback of rejected tokens" a variable-length layout
+ * needs ([CF] §2): their KV rows lie past the new length.
+ * The pages give no algorithm for EXSPEC's scheduler; the selection policy
+ * (spec_group_by_length over a window) and these operations are this
+ * library's.
+ */
+
+/* pool_len[idx[b]] += n_emit[b] for the B sequences of a round (idx [B] pool
+ * indices, distinct).  err [1]: SPEC_REALIGN_OK, SPEC_REALIGN_LAYOUT (an index
+ * outside [0, N) or repeated, or a negative count) or SPEC_REALIGN_CAPACITY (a
+ * length past S); on an error nothing changes.  0 <= N <= SPEC_MAX_POOL. */
+SPEC_API int spec_commit_ragged(int N, int32_t *pool_len, int B, const int32_t *idx, const int32_t *n_emit,
+                       int S, int32_t *err, void *cuda_stream);
+
+/* Repad: batch[L, 2, B, H, S, D] row b receives pool sequence idx[b]'s rows
+ * 0 .. pool_len[idx[b]] - 2 at slot pad_b = W - pool_len[idx[b]], W = the
+ * longest of them; no other batch byte changes.  len_out, pad_out [B] and
+ * width_out [1] describe the batch (rectangular alignment holds; the caller
+ * rebuilds positions and the mask with spec_rebuild_pos_mask).  err [1]:
+ * SPEC_REALIGN_OK or SPEC_REALIGN_LAYOUT (bad or repeated index, a length
+ * outside [1, S]; nothing written).  pool and batch must not overlap. */
+SPEC_API int spec_repad_gather(const void *pool, void *batch, spec_dtype dt, int L, int N, int B, int H, int S,
+                      int D, const int32_t *idx, const int32_t *pool_len, int32_t *len_out,
+                      int32_t *pad_out, int32_t *width_out, int32_t *err, void *workspace,
+                      size_t workspace_bytes, void *cuda_stream);
+
+/* Unpad: batch row b's rows pad[b] .. pad[b] + len[b] - 2 go back to slot 0 of
+ * pool sequence idx[b], and pool_len[idx[b]] = len[b]; no other pool byte
+ * changes.  err [1]: SPEC_REALIGN_OK or SPEC_REALIGN_LAYOUT (bad or repeated
+ * index, len < 1, pad < 0 or a run past S; nothing written). */
+SPEC_API int spec_unpad_scatter(const void *batch, void *pool, spec_dtype dt, int L, int N, int B, int H, int S,
+                       int D, const int32_t *idx, const int32_t *len, const int32_t *pad,
+                       int32_t *pool_len, int32_t *err, void *workspace, size_t workspace_bytes,
+                       void *cuda_stream);
 
 #ifdef __cplusplus
 }

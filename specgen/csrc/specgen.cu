@@ -116,6 +116,35 @@ __global__ void write_query_kernel(void *kv, int elt, Shape sh, const int32_t *q
     }
 }
 
+// the forward's KV write on a ragged pool [L, 2, N, H, S, D]: batch row b is
+// pool sequence seq[b] and its k1 query slots start at base[b]; in a pool the
+// position of a slot is its index
+__global__ void write_query_pool_kernel(void *kv, int elt, Shape sh, const int32_t *qtok, int k1, int B,
+                                        const int32_t *seq, const int32_t *base)
+{
+    const long long rows = (long long)sh.L * 2 * B * sh.H * k1;
+    const int lane = threadIdx.x & 31;
+    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+        long long x = r;
+        const int j = (int)(x % k1);
+        x /= k1;
+        const int h = (int)(x % sh.H);
+        x /= sh.H;
+        const int b = (int)(x % B);
+        x /= B;
+        const int c = (int)(x % 2);
+        const int l = (int)(x / 2);
+        const int n = seq[b], slot = base[b] + j;
+        if (n < 0 || n >= sh.B || slot < 0 || slot >= sh.S)
+            continue;
+        const uint64_t h1 = row_hash((uint32_t)n, (uint32_t)qtok[(size_t)b * k1 + j], (uint32_t)slot);
+        const size_t at = ((((size_t)(l * 2 + c) * sh.B + n) * sh.H + h) * sh.S + slot) * sh.D;
+        for (int d = lane; d < sh.D; d += 32)
+            store(kv, elt, at + d, kv_value(h1, l, c, h, d));
+    }
+}
+
 // invariant I2 over the whole cache: slot pad'_b + p holds f(b, tok_p, p) for
 // every p < len'_b - 1; counts the elements that differ
 __global__ void check_kernel(const void *kv, int elt, Shape sh, const int32_t *tokens, const int32_t *pad_new,
@@ -176,6 +205,15 @@ int specgen_kv_write_query(void *kv, int elt, int L, int B, int H, int S, int D,
     Shape sh{L, B, H, S, D};
     write_query_kernel<<<grid_for((long long)L * 2 * B * H * k1), 256, 0, (cudaStream_t)stream>>>(kv, elt, sh, qtok,
                                                                                                  k1, pos, W);
+    return (int)cudaGetLastError();
+}
+
+int specgen_kv_write_query_pool(void *kv, int elt, int L, int N, int H, int S, int D, const int32_t *qtok, int k1,
+                                int B, const int32_t *seq, const int32_t *base, void *stream)
+{
+    Shape sh{L, N, H, S, D};
+    write_query_pool_kernel<<<grid_for((long long)L * 2 * B * H * k1), 256, 0, (cudaStream_t)stream>>>(
+        kv, elt, sh, qtok, k1, B, seq, base);
     return (int)cudaGetLastError();
 }
 

@@ -37,7 +37,9 @@ def _load():
         lib.specgen_kv_fill.argtypes = [vp, i, i, i, i, i, i, vp, vp, vp, i, vp]
         lib.specgen_kv_write_query.argtypes = [vp, i, i, i, i, i, i, vp, i, vp, i, vp]
         lib.specgen_kv_check.argtypes = [vp, i, i, i, i, i, i, vp, vp, vp, vp, vp]
-        for f in (lib.specgen_kv_fill, lib.specgen_kv_write_query, lib.specgen_kv_check):
+        lib.specgen_kv_write_query_pool.argtypes = [vp, i, i, i, i, i, i, vp, i, i, vp, vp, vp]
+        for f in (lib.specgen_kv_fill, lib.specgen_kv_write_query, lib.specgen_kv_check,
+                  lib.specgen_kv_write_query_pool):
             f.restype = i
         _lib = lib
     return _lib
@@ -66,6 +68,15 @@ def kv_write_query(kv, qtok, pos, W):
     L, _, B, H, S, D = kv.shape
     rc = _load().specgen_kv_write_query(_p(kv), _ELT[kv.dtype], L, B, H, S, D, _p(qtok), qtok.shape[1], _p(pos),
                                         int(W), _s())
+    assert rc == 0, rc
+
+
+def kv_write_query_pool(pool, qtok, seq, base):
+    """The forward's KV write on a ragged pool: batch row b (pool sequence
+    seq[b]) writes f(seq[b], qtok[b, j], base[b] + j) at slot base[b] + j."""
+    L, _, N, H, S, D = pool.shape
+    rc = _load().specgen_kv_write_query_pool(_p(pool), _ELT[pool.dtype], L, N, H, S, D, _p(qtok), qtok.shape[1],
+                                             qtok.shape[0], _p(seq), _p(base), _s())
     assert rc == 0, rc
 
 

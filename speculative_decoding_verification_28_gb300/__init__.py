@@ -20,7 +20,11 @@ from .api import (  # noqa: F401
     REALIGN_TIMEOUT,
     SpecError,
     Workspace,
+    spec_commit_ragged,
     spec_group_by_length,
+    spec_repad_gather,
+    spec_unpad_scatter,
+    MAX_POOL,
     spec_realign_kv,
     spec_realign_kv_multi,
     MAX_CACHES,

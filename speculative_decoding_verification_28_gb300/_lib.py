@@ -38,6 +38,12 @@ class KVCacheDesc(ctypes.Structure):
 SIGNATURES["spec_realign_kv_multi"] = ([_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
                                        _i32)
 
+SIGNATURES["spec_commit_ragged"] = ([_i32, _vp, _i32, _vp, _vp, _i32, _vp, _vp], _i32)
+SIGNATURES["spec_repad_gather"] = ([_vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
+                                    _vp, _sz, _vp], _i32)
+SIGNATURES["spec_unpad_scatter"] = ([_vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
+                                     _vp, _sz, _vp], _i32)
+
 _lib = None
 
 

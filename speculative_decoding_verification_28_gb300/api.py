@@ -276,3 +276,68 @@ def spec_group_by_length(length, B, active=None, out_idx=None, out_count_equal=N
     _check(lib.spec_group_by_length(N, _p(length), _p(active), int(B), _p(out_idx), _p(out_count_equal),
                                     _p(out_group_len), st))
     return out_idx, out_count_equal, out_group_len
+
+
+MAX_POOL = 65536
+
+
+def spec_commit_ragged(pool_len, idx, n_emit, S, err=None, stream=None):
+    """pool_len [N] += n_emit at idx (in place). -> err [1] int32."""
+    lib = _lib.load()
+    dev = pool_len.device
+    (N,) = pool_len.shape
+    (B,) = idx.shape
+    _need(pool_len, torch.int32, "pool_len", dev)
+    _need(idx, torch.int32, "idx", dev)
+    _need(n_emit, torch.int32, "n_emit", dev, (B,))
+    err = torch.empty(1, dtype=torch.int32, device=dev) if err is None else err
+    _check(lib.spec_commit_ragged(N, _p(pool_len), B, _p(idx), _p(n_emit), int(S), _p(err), _stream(stream, dev)))
+    return err
+
+
+def spec_repad_gather(pool, batch, idx, pool_len, len_out=None, pad_out=None, width_out=None, err=None,
+                      workspace=None, stream=None):
+    """pool [L,2,N,H,S,D] -> batch [L,2,B,H,S,D] (left-padded).
+    -> (len [B], pad [B], width [1], err [1]) int32."""
+    lib = _lib.load()
+    L, two, N, H, S, D = pool.shape
+    B = batch.shape[2]
+    dev = pool.device
+    if two != 2 or batch.shape != (L, 2, B, H, S, D) or batch.dtype != pool.dtype:
+        raise ValueError("pool [L,2,N,H,S,D] and batch [L,2,B,H,S,D] of one dtype")
+    _need(pool, None, "pool", dev)
+    _need(batch, None, "batch", dev)
+    _need(idx, torch.int32, "idx", dev, (B,))
+    _need(pool_len, torch.int32, "pool_len", dev, (N,))
+    len_out = torch.empty(B, dtype=torch.int32, device=dev) if len_out is None else len_out
+    pad_out = torch.empty(B, dtype=torch.int32, device=dev) if pad_out is None else pad_out
+    width_out = torch.empty(1, dtype=torch.int32, device=dev) if width_out is None else width_out
+    err = torch.empty(1, dtype=torch.int32, device=dev) if err is None else err
+    st = _stream(stream, dev)
+    ws = _workspace(workspace, B, 0, 1, dev, st)
+    _check(lib.spec_repad_gather(_p(pool), _p(batch), _DT[pool.dtype], L, N, B, H, S, D, _p(idx), _p(pool_len),
+                                 _p(len_out), _p(pad_out), _p(width_out), _p(err), ws.ptr(), ws.nbytes, st))
+    return len_out, pad_out, width_out, err
+
+
+def spec_unpad_scatter(batch, pool, idx, length, pad, pool_len, err=None, workspace=None, stream=None):
+    """batch [L,2,B,H,S,D] -> pool [L,2,N,H,S,D]; pool_len [N] updated in
+    place. -> err [1] int32."""
+    lib = _lib.load()
+    L, two, N, H, S, D = pool.shape
+    B = batch.shape[2]
+    dev = pool.device
+    if two != 2 or batch.shape != (L, 2, B, H, S, D) or batch.dtype != pool.dtype:
+        raise ValueError("pool [L,2,N,H,S,D] and batch [L,2,B,H,S,D] of one dtype")
+    _need(pool, None, "pool", dev)
+    _need(batch, None, "batch", dev)
+    _need(idx, torch.int32, "idx", dev, (B,))
+    for t, nm in ((length, "len"), (pad, "pad")):
+        _need(t, torch.int32, nm, dev, (B,))
+    _need(pool_len, torch.int32, "pool_len", dev, (N,))
+    err = torch.empty(1, dtype=torch.int32, device=dev) if err is None else err
+    st = _stream(stream, dev)
+    ws = _workspace(workspace, B, 0, 1, dev, st)
+    _check(lib.spec_unpad_scatter(_p(batch), _p(pool), _DT[pool.dtype], L, N, B, H, S, D, _p(idx), _p(length),
+                                  _p(pad), _p(pool_len), _p(err), ws.ptr(), ws.nbytes, st))
+    return err

@@ -248,4 +248,99 @@ int spec_group_by_length(int N, const int32_t *len, const uint8_t *active, int B
         launch_group(N, len, active, B, out_idx, out_count_equal, out_group_len, (cudaStream_t)cuda_stream));
 }
 
+int spec_commit_ragged(int N, int32_t *pool_len, int B, const int32_t *idx, const int32_t *n_emit, int S, int32_t *err,
+                       void *cuda_stream)
+{
+    if (N < 0 || N > SPEC_MAX_POOL || B < 0 || S < 1)
+        return SPEC_EINVAL;
+    if (B == 0)
+        return SPEC_OK;
+    if (!pool_len || !idx || !n_emit || !err)
+        return SPEC_EINVAL;
+    if (!aligned(pool_len, 4) || !aligned(idx, 4) || !aligned(n_emit, 4) || !aligned(err, 4))
+        return SPEC_EALIGN;
+    return launched(launch_commit_ragged(N, pool_len, B, idx, n_emit, S, err, (cudaStream_t)cuda_stream));
+}
+
+static int pool_common(const void *src, const void *dst, int dt, int L, int N, int B, int H, int S, int D,
+                       const int32_t *idx, const int32_t *err, void *workspace, size_t workspace_bytes)
+{
+    if (L < 1 || N < 0 || N > SPEC_MAX_POOL || B < 0 || H < 1 || S < 1 || D < 1)
+        return SPEC_EINVAL;
+    if (!dtype_ok(dt))
+        return SPEC_EDTYPE;
+    if (B == 0)
+        return SPEC_OK;
+    if (!src || !dst || !idx || !err)
+        return SPEC_EINVAL;
+    if ((long long)(B > N ? B : N) * L * 2 * H > INT_MAX)
+        return SPEC_EINVAL;
+    if (!aligned(src, dtype_bytes(dt)) || !aligned(dst, dtype_bytes(dt)) || !aligned(idx, 4) || !aligned(err, 4))
+        return SPEC_EALIGN;
+    return check_workspace(workspace, workspace_bytes, spec_workspace_bytes(B, 0, 1));
+}
+
+int spec_repad_gather(const void *pool, void *batch, spec_dtype dt, int L, int N, int B, int H, int S, int D,
+                      const int32_t *idx, const int32_t *pool_len, int32_t *len_out, int32_t *pad_out,
+                      int32_t *width_out, int32_t *err, void *workspace, size_t workspace_bytes, void *cuda_stream)
+{
+    int rc = pool_common(pool, batch, dt, L, N, B, H, S, D, idx, err, workspace, workspace_bytes);
+    if (rc != SPEC_OK || B == 0)
+        return rc;
+    if (!pool_len || !len_out || !pad_out || !width_out)
+        return SPEC_EINVAL;
+    if (!aligned(pool_len, 4) || !aligned(len_out, 4) || !aligned(pad_out, 4) || !aligned(width_out, 4))
+        return SPEC_EALIGN;
+    PoolArgs a{};
+    a.src = pool;
+    a.dst = batch;
+    a.elt_bytes = dtype_bytes(dt);
+    a.L = L;
+    a.N = N;
+    a.B = B;
+    a.H = H;
+    a.S = S;
+    a.D = D;
+    a.repad = 1;
+    a.idx = idx;
+    a.pool_len = pool_len;
+    a.len_out = len_out;
+    a.pad_out = pad_out;
+    a.width_out = width_out;
+    a.err = err;
+    a.ws = workspace;
+    return launched(launch_pool_copy(a, (cudaStream_t)cuda_stream));
+}
+
+int spec_unpad_scatter(const void *batch, void *pool, spec_dtype dt, int L, int N, int B, int H, int S, int D,
+                       const int32_t *idx, const int32_t *len, const int32_t *pad, int32_t *pool_len, int32_t *err,
+                       void *workspace, size_t workspace_bytes, void *cuda_stream)
+{
+    int rc = pool_common(batch, pool, dt, L, N, B, H, S, D, idx, err, workspace, workspace_bytes);
+    if (rc != SPEC_OK || B == 0)
+        return rc;
+    if (!len || !pad || !pool_len)
+        return SPEC_EINVAL;
+    if (!aligned(len, 4) || !aligned(pad, 4) || !aligned(pool_len, 4))
+        return SPEC_EALIGN;
+    PoolArgs a{};
+    a.src = batch;
+    a.dst = pool;
+    a.elt_bytes = dtype_bytes(dt);
+    a.L = L;
+    a.N = N;
+    a.B = B;
+    a.H = H;
+    a.S = S;
+    a.D = D;
+    a.repad = 0;
+    a.idx = idx;
+    a.len = len;
+    a.pad = pad;
+    a.pool_len_out = pool_len;
+    a.err = err;
+    a.ws = workspace;
+    return launched(launch_pool_copy(a, (cudaStream_t)cuda_stream));
+}
+
 }  // extern "C"

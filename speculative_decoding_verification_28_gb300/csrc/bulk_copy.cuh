@@ -72,6 +72,120 @@ __device__ __forceinline__ void bulk_wait_read()
 
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// ---------------------------------------------------------------------------
+// A copy engine on one thread: runs of bytes staged global -> shared ->
+// global through kBulkStages stages of kBulkTile bytes.  Loads run up to
+// kBulkStages - 1 tiles ahead of the stores; each store is issued after its
+// tile's load completed on the stage's mbarrier, strictly in tile order, and
+// a stage is reloaded only after the store that read it has finished reading.
+// The tile source decides the order, so an in-place move that takes its tiles
+// from the end the run moves towards never overwrites bytes not yet loaded.
+// ---------------------------------------------------------------------------
+constexpr int kBulkStages = 4;
+constexpr int kBulkTile = 48 * 1024;  // bytes per stage
+constexpr int kBulkSmem = kBulkStages * kBulkTile;
+constexpr int kBulkWaitLimit = 4000;  // probes of up to ~1 ms each before giving up
+
+// tiles of one contiguous run: ascending, or descending (from the top) when
+// `desc` (an in-place move towards higher addresses)
+struct RunTiles {
+    const char *src;
+    char *dst;
+    long long nbytes, done;
+    int desc;
+    __device__ bool next(const char *&s, char *&d, uint32_t &bytes)
+    {
+        if (done >= nbytes)
+            return false;
+        long long take = nbytes - done;
+        if (take > kBulkTile)
+            take = kBulkTile;
+        const long long lo = desc ? nbytes - done - take : done;
+        s = src + lo;
+        d = dst + lo;
+        bytes = (uint32_t)take;
+        done += take;
+        return true;
+    }
+};
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read_upto(int newer)
+{
+    if constexpr (N > 0) {
+        if (newer >= N) {
+            bulk_wait_read<N>();
+            return;
+        }
+        bulk_wait_read_upto<N - 1>(newer);
+    } else {
+        bulk_wait_read<0>();
+    }
+}
+
+// Copies every tile `source.next(src, dst, bytes)` yields (16-byte aligned
+// addresses and sizes).  One thread.  Returns false when a bounded wait gave
+// up (after waiting, bounded, for the copies still in flight).
+template <class Source>
+__device__ bool bulk_copy_pipeline(Source &source, unsigned char *stage_mem, uint64_t *full)
+{
+    for (int s = 0; s < kBulkStages; ++s)
+        mbar_init(&full[s], 1);
+    fence_mbar_init();
+    char *dst_of[kBulkStages];
+    uint32_t bytes_of[kBulkStages];
+    uint32_t parity = 0;
+    long long issued = 0, done = 0;
+    bool more = true, failed = false;
+    while (true) {
+        while (more && issued - done < kBulkStages - 1) {
+            const char *src;
+            char *dst;
+            uint32_t bytes;
+            if (!source.next(src, dst, bytes)) {
+                more = false;
+                break;
+            }
+            const int s = (int)(issued % kBulkStages);
+            if (issued >= kBulkStages)
+                bulk_wait_read_upto<kBulkStages - 1>((int)(done - 1 - (issued - kBulkStages)));
+            mbar_arrive_expect_tx(&full[s], bytes);
+            bulk_g2s(stage_mem + (size_t)s * kBulkTile, src, bytes, &full[s]);
+            dst_of[s] = dst;
+            bytes_of[s] = bytes;
+            ++issued;
+        }
+        if (done == issued)
+            break;
+        const int s = (int)(done % kBulkStages);
+        const uint32_t par = (parity >> s) & 1u;
+        int probes = 0;
+        while (!mbar_try_wait(&full[s], par)) {
+            if (++probes >= kBulkWaitLimit) {
+                failed = true;
+                break;
+            }
+        }
+        if (failed)
+            break;
+        parity ^= 1u << s;
+        bulk_s2g(dst_of[s], stage_mem + (size_t)s * kBulkTile, bytes_of[s]);
+        bulk_commit();
+        ++done;
+    }
+    if (failed) {  // wait (bounded) for the loads still in flight
+        for (long long i = done; i < issued; ++i) {
+            const int s = (int)(i % kBulkStages);
+            const uint32_t par = (parity >> s) & 1u;
+            for (int p = 0; p < kBulkWaitLimit && !mbar_try_wait(&full[s], par); ++p) {
+            }
+            parity ^= 1u << s;
+        }
+    }
+    bulk_wait_all();
+    return !failed;
+}
+
 // Programmatic dependent launch (griddepcontrol, sm_90+).  `dep_wait` blocks
 // until the grids this one depends on have completed and their memory is
 // visible (a no-op when the launch was not programmatic); `dep_release` lets

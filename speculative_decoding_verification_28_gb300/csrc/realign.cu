@@ -172,159 +172,78 @@ __global__ void __launch_bounds__(kPlanThreads) realign_plan_kernel(RealignArgs 
 // ---------------------------------------------------------------------------
 // bulk-copy shift
 // ---------------------------------------------------------------------------
-constexpr int kStages = 4;
-constexpr int kTile = 48 * 1024;  // bytes per stage
-constexpr int kShiftSmem = kStages * kTile;
-constexpr int kWaitLimit = 4000;  // probes of up to ~1 ms each before giving up
+constexpr int kShiftSmem = kBulkSmem;
 
-struct TileGen {
-    char *slab;
-    long long src, dst, nbytes, done;  // byte offsets within the slab
-    int desc;                          // 1: tiles from the top of the run down
-};
-
-__device__ __forceinline__ bool tile_next(TileGen &g, const char *&src, char *&dst, uint32_t &bytes)
-{
-    if (g.done >= g.nbytes)
-        return false;
-    long long take = g.nbytes - g.done;
-    if (take > kTile)
-        take = kTile;
-    const long long lo = g.desc ? g.nbytes - g.done - take : g.done;
-    src = g.slab + g.src + lo;
-    dst = g.slab + g.dst + lo;
-    bytes = (uint32_t)take;
-    g.done += take;
-    return true;
-}
-
-template <int N>
-__device__ __forceinline__ void wait_read_upto(int newer)
-{
-    if constexpr (N > 0) {
-        if (newer >= N) {
-            bulk_wait_read<N>();
-            return;
-        }
-        wait_read_upto<N - 1>(newer);
-    } else {
-        bulk_wait_read<0>();
-    }
-}
-
-__global__ void __launch_bounds__(32) kv_shift_bulk_kernel(RealignArgs a)
-{
-    extern __shared__ __align__(128) unsigned char stage_mem[];
-    __shared__ __align__(8) uint64_t full[kStages];
-    if (threadIdx.x != 0)
-        return;
-    dep_wait();     // the plan kernel's results are complete and visible
-    dep_release();  // a following position/mask rebuild may run alongside
-    const PlanView pv = plan_view(a.ws, a.B);
-    const int n_moving = pv.misc[MISC_NMOVING];
-    if (n_moving <= 0)
-        return;
-    // work items: the moving slabs of every bulk cache, cache after cache
-    long long n_items = 0;
-    for (int c = 0; c < a.n_caches; ++c)
-        if (a.bulk_mask & (1u << c))
-            n_items += (long long)n_moving * a.cache[c].L * 2 * a.cache[c].H;
-
-    for (int s = 0; s < kStages; ++s)
-        mbar_init(&full[s], 1);
-    fence_mbar_init();
-
-    // work items: (rank in the longest-first list, slab within the sequence)
-    long long item = atomicAdd(pv.misc + MISC_WORK, 1);
-    TileGen g{nullptr, 0, 0, 0, 0, 0};
-    auto open_item = [&](long long it) -> bool {
+// the moving slabs of every bulk cache, fetched longest-first from a shared
+// counter; each slab's run is tiled from the end it moves towards
+struct ShiftSource {
+    const RealignArgs *a;
+    PlanView pv;
+    int n_moving;
+    long long n_items, item;
+    RunTiles cur;
+    __device__ bool open(long long it)
+    {
         if (it >= n_items)
             return false;
         int c = 0;
-        for (; c < a.n_caches; ++c) {
-            if (!(a.bulk_mask & (1u << c)))
+        for (; c < a->n_caches; ++c) {
+            if (!(a->bulk_mask & (1u << c)))
                 continue;
-            const long long cnt = (long long)n_moving * a.cache[c].L * 2 * a.cache[c].H;
+            const long long cnt = (long long)n_moving * a->cache[c].L * 2 * a->cache[c].H;
             if (it < cnt)
                 break;
             it -= cnt;
         }
-        const CacheDesc &cd = a.cache[c];
+        const CacheDesc &cd = a->cache[c];
         const int sps = cd.L * 2 * cd.H;  // slabs per sequence
         const long long row_bytes = (long long)cd.D * cd.elt_bytes;
-        const long long slab_bytes = row_bytes * a.S;
+        const long long slab_bytes = row_bytes * a->S;
         const int r = (int)(it / sps), within = (int)(it % sps);
         const int b = pv.order[r];
         const int h = within % cd.H, lc = within / cd.H;  // lc = l * 2 + k/v
-        const long long slab = ((long long)lc * a.B + b) * cd.H + h;
+        char *slab = reinterpret_cast<char *>(cd.kv) + (((long long)lc * a->B + b) * cd.H + h) * slab_bytes;
         const int d = pv.delta[b];
-        g.slab = reinterpret_cast<char *>(cd.kv) + slab * slab_bytes;
-        g.src = (long long)pv.src_pad[b] * row_bytes;
-        g.dst = (long long)(pv.src_pad[b] + d) * row_bytes;
-        g.nbytes = (long long)pv.run[b] * row_bytes;
-        g.done = 0;
-        g.desc = d > 0;
+        cur.src = slab + (long long)pv.src_pad[b] * row_bytes;
+        cur.dst = slab + (long long)(pv.src_pad[b] + d) * row_bytes;
+        cur.nbytes = (long long)pv.run[b] * row_bytes;
+        cur.done = 0;
+        cur.desc = d > 0;
         return true;
-    };
-    bool more = open_item(item);
-    if (more)
-        item = atomicAdd(pv.misc + MISC_WORK, 1);  // prefetch the next item
+    }
+    __device__ bool next(const char *&s, char *&d, uint32_t &bytes)
+    {
+        while (!cur.next(s, d, bytes)) {
+            if (!open(item))
+                return false;
+            item = atomicAdd(pv.misc + MISC_WORK, 1);  // the item after, fetched ahead
+        }
+        return true;
+    }
+};
 
-    char *dst_of[kStages];
-    uint32_t bytes_of[kStages];
-    uint32_t parity = 0;
-    long long issued = 0, done = 0;
-    bool failed = false;
-    while (true) {
-        while (more && issued - done < kStages - 1) {
-            const char *src;
-            char *dst;
-            uint32_t bytes;
-            if (!tile_next(g, src, dst, bytes)) {
-                more = open_item(item);
-                if (more)
-                    item = atomicAdd(pv.misc + MISC_WORK, 1);
-                continue;
-            }
-            const int s = (int)(issued % kStages);
-            if (issued >= kStages)
-                wait_read_upto<kStages - 1>((int)(done - 1 - (issued - kStages)));
-            mbar_arrive_expect_tx(&full[s], bytes);
-            bulk_g2s(stage_mem + (size_t)s * kTile, src, bytes, &full[s]);
-            dst_of[s] = dst;
-            bytes_of[s] = bytes;
-            ++issued;
-        }
-        if (done == issued)
-            break;
-        const int s = (int)(done % kStages);
-        const uint32_t par = (parity >> s) & 1u;
-        int probes = 0;
-        while (!mbar_try_wait(&full[s], par)) {
-            if (++probes >= kWaitLimit) {
-                failed = true;
-                break;
-            }
-        }
-        if (failed)
-            break;
-        parity ^= 1u << s;
-        bulk_s2g(dst_of[s], stage_mem + (size_t)s * kTile, bytes_of[s]);
-        bulk_commit();
-        ++done;
-    }
-    if (failed) {
-        // record the error, then wait (bounded) for the loads still in flight
+__global__ void __launch_bounds__(32) kv_shift_bulk_kernel(RealignArgs a)
+{
+    extern __shared__ __align__(128) unsigned char stage_mem[];
+    __shared__ __align__(8) uint64_t full[kBulkStages];
+    if (threadIdx.x != 0)
+        return;
+    dep_wait();     // the plan kernel's results are complete and visible
+    dep_release();  // a following position/mask rebuild may run alongside
+    ShiftSource src;
+    src.a = &a;
+    src.pv = plan_view(a.ws, a.B);
+    src.n_moving = src.pv.misc[MISC_NMOVING];
+    if (src.n_moving <= 0)
+        return;
+    src.n_items = 0;
+    for (int c = 0; c < a.n_caches; ++c)
+        if (a.bulk_mask & (1u << c))
+            src.n_items += (long long)src.n_moving * a.cache[c].L * 2 * a.cache[c].H;
+    src.cur = RunTiles{nullptr, nullptr, 0, 0, 0};
+    src.item = atomicAdd(src.pv.misc + MISC_WORK, 1);
+    if (!bulk_copy_pipeline(src, stage_mem, full))
         *a.err = SPEC_REALIGN_TIMEOUT;
-        for (long long i = done; i < issued; ++i) {
-            const int s = (int)(i % kStages);
-            const uint32_t par = (parity >> s) & 1u;
-            for (int p = 0; p < kWaitLimit && !mbar_try_wait(&full[s], par); ++p) {
-            }
-            parity ^= 1u << s;
-        }
-    }
-    bulk_wait_all();
 }
 
 // Plain path for rows that are not a multiple of 16 bytes (or an unaligned

@@ -61,7 +61,7 @@ __host__ __device__ inline int draw_chunks(int V) { return (V + kDrawChunk - 1) 
 // ---------------------------------------------------------------------------
 struct Layout {
     // realignment plan
-    size_t order, delta, src_pad, run, misc;
+    size_t order, delta, src_pad, run, seq_src, seq_dst, misc;
     // counters that every verify call leaves at zero
     size_t zero_begin, seq_cnt, stop_enc, res_cnt, row_cnt, zero_end;
     // verify scratch
@@ -87,6 +87,8 @@ __host__ __device__ inline Layout make_layout(int B, int k, int V)
     L.delta = take(b * 4);
     L.src_pad = take(b * 4);
     L.run = take(b * 4);
+    L.seq_src = take(b * 4);
+    L.seq_dst = take(b * 4);
     L.misc = take(64);
     L.zero_begin = o;
     L.seq_cnt = take(b * 4);

@@ -60,6 +60,25 @@ struct RealignArgs {
 };
 cudaError_t launch_realign(const RealignArgs &a, cudaStream_t st);
 
+// ragged pool (EXSPEC): move runs between a pool [L,2,N,H,S,D] and a
+// left-padded batch [L,2,B,H,S,D]
+struct PoolArgs {
+    const void *src;  // pool (repad) or batch (unpad)
+    void *dst;        // batch (repad) or pool (unpad)
+    int elt_bytes, L, N, B, H, S, D;
+    int repad;        // 1: pool -> batch, 0: batch -> pool
+    const int32_t *idx;       // [B] pool index of each batch row
+    const int32_t *pool_len;  // repad: [N] lengths in the pool
+    const int32_t *len, *pad; // unpad: [B] batch lengths and paddings
+    int32_t *len_out, *pad_out, *width_out;  // repad outputs
+    int32_t *pool_len_out;    // unpad: [N] lengths written back
+    int32_t *err;
+    void *ws;
+};
+cudaError_t launch_pool_copy(const PoolArgs &a, cudaStream_t st);
+cudaError_t launch_commit_ragged(int N, int32_t *pool_len, int B, const int32_t *idx, const int32_t *n_emit, int S,
+                                 int32_t *err, cudaStream_t st);
+
 cudaError_t launch_pos_mask(int B, int S, const int32_t *pad_old, const int32_t *pad_new, int32_t *pos,
                             uint8_t *mask, cudaStream_t st);
 

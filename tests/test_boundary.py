@@ -177,3 +177,20 @@ def test_multi_cache_argument_errors(lib):
     assert multi([good], ws=None) == -3
     assert lib.spec_realign_kv_multi(None, 1, 3, 64, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20,
                                      None) == -1
+
+
+def test_pool_argument_errors(lib):
+    assert lib.spec_commit_ragged(-1, FAKE, 2, FAKE, FAKE, 16, FAKE, None) == -1
+    assert lib.spec_commit_ragged(65537, FAKE, 2, FAKE, FAKE, 16, FAKE, None) == -1
+    assert lib.spec_commit_ragged(8, FAKE, 0, FAKE, FAKE, 16, FAKE, None) == 0
+    assert lib.spec_commit_ragged(8, None, 2, FAKE, FAKE, 16, FAKE, None) == -1
+
+    def repad(pool=FAKE, batch=FAKE, dt=1, L=2, N=8, B=2, H=2, S=64, D=8, ws=FAKE, pl=FAKE):
+        return lib.spec_repad_gather(pool, batch, dt, L, N, B, H, S, D, FAKE, pl, FAKE, FAKE, FAKE, FAKE, ws,
+                                     1 << 20, None)
+
+    assert repad(L=0) == -1 and repad(N=70000) == -1 and repad(dt=7) == -2
+    assert repad(B=0) == 0 and repad(pool=None) == -1 and repad(pl=None) == -1
+    assert repad(ws=None) == -3 and repad(batch=FAKE_ODD) == -5
+    assert lib.spec_unpad_scatter(FAKE, FAKE, 1, 2, 8, 2, 2, 64, 8, FAKE, None, FAKE, FAKE, FAKE, FAKE, 1 << 20,
+                                  None) == -1
