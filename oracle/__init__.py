@@ -15,6 +15,8 @@ from .core import (  # noqa: F401
     DT_F32,
     MUTANTS,
     build,
+    filter_cut,
+    q40_weight,
     commit_ragged,
     repad_gather,
     unpad_scatter,

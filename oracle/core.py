@@ -30,6 +30,11 @@ MUTANTS = {
     "stale_positions": 8,
     "bonus_always": 9,
     "shift_one_short": 10,
+    "topk_strict": 11,
+    "topp_below": 12,
+    "ratio_unfiltered": 13,
+    "resid_unfiltered": 14,
+    "topp_first": 15,
 }
 
 _lock = threading.Lock()
@@ -41,7 +46,8 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(
-            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math", "-o", tmp, _SRC, "-lm"]
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math", "-ffp-contract=off", "-o", tmp, _SRC,
+             "-lm"]
         )
         os.replace(tmp, _LIB)
     return _LIB
@@ -56,11 +62,16 @@ def _load():
             vp, i32, i64, f64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
             lib.oracle_set_mutant.argtypes = [i32]
             lib.oracle_verify_greedy.argtypes = [vp, i32, i32, i32, i32, vp, vp, ctypes.c_int32, vp, vp, vp, vp]
+            f32 = ctypes.c_float
             lib.oracle_verify_sample.argtypes = [
-                vp, i32, f64, vp, vp, vp, i32, i32, i32, vp, ctypes.c_int32, vp, vp, vp, vp, vp, vp,
+                vp, i32, f64, vp, vp, vp, i32, i32, i32, vp, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, vp,
             ]
-            lib.oracle_softmax_row.argtypes = [vp, i32, i64, i32, f64, vp]
+            lib.oracle_softmax_row.argtypes = [vp, i32, i64, i32, f64, i32, f32, vp]
             lib.oracle_softmax_row.restype = i32
+            lib.oracle_filter_cut.argtypes = [vp, i32, i64, i32, f32, i32, f32]
+            lib.oracle_filter_cut.restype = f64
+            lib.oracle_q40_weight.argtypes = [f32, f32]
+            lib.oracle_q40_weight.restype = ctypes.c_uint64
             lib.oracle_realign_plan.argtypes = [i32, i32, vp, vp, vp, vp, vp, vp]
             lib.oracle_realign_plan.restype = i32
             lib.oracle_shift_slab.argtypes = [vp, i64, i32, i32, i32]
@@ -125,9 +136,18 @@ def verify_greedy(logits, dt, draft_tokens, draft_len=None, eos_id=-1, remaining
     return out, na, ne
 
 
+def _per_seq(v, B, dtype):
+    """None, a scalar for every sequence, or a [B] array."""
+    if v is None:
+        return None
+    a = np.asarray(v, dtype=dtype)
+    return np.ascontiguousarray(np.broadcast_to(a, (B,)), dtype=dtype)
+
+
 def verify_sample(logits, dt, draft_probs, draft_tokens, uniforms, temperature=1.0,
-                  draft_len=None, eos_id=-1, remaining=None, want_residual=False):
-    """-> (out_tokens, n_accept, n_emit, flags, residual [B,V] fp64 or None)."""
+                  draft_len=None, eos_id=-1, remaining=None, want_residual=False, top_k=None, top_p=None):
+    """-> (out_tokens, n_accept, n_emit, flags, residual [B,V] fp64 or None).
+    top_k / top_p: None (off), a scalar, or per-sequence [B] (int32 / fp32)."""
     lib = _load()
     x = _logits(logits, dt)
     B, k1, V = x.shape
@@ -142,20 +162,35 @@ def verify_sample(logits, dt, draft_probs, draft_tokens, uniforms, temperature=1
     ne = np.empty(B, np.int32)
     fl = np.empty(B, np.uint32)
     res = np.full((B, V), np.nan, np.float64) if want_residual else None
+    tk, tp = _per_seq(top_k, B, np.int32), _per_seq(top_p, B, np.float32)
     lib.oracle_verify_sample(_ptr(x), dt, float(temperature), _ptr(q), _ptr(d), _ptr(u), B, k, V,
                              _ptr(dl), int(eos_id), _ptr(rem), _ptr(out), _ptr(na), _ptr(ne),
-                             _ptr(res), _ptr(fl))
+                             _ptr(res), _ptr(fl), _ptr(tk), _ptr(tp))
     return out, na, ne, fl, res
 
 
-def softmax_row(logits, dt, row, temperature=1.0):
-    """fp64 softmax of row ``row`` of a [rows, V] view of the logits."""
+def softmax_row(logits, dt, row, temperature=1.0, top_k=0, top_p=1.0):
+    """fp64 processed distribution (softmax, then top-k / top-p) of row
+    ``row`` of a [rows, V] view of the logits."""
     lib = _load()
     x = _logits(logits, dt)
     V = x.shape[-1]
     p = np.empty(V, np.float64)
-    bad = lib.oracle_softmax_row(_ptr(x), dt, int(row), V, float(temperature), _ptr(p))
+    bad = lib.oracle_softmax_row(_ptr(x), dt, int(row), V, float(temperature), int(top_k), float(top_p), _ptr(p))
     return p, bool(bad)
+
+
+def filter_cut(logits, dt, row, temperature=1.0, top_k=0, top_p=1.0):
+    """Smallest logit top-k / top-p keep in row ``row`` (-inf: no filter)."""
+    lib = _load()
+    x = _logits(logits, dt)
+    return lib.oracle_filter_cut(_ptr(x), dt, int(row), x.shape[-1], float(temperature), int(top_k), float(top_p))
+
+
+def q40_weight(d, c):
+    """The nucleus decision's fixed-point weight of a logit difference d <= 0
+    at scale c (both fp32)."""
+    return int(_load().oracle_q40_weight(float(d), float(c)))
 
 
 def realign_plan(S, length, pad, n_emit):

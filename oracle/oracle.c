@@ -86,7 +86,12 @@ enum {
     MUT_SKIP_KV_SHIFT = 7,    /* realign updates lengths but moves no KV    */
     MUT_STALE_POSITIONS = 8,  /* position/mask rebuild writes nothing       */
     MUT_BONUS_ALWAYS = 9,     /* bonus appended even after a rejection      */
-    MUT_SHIFT_ONE_SHORT = 10  /* KV run moved one row short                 */
+    MUT_SHIFT_ONE_SHORT = 10, /* KV run moved one row short                 */
+    MUT_TOPK_STRICT = 11,     /* top-k drops the ties at the k-th value     */
+    MUT_TOPP_BELOW = 12,      /* nucleus = largest top set of mass <= top_p */
+    MUT_RATIO_UNFILTERED = 13,/* ratio test on p before the transforms      */
+    MUT_RESID_UNFILTERED = 14,/* residual built from p before the transforms*/
+    MUT_TOPP_FIRST = 15       /* top-p applied before top-k                 */
 };
 static int g_mutant = MUT_NONE;
 void oracle_set_mutant(int m) { g_mutant = m; }
@@ -206,6 +211,165 @@ static int softmax_row(const void *x, int dtype, int64_t off, int V, double T, d
     return bad;
 }
 
+/* ------------------------------------------------------------------ */
+/* O2b  sampling transforms: temperature, top-k, top-p                  */
+/* ------------------------------------------------------------------ */
+
+/*
+ * The ratio test, the residual and the bonus use the distribution the sampler
+ * actually draws from: "if temperature, Top-k, or Top-p is applied, retain the
+ * processed probabilities" ([ZS] §5.1), the same transforms on the same
+ * events ([AL] "The mechanism" step 1).  The pages name the transforms
+ * without defining them; this oracle takes the usual definitions, applied in
+ * the order temperature, top-k, top-p:
+ *
+ *   top-k (k >= 1, off when k <= 0 or k >= V): keep the tokens whose logit is
+ *     at least the k-th largest logit (counting repeats), so tokens tied with
+ *     the k-th value are all kept;
+ *   top-p (off when top_p >= 1 or NaN): among the top-k survivors, keep token
+ *     v iff the mass of the tokens with a strictly larger logit is below
+ *     top_p * (total mass) -- the smallest set of top values whose mass
+ *     reaches top_p, with ties at the boundary kept; the most probable value
+ *     is always kept (so top_p <= 0 keeps only it);
+ *   then p = softmax(x / T) renormalised over the kept tokens (fp64).
+ *
+ * The top-p boundary is a floating-point decision: at V ~ 1e5 the masses of
+ * neighbouring tokens differ by ~1e-6 of the total, below the error of any
+ * fp32 sum.  It is therefore taken in a stated precision, the same on every
+ * side that claims this definition:
+ *   c = fp32(log2(e) / T)        (T the fp32 temperature, quotient in double)
+ *   t = fp32(fp32(x_v - x_max) * c)
+ *   w = 2^t by range reduction (t = i + f, i = rint(t), |f| <= 1/2; Cody and
+ *       Waite) and the degree-7 Taylor polynomial of 2^f = e^(f ln 2)
+ *       evaluated in fp32 by Horner's rule with fused multiply-adds;
+ *   Q = floor(w * 2^40) as an unsigned 64-bit integer (0 for t < -64), and
+ *       every mass in the decision is an exact integer sum of Q;
+ *   keep v iff x_v = x_max or double(A(v)) < double(top_p) * double(T_Q),
+ *       A(v) = sum of Q over kept-by-top-k tokens with a larger logit, T_Q the
+ *       sum over all kept-by-top-k tokens.
+ * Exact integer sums make the decision independent of summation order.
+ */
+
+/* (ln 2)^n / n!, n = 0..7, rounded to fp32 */
+static const float kExp2Taylor[8] = {
+    0x1p+0f, 0x1.62e430p-1f, 0x1.ebfbe0p-3f, 0x1.c6b08ep-5f,
+    0x1.3b2ab6p-7f, 0x1.5d87fep-10f, 0x1.430912p-13f, 0x1.ffcbfcp-17f,
+};
+
+/* Q40 weight of a logit whose difference to the row maximum is d (<= 0). */
+uint64_t oracle_q40_weight(float d, float c)
+{
+    float t = d * c;
+    if (!(t >= -64.0f))
+        return 0; /* also -inf */
+    float i = rintf(t);
+    float f = t - i;
+    float poly = kExp2Taylor[7];
+    for (int n = 6; n >= 0; --n)
+        poly = fmaf(poly, f, kExp2Taylor[n]);
+    float w = ldexpf(poly, (int)i + 40);
+    return (uint64_t)w;
+}
+
+typedef struct {
+    double x;
+    int v;
+} ValIdx;
+
+/* descending by value; equal values in index order (irrelevant to the result) */
+static int cmp_desc(const void *a, const void *b)
+{
+    const ValIdx *p = (const ValIdx *)a, *q = (const ValIdx *)b;
+    if (p->x > q->x)
+        return -1;
+    if (p->x < q->x)
+        return 1;
+    return (p->v > q->v) - (p->v < q->v);
+}
+
+/* Smallest kept logit (the keep test is x >= cut) of a row after top-k and
+   top-p; -inf when nothing is filtered.  vals is scratch of V entries. */
+static double filter_cut(const void *x, int dtype, int64_t off, int V, float T, int top_k, float top_p,
+                         ValIdx *vals)
+{
+    int use_k = top_k > 0 && top_k < V;
+    int use_p = top_p < 1.0f;
+    if (!use_k && !use_p)
+        return -INFINITY;
+    for (int v = 0; v < V; ++v) {
+        vals[v].x = logit_at(x, dtype, off + v);
+        vals[v].v = v;
+    }
+    qsort(vals, (size_t)V, sizeof *vals, cmp_desc);
+    double cut_k = -INFINITY;
+    if (use_k && g_mutant != MUT_TOPP_FIRST)
+        cut_k = vals[top_k - 1].x;
+    /* top-k survivors are vals[0 .. nk) */
+    int nk = 0;
+    while (nk < V && vals[nk].x >= cut_k && !(g_mutant == MUT_TOPK_STRICT && use_k && vals[nk].x == cut_k))
+        ++nk;
+    if (!use_p) {
+        if (nk == 0)
+            return INFINITY;
+        return vals[nk - 1].x;
+    }
+    const float c = (float)(1.44269504088896340736 / (double)T);
+    const float xmax = (float)vals[0].x;
+    uint64_t total = 0;
+    for (int i = 0; i < nk; ++i)
+        total += oracle_q40_weight((float)vals[i].x - xmax, c);
+    const double bound = (double)top_p * (double)total;
+    uint64_t above = 0;
+    int i = 0;
+    double cut = vals[0].x;
+    while (i < nk) {
+        int e = i; /* the group of values equal to vals[i] */
+        uint64_t gm = 0;
+        while (e < nk && vals[e].x == vals[i].x) {
+            gm += oracle_q40_weight((float)vals[e].x - xmax, c);
+            ++e;
+        }
+        int keep = (i == 0) || ((double)above < bound);
+        if (g_mutant == MUT_TOPP_BELOW)
+            keep = (i == 0) || ((double)(above + gm) <= bound);
+        if (!keep)
+            break;
+        cut = vals[i].x;
+        above += gm;
+        i = e;
+    }
+    if (g_mutant == MUT_TOPP_FIRST && use_k) {
+        /* mistaken order: the top-k cut taken after the nucleus */
+        double ck = vals[top_k - 1].x;
+        if (ck > cut)
+            cut = ck;
+    }
+    return cut;
+}
+
+/* p = the processed distribution of one row: softmax(x / T) restricted to the
+   tokens top-k and top-p keep, renormalised, in fp64.  Returns the undefined
+   flag of softmax_row (no filtering is applied to an undefined row). */
+static int processed_row(const void *x, int dtype, int64_t off, int V, double T, int top_k, float top_p, double *p,
+                         ValIdx *vals)
+{
+    int bad = softmax_row(x, dtype, off, V, T, p);
+    if (bad)
+        return bad;
+    double cut = filter_cut(x, dtype, off, V, (float)T, top_k, top_p, vals);
+    if (cut == -INFINITY)
+        return 0;
+    double s = 0.0;
+    for (int v = 0; v < V; ++v) {
+        if (!(logit_at(x, dtype, off + v) >= cut))
+            p[v] = 0.0;
+        s += p[v];
+    }
+    for (int v = 0; v < V; ++v)
+        p[v] /= s;
+    return 0;
+}
+
 /* Inverse CDF of the weights w[0..V) at uniform u in [0,1): the smallest i
    whose sequential fp64 prefix sum C_i exceeds u * sum(w).  If rounding leaves
    no such i, the last index with positive weight.  A zero-weight index is
@@ -263,11 +427,16 @@ void oracle_verify_sample(const void *logits, int dtype, double temperature,
                           const int32_t *draft_len, int32_t eos_id,
                           const int32_t *remaining, int32_t *out_tokens,
                           int32_t *n_accept, int32_t *n_emit, double *out_residual,
-                          uint32_t *flags)
+                          uint32_t *flags, const int32_t *top_k, const float *top_p)
 {
-    double *p = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
-    double *w = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    size_t nv = (size_t)(V > 0 ? V : 1);
+    double *p = (double *)malloc(sizeof(double) * nv);
+    double *w = (double *)malloc(sizeof(double) * nv);
+    double *praw = (double *)malloc(sizeof(double) * nv);
+    ValIdx *vals = (ValIdx *)malloc(sizeof(ValIdx) * nv);
     for (int b = 0; b < B; ++b) {
+        int tk = top_k ? top_k[b] : 0;
+        float tp = top_p ? top_p[b] : 1.0f;
         int kb = draft_len ? draft_len[b] : k;
         int64_t rem = remaining ? remaining[b] : INT64_MAX;
         int32_t *out = out_tokens + (int64_t)b * (k + 1);
@@ -280,8 +449,11 @@ void oracle_verify_sample(const void *logits, int dtype, double temperature,
             for (int j = 0; j < kb; ++j) {
                 int y = draft_tokens[(int64_t)b * k + j];
                 const float *q = draft_probs + ((int64_t)b * k + j) * V;
-                if (softmax_row(logits, dtype, ((int64_t)b * (k + 1) + j) * V, V, temperature, p))
+                const int64_t roff = ((int64_t)b * (k + 1) + j) * V;
+                if (processed_row(logits, dtype, roff, V, temperature, tk, tp, p, vals))
                     fl |= 4;
+                if (g_mutant == MUT_RATIO_UNFILTERED || g_mutant == MUT_RESID_UNFILTERED)
+                    softmax_row(logits, dtype, roff, V, temperature, praw);
                 /* a proposal outside the vocabulary has no probability under
                    either model: flag 8 and treat it as rejected */
                 int valid = y >= 0 && y < V;
@@ -289,7 +461,8 @@ void oracle_verify_sample(const void *logits, int dtype, double temperature,
                     fl |= 8;
                 if (valid && q[y] == 0.0f)
                     fl |= 1;
-                double ratio = valid ? p[y] / (double)q[y] : 0.0;
+                const double *pr = (g_mutant == MUT_RATIO_UNFILTERED) ? praw : p;
+                double ratio = valid ? pr[y] / (double)q[y] : 0.0;
                 if (valid && (double)u[j] < ratio) {
                     out[ne++] = y;
                     na++;
@@ -301,8 +474,9 @@ void oracle_verify_sample(const void *logits, int dtype, double temperature,
                 }
                 /* first rejection: correction from the positive residual */
                 double total = 0.0;
+                const double *pw = (g_mutant == MUT_RESID_UNFILTERED) ? praw : p;
                 for (int v = 0; v < V; ++v) {
-                    double d = p[v] - (double)q[v];
+                    double d = pw[v] - (double)q[v];
                     w[v] = (g_mutant == MUT_NO_CLAMP) ? d : (d > 0.0 ? d : 0.0);
                     total += w[v];
                 }
@@ -323,7 +497,8 @@ void oracle_verify_sample(const void *logits, int dtype, double temperature,
                     for (int v = 0; v < V; ++v)
                         w[v] = (double)q[v];
                 } else {
-                    if (softmax_row(logits, dtype, ((int64_t)b * (k + 1) + kb) * V, V, temperature, p))
+                    if (processed_row(logits, dtype, ((int64_t)b * (k + 1) + kb) * V, V, temperature, tk, tp, p,
+                                      vals))
                         fl |= 4;
                     memcpy(w, p, sizeof(double) * (size_t)V);
                 }
@@ -348,13 +523,29 @@ void oracle_verify_sample(const void *logits, int dtype, double temperature,
     }
     free(p);
     free(w);
+    free(praw);
+    free(vals);
 }
 
-/* fp64 softmax of one logits row, exported for the tests' tolerance
-   accounting (they recompute p/q and CDF boundaries next to a mismatch). */
-int oracle_softmax_row(const void *logits, int dtype, int64_t row, int V, double T, double *p)
+/* fp64 processed distribution of one logits row (top_k <= 0 and top_p >= 1:
+   plain softmax), exported for the tests' tolerance accounting (they
+   recompute p/q and CDF boundaries next to a mismatch). */
+int oracle_softmax_row(const void *logits, int dtype, int64_t row, int V, double T, int top_k, float top_p,
+                       double *p)
 {
-    return softmax_row(logits, dtype, row * V, V, T, p);
+    ValIdx *vals = (ValIdx *)malloc(sizeof(ValIdx) * (size_t)(V > 0 ? V : 1));
+    int bad = processed_row(logits, dtype, row * V, V, T, top_k, top_p, p, vals);
+    free(vals);
+    return bad;
+}
+
+/* The smallest kept logit of a row after top-k / top-p (-inf: no filter). */
+double oracle_filter_cut(const void *logits, int dtype, int64_t row, int V, float T, int top_k, float top_p)
+{
+    ValIdx *vals = (ValIdx *)malloc(sizeof(ValIdx) * (size_t)(V > 0 ? V : 1));
+    double cut = filter_cut(logits, dtype, row * V, V, T, top_k, top_p, vals);
+    free(vals);
+    return cut;
 }
 
 /* ------------------------------------------------------------------ */

@@ -1,0 +1,193 @@
+"""Pins of the oracle's sampling transforms (top-k, top-p, temperature) on
+the target distribution of stochastic verification (CPU only).
+
+The pages require the ratio test, the residual and the bonus to use the
+processed distribution ("Chapter 10 Speculative Decoding (Code Walkthrough)",
+§5.1; "Speculative decoding: proposals and verified output", "The mechanism"
+step 1) without defining the transforms.  Pinned here:
+  - a hand-worked example with exact power-of-two weights (tests/golden);
+  - brute force on tiny inputs in exact rational arithmetic, from the
+    definitions restated independently (top-k: fewer than k tokens strictly
+    larger; top-p: the smallest upper set of mass >= top_p);
+  - top_k = 1 (and top_p -> 0) turns stochastic verification into greedy
+    verification, checked against the greedy oracle;
+  - top_k >= V, top_p = 1 leave every output unchanged;
+  - the committed token's distribution equals the processed distribution
+    (midpoint grid over the uniforms), and acceptance = sum min(p', q);
+  - the fixed-point weight of the nucleus decision against 2^t;
+  - five planted mistakes each fail at least one of these.
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from conftest import golden
+from oracle import DT_F32
+
+T_UNIT = float(np.float32(np.log2(np.e)))  # fp32(log2 e): the decision scale c is exactly 1
+
+
+def _case_table():
+    g = golden("filter_worked_example.txt")
+    cases = {"none": (0, 1.0), "k1": (1, 1.0), "k2": (2, 1.0), "k3": (3, 1.0), "k4": (4, 1.0),
+             "p0500": (0, 0.5), "p0625": (0, 0.625), "p0875": (0, 0.875), "p09375": (0, 0.9375),
+             "k3p05625": (3, 0.5625)}
+    return g, cases
+
+
+def test_worked_example():
+    g, cases = _case_table()
+    x = np.array(g["x"], np.float32)[None]
+    for name, (tk, tp) in cases.items():
+        p, bad = oracle.softmax_row(x, DT_F32, 0, T_UNIT, tk, tp)
+        assert not bad
+        assert np.allclose(p, g[name], atol=1e-7), (name, p)
+        cut = oracle.filter_cut(x, DT_F32, 0, T_UNIT, tk, tp)
+        want = x[0][np.array(g[name]) > 0].min()
+        assert cut == (-np.inf if name == "none" else want) or (cut == want), (name, cut)
+
+
+def test_temperature_enters_the_nucleus():
+    """Doubling the logits and the temperature leaves the processed
+    distribution unchanged; doubling the logits alone sharpens it and top-p
+    keeps fewer tokens."""
+    g, _ = _case_table()
+    x = np.array(g["x"], np.float32)[None]
+    T2 = float(np.float32(2 * T_UNIT))
+    p1, _ = oracle.softmax_row(x, DT_F32, 0, T_UNIT, 0, 0.875)
+    p2, _ = oracle.softmax_row(2 * x, DT_F32, 0, T2, 0, 0.875)
+    assert np.allclose(p1, p2, atol=1e-7)
+    p3, _ = oracle.softmax_row(2 * x, DT_F32, 0, T_UNIT, 0, 0.875)
+    assert np.count_nonzero(p3) == 2 and np.count_nonzero(p1) == 3
+
+
+def _brute_kept(x, top_k, top_p):
+    """Kept set from the definitions, exact rationals; weights 2^x (integer x,
+    scale exactly 1)."""
+    V = len(x)
+    w = [Fraction(2) ** int(v) for v in x]
+    keep = [True] * V
+    if 0 < top_k < V:
+        keep = [sum(1 for u in x if u > x[v]) < top_k for v in range(V)]
+    if top_p < 1.0:
+        tot = sum(w[v] for v in range(V) if keep[v])
+        bound = Fraction(float(np.float32(top_p))) * tot
+        for t in sorted({x[v] for v in range(V) if keep[v]}, reverse=True):
+            upper = [v for v in range(V) if keep[v] and x[v] >= t]
+            if sum(w[v] for v in upper) >= bound:
+                keep = [v in upper for v in range(V)]
+                break
+    return keep
+
+
+def test_brute_force_tiny_rows():
+    rng = np.random.default_rng(7)
+    for _ in range(3000):
+        V = int(rng.integers(1, 8))
+        x = rng.integers(-6, 1, size=V).astype(np.float32)
+        top_k = int(rng.integers(0, V + 2))
+        top_p = float(np.float32(rng.choice([rng.random(), 1.0, 0.0, rng.integers(1, 16) / 16])))
+        p, bad = oracle.softmax_row(x[None], DT_F32, 0, T_UNIT, top_k, top_p)
+        keep = _brute_kept(list(x), top_k, top_p)
+        assert not bad
+        assert list(p > 0) == keep, (x, top_k, top_p, p)
+        w = np.where(keep, 2.0 ** x.astype(np.float64), 0.0)
+        assert np.allclose(p, w / w.sum(), atol=1e-7)
+
+
+def _round_inputs(rng, B, k, V, sigma=2.0):
+    x = (rng.standard_normal((B, k + 1, V)) * sigma).astype(np.float32)
+    dl = x[:, :k] + rng.standard_normal((B, k, V)).astype(np.float32)
+    q = np.exp(dl - dl.max(-1, keepdims=True))
+    q = (q / q.sum(-1, keepdims=True)).astype(np.float32)
+    d = np.array([[rng.choice(V, p=q[b, j] / q[b, j].sum()) for j in range(k)] for b in range(B)], np.int32)
+    u = rng.random((B, k + 1)).astype(np.float32)
+    return x, q, d, u
+
+
+def test_top_k_one_is_greedy():
+    """With top_k = 1 (or top_p = 0) the processed p is one-hot at the argmax:
+    a proposal is accepted iff it is the argmax and the correction or bonus is
+    the argmax, so the round equals greedy verification."""
+    rng = np.random.default_rng(11)
+    x, q, d, u = _round_inputs(rng, 64, 4, 50)
+    # make half of the proposals the argmax so that rounds run long
+    am = x[:, :4].argmax(-1).astype(np.int32)
+    d = np.where(rng.random(d.shape) < 0.7, am, d).astype(np.int32)
+    g_out, g_na, g_ne = oracle.verify_greedy(x, DT_F32, d)
+    for kw in (dict(top_k=1), dict(top_p=0.0), dict(top_k=1, top_p=0.3)):
+        out, na, ne, fl, _ = oracle.verify_sample(x, DT_F32, q, d, u, **kw)
+        assert np.array_equal(out, g_out) and np.array_equal(na, g_na) and np.array_equal(ne, g_ne), kw
+
+
+def test_off_values_change_nothing():
+    rng = np.random.default_rng(12)
+    x, q, d, u = _round_inputs(rng, 32, 3, 40)
+    ref = oracle.verify_sample(x, DT_F32, q, d, u, want_residual=True)
+    for kw in (dict(top_k=0, top_p=1.0), dict(top_k=40, top_p=1.0), dict(top_k=1000), dict(top_p=np.nan),
+               dict(top_k=-3, top_p=1.5)):
+        got = oracle.verify_sample(x, DT_F32, q, d, u, want_residual=True, **kw)
+        for a, b in zip(ref, got):
+            assert np.array_equal(a, b), kw
+
+
+def exact_first_token_distribution(x, q, top_k, top_p, n=600):
+    """Distribution of the first committed token for k = 1 and proposal y ~ q,
+    the uniforms swept over an n x n midpoint grid (target rows 0 and 1 equal)."""
+    V = len(x)
+    ug = ((np.arange(n) + 0.5) / n).astype(np.float32)
+    u0, u1 = np.meshgrid(ug, ug, indexing="ij")
+    Bn = n * n
+    xx = np.broadcast_to(np.stack([x, x]).astype(np.float32), (Bn, 2, V)).copy()
+    qq = np.broadcast_to(np.asarray(q, np.float32), (Bn, 1, V)).copy()
+    u = np.stack([u0.ravel(), u1.ravel()], axis=1)
+    dist, acc = np.zeros(V), 0.0
+    for y in range(V):
+        if q[y] == 0:
+            continue
+        out, na, _, _, _ = oracle.verify_sample(xx, DT_F32, qq, np.full((Bn, 1), y, np.int32), u,
+                                                temperature=T_UNIT, top_k=top_k, top_p=top_p)
+        dist += q[y] * np.bincount(out[:, 0], minlength=V) / Bn
+        acc += q[y] * na.mean()
+    return dist, acc
+
+
+@pytest.mark.parametrize("name", ["k2", "k3", "p0625", "p0875", "k3p05625"])
+def test_output_distribution_is_the_processed_target(name):
+    g, cases = _case_table()
+    tk, tp = cases[name]
+    x = np.array(g["x"], np.float32)
+    q = np.array([0.3, 0.1, 0.25, 0.15, 0.2])
+    dist, acc = exact_first_token_distribution(x, q, tk, tp)
+    pp = np.array(g[name])
+    assert np.allclose(dist, pp, atol=4e-3), (name, dist)
+    assert abs(acc - np.minimum(pp, q).sum()) < 4e-3
+
+
+def test_q40_weight_against_powers_of_two():
+    for t in range(-64, 1):
+        assert oracle.q40_weight(float(t), 1.0) == (2 ** (40 + t) if t >= -40 else 0)
+    assert oracle.q40_weight(-65.0, 1.0) == 0 and oracle.q40_weight(-np.inf, 1.0) == 0
+    rng = np.random.default_rng(3)
+    for t in rng.uniform(-30, 0, size=4000).astype(np.float32):
+        want = 2.0 ** (40 + float(t))
+        got = oracle.q40_weight(float(t), 1.0)
+        assert abs(got - want) <= want * 2.5e-7 + 1.0, (t, got, want)
+
+
+@pytest.mark.parametrize("mut", ["topk_strict", "topp_below", "ratio_unfiltered", "resid_unfiltered",
+                                 "topp_first"])
+def test_planted_mistakes_fail_a_pin(mut):
+    checks = [test_worked_example, test_top_k_one_is_greedy, test_brute_force_tiny_rows,
+              lambda: [test_output_distribution_is_the_processed_target(n)
+                       for n in ("k2", "k3", "p0625", "p0875", "k3p05625")]]
+    failed = 0
+    with oracle.mutant(mut):
+        for c in checks:
+            try:
+                c()
+            except AssertionError:
+                failed += 1
+    assert failed >= 1, mut
