@@ -151,6 +151,36 @@ SPEC_API int spec_verify_sample(const void *target_logits, spec_dtype dt, float 
                        void *workspace, size_t workspace_bytes, void *cuda_stream);
 
 /*
+ * Stochastic verification with top-k / top-p applied to the target
+ * distribution: the ratio test, the residual and the bonus use the processed
+ * distribution ([ZS] §5.1: with temperature, Top-k or Top-p, keep the
+ * processed probabilities; [AL] "The mechanism" step 1).  Order: temperature,
+ * top-k, top-p.  Per sequence b:
+ *   top_k[b] in (0, V): keep the logits >= the k-th largest (ties kept);
+ *     <= 0 or >= V: off.  top_k == NULL: off for every sequence.
+ *   top_p[b] < 1: among those, keep v iff the mass of strictly larger logits
+ *     is below top_p[b] times their total (the smallest set of top values
+ *     reaching top_p, ties kept; the largest value is always kept, so
+ *     top_p <= 0 keeps only it); >= 1 or NaN: off.  top_p == NULL: off.
+ *   p = softmax(x / T) renormalised over the kept tokens.
+ * The top-p boundary is decided on exact integer sums of fixed-point weights
+ * Q = floor(2^40 * 2^t), t = fp32(fp32(x - x_max) * fp32(log2(e) / T)), 2^t by
+ * range reduction and the degree-7 Taylor polynomial of 2^f evaluated in fp32
+ * with fused multiply-adds, so the kept set does not depend on summation
+ * order.  The draft probabilities are taken as given: they must already be
+ * the draft's processed distribution.
+ * Everything else -- arguments, layouts, flags, outputs, errors -- is as in
+ * spec_verify_sample; top_k [B] int32 and top_p [B] fp32 are device arrays
+ * (4-byte aligned).  With both NULL this is spec_verify_sample.
+ */
+SPEC_API int spec_verify_sample_filtered(const void *target_logits, spec_dtype dt, float temperature,
+                                const int32_t *top_k, const float *top_p, const float *draft_probs,
+                                const int32_t *draft_tokens, const float *uniforms, int B, int k, int V,
+                                const int32_t *draft_len, int32_t eos_id, const int32_t *remaining,
+                                int32_t *out_tokens, int32_t *n_accept, int32_t *n_emit, float *out_residual,
+                                uint32_t *flags, void *workspace, size_t workspace_bytes, void *cuda_stream);
+
+/*
  * Realignment of a contiguous left-padded KV cache after a round
  * ("unpad-append-repad", [CF] §3.2 and App. B).
  * Layout: kv [L, 2, B, H, S, D] of `dt` elements; the (layer, K/V, sequence,

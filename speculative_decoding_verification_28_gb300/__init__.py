@@ -33,5 +33,6 @@ from .api import (  # noqa: F401
     spec_verify_greedy_static,
     STATIC_SCRATCH_BYTES,
     spec_verify_sample,
+    spec_verify_sample_filtered,
     spec_workspace_bytes,
 )

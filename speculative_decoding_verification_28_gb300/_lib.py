@@ -21,6 +21,8 @@ SIGNATURES = {
                             _vp], _i32),
     "spec_verify_sample": ([_vp, _i32, _f32, _vp, _vp, _vp, _i32, _i32, _i32, _vp, ctypes.c_int32, _vp, _vp, _vp,
                             _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "spec_verify_sample_filtered": ([_vp, _i32, _f32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, ctypes.c_int32,
+                                     _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "spec_realign_kv": ([_vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
                         _i32),
     "spec_rebuild_pos_mask": ([_i32, _i32, _vp, _vp, _vp, _vp, _vp], _i32),

@@ -157,6 +157,33 @@ def spec_verify_sample(target_logits, draft_probs, draft_tokens, uniforms, tempe
                        out_residual=None, flags=None, want_residual=False, workspace=None, stream=None):
     """-> (out_tokens, n_accept, n_emit, flags [B] int32 view of the uint32
     flag words, out_residual [B, V] fp32 or None)."""
+    return _verify_sample(None, None, target_logits, draft_probs, draft_tokens, uniforms, temperature, draft_len,
+                          eos_id, remaining, out_tokens, n_accept, n_emit, out_residual, flags, want_residual,
+                          workspace, stream)
+
+
+def spec_verify_sample_filtered(target_logits, draft_probs, draft_tokens, uniforms, top_k=None, top_p=None,
+                                temperature=1.0, draft_len=None, eos_id=-1, remaining=None, out_tokens=None,
+                                n_accept=None, n_emit=None, out_residual=None, flags=None, want_residual=False,
+                                workspace=None, stream=None):
+    """spec_verify_sample on the target distribution after top-k / top-p.
+    top_k: None, an int for every sequence, or [B] int32 on the device;
+    top_p: None, a float for every sequence, or [B] fp32 on the device."""
+    B = target_logits.shape[0]
+    dev = target_logits.device
+    if top_k is not None and not torch.is_tensor(top_k):
+        top_k = torch.full((B,), int(top_k), dtype=torch.int32, device=dev)
+    if top_p is not None and not torch.is_tensor(top_p):
+        top_p = torch.full((B,), float(top_p), dtype=torch.float32, device=dev)
+    _need(top_k, torch.int32, "top_k", dev, (B,))
+    _need(top_p, torch.float32, "top_p", dev, (B,))
+    return _verify_sample(top_k, top_p, target_logits, draft_probs, draft_tokens, uniforms, temperature, draft_len,
+                          eos_id, remaining, out_tokens, n_accept, n_emit, out_residual, flags, want_residual,
+                          workspace, stream)
+
+
+def _verify_sample(top_k, top_p, target_logits, draft_probs, draft_tokens, uniforms, temperature, draft_len, eos_id,
+                   remaining, out_tokens, n_accept, n_emit, out_residual, flags, want_residual, workspace, stream):
     lib = _lib.load()
     B, k1, V = target_logits.shape
     k = k1 - 1
@@ -179,10 +206,17 @@ def spec_verify_sample(target_logits, draft_probs, draft_tokens, uniforms, tempe
     _need(flags, torch.int32, "flags", dev, (B,))
     st = _stream(stream, dev)
     ws = _workspace(workspace, B, k, V, dev, st)
-    _check(lib.spec_verify_sample(_p(target_logits), _DT[target_logits.dtype], float(temperature),
-                                  _p(draft_probs), _p(draft_tokens), _p(uniforms), B, k, V, _p(draft_len),
-                                  int(eos_id), _p(remaining), _p(out_tokens), _p(n_accept), _p(n_emit),
-                                  _p(out_residual), _p(flags), ws.ptr(), ws.nbytes, st))
+    if top_k is None and top_p is None:
+        _check(lib.spec_verify_sample(_p(target_logits), _DT[target_logits.dtype], float(temperature),
+                                      _p(draft_probs), _p(draft_tokens), _p(uniforms), B, k, V, _p(draft_len),
+                                      int(eos_id), _p(remaining), _p(out_tokens), _p(n_accept), _p(n_emit),
+                                      _p(out_residual), _p(flags), ws.ptr(), ws.nbytes, st))
+    else:
+        _check(lib.spec_verify_sample_filtered(_p(target_logits), _DT[target_logits.dtype], float(temperature),
+                                               _p(top_k), _p(top_p), _p(draft_probs), _p(draft_tokens),
+                                               _p(uniforms), B, k, V, _p(draft_len), int(eos_id), _p(remaining),
+                                               _p(out_tokens), _p(n_accept), _p(n_emit), _p(out_residual),
+                                               _p(flags), ws.ptr(), ws.nbytes, st))
     return out_tokens, n_accept, n_emit, flags, out_residual
 
 

@@ -115,11 +115,12 @@ int spec_verify_greedy(const void *target_logits, spec_dtype dt, int B, int k, i
     return launched(launch_verify_greedy(a, dt, (cudaStream_t)cuda_stream));
 }
 
-int spec_verify_sample(const void *target_logits, spec_dtype dt, float temperature, const float *draft_probs,
-                       const int32_t *draft_tokens, const float *uniforms, int B, int k, int V,
-                       const int32_t *draft_len, int32_t eos_id, const int32_t *remaining, int32_t *out_tokens,
-                       int32_t *n_accept, int32_t *n_emit, float *out_residual, uint32_t *flags,
-                       void *workspace, size_t workspace_bytes, void *cuda_stream)
+static int verify_sample_impl(const void *target_logits, spec_dtype dt, float temperature, const int32_t *top_k,
+                              const float *top_p, const float *draft_probs, const int32_t *draft_tokens,
+                              const float *uniforms, int B, int k, int V, const int32_t *draft_len, int32_t eos_id,
+                              const int32_t *remaining, int32_t *out_tokens, int32_t *n_accept, int32_t *n_emit,
+                              float *out_residual, uint32_t *flags, void *workspace, size_t workspace_bytes,
+                              void *cuda_stream)
 {
     int rc = check_verify_common(target_logits, dt, B, k, V, draft_tokens, out_tokens, n_accept, n_emit);
     if (rc != SPEC_OK || B == 0)
@@ -127,7 +128,8 @@ int spec_verify_sample(const void *target_logits, spec_dtype dt, float temperatu
     if (!(temperature > 0.0f) || !(temperature <= 3.0e38f) || !uniforms || (k > 0 && !draft_probs))
         return SPEC_EINVAL;
     if (!aligned(uniforms, 4) || (draft_probs && !aligned(draft_probs, 4)) ||
-        (out_residual && !aligned(out_residual, 4)) || (flags && !aligned(flags, 4)))
+        (out_residual && !aligned(out_residual, 4)) || (flags && !aligned(flags, 4)) ||
+        (top_k && !aligned(top_k, 4)) || (top_p && !aligned(top_p, 4)))
         return SPEC_EALIGN;
     rc = check_workspace(workspace, workspace_bytes, spec_workspace_bytes(B, k, V));
     if (rc != SPEC_OK)
@@ -151,7 +153,34 @@ int spec_verify_sample(const void *target_logits, spec_dtype dt, float temperatu
     a.u = uniforms;
     a.out_residual = out_residual;
     a.flags = flags;
+    a.filtered = (top_k || top_p) ? 1 : 0;
+    a.top_k = top_k;
+    a.top_p = top_p;
+    a.dec_scale = (float)(1.44269504088896340736 / (double)temperature);
     return launched(launch_verify_sample(a, dt, (cudaStream_t)cuda_stream));
+}
+
+int spec_verify_sample(const void *target_logits, spec_dtype dt, float temperature, const float *draft_probs,
+                       const int32_t *draft_tokens, const float *uniforms, int B, int k, int V,
+                       const int32_t *draft_len, int32_t eos_id, const int32_t *remaining, int32_t *out_tokens,
+                       int32_t *n_accept, int32_t *n_emit, float *out_residual, uint32_t *flags,
+                       void *workspace, size_t workspace_bytes, void *cuda_stream)
+{
+    return verify_sample_impl(target_logits, dt, temperature, nullptr, nullptr, draft_probs, draft_tokens, uniforms,
+                              B, k, V, draft_len, eos_id, remaining, out_tokens, n_accept, n_emit, out_residual,
+                              flags, workspace, workspace_bytes, cuda_stream);
+}
+
+int spec_verify_sample_filtered(const void *target_logits, spec_dtype dt, float temperature, const int32_t *top_k,
+                                const float *top_p, const float *draft_probs, const int32_t *draft_tokens,
+                                const float *uniforms, int B, int k, int V, const int32_t *draft_len,
+                                int32_t eos_id, const int32_t *remaining, int32_t *out_tokens, int32_t *n_accept,
+                                int32_t *n_emit, float *out_residual, uint32_t *flags, void *workspace,
+                                size_t workspace_bytes, void *cuda_stream)
+{
+    return verify_sample_impl(target_logits, dt, temperature, top_k, top_p, draft_probs, draft_tokens, uniforms, B,
+                              k, V, draft_len, eos_id, remaining, out_tokens, n_accept, n_emit, out_residual, flags,
+                              workspace, workspace_bytes, cuda_stream);
 }
 
 int spec_realign_kv_multi(const spec_kv_cache *caches, int n_caches, int B, int S, const int32_t *len,

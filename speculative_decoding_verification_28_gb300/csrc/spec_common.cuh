@@ -65,7 +65,7 @@ struct Layout {
     // counters that every verify call leaves at zero
     size_t zero_begin, seq_cnt, stop_enc, res_cnt, row_cnt, zero_end;
     // verify scratch
-    size_t row_tok, row_ms, row_flag, part, draw_row, rpart, rtot;
+    size_t row_tok, row_ms, row_flag, row_cut, part, draw_row, rpart, rtot;
     size_t total;
 };
 
@@ -99,6 +99,7 @@ __host__ __device__ inline Layout make_layout(int B, int k, int V)
     L.row_tok = take(rows * 4);
     L.row_ms = take(rows * 8);
     L.row_flag = take(rows * 4);
+    L.row_cut = take(rows * 4);
     L.part = take(rows * C * 16);
     L.draw_row = take(b * 4);
     L.rpart = take(b * (size_t)draw_chunks(V > 0 ? V : 1) * 8);

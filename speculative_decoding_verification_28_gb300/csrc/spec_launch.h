@@ -35,6 +35,12 @@ struct VerifyArgs {
     const float *u;
     float *out_residual;
     uint32_t *flags;
+    // top-k / top-p (filtered = 0: neither, the plain statistics kernel runs)
+    int filtered;
+    const int32_t *top_k;  // [B] or null
+    const float *top_p;    // [B] or null
+    float dec_scale;       // fp32(log2(e) / T), the scale of the top-p decision weights
+    float *row_cut;        // workspace: smallest kept logit per row
 };
 
 // fills C, chunk and the workspace pointers of `a` from B, k, V and ws

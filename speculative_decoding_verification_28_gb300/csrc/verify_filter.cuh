@@ -1,0 +1,368 @@
+// verify_filter.cuh -- top-k / top-p on the target rows of stochastic
+// verification (included by verify_sample.cu, which owns the launch).
+//
+// The ratio test, the residual and the bonus use the distribution the target
+// samples from ("Chapter 10 Speculative Decoding (Code Walkthrough)", §5.1:
+// with temperature, top-k or top-p the processed probabilities are kept;
+// "Speculative decoding: proposals and verified output", "The mechanism"
+// step 1).  Definitions (temperature, then top-k, then top-p):
+//   top-k, 0 < k < V: keep x >= the k-th largest logit (ties kept);
+//   top-p, top_p < 1: among those, keep v iff the mass of strictly larger
+//     logits is below top_p times their total (ties kept; the largest value
+//     always kept);
+//   p = softmax(x / T) renormalised over the kept tokens.
+// The top-p boundary is decided on exact integer sums of fixed-point weights
+// Q = floor(2^40 * w), w = 2^t with t = fp32(fp32(x - x_max) * c) and
+// c = fp32(log2(e) / T): t = i + f, i = rint(t), |f| <= 1/2 (Cody-Waite range
+// reduction) and 2^f from its degree-7 Taylor polynomial (coefficients
+// (ln 2)^n / n! in fp32) by Horner's rule with fused multiply-adds.  Integer
+// sums do not depend on the order of summation, so the decision is
+// reproducible; the kept token probabilities use the same ex2-based softmax
+// as the unfiltered path.
+//
+// One CTA per target row (rows j-major, skipped once an earlier stop of the
+// sequence is known, as in the statistics kernel).  Pass 1 reads the row
+// from HBM: maximum, softmax sum, flags.  The cuts are radix selections on an
+// order-preserving 32-bit key of the logit, 11-bit digits (two levels for
+// 16-bit logits, whose keys carry at most 22 significant bits; three for
+// fp32): each level is one more pass over the row (now in L2) building
+// per-digit counts and Q masses in shared memory, then a block scan from the
+// top digit finds the digit holding the k-th largest key (counts) or the
+// top-p boundary (masses).  Roofline: HBM reads V * sizeof(T) per needed row;
+// the later passes are L2 reads plus shared-memory atomics.
+#pragma once
+
+#include "sample_final.cuh"
+
+namespace spec {
+
+constexpr int kFBins = 2048;
+
+struct FilterHist {
+    unsigned int cnt[kFBins];
+    unsigned long long mass[kFBins];
+};
+
+struct FilterSel {
+    int bin;                       // selected digit
+    unsigned int cnt_above;        // count of the digits above it (this level)
+    unsigned long long mass_above; // Q mass of the digits above it (this level)
+    double bound;                  // top_p * total Q mass (set at the first top-p level)
+    int low_thread;                // last thread holding a non-empty digit
+};
+
+// order-preserving key of a logit; -0 and +0 share one key
+__device__ __forceinline__ uint32_t order_key(float f)
+{
+    uint32_t u = __float_as_uint(f);
+    if (f == 0.0f)
+        u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// digit layout: level 0 = key bits 31..21, level 1 = bits 20..10, level 2 =
+// bits 9..0
+__device__ __forceinline__ int lvl_shift(int l) { return l == 0 ? 21 : (l == 1 ? 10 : 0); }
+__device__ __forceinline__ int lvl_bins(int l) { return l == 2 ? 1024 : 2048; }
+template <typename T>
+struct KeyLevels {
+    static constexpr int kLevels = 2;  // 16-bit logits: keys carry <= 22 significant bits
+};
+template <>
+struct KeyLevels<float> {
+    static constexpr int kLevels = 3;
+};
+
+// Q40 weight of a logit at difference d = x - x_max (<= 0) and scale c
+__device__ __forceinline__ unsigned long long q40_weight(float d, float c)
+{
+    const float t = __fmul_rn(d, c);
+    if (!(t >= -64.0f))
+        return 0ull;
+    const float i = rintf(t);
+    const float f = __fsub_rn(t, i);
+    float p = 0x1.ffcbfcp-17f;
+    p = __fmaf_rn(p, f, 0x1.430912p-13f);
+    p = __fmaf_rn(p, f, 0x1.5d87fep-10f);
+    p = __fmaf_rn(p, f, 0x1.3b2ab6p-7f);
+    p = __fmaf_rn(p, f, 0x1.c6b08ep-5f);
+    p = __fmaf_rn(p, f, 0x1.ebfbe0p-3f);
+    p = __fmaf_rn(p, f, 0x1.62e430p-1f);
+    p = __fmaf_rn(p, f, 1.0f);
+    const float scale = __int_as_float(((int)i + 40 + 127) << 23);  // 2^(i+40), i in [-64, 0]
+    return __float2ull_rz(__fmul_rn(p, scale));
+}
+
+// f(x) for every logit of the row: 16-byte vectors, scalar head and tail
+template <typename T, typename F>
+__device__ __forceinline__ void row_for_each(const T *row, int V, F &f)
+{
+    constexpr int VEC = Storage<T>::kVec;
+    constexpr int UNROLL = 4;
+    const ChunkSplit<T> cs(row, 0, V);
+    const int t = threadIdx.x;
+    for (int v = t; v < cs.head_end; v += kThreads)
+        f(Storage<T>::at(row, v));
+    const T *body = row + cs.head_end;
+    for (int base = 0; base < cs.nvec; base += UNROLL * kThreads) {
+        uint4 r[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int vi = base + t + u * kThreads;
+            if (vi < cs.nvec)
+                r[u] = ld_stream16(body + (size_t)vi * VEC);
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int vi = base + t + u * kThreads;
+            if (vi < cs.nvec) {
+                float e[VEC];
+                Storage<T>::unpack(r[u], e);
+#pragma unroll
+                for (int q = 0; q < VEC; ++q)
+                    f(e[q]);
+            }
+        }
+    }
+    for (int v = cs.tail_beg + t; v < V; v += kThreads)
+        f(Storage<T>::at(row, v));
+}
+
+__device__ __forceinline__ void hist_clear(FilterHist &h, int nb)
+{
+    for (int i = threadIdx.x; i < nb; i += kThreads) {
+        h.cnt[i] = 0u;
+        h.mass[i] = 0ull;
+    }
+}
+
+// Counts (and Q masses) per digit of level l over the logits whose key is
+// >= lo_key and whose higher digits equal `prefix`.
+template <typename T, bool kMass>
+__device__ void hist_pass(const T *row, int V, int l, uint32_t prefix, uint32_t lo_key, float xmax, float cdec,
+                          FilterHist &h)
+{
+    const int sh = lvl_shift(l), msk = lvl_bins(l) - 1;
+    const int shp = (l == 0) ? 0 : lvl_shift(l - 1);
+    auto add = [&](float x) {
+        const uint32_t key = order_key(x);
+        if (key < lo_key || (l > 0 && (key >> shp) != prefix))
+            return;
+        const int dg = (int)((key >> sh) & (uint32_t)msk);
+        atomicAdd(&h.cnt[dg], 1u);
+        if (kMass)
+            atomicAdd(&h.mass[dg], q40_weight(__fsub_rn(x, xmax), cdec));
+    };
+    row_for_each<T>(row, V, add);
+}
+
+// First digit from the top whose inclusive cumulative count reaches `need`
+// (counts), or the first non-empty digit from the top with
+// double(base + cumulative mass) >= bound (masses; bound = top_p * total at
+// the first level).  With masses and no such digit, the lowest non-empty one.
+// Thread t owns digits nb-1-tP .. nb-P-tP (P = nb / kThreads), scanned in
+// descending order.  Ends with a barrier; the result is in `sel`.
+template <bool kMass>
+__device__ void hist_select(const FilterHist &h, int nb, unsigned int need, unsigned long long base, float top_p,
+                            bool first_level, FilterSel &sel, unsigned int *s_wc, unsigned long long *s_wm)
+{
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int P = nb / kThreads, top = nb - 1 - t * P;
+    unsigned int lc = 0;
+    unsigned long long lm = 0;
+    for (int i = 0; i < P; ++i) {
+        lc += h.cnt[top - i];
+        lm += h.mass[top - i];
+    }
+    unsigned int ic = lc;
+    unsigned long long im = lm;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned int oc = __shfl_up_sync(0xFFFFFFFFu, ic, o);
+        const unsigned long long om = __shfl_up_sync(0xFFFFFFFFu, im, o);
+        if (lane >= o) {
+            ic += oc;
+            im += om;
+        }
+    }
+    if (lane == 31) {
+        s_wc[w] = ic;
+        s_wm[w] = im;
+    }
+    if (t == 0) {
+        sel.bin = -1;
+        sel.low_thread = -1;
+    }
+    __syncthreads();
+    unsigned int cb = ic - lc;
+    unsigned long long mb = im - lm, total = 0;
+    for (int i = 0; i < kThreads / 32; ++i) {
+        if (i < w) {
+            cb += s_wc[i];
+            mb += s_wm[i];
+        }
+        total += s_wm[i];
+    }
+    double bound = 0.0;
+    if (kMass)
+        bound = first_level ? (double)top_p * (double)total : sel.bound;
+    const bool earlier = kMass ? (cb > 0u && (double)(base + mb) >= bound) : (cb >= need);
+    if (!earlier) {
+        unsigned int cc = cb;
+        unsigned long long mm = mb;
+        for (int i = 0; i < P; ++i) {
+            const int bin = top - i;
+            const unsigned int c1 = h.cnt[bin];
+            const unsigned long long m1 = h.mass[bin];
+            const bool hit = kMass ? (c1 > 0u && (double)(base + mm + m1) >= bound) : (cc + c1 >= need);
+            if (hit) {
+                sel.bin = bin;
+                sel.cnt_above = cc;
+                sel.mass_above = mm;
+                break;
+            }
+            cc += c1;
+            mm += m1;
+        }
+    }
+    if (kMass && lc > 0u)
+        atomicMax(&sel.low_thread, t);
+    __syncthreads();
+    if (kMass) {
+        if (sel.bin < 0 && t == sel.low_thread) {
+            unsigned int cc = cb;
+            unsigned long long mm = mb;
+            int lowest = -1;
+            unsigned int c_at = 0;
+            unsigned long long m_at = 0;
+            for (int i = 0; i < P; ++i) {
+                const int bin = top - i;
+                if (h.cnt[bin] > 0u) {
+                    lowest = bin;
+                    c_at = cc;
+                    m_at = mm;
+                }
+                cc += h.cnt[bin];
+                mm += h.mass[bin];
+            }
+            sel.bin = lowest;
+            sel.cnt_above = c_at;
+            sel.mass_above = m_at;
+        }
+        if (first_level && t == 0)
+            sel.bound = bound;
+        __syncthreads();
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) verify_filter_kernel(VerifyArgs a)
+{
+    constexpr int L = KeyLevels<T>::kLevels;
+    __shared__ FilterHist h;
+    __shared__ float s_f[4 * kThreads / 32];
+    __shared__ unsigned int s_wc[kThreads / 32];
+    __shared__ unsigned long long s_wm[kThreads / 32];
+    __shared__ FilterSel sel;
+    __shared__ float s_m, s_s, s_xmax;
+    __shared__ int s_bad, s_skip;
+    const float c = scale_of(a);
+    const Unit u = decode_unit(a);
+    const T *row = reinterpret_cast<const T *>(a.logits) + (size_t)u.row * a.V;
+    const int t = threadIdx.x;
+    if (t == 0)
+        s_skip = (!u.needed || stopped_before(a.stop_enc, u.b, u.j)) ? 1 : 0;
+    __syncthreads();
+    float cut = -INFINITY, s_kept = 0.0f;
+    if (!s_skip) {
+        float m, s, xm;
+        bool bad;
+        chunk_softmax_stats<T, true>(row, 0, a.V, c, m, s, bad, s_f, StopProbe{a.stop_enc, u.b, u.j}, &xm);
+        if (t == 0) {
+            s_m = m;
+            s_s = s;
+            s_xmax = xm;
+            s_bad = (bad || !(s > 0.0f) || !(s <= FLT_MAX)) ? 1 : 0;
+            s_skip = stopped_before(a.stop_enc, u.b, u.j) ? 1 : 0;
+        }
+        __syncthreads();
+        const int tk = a.top_k ? a.top_k[u.b] : 0;
+        const float tp = a.top_p ? a.top_p[u.b] : 1.0f;
+        const bool use_k = tk > 0 && tk < a.V, use_p = tp < 1.0f;
+        s_kept = s_s;
+        if (!s_skip && !s_bad && (use_k || use_p)) {
+            const float xmax = s_xmax, cdec = a.dec_scale;
+            uint32_t K = 0u;
+            unsigned long long kept_mass = 0ull;
+            if (use_k) {
+                uint32_t prefix = 0u;
+                unsigned int need = (unsigned int)tk;
+                unsigned long long above = 0ull;
+                for (int l = 0; l < L; ++l) {
+                    const int nb = lvl_bins(l);
+                    hist_clear(h, nb);
+                    __syncthreads();
+                    if (use_p)
+                        hist_pass<T, false>(row, a.V, l, prefix, 0u, xmax, cdec, h);
+                    else
+                        hist_pass<T, true>(row, a.V, l, prefix, 0u, xmax, cdec, h);
+                    __syncthreads();
+                    hist_select<false>(h, nb, need, 0ull, 0.0f, false, sel, s_wc, s_wm);
+                    const int bin = sel.bin < 0 ? 0 : sel.bin;  // a digit is always found
+                    need -= sel.cnt_above;
+                    above += sel.mass_above;
+                    if (l == L - 1)
+                        kept_mass = above + h.mass[bin];
+                    prefix = (l == 0) ? (uint32_t)bin : ((prefix << (lvl_shift(l - 1) - lvl_shift(l))) | (uint32_t)bin);
+                    __syncthreads();
+                }
+                K = prefix << lvl_shift(L - 1);
+            }
+            if (use_p) {
+                uint32_t prefix = 0u;
+                unsigned long long A = 0ull;
+                for (int l = 0; l < L; ++l) {
+                    const int nb = lvl_bins(l);
+                    hist_clear(h, nb);
+                    __syncthreads();
+                    hist_pass<T, true>(row, a.V, l, prefix, K, xmax, cdec, h);
+                    __syncthreads();
+                    hist_select<true>(h, nb, 0u, A, tp, l == 0, sel, s_wc, s_wm);
+                    const int bin = sel.bin < 0 ? 0 : sel.bin;  // a digit is always found
+                    A += sel.mass_above;
+                    if (l == L - 1)
+                        kept_mass = A + h.mass[bin];
+                    prefix = (l == 0) ? (uint32_t)bin : ((prefix << (lvl_shift(l - 1) - lvl_shift(l))) | (uint32_t)bin);
+                    __syncthreads();
+                }
+                K = prefix << lvl_shift(L - 1);
+            }
+            const uint32_t low = (1u << lvl_shift(L - 1)) - 1u;  // key bits below the last digit
+            cut = key_value(K | ((K & 0x80000000u) ? 0u : low));
+            s_kept = (float)((double)kept_mass * 0x1p-40);
+        }
+    }
+    if (t >= 32)
+        return;
+    int eval = 0;
+    if (t == 0)
+        eval = (u.needed && !stopped_before(a.stop_enc, u.b, u.j)) ? 1 : 0;
+    if (eval)
+        sample_row_decide<T>(a, u, row, s_m, s_kept, cut, s_bad != 0);
+    sample_seq_finish(a, u);
+}
+
+template <typename T>
+cudaError_t launch_filter_rows(const VerifyArgs &args, cudaStream_t st)
+{
+    VerifyArgs f = args;
+    f.C = 1;  // one CTA per row
+    verify_filter_kernel<T><<<(unsigned)(f.B * (f.k + 1)), kThreads, 0, st>>>(f);
+    return cudaGetLastError();
+}
+
+}  // namespace spec

@@ -207,6 +207,7 @@ void resolve_verify_args(VerifyArgs &a)
     a.draw_row = ws_at<int>(a.ws, lay.draw_row);
     a.row_ms = ws_at<float2>(a.ws, lay.row_ms);
     a.row_flag = ws_at<uint32_t>(a.ws, lay.row_flag);
+    a.row_cut = ws_at<float>(a.ws, lay.row_cut);
     a.part = ws_at<void>(a.ws, lay.part);
     a.rpart = ws_at<float>(a.ws, lay.rpart);
     a.rtot = ws_at<double>(a.ws, lay.rtot);

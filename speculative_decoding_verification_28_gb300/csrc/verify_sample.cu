@@ -28,30 +28,29 @@
 #include <float.h>
 
 #include "bulk_copy.cuh"
-#include "verify_common.cuh"
+#include "sample_final.cuh"
 
 namespace spec {
 
-struct RowStats {
-    float m, s;  // base-2 row maximum of x * c and sum of 2^(x c - m)
-};
-
-__device__ __forceinline__ float scale_of(const VerifyArgs &a) { return a.unit_temp ? kLog2e : a.inv_temp * kLog2e; }
 
 // ---------------------------------------------------------------------------
 // stats kernel
 // ---------------------------------------------------------------------------
-template <typename T>
+// kRaw: also the unscaled maximum of the logits (to xmax_out of warp 0;
+// s_f then needs 4 * kThreads / 32 floats)
+template <typename T, bool kRaw>
 __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float &m_out, float &s_out,
-                                    bool &bad_out, float *s_f, const StopProbe &probe)
+                                    bool &bad_out, float *s_f, const StopProbe &probe, float *xmax_out)
 {
     constexpr int VEC = Storage<T>::kVec;
     constexpr int UNROLL = 4;
     const ChunkSplit<T> cs(row, lo, hi);
-    float m = -INFINITY, s = 0.0f;
+    float m = -INFINITY, s = 0.0f, xr = -INFINITY;
     bool bad = false;
     // one element (head / tail)
     auto add1 = [&](float x) {
+        if (kRaw)
+            xr = max_nan(xr, x);
         const float z = x * c;
         bad |= !(z < INFINITY);  // NaN or +inf; -inf is a masked token
         if (z > m) {
@@ -80,7 +79,10 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
         for (int u = 0; u < UNROLL; ++u) {
             const int vi = i + u * kThreads;
             if (vi < cs.nvec) {
-                const float vm = vec_max<T>(r[u]) * c;  // c > 0: the maximum commutes with the scale
+                const float vraw = vec_max<T>(r[u]);
+                if (kRaw)
+                    xr = max_nan(xr, vraw);
+                const float vm = vraw * c;  // c > 0: the maximum commutes with the scale
                 bad |= !(vm < INFINITY);                // NaN or +inf in the vector
                 if (vm > m) {
                     s = (m > -INFINITY) ? s * exp2f(m - vm) : 0.0f;
@@ -112,10 +114,17 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
     for (int k = 16; k > 0; k >>= 1)
         merge(m, s, __shfl_xor_sync(0xFFFFFFFFu, m, k), __shfl_xor_sync(0xFFFFFFFFu, s, k));
     const bool wbad = __any_sync(0xFFFFFFFFu, bad);
+    if (kRaw) {
+#pragma unroll
+        for (int k = 16; k > 0; k >>= 1)
+            xr = max_nan(xr, __shfl_xor_sync(0xFFFFFFFFu, xr, k));
+    }
     if (l == 0) {
         s_f[w] = m;
         s_f[kThreads / 32 + w] = wbad ? -s : s;  // the sign carries the warp's flag (s >= 0)
         s_f[2 * (kThreads / 32) + w] = wbad ? 1.0f : 0.0f;
+        if (kRaw)
+            s_f[3 * (kThreads / 32) + w] = xr;
     }
     __syncthreads();
     if (t < 32) {
@@ -128,6 +137,13 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
         m_out = mm;
         s_out = ss;
         bad_out = __any_sync(0xFFFFFFFFu, bb);
+        if (kRaw) {
+            float xx = (l < kThreads / 32) ? s_f[3 * (kThreads / 32) + l] : -INFINITY;
+#pragma unroll
+            for (int k = 16; k > 0; k >>= 1)
+                xx = max_nan(xx, __shfl_xor_sync(0xFFFFFFFFu, xx, k));
+            *xmax_out = xx;
+        }
     }
 }
 
@@ -136,11 +152,8 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(VerifyArgs a)
 {
     __shared__ float s_f[3 * kThreads / 32];
     __shared__ int s_skip, s_last;  // written once each: no read/write race between them
-    int *stop_enc = a.stop_enc, *row_cnt = a.row_cnt, *seq_cnt = a.seq_cnt, *row_acc = a.row_tok;
-    RowStats *row_ms = reinterpret_cast<RowStats *>(a.row_ms);
-    uint32_t *row_flag = a.row_flag;
+    int *stop_enc = a.stop_enc, *row_cnt = a.row_cnt;
     float4 *part = static_cast<float4 *>(a.part);
-    int *draw_row = a.draw_row;
     const float c = scale_of(a);
 
     const Unit u = decode_unit(a);
@@ -153,7 +166,7 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(VerifyArgs a)
         const int hi = min(a.V, lo + a.chunk);
         float m, s;
         bool bad;
-        chunk_softmax_stats<T>(row, lo, hi, c, m, s, bad, s_f, StopProbe{stop_enc, u.b, u.j});
+        chunk_softmax_stats<T, false>(row, lo, hi, c, m, s, bad, s_f, StopProbe{stop_enc, u.b, u.j}, nullptr);
         if (threadIdx.x == 0)
             part[(size_t)u.row * a.C + u.c] = make_float4(m, s, bad ? 1.0f : 0.0f, 0.0f);
     }
@@ -194,83 +207,19 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(VerifyArgs a)
             s += __shfl_xor_sync(0xFFFFFFFFu, s, k);
             bad = fmaxf(bad, __shfl_xor_sync(0xFFFFFFFFu, bad, k));
         }
-        if (lane == 0) {
-            uint32_t fl = (bad > 0.0f || !(s <= FLT_MAX) || !(s > 0.0f)) ? SPEC_FLAG_NONFINITE : 0u;
-            int acc = 0;
-            bool stop;
-            if (u.j < u.kb) {
-                const int y = a.draft[(size_t)u.b * a.k + u.j];
-                if (y < 0 || y >= a.V) {
-                    fl |= SPEC_FLAG_BAD_TOKEN;
-                } else {
-                    const float py = exp2f(fmaf(Storage<T>::at(row, y), c, -m)) / s;
-                    const float qy = a.q[((size_t)u.b * a.k + u.j) * a.V + y];
-                    if (qy == 0.0f)
-                        fl |= SPEC_FLAG_Q_ZERO;
-                    acc = (a.u[(size_t)u.b * (a.k + 1) + u.j] < py / qy) ? 1 : 0;
-                }
-                stop = !acc || (a.eos >= 0 && y == a.eos) || (u.j + 1 == u.rem);
-            } else {
-                stop = true;  // the bonus row ends the round
-            }
-            row_acc[u.row] = acc;
-            row_ms[u.row] = RowStats{m, s};
-            row_flag[u.row] = fl;
-            if (stop)
-                atomicMax(stop_enc + u.b, kStopBase - u.j);
-        }
+        if (lane == 0)
+            sample_row_decide<T>(a, u, row, m, s, -INFINITY, bad > 0.0f);
     }
-    int last_row = 0;
-    if (lane == 0) {
+    if (lane == 0)
         row_cnt[u.row] = 0;
-        __threadfence();
-        last_row = (atomicAdd(seq_cnt + u.b, 1) == a.k) ? 1 : 0;
-    }
-    last_row = __shfl_sync(0xFFFFFFFFu, last_row, 0);
-    if (!last_row)
-        return;
-    __threadfence();
-
-    // sequence finaliser: first stop by ballot, commit the accepted prefix,
-    // hand the draw (correction or bonus) to the draw kernel
-    const int b = u.b, kb = u.kb, rem = u.rem, j = lane;
-    int acc = 0, d = -1;
-    uint32_t fl = 0;
-    bool stop = false;
-    if (j <= a.k && rem > 0) {
-        acc = row_acc[b * (a.k + 1) + j];
-        fl = row_flag[b * (a.k + 1) + j];
-        if (j < kb) {
-            d = a.draft[(size_t)b * a.k + j];
-            stop = !acc || (a.eos >= 0 && d == a.eos) || (j + 1 == rem);
-        } else {
-            stop = (j == kb);
-        }
-    }
-    const unsigned mask = __ballot_sync(0xFFFFFFFFu, stop);
-    const int js = mask ? __ffs(mask) - 1 : -1;
-    const int acc_js = __shfl_sync(0xFFFFFFFFu, acc, js < 0 ? 0 : js);
-    const bool accepted_stop = js >= 0 && js < kb && acc_js;  // EOS / budget on an accepted proposal
-    uint32_t seq_fl = (j <= js) ? fl : 0u;
-#pragma unroll
-    for (int k = 16; k > 0; k >>= 1)
-        seq_fl |= __shfl_xor_sync(0xFFFFFFFFu, seq_fl, k);
-    if (j <= a.k) {
-        int tok = -1;
-        if (j < js || (j == js && accepted_stop))
-            tok = d;
-        a.out_tokens[(size_t)b * (a.k + 1) + j] = tok;
-    }
-    if (lane == 0) {
-        a.n_emit[b] = js + 1;
-        a.n_accept[b] = js < 0 ? 0 : (accepted_stop ? js + 1 : js);
-        draw_row[b] = (js >= 0 && !accepted_stop) ? js : -1;
-        if (a.flags)
-            a.flags[b] = seq_fl;
-        seq_cnt[b] = 0;
-        stop_enc[b] = 0;
-    }
+    sample_seq_finish(a, u);
 }
+
+}  // namespace spec
+
+#include "verify_filter.cuh"
+
+namespace spec {
 
 // ---------------------------------------------------------------------------
 // draw kernel: inverse CDF of the residual (or of p) for one row per sequence
@@ -279,8 +228,9 @@ template <typename T>
 struct DrawRow {
     const T *x;      // target logits row
     const float *q;  // draft row (residual mode) or nullptr
-    float m, inv_s, c;  // base-2 row maximum, 1 / sum, scale log2(e)/T
-    __device__ float p(float x_v) const { return exp2_sfu(fmaf(x_v, c, -m)) * inv_s; }
+    float m, inv_s, c;  // base-2 row maximum, 1 / kept sum, scale log2(e)/T
+    float cut;          // smallest kept logit (-inf: no top-k / top-p)
+    __device__ float p(float x_v) const { return (x_v >= cut) ? exp2_sfu(fmaf(x_v, c, -m)) * inv_s : 0.0f; }
     __device__ float pv(int v) const { return p(Storage<T>::at(x, v)); }
     // weight of index v; residual mode needs q
     __device__ float w(int v, bool residual) const
@@ -300,6 +250,7 @@ __device__ DrawRow<T> draw_row_of(const VerifyArgs &a, int b, int r, int kb)
     d.m = ms.m;
     d.inv_s = 1.0f / ms.s;
     d.c = scale_of(a);
+    d.cut = a.filtered ? a.row_cut[b * (a.k + 1) + r] : -INFINITY;
     return d;
 }
 
@@ -631,7 +582,13 @@ static cudaError_t launch_sample_t(const VerifyArgs &args, cudaStream_t st)
     resolve_verify_args(a);
     const unsigned g1 = (unsigned)(a.B * (a.k + 1) * a.C);
     const unsigned g2 = (unsigned)(a.B * draw_chunks(a.V));
-    verify_stats_kernel<T><<<g1, kThreads, 0, st>>>(a);
+    if (a.filtered) {
+        const cudaError_t ef = launch_filter_rows<T>(a, st);
+        if (ef != cudaSuccess)
+            return ef;
+    } else {
+        verify_stats_kernel<T><<<g1, kThreads, 0, st>>>(a);
+    }
     // the draw kernel becomes resident while the stats kernel drains and
     // waits for it on the device (griddepcontrol.wait)
     cudaLaunchAttribute attr;

@@ -89,6 +89,18 @@ def test_sample_argument_errors(lib):
     assert sample(u=FAKE_ODD) == -5
 
 
+def test_filtered_sample_argument_errors(lib):
+    def sample(temp=1.0, tk=FAKE, tp=FAKE, u=FAKE):
+        return lib.spec_verify_sample_filtered(FAKE, 0, temp, tk, tp, FAKE, FAKE, u, 2, 2, 50, None, -1, None, FAKE,
+                                               FAKE, FAKE, None, None, FAKE, 1 << 30, None)
+
+    assert sample(temp=0.0) == -1
+    assert sample(u=None) == -1
+    assert sample(tk=FAKE_ODD) == -5
+    assert sample(tp=FAKE_ODD) == -5
+    assert sample(tk=FAKE, tp=None, u=FAKE_ODD) == -5
+
+
 def test_realign_argument_errors(lib):
     def realign(kv=FAKE, dt=1, L=2, B=3, H=2, S=64, D=8, ws=FAKE, wsb=1 << 20, err=FAKE):
         return lib.spec_realign_kv(kv, dt, L, B, H, S, D, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, err, ws, wsb, None)

@@ -1,0 +1,133 @@
+"""Stochastic verification with top-k / top-p on the target distribution:
+the CUDA path (spec_verify_sample_filtered) vs the CPU oracle.
+
+Same bar as the unfiltered stochastic tests (tokens and counts equal except
+counted boundary decisions of the ratio test or the draw; normalised draw
+distributions within 1e-6), plus: the kept set itself is exact -- wherever a
+sequence draws its bonus from the processed target distribution, the support
+of that distribution equals the oracle's.  Both sides decide the top-p
+boundary with the same stated fixed-point arithmetic, so it has no tolerance.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_verification_28_gb300 as sv
+from gpu_util import DT_OF, dev, storage_of, to_dev
+from specgen import CONFIGS, sample_round_inputs
+from specgen import torch_gen
+from test_gpu_verify_sample import STATS, check
+
+pytestmark = pytest.mark.gpu
+
+
+def _params(rng, B, V):
+    """Per-sequence top_k / top_p covering off values, the extremes and
+    typical settings."""
+    tk = rng.choice([0, 1, 2, 5, 50, V - 1, V, V + 7, -1, int(rng.integers(1, V + 1))], size=B).astype(np.int32)
+    tp = rng.choice([1.0, 0.0, 1e-6, 0.3, 0.5, 0.8, 0.9, 0.95, 0.999, np.nan, float(rng.random())],
+                    size=B).astype(np.float32)
+    return tk, tp
+
+
+@pytest.mark.parametrize("V", [2, 3, 8, 100, 8193, 20000])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_small_vocabularies(V, dtype):
+    B = 1024 if V <= 100 else 64
+    rng = np.random.default_rng(V + 7)
+    x, q, d, u = sample_round_inputs(B, 3, V, 0.8, seed=V + 1, dtype=dtype)
+    tk, tp = _params(rng, B, V)
+    check(x, DT_OF[dtype], q, d, u, top_k=tk, top_p=tp)
+
+
+@pytest.mark.parametrize("only", ["k", "p"])
+def test_one_transform_at_a_time(only):
+    rng = np.random.default_rng(3 if only == "k" else 4)
+    B, k, V = 128, 4, 30000
+    x, q, d, u = sample_round_inputs(B, k, V, 0.5, seed=33, dtype="bf16")
+    tk, tp = _params(rng, B, V)
+    check(x, oracle.DT_BF16, q, d, u, top_k=tk if only == "k" else None, top_p=tp if only == "p" else None)
+
+
+def test_ties_at_the_cut():
+    """Coarsely quantised logits: many tokens share each value, so the k-th
+    value and the top-p boundary fall inside groups of equal logits."""
+    rng = np.random.default_rng(5)
+    B, k, V = 256, 3, 4000
+    x, q, d, u = sample_round_inputs(B, k, V, 0.5, seed=55, dtype="f32")
+    x = (np.round(x * 4) / 4).astype(np.float32)
+    tk, tp = _params(rng, B, V)
+    check(x, oracle.DT_F32, q, d, u, top_k=tk, top_p=tp)
+    check(x, oracle.DT_F32, q, d, u, top_k=np.full(B, 37, np.int32), top_p=np.full(B, 0.9, np.float32))
+
+
+@pytest.mark.parametrize("T", [0.6, 1.0, 2.5])
+def test_temperature_with_transforms(T):
+    rng = np.random.default_rng(int(T * 10))
+    B, k, V = 96, 4, 12000
+    x, q, d, u = sample_round_inputs(B, k, V, 0.5, seed=int(T * 100), dtype="f32")
+    tk, tp = _params(rng, B, V)
+    check(x, oracle.DT_F32, q, d, u, T=T, top_k=tk, top_p=tp)
+
+
+def test_masked_tokens_and_stop_rules():
+    rng = np.random.default_rng(9)
+    B, k, V = 256, 5, 2000
+    x, q, d, u = sample_round_inputs(B, k, V, 0.4, seed=99, dtype="bf16")
+    xf = x.astype(np.uint32) << 16
+    mask = rng.random(x.shape) < 0.7
+    mask[np.arange(B)[:, None], np.arange(k)[None, :], d] = False  # proposals stay finite
+    xf[mask] = np.uint32(0xFF800000)  # -inf
+    xm = (xf >> 16).astype(np.uint16)
+    tk, tp = _params(rng, B, V)
+    dl = rng.integers(0, k + 1, size=B).astype(np.int32)
+    rem = rng.integers(0, k + 3, size=B).astype(np.int32)
+    check(xm, oracle.DT_BF16, q, d, u, draft_len=dl, eos=int(rng.integers(0, V)), remaining=rem, top_k=tk, top_p=tp)
+
+
+def test_top_k_one_equals_greedy_on_device():
+    """top_k = 1 turns stochastic verification into greedy verification where
+    every row's maximum is unique (fp32 logits; tied maxima are all kept by
+    top-k and then sampled, while greedy takes the lowest index)."""
+    B, k, V = 128, 4, 50000
+    x, q, d, u = sample_round_inputs(B, k, V, 0.3, seed=7, dtype="f32")
+    top2 = np.sort(x, axis=-1)[..., -2:]
+    assert (top2[..., 1] > top2[..., 0]).all()
+    best = x[:, :k].argmax(-1).astype(np.int32)
+    d = np.where(np.random.default_rng(1).random((B, k)) < 0.8, best, d).astype(np.int32)
+    xt = to_dev(x)
+    g = sv.spec_verify_sample_filtered(xt, to_dev(q), to_dev(d), to_dev(u), top_k=1)
+    gg = sv.spec_verify_greedy(xt, to_dev(d))
+    assert np.array_equal(g[0].cpu().numpy(), gg[0].cpu().numpy())
+    assert np.array_equal(g[2].cpu().numpy(), gg[2].cpu().numpy())
+
+
+def test_config3_shape_typical_settings():
+    """B=32, k=4, V=128256 fp32 with top_k=50 / top_p=0.9 and mixed settings."""
+    c = CONFIGS["c3"]
+    g = torch.Generator(device=dev()).manual_seed(2003)
+    rng = np.random.default_rng(2003)
+    for r in range(3):
+        xt, qt, dt_, ut = torch_gen.sample_round_inputs(c["B"], c["k"], c["V"], c["noise"], g, torch.float32, dev())
+        if r == 0:
+            tk, tp = np.full(c["B"], 50, np.int32), np.full(c["B"], 0.9, np.float32)
+        else:
+            tk, tp = _params(rng, c["B"], c["V"])
+        check(xt.cpu().numpy(), oracle.DT_F32, qt.cpu().numpy(), dt_.cpu().numpy(), ut.cpu().numpy(),
+              top_k=tk, top_p=tp)
+
+
+def test_config5_shape_bf16():
+    """B=64 of config 5's rows (k=8, V=128256 bf16), top_p = 0.95."""
+    c = CONFIGS["c5"]
+    g = torch.Generator(device=dev()).manual_seed(2005)
+    xt, qt, dt_, ut = torch_gen.sample_round_inputs(64, c["k"], c["V"], c["noise"], g, torch.bfloat16, dev())
+    check(storage_of(xt), oracle.DT_BF16, qt.cpu().numpy(), dt_.cpu().numpy(), ut.cpu().numpy(),
+          top_k=None, top_p=np.full(64, 0.95, np.float32))
+
+
+def test_zz_filter_statistics():
+    assert STATS.get("kept_sets", 0) > 500, STATS
+    assert STATS["boundary"] < 1e-4 * max(STATS["decisions"], 1) + 1, STATS
+    print("filtered sampling statistics:", STATS)

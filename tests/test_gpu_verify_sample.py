@@ -26,7 +26,14 @@ RES_TOL = 1e-6
 STATS = {"decisions": 0, "boundary": 0, "residual_rows": 0, "widened_rows": 0}
 
 
-def residual_tolerance(x, dt, q, T, b, k, row, bonus, r_o):
+def _per_seq(v, b):
+    if v is None:
+        return None
+    a = np.asarray(v)
+    return a.item() if a.ndim == 0 else a[b].item()
+
+
+def residual_tolerance(x, dt, q, T, b, k, row, bonus, r_o, top_k=None, top_p=None):
     """Per-element tolerance of the normalised draw distribution.
 
     1e-6 absolute, widened only where fp32 arithmetic cannot reach it:
@@ -35,7 +42,7 @@ def residual_tolerance(x, dt, q, T, b, k, row, bonus, r_o):
     amplified by p_v / W, and the error of W itself.  The bound used,
     1e-6 * (1 + (p_v + r_v * sum_{w>0} p) / W), is that estimate with a 3x
     margin; with large vocabularies (p_v << W) it is the plain 1e-6."""
-    p, _ = oracle.softmax_row(x.reshape(-1, x.shape[-1]), dt, b * (k + 1) + row, T)
+    p, _ = oracle.softmax_row(x.reshape(-1, x.shape[-1]), dt, b * (k + 1) + row, T, *_filt(top_k, top_p, b))
     w = p if bonus else np.maximum(p - q[b, row].astype(np.float64), 0.0)
     if not bonus and not (w.sum() > 0):
         w = p
@@ -44,7 +51,13 @@ def residual_tolerance(x, dt, q, T, b, k, row, bonus, r_o):
     return RES_TOL * (1.0 + (p + r_o * ppos) / W)
 
 
-def _boundary_explains(x, dt, q, d, u, T, b, o_out, o_na, o_ne, o_res, g_out, g_na, g_ne, kb):
+def _filt(top_k, top_p, b):
+    tk, tp = _per_seq(top_k, b), _per_seq(top_p, b)
+    return (0 if tk is None else int(tk)), (1.0 if tp is None else float(tp))
+
+
+def _boundary_explains(x, dt, q, d, u, T, b, o_out, o_na, o_ne, o_res, g_out, g_na, g_ne, kb, top_k=None,
+                       top_p=None):
     """True when the first difference between the two results of sequence b
     is a decision on a boundary of the oracle's arithmetic."""
     k = d.shape[1]
@@ -54,7 +67,7 @@ def _boundary_explains(x, dt, q, d, u, T, b, o_out, o_na, o_ne, o_res, g_out, g_
         if j >= o_ne or j >= g_ne:
             break
         if (j < o_na) != (j < g_na):
-            p, _ = oracle.softmax_row(x.reshape(-1, x.shape[-1]), dt, b * (k + 1) + j, T)
+            p, _ = oracle.softmax_row(x.reshape(-1, x.shape[-1]), dt, b * (k + 1) + j, T, *_filt(top_k, top_p, b))
             y = int(d[b, j])
             r = p[y] / float(q[b, j, y])
             return abs(float(u[b, j]) - r) <= TOL * r
@@ -73,14 +86,24 @@ def _boundary_explains(x, dt, q, d, u, T, b, o_out, o_na, o_ne, o_res, g_out, g_
     return bool(np.all(np.abs(c[lo:hi] - uu) <= TOL * uu))
 
 
-def check(x, dt, q, d, u, T=1.0, draft_len=None, eos=-1, remaining=None, residual=True):
-    g = sv.spec_verify_sample(logits_to_dev(x, dt), to_dev(q), to_dev(d), to_dev(u), temperature=T,
-                              draft_len=None if draft_len is None else to_dev(draft_len), eos_id=eos,
-                              remaining=None if remaining is None else to_dev(remaining), want_residual=residual)
+def check(x, dt, q, d, u, T=1.0, draft_len=None, eos=-1, remaining=None, residual=True, top_k=None, top_p=None):
+    """top_k / top_p: None, or per-sequence numpy arrays (int32 / fp32): the
+    filtered entry point runs and the oracle applies the same transforms.
+    Where filtering is on, the support of every drawn bonus distribution
+    (the kept set itself) must equal the oracle's exactly."""
+    kw = dict(temperature=T, draft_len=None if draft_len is None else to_dev(draft_len), eos_id=eos,
+              remaining=None if remaining is None else to_dev(remaining), want_residual=residual)
+    if top_k is None and top_p is None:
+        g = sv.spec_verify_sample(logits_to_dev(x, dt), to_dev(q), to_dev(d), to_dev(u), **kw)
+    else:
+        g = sv.spec_verify_sample_filtered(logits_to_dev(x, dt), to_dev(q), to_dev(d), to_dev(u),
+                                           top_k=None if top_k is None else to_dev(np.asarray(top_k, np.int32)),
+                                           top_p=None if top_p is None else to_dev(np.asarray(top_p, np.float32)),
+                                           **kw)
     g_out, g_na, g_ne, g_fl = (t.cpu().numpy() for t in g[:4])
     g_res = g[4].cpu().numpy() if residual else None
     o_out, o_na, o_ne, o_fl, o_res = oracle.verify_sample(x, dt, q, d, u, T, draft_len, eos, remaining,
-                                                          want_residual=True)
+                                                          want_residual=True, top_k=top_k, top_p=top_p)
     B, k1 = o_out.shape
     kbs = np.full(B, k1 - 1) if draft_len is None else draft_len
     for b in range(B):
@@ -91,17 +114,21 @@ def check(x, dt, q, d, u, T=1.0, draft_len=None, eos=-1, remaining=None, residua
         same = (np.array_equal(g_out[b], o_out[b]) and g_na[b] == o_na[b] and g_ne[b] == o_ne[b])
         if not same:
             assert _boundary_explains(x, dt, q, d, u, T, b, o_out, o_na[b], o_ne[b], o_res, g_out, g_na[b],
-                                      g_ne[b], int(kbs[b])), (b, g_out[b], o_out[b], g_na[b], o_na[b])
+                                      g_ne[b], int(kbs[b]), top_k, top_p), (b, g_out[b], o_out[b], g_na[b], o_na[b])
             STATS["boundary"] += 1
             continue
         assert (int(g_fl[b]) & ~4) == (int(o_fl[b]) & ~4), (b, g_fl[b], o_fl[b])
         if residual and not np.isnan(o_res[b]).all():
             err = np.abs(g_res[b].astype(np.float64) - o_res[b])
             STATS["residual_rows"] += 1
+            row = int(o_na[b])
+            kb = int(kbs[b])
+            if (top_k is not None or top_p is not None) and (row == kb or int(o_fl[b]) & 2):
+                assert np.array_equal(g_res[b] > 0, o_res[b] > 0), (b, np.flatnonzero(g_res[b] > 0)[:20],
+                                                                     np.flatnonzero(o_res[b] > 0)[:20])
+                STATS["kept_sets"] = STATS.get("kept_sets", 0) + 1
             if err.max() > RES_TOL:
-                row = int(o_na[b])
-                kb = int(kbs[b])
-                tol = residual_tolerance(x, dt, q, T, b, k1 - 1, row, row == kb, o_res[b])
+                tol = residual_tolerance(x, dt, q, T, b, k1 - 1, row, row == kb, o_res[b], top_k, top_p)
                 assert (err <= tol).all(), (b, err.max(), tol[np.argmax(err - tol)])
                 STATS["widened_rows"] += 1
     return g, (o_out, o_na, o_ne, o_fl, o_res)
