@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--pool-lengths", choices=["a", "b"], default="a",
                     help="c4x pool lengths: a = U[128,1024] (as configured), b = uniform over {128, 256, ..., 1024}")
     ap.add_argument("--window", type=int, default=None, help="c4x: sliding window (default: the whole pool)")
+    ap.add_argument("--top-k", type=int, default=None, help="stochastic workloads: top-k on the target distribution")
+    ap.add_argument("--top-p", type=float, default=None, help="stochastic workloads: top-p on the target distribution")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the cache's layer count (small profiling captures only)")
     return ap.parse_args()
@@ -78,6 +80,9 @@ def workload_params(args):
     if args.layers:
         c["L"] = args.layers
     c["draft"] = tuple(int(x) for x in args.draft_cache.split(",")) if args.draft_cache else None
+    c["top_k"], c["top_p"] = args.top_k, args.top_p
+    if (args.top_k is not None or args.top_p is not None) and c["mode"] != "sample":
+        raise SystemExit("--top-k / --top-p apply to the stochastic workloads (c3, c5s)")
     if c["mode"] in ("greedy", "exspec"):
         c["alpha"] = args.alpha if args.alpha is not None else max(c["alphas"])
     else:
@@ -91,6 +96,8 @@ def describe(c):
         Ld, Hd, Dd = c["draft"]
         kv += f" + draft cache {Ld}x2x{c['B']}x{Hd}x{c['S']}x{Dd} bf16 (one multi-cache realignment)"
     s = f"{c['mode']} round: B={c['B']} k={c['k']} V={c['V']} {c['logit_dtype']} logits"
+    if c.get("top_k") is not None or c.get("top_p") is not None:
+        s += f", target top_k={c.get('top_k')} top_p={c.get('top_p')}"
     s += f", alpha={c['alpha']}" if c["alpha"] is not None else f", draft=target+N(0,{c['noise']})"
     return s + f"; KV {kv}; prompts U{list(c['prompt'])}"
 
@@ -285,11 +292,32 @@ class Round:
             self.tg.kv_write_query(self.draft, qtok[:, :-1].contiguous(), self.pos, self.W)
         self.flush.zero_()
 
+    def filtered(self):
+        return self.c.get("top_k") is not None or self.c.get("top_p") is not None
+
+    def filter_args(self):
+        """Per-sequence top_k / top_p device arrays (made once)."""
+        import torch
+
+        if not hasattr(self, "_filt"):
+            B = self.c["B"]
+            tk, tp = self.c.get("top_k"), self.c.get("top_p")
+            self._filt = (None if tk is None else torch.full((B,), tk, dtype=torch.int32, device=self.dev),
+                          None if tp is None else torch.full((B,), tp, dtype=torch.float32, device=self.dev))
+        return self._filt
+
+    def verify_sample(self, **kw):
+        if self.filtered():
+            tk, tp = self.filter_args()
+            return self.sv.spec_verify_sample_filtered(self.x, self.q, self.d, self.u, top_k=tk, top_p=tp,
+                                                       workspace=self.ws, **kw)
+        return self.sv.spec_verify_sample(self.x, self.q, self.d, self.u, workspace=self.ws, **kw)
+
     def verify(self):
         if self.c["mode"] == "greedy":
             _, self.na, ne = self.sv.spec_verify_greedy(self.x, self.d, workspace=self.ws)
         else:
-            _, self.na, ne, _, _ = self.sv.spec_verify_sample(self.x, self.q, self.d, self.u, workspace=self.ws)
+            _, self.na, ne, _, _ = self.verify_sample()
         return ne
 
     def verify_alg_bytes(self, ne):
@@ -433,7 +461,8 @@ def run_ours(args, c, rank, local_rank, world):
                    "parallelism": f"independent batch per GPU x{world}"},
         "roofline": roofline,
         "verify_roofline": {"bound": "hbm", "kernels": ("verify_greedy_kernel" if c["mode"] == "greedy" else
-                                                        "verify_stats_kernel + verify_draw_kernel"),
+                                                        ("verify_filter_kernel" if R.filtered() else
+                                                         "verify_stats_kernel") + " + verify_draw_kernel"),
                             "achieved": round(float(np.sum(verify_bytes) / (per[:, 1].sum() / 1e3) / 1e9), 1),
                             "peak": peak, "unit": "GB/s",
                             "frac": round(float(np.sum(verify_bytes) / (per[:, 1].sum() / 1e3) / 1e9) / peak, 4),
@@ -514,7 +543,7 @@ def run_e2e(args, R, st, dev, pg, world):
         if c["mode"] == "greedy":
             R.sv.spec_verify_greedy(R.x, R.d, out_tokens=out, n_accept=na, n_emit=ne, workspace=R.ws)
         else:
-            R.sv.spec_verify_sample(R.x, R.q, R.d, R.u, out_tokens=out, n_accept=na, n_emit=ne, workspace=R.ws)
+            R.verify_sample(out_tokens=out, n_accept=na, n_emit=ne)
         if R.draft is not None:
             R.sv.spec_realign_kv_multi([R.kv, R.draft], R.ln, R.pad, ne, len_new=ln_new, pad_new=pad_new,
                                        width_new=width, err=err, workspace=R.ws)
@@ -572,7 +601,7 @@ def oracle_rounds(c, n_rounds, seed, kv_host=None, state=None, R=None):
         else:
             x, q, d, u = sample_round_inputs(B, k, V, c["noise"], seed=rng, dtype=c["logit_dtype"])
             t0 = time.perf_counter()
-            _, _, ne, _, _ = oracle.verify_sample(x, dt, q, d, u)
+            _, _, ne, _, _ = oracle.verify_sample(x, dt, q, d, u, top_k=c.get("top_k"), top_p=c.get("top_p"))
         st, ln, pad2, w = oracle.realign_kv(kv_host, ln, pad, ne)
         oracle.rebuild_pos_mask(S, pad2, pos, mask)
         spent += time.perf_counter() - t0

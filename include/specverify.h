@@ -77,6 +77,9 @@ enum {
 /* Most caches one spec_realign_kv_multi call moves. */
 #define SPEC_MAX_CACHES 4
 
+/* Largest vocabulary of spec_verify_sample_filtered. */
+#define SPEC_MAX_FILTER_V (1 << 18)
+
 /* Largest pool (sequences) of the ragged-pool entry points. */
 #define SPEC_MAX_POOL 65536
 
@@ -171,7 +174,8 @@ SPEC_API int spec_verify_sample(const void *target_logits, spec_dtype dt, float 
  * the draft's processed distribution.
  * Everything else -- arguments, layouts, flags, outputs, errors -- is as in
  * spec_verify_sample; top_k [B] int32 and top_p [B] fp32 are device arrays
- * (4-byte aligned).  With both NULL this is spec_verify_sample.
+ * (4-byte aligned).  With both NULL this is spec_verify_sample.  With either
+ * given, V > SPEC_MAX_FILTER_V returns SPEC_EINVAL.
  */
 SPEC_API int spec_verify_sample_filtered(const void *target_logits, spec_dtype dt, float temperature,
                                 const int32_t *top_k, const float *top_p, const float *draft_probs,

@@ -127,6 +127,8 @@ static int verify_sample_impl(const void *target_logits, spec_dtype dt, float te
         return rc;
     if (!(temperature > 0.0f) || !(temperature <= 3.0e38f) || !uniforms || (k > 0 && !draft_probs))
         return SPEC_EINVAL;
+    if ((top_k || top_p) && V > SPEC_MAX_FILTER_V)
+        return SPEC_EINVAL;
     if (!aligned(uniforms, 4) || (draft_probs && !aligned(draft_probs, 4)) ||
         (out_residual && !aligned(out_residual, 4)) || (flags && !aligned(flags, 4)) ||
         (top_k && !aligned(top_k, 4)) || (top_p && !aligned(top_p, 4)))

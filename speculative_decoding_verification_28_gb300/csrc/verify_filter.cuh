@@ -26,9 +26,9 @@
 // order-preserving 32-bit key of the logit, 11-bit digits (two levels for
 // 16-bit logits, whose keys carry at most 22 significant bits; three for
 // fp32): each level is one more pass over the row (now in L2) building
-// per-digit counts and Q masses in shared memory, then a block scan from the
-// top digit finds the digit holding the k-th largest key (counts) or the
-// top-p boundary (masses).  Roofline: HBM reads V * sizeof(T) per needed row;
+// per-digit counts and Q masses in shared memory (32-bit atomics on three
+// parts of each mass), then a block scan from the top digit finds the digit
+// holding the k-th largest key (counts) or the top-p boundary (masses).  Roofline: HBM reads V * sizeof(T) per needed row;
 // the later passes are L2 reads plus shared-memory atomics.
 #pragma once
 
@@ -38,9 +38,18 @@ namespace spec {
 
 constexpr int kFBins = 2048;
 
+// Counts and Q masses per digit.  A mass is kept as three 32-bit parts
+// (Q = lo + mid 2^14 + hi 2^28): 32-bit shared-memory atomics are native,
+// 64-bit adds are not, and the parts' sums stay exact for rows of at most
+// 2^18 logits.
 struct FilterHist {
     unsigned int cnt[kFBins];
-    unsigned long long mass[kFBins];
+    unsigned int mlo[kFBins], mmid[kFBins], mhi[kFBins];
+    __device__ unsigned long long mass(int i) const
+    {
+        return (unsigned long long)mlo[i] + ((unsigned long long)mmid[i] << 14) +
+               ((unsigned long long)mhi[i] << 28);
+    }
 };
 
 struct FilterSel {
@@ -136,7 +145,7 @@ __device__ __forceinline__ void hist_clear(FilterHist &h, int nb)
 {
     for (int i = threadIdx.x; i < nb; i += kThreads) {
         h.cnt[i] = 0u;
-        h.mass[i] = 0ull;
+        h.mlo[i] = h.mmid[i] = h.mhi[i] = 0u;
     }
 }
 
@@ -154,8 +163,12 @@ __device__ void hist_pass(const T *row, int V, int l, uint32_t prefix, uint32_t 
             return;
         const int dg = (int)((key >> sh) & (uint32_t)msk);
         atomicAdd(&h.cnt[dg], 1u);
-        if (kMass)
-            atomicAdd(&h.mass[dg], q40_weight(__fsub_rn(x, xmax), cdec));
+        if (kMass) {
+            const unsigned long long q = q40_weight(__fsub_rn(x, xmax), cdec);
+            atomicAdd(&h.mlo[dg], (unsigned int)(q & 0x3FFFull));
+            atomicAdd(&h.mmid[dg], (unsigned int)((q >> 14) & 0x3FFFull));
+            atomicAdd(&h.mhi[dg], (unsigned int)(q >> 28));
+        }
     };
     row_for_each<T>(row, V, add);
 }
@@ -176,7 +189,7 @@ __device__ void hist_select(const FilterHist &h, int nb, unsigned int need, unsi
     unsigned long long lm = 0;
     for (int i = 0; i < P; ++i) {
         lc += h.cnt[top - i];
-        lm += h.mass[top - i];
+        lm += h.mass(top - i);
     }
     unsigned int ic = lc;
     unsigned long long im = lm;
@@ -217,7 +230,7 @@ __device__ void hist_select(const FilterHist &h, int nb, unsigned int need, unsi
         for (int i = 0; i < P; ++i) {
             const int bin = top - i;
             const unsigned int c1 = h.cnt[bin];
-            const unsigned long long m1 = h.mass[bin];
+            const unsigned long long m1 = h.mass(bin);
             const bool hit = kMass ? (c1 > 0u && (double)(base + mm + m1) >= bound) : (cc + c1 >= need);
             if (hit) {
                 sel.bin = bin;
@@ -247,7 +260,7 @@ __device__ void hist_select(const FilterHist &h, int nb, unsigned int need, unsi
                     m_at = mm;
                 }
                 cc += h.cnt[bin];
-                mm += h.mass[bin];
+                mm += h.mass(bin);
             }
             sel.bin = lowest;
             sel.cnt_above = c_at;
@@ -279,13 +292,12 @@ __global__ void __launch_bounds__(kThreads) verify_filter_kernel(VerifyArgs a)
     __syncthreads();
     float cut = -INFINITY, s_kept = 0.0f;
     if (!s_skip) {
-        float m, s, xm;
+        float m, s;
         bool bad;
-        chunk_softmax_stats<T, true>(row, 0, a.V, c, m, s, bad, s_f, StopProbe{a.stop_enc, u.b, u.j}, &xm);
+        chunk_softmax_stats<T, true>(row, 0, a.V, c, m, s, bad, s_f, StopProbe{a.stop_enc, u.b, u.j}, &s_xmax);
         if (t == 0) {
             s_m = m;
             s_s = s;
-            s_xmax = xm;
             s_bad = (bad || !(s > 0.0f) || !(s <= FLT_MAX)) ? 1 : 0;
             s_skip = stopped_before(a.stop_enc, u.b, u.j) ? 1 : 0;
         }
@@ -316,7 +328,7 @@ __global__ void __launch_bounds__(kThreads) verify_filter_kernel(VerifyArgs a)
                     need -= sel.cnt_above;
                     above += sel.mass_above;
                     if (l == L - 1)
-                        kept_mass = above + h.mass[bin];
+                        kept_mass = above + h.mass(bin);
                     prefix = (l == 0) ? (uint32_t)bin : ((prefix << (lvl_shift(l - 1) - lvl_shift(l))) | (uint32_t)bin);
                     __syncthreads();
                 }
@@ -335,7 +347,7 @@ __global__ void __launch_bounds__(kThreads) verify_filter_kernel(VerifyArgs a)
                     const int bin = sel.bin < 0 ? 0 : sel.bin;  // a digit is always found
                     A += sel.mass_above;
                     if (l == L - 1)
-                        kept_mass = A + h.mass[bin];
+                        kept_mass = A + h.mass(bin);
                     prefix = (l == 0) ? (uint32_t)bin : ((prefix << (lvl_shift(l - 1) - lvl_shift(l))) | (uint32_t)bin);
                     __syncthreads();
                 }

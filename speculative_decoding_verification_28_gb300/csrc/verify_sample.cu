@@ -567,7 +567,7 @@ __global__ void __launch_bounds__(kThreads) verify_residual_kernel(VerifyArgs a)
     kb = kb < 0 ? 0 : (kb > a.k ? a.k : kb);
     const DrawRow<T> dr = draw_row_of<T>(a, b, r, kb);
     const double W = a.rtot[b];
-    const bool use_res = W > 0.0;
+    const bool use_res = W > 0.0 && r < kb;  // the bonus row has no draft row
     const float inv = (float)(1.0 / (use_res ? W : -W));
     const int lo = c * kDrawChunk, hi = min(a.V, lo + kDrawChunk);
     float *out = a.out_residual + (size_t)b * a.V;
