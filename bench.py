@@ -271,6 +271,17 @@ class Round:
             self.tg.kv_fill(self.draft, self.tokens, self.pad, self.ln - 1, junk=False)
         self.sv.spec_rebuild_pos_mask(self.pad, self.pos, self.mask)
 
+    def restart(self, seed):
+        """Back to the state right after construction with this seed, so that
+        the same rounds can be replayed (the end-to-end leg)."""
+        import torch
+
+        self.g.manual_seed(seed)
+        self.rng = np.random.default_rng(seed)
+        self.tokens = torch.randint(0, self.c["V"], tuple(self.tokens.shape), device=self.dev, dtype=torch.int32,
+                                    generator=self.g)
+        self.reset()
+
     def prepare(self):
         """The target forward of this round (untimed): logits, proposals and
         the KV of the query slots; then an L2 flush."""
@@ -478,7 +489,7 @@ def run_ours(args, c, rank, local_rank, world):
         "clocks": clk.summary(),
     }
     if not args.no_e2e:
-        line["e2e"] = run_e2e(args, R, st, dev, pg, world)
+        line["e2e"] = run_e2e(args, R, st, dev, pg, world, rank_seed(args.seed, rank))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = run_cpu_baseline(c, args, R)
     if pg:
@@ -486,12 +497,15 @@ def run_ours(args, c, rank, local_rank, world):
     return line
 
 
-def run_e2e(args, R, st, dev, pg, world):
-    """Same rounds through the public API with HOST inputs and outputs: the
-    timed region of every step includes the pinned host->device copy of the
-    round's logits and proposals, the library calls, and one device->host
-    copy of the round's results (committed tokens, counts, new lengths and
-    paddings, width, error word), which the calls write into one block."""
+def run_e2e(args, R, st, dev, pg, world, seed):
+    """The same rounds as the device-timed steps (the round state restarts
+    from the same seed and runs the same warm-up), now through the public
+    API with HOST inputs and outputs: the timed region of every step
+    includes the pinned host->device copy of the round's logits and
+    proposals, the library calls, and one device->host copy of the round's
+    results (committed tokens, counts, new lengths and paddings, width, error
+    word), which the calls write into one block.  Host enqueue time is inside
+    the timed region (no gate)."""
     import torch
 
     c = R.c
@@ -515,11 +529,12 @@ def run_e2e(args, R, st, dev, pg, world):
         o += 4 * B
         return out, na, ne, ln, pad, blk[o:o + 1], blk[o + 1:o + 2]
 
+    R.restart(seed)
     views(blocks[0])[3].copy_(R.ln)
     views(blocks[0])[4].copy_(R.pad)
     cur = 0
     total = 0.0
-    for _ in range(steps):
+    for step in range(args.warmup + steps):
         R.ln, R.pad = views(blocks[cur])[3], views(blocks[cur])[4]
         R.prepare()
         if views(blocks[cur])[3].data_ptr() != R.ln.data_ptr():  # prepare() reset the state
@@ -554,7 +569,8 @@ def run_e2e(args, R, st, dev, pg, world):
         h_res.copy_(blocks[1 - cur], non_blocking=True)
         e1.record(st)
         torch.cuda.synchronize(dev)
-        total += e0.elapsed_time(e1) / 1e3
+        if step >= args.warmup:
+            total += e0.elapsed_time(e1) / 1e3
         assert int(h_res[-1]) == 0
         R.W = int(h_res[-2])
         cur = 1 - cur

@@ -107,27 +107,27 @@ __device__ __forceinline__ unsigned long long q40_weight(float d, float c)
 }
 
 // f(x) for every logit of the row: 16-byte vectors, scalar head and tail
-template <typename T, typename F>
+template <typename T, int NT, typename F>
 __device__ __forceinline__ void row_for_each(const T *row, int V, F &f)
 {
     constexpr int VEC = Storage<T>::kVec;
     constexpr int UNROLL = 4;
     const ChunkSplit<T> cs(row, 0, V);
     const int t = threadIdx.x;
-    for (int v = t; v < cs.head_end; v += kThreads)
+    for (int v = t; v < cs.head_end; v += NT)
         f(Storage<T>::at(row, v));
     const T *body = row + cs.head_end;
-    for (int base = 0; base < cs.nvec; base += UNROLL * kThreads) {
+    for (int base = 0; base < cs.nvec; base += UNROLL * NT) {
         uint4 r[UNROLL];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int vi = base + t + u * kThreads;
+            const int vi = base + t + u * NT;
             if (vi < cs.nvec)
                 r[u] = ld_stream16(body + (size_t)vi * VEC);
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int vi = base + t + u * kThreads;
+            const int vi = base + t + u * NT;
             if (vi < cs.nvec) {
                 float e[VEC];
                 Storage<T>::unpack(r[u], e);
@@ -137,13 +137,14 @@ __device__ __forceinline__ void row_for_each(const T *row, int V, F &f)
             }
         }
     }
-    for (int v = cs.tail_beg + t; v < V; v += kThreads)
+    for (int v = cs.tail_beg + t; v < V; v += NT)
         f(Storage<T>::at(row, v));
 }
 
+template <int NT>
 __device__ __forceinline__ void hist_clear(FilterHist &h, int nb)
 {
-    for (int i = threadIdx.x; i < nb; i += kThreads) {
+    for (int i = threadIdx.x; i < nb; i += NT) {
         h.cnt[i] = 0u;
         h.mlo[i] = h.mmid[i] = h.mhi[i] = 0u;
     }
@@ -151,7 +152,7 @@ __device__ __forceinline__ void hist_clear(FilterHist &h, int nb)
 
 // Counts (and Q masses) per digit of level l over the logits whose key is
 // >= lo_key and whose higher digits equal `prefix`.
-template <typename T, bool kMass>
+template <typename T, bool kMass, int NT>
 __device__ void hist_pass(const T *row, int V, int l, uint32_t prefix, uint32_t lo_key, float xmax, float cdec,
                           FilterHist &h)
 {
@@ -170,21 +171,21 @@ __device__ void hist_pass(const T *row, int V, int l, uint32_t prefix, uint32_t 
             atomicAdd(&h.mhi[dg], (unsigned int)(q >> 28));
         }
     };
-    row_for_each<T>(row, V, add);
+    row_for_each<T, NT>(row, V, add);
 }
 
 // First digit from the top whose inclusive cumulative count reaches `need`
 // (counts), or the first non-empty digit from the top with
 // double(base + cumulative mass) >= bound (masses; bound = top_p * total at
 // the first level).  With masses and no such digit, the lowest non-empty one.
-// Thread t owns digits nb-1-tP .. nb-P-tP (P = nb / kThreads), scanned in
+// Thread t owns digits nb-1-tP .. nb-P-tP (P = nb / NT), scanned in
 // descending order.  Ends with a barrier; the result is in `sel`.
-template <bool kMass>
+template <bool kMass, int NT>
 __device__ void hist_select(const FilterHist &h, int nb, unsigned int need, unsigned long long base, float top_p,
                             bool first_level, FilterSel &sel, unsigned int *s_wc, unsigned long long *s_wm)
 {
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-    const int P = nb / kThreads, top = nb - 1 - t * P;
+    const int P = nb / NT, top = nb - 1 - t * P;
     unsigned int lc = 0;
     unsigned long long lm = 0;
     for (int i = 0; i < P; ++i) {
@@ -213,7 +214,7 @@ __device__ void hist_select(const FilterHist &h, int nb, unsigned int need, unsi
     __syncthreads();
     unsigned int cb = ic - lc;
     unsigned long long mb = im - lm, total = 0;
-    for (int i = 0; i < kThreads / 32; ++i) {
+    for (int i = 0; i < NT / 32; ++i) {
         if (i < w) {
             cb += s_wc[i];
             mb += s_wm[i];
@@ -272,14 +273,14 @@ __device__ void hist_select(const FilterHist &h, int nb, unsigned int need, unsi
     }
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kThreads) verify_filter_kernel(VerifyArgs a)
+template <typename T, int NT>
+__global__ void __launch_bounds__(NT) verify_filter_kernel(VerifyArgs a)
 {
     constexpr int L = KeyLevels<T>::kLevels;
     __shared__ FilterHist h;
-    __shared__ float s_f[4 * kThreads / 32];
-    __shared__ unsigned int s_wc[kThreads / 32];
-    __shared__ unsigned long long s_wm[kThreads / 32];
+    __shared__ float s_f[4 * NT / 32];
+    __shared__ unsigned int s_wc[NT / 32];
+    __shared__ unsigned long long s_wm[NT / 32];
     __shared__ FilterSel sel;
     __shared__ float s_m, s_s, s_xmax;
     __shared__ int s_bad, s_skip;
@@ -294,7 +295,7 @@ __global__ void __launch_bounds__(kThreads) verify_filter_kernel(VerifyArgs a)
     if (!s_skip) {
         float m, s;
         bool bad;
-        chunk_softmax_stats<T, true>(row, 0, a.V, c, m, s, bad, s_f, StopProbe{a.stop_enc, u.b, u.j}, &s_xmax);
+        chunk_softmax_stats<T, true, NT>(row, 0, a.V, c, m, s, bad, s_f, StopProbe{a.stop_enc, u.b, u.j}, &s_xmax);
         if (t == 0) {
             s_m = m;
             s_s = s;
@@ -316,14 +317,14 @@ __global__ void __launch_bounds__(kThreads) verify_filter_kernel(VerifyArgs a)
                 unsigned long long above = 0ull;
                 for (int l = 0; l < L; ++l) {
                     const int nb = lvl_bins(l);
-                    hist_clear(h, nb);
+                    hist_clear<NT>(h, nb);
                     __syncthreads();
                     if (use_p)
-                        hist_pass<T, false>(row, a.V, l, prefix, 0u, xmax, cdec, h);
+                        hist_pass<T, false, NT>(row, a.V, l, prefix, 0u, xmax, cdec, h);
                     else
-                        hist_pass<T, true>(row, a.V, l, prefix, 0u, xmax, cdec, h);
+                        hist_pass<T, true, NT>(row, a.V, l, prefix, 0u, xmax, cdec, h);
                     __syncthreads();
-                    hist_select<false>(h, nb, need, 0ull, 0.0f, false, sel, s_wc, s_wm);
+                    hist_select<false, NT>(h, nb, need, 0ull, 0.0f, false, sel, s_wc, s_wm);
                     const int bin = sel.bin < 0 ? 0 : sel.bin;  // a digit is always found
                     need -= sel.cnt_above;
                     above += sel.mass_above;
@@ -339,11 +340,11 @@ __global__ void __launch_bounds__(kThreads) verify_filter_kernel(VerifyArgs a)
                 unsigned long long A = 0ull;
                 for (int l = 0; l < L; ++l) {
                     const int nb = lvl_bins(l);
-                    hist_clear(h, nb);
+                    hist_clear<NT>(h, nb);
                     __syncthreads();
-                    hist_pass<T, true>(row, a.V, l, prefix, K, xmax, cdec, h);
+                    hist_pass<T, true, NT>(row, a.V, l, prefix, K, xmax, cdec, h);
                     __syncthreads();
-                    hist_select<true>(h, nb, 0u, A, tp, l == 0, sel, s_wc, s_wm);
+                    hist_select<true, NT>(h, nb, 0u, A, tp, l == 0, sel, s_wc, s_wm);
                     const int bin = sel.bin < 0 ? 0 : sel.bin;  // a digit is always found
                     A += sel.mass_above;
                     if (l == L - 1)
@@ -368,12 +369,18 @@ __global__ void __launch_bounds__(kThreads) verify_filter_kernel(VerifyArgs a)
     sample_seq_finish(a, u);
 }
 
+// Block size: 1024 threads when the batch has at most two rows per SM (a
+// row is one CTA, so a few rows would otherwise leave the GPU idle), else 256.
 template <typename T>
 cudaError_t launch_filter_rows(const VerifyArgs &args, cudaStream_t st)
 {
     VerifyArgs f = args;
     f.C = 1;  // one CTA per row
-    verify_filter_kernel<T><<<(unsigned)(f.B * (f.k + 1)), kThreads, 0, st>>>(f);
+    const unsigned rows = (unsigned)(f.B * (f.k + 1));
+    if (rows <= 2u * 152u)
+        verify_filter_kernel<T, 1024><<<rows, 1024, 0, st>>>(f);
+    else
+        verify_filter_kernel<T, kThreads><<<rows, kThreads, 0, st>>>(f);
     return cudaGetLastError();
 }
 

@@ -37,8 +37,8 @@ namespace spec {
 // stats kernel
 // ---------------------------------------------------------------------------
 // kRaw: also the unscaled maximum of the logits (to xmax_out of warp 0;
-// s_f then needs 4 * kThreads / 32 floats)
-template <typename T, bool kRaw>
+// s_f then needs 4 * NT / 32 floats); NT = threads of the block
+template <typename T, bool kRaw, int NT = kThreads>
 __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float &m_out, float &s_out,
                                     bool &bad_out, float *s_f, const StopProbe &probe, float *xmax_out)
 {
@@ -64,20 +64,20 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
     if (lo + t < cs.head_end)
         add1(Storage<T>::at(row, lo + t));
     const T *body = row + cs.head_end;
-    for (int base = 0; base < cs.nvec; base += UNROLL * kThreads) {  // warp-uniform trip count
+    for (int base = 0; base < cs.nvec; base += UNROLL * NT) {  // warp-uniform trip count
         if (base > 0 && probe.dropped())
             break;
         const int i = base + t;
         uint4 r[UNROLL];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int vi = i + u * kThreads;
+            const int vi = i + u * NT;
             if (vi < cs.nvec)
                 r[u] = ld_stream16(body + (size_t)vi * VEC);
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int vi = i + u * kThreads;
+            const int vi = i + u * NT;
             if (vi < cs.nvec) {
                 const float vraw = vec_max<T>(r[u]);
                 if (kRaw)
@@ -121,16 +121,16 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
     }
     if (l == 0) {
         s_f[w] = m;
-        s_f[kThreads / 32 + w] = wbad ? -s : s;  // the sign carries the warp's flag (s >= 0)
-        s_f[2 * (kThreads / 32) + w] = wbad ? 1.0f : 0.0f;
+        s_f[NT / 32 + w] = wbad ? -s : s;  // the sign carries the warp's flag (s >= 0)
+        s_f[2 * (NT / 32) + w] = wbad ? 1.0f : 0.0f;
         if (kRaw)
-            s_f[3 * (kThreads / 32) + w] = xr;
+            s_f[3 * (NT / 32) + w] = xr;
     }
     __syncthreads();
     if (t < 32) {
-        float mm = (l < kThreads / 32) ? s_f[l] : -INFINITY;
-        float ss = (l < kThreads / 32) ? fabsf(s_f[kThreads / 32 + l]) : 0.0f;
-        const bool bb = (l < kThreads / 32) && s_f[2 * (kThreads / 32) + l] > 0.0f;
+        float mm = (l < NT / 32) ? s_f[l] : -INFINITY;
+        float ss = (l < NT / 32) ? fabsf(s_f[NT / 32 + l]) : 0.0f;
+        const bool bb = (l < NT / 32) && s_f[2 * (NT / 32) + l] > 0.0f;
 #pragma unroll
         for (int k = 16; k > 0; k >>= 1)
             merge(mm, ss, __shfl_xor_sync(0xFFFFFFFFu, mm, k), __shfl_xor_sync(0xFFFFFFFFu, ss, k));
@@ -138,7 +138,7 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
         s_out = ss;
         bad_out = __any_sync(0xFFFFFFFFu, bb);
         if (kRaw) {
-            float xx = (l < kThreads / 32) ? s_f[3 * (kThreads / 32) + l] : -INFINITY;
+            float xx = (l < NT / 32) ? s_f[3 * (NT / 32) + l] : -INFINITY;
 #pragma unroll
             for (int k = 16; k > 0; k >>= 1)
                 xx = max_nan(xx, __shfl_xor_sync(0xFFFFFFFFu, xx, k));
