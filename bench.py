@@ -498,28 +498,55 @@ def run_ours(args, c, rank, local_rank, world):
 
 
 def run_e2e(args, R, st, dev, pg, world, seed):
+    """End to end through the public API with HOST inputs and outputs, over
+    the same rounds as the device-timed steps, twice: replayed from a CUDA
+    graph (`value`: RoundGraph, one capture per buffer parity) and with a
+    direct spec_round_* call per round (`eager_value`)."""
+    graph = e2e_pass(args, R, st, dev, pg, world, seed, use_graph=True)
+    eager = e2e_pass(args, R, st, dev, pg, world, seed, use_graph=False)
+    graph["eager_value"] = eager["value"]
+    graph["path"] = ("per round: one pinned H2D copy of the inputs, spec_round_" + R.c["mode"] +
+                     " (verify, realign, pos/mask), one D2H copy of the results; value = the round replayed "
+                     "from a CUDA graph (RoundGraph), eager_value = a direct call per round")
+    return graph
+
+
+def e2e_pass(args, R, st, dev, pg, world, seed, use_graph):
     """The same rounds as the device-timed steps (the round state restarts
-    from the same seed and runs the same warm-up), now through the public
-    API with HOST inputs and outputs: the timed region of every step
-    includes the pinned host->device copy of the round's logits and
-    proposals, the library calls, and one device->host copy of the round's
-    results (committed tokens, counts, new lengths and paddings, width, error
-    word), which the calls write into one block.  Host enqueue time is inside
-    the timed region (no gate)."""
+    from the same seed and runs the same warm-up).  The timed region of every
+    step: one host->device copy of the round's inputs (logits and proposals,
+    plus draft probabilities and uniforms when stochastic) from one pinned
+    block, one round of library calls (verify, realign, pos/mask), and one
+    device->host copy of the round's results (committed tokens, counts, new
+    lengths and paddings, width, error word), which the calls write into one
+    block.  Host enqueue time is inside the timed region (no gate)."""
     import torch
 
     c = R.c
     B, k = c["B"], c["k"]
     steps = max(1, args.steps)
-    hx = torch.empty(tuple(R.x.shape), dtype=R.x.dtype).pin_memory()
-    hd = torch.empty(tuple(R.d.shape), dtype=torch.int32).pin_memory()
-    extra = []
+    parts = [("x", R.x.dtype, tuple(R.x.shape)), ("d", torch.int32, tuple(R.d.shape))]
     if c["mode"] == "sample":
-        extra = [torch.empty(tuple(R.q.shape), dtype=torch.float32).pin_memory(),
-                 torch.empty(tuple(R.u.shape), dtype=torch.float32).pin_memory()]
+        parts += [("q", torch.float32, tuple(R.q.shape)), ("u", torch.float32, tuple(R.u.shape))]
+    offs, off = {}, 0
+    for name, dt, shape in parts:  # 256-byte aligned sub-blocks of one byte buffer
+        nbytes = int(np.prod(shape)) * torch.empty((), dtype=dt).element_size()
+        offs[name] = (off, nbytes, dt, shape)
+        off = (off + nbytes + 255) // 256 * 256
+    h_in = torch.empty(off, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(off, dtype=torch.uint8, device=dev)
+
+    def view_of(buf, name):
+        o, n, dt, shape = offs[name]
+        return buf[o:o + n].view(dt).view(shape)
+
+    dx, dd = view_of(d_in, "x"), view_of(d_in, "d")
+    dq, du = (view_of(d_in, "q"), view_of(d_in, "u")) if c["mode"] == "sample" else (None, None)
     n_out = B * (k + 1) + 4 * B + 2
     blocks = [torch.empty(n_out, dtype=torch.int32, device=dev) for _ in range(2)]
     h_res = torch.empty(n_out, dtype=torch.int32).pin_memory()
+    caches = [R.kv] + ([R.draft] if R.draft is not None else [])
+    tk, tp = R.filter_args() if (c["mode"] == "sample" and R.filtered()) else (None, None)
 
     def views(blk):
         o = 0
@@ -529,6 +556,21 @@ def run_e2e(args, R, st, dev, pg, world, seed):
         o += 4 * B
         return out, na, ne, ln, pad, blk[o:o + 1], blk[o + 1:o + 2]
 
+    def enqueue(par):
+        out, na, ne, ln_new, pad_new, width, err = views(blocks[1 - par])
+        ln, pad = views(blocks[par])[3], views(blocks[par])[4]
+        d_in.copy_(h_in, non_blocking=True)
+        if c["mode"] == "greedy":
+            R.sv.spec_round_greedy(dx, dd, caches, ln, pad, R.pos, R.mask, out_tokens=out, n_accept=na,
+                                   n_emit=ne, len_new=ln_new, pad_new=pad_new, width_new=width, err=err,
+                                   workspace=R.ws)
+        else:
+            R.sv.spec_round_sample(dx, dq, dd, du, caches, ln, pad, R.pos, R.mask, top_k=tk, top_p=tp,
+                                   out_tokens=out, n_accept=na, n_emit=ne, len_new=ln_new, pad_new=pad_new,
+                                   width_new=width, err=err, workspace=R.ws)
+        h_res.copy_(blocks[1 - par], non_blocking=True)
+
+    graphs = [R.sv.RoundGraph(lambda p=p: enqueue(p), dev) for p in (0, 1)] if use_graph else None
     R.restart(seed)
     views(blocks[0])[3].copy_(R.ln)
     views(blocks[0])[4].copy_(R.pad)
@@ -541,32 +583,18 @@ def run_e2e(args, R, st, dev, pg, world, seed):
             views(blocks[cur])[3].copy_(R.ln)
             views(blocks[cur])[4].copy_(R.pad)
             R.ln, R.pad = views(blocks[cur])[3], views(blocks[cur])[4]
-        hx.copy_(R.x)
-        hd.copy_(R.d)
-        if extra:
-            extra[0].copy_(R.q)
-            extra[1].copy_(R.u)
+        view_of(h_in, "x").copy_(R.x)
+        view_of(h_in, "d").copy_(R.d)
+        if c["mode"] == "sample":
+            view_of(h_in, "q").copy_(R.q)
+            view_of(h_in, "u").copy_(R.u)
         torch.cuda.synchronize(dev)
-        out, na, ne, ln_new, pad_new, width, err = views(blocks[1 - cur])
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(st)
-        R.x.copy_(hx, non_blocking=True)
-        R.d.copy_(hd, non_blocking=True)
-        if extra:
-            R.q.copy_(extra[0], non_blocking=True)
-            R.u.copy_(extra[1], non_blocking=True)
-        if c["mode"] == "greedy":
-            R.sv.spec_verify_greedy(R.x, R.d, out_tokens=out, n_accept=na, n_emit=ne, workspace=R.ws)
+        if use_graph:
+            graphs[cur].replay()
         else:
-            R.verify_sample(out_tokens=out, n_accept=na, n_emit=ne)
-        if R.draft is not None:
-            R.sv.spec_realign_kv_multi([R.kv, R.draft], R.ln, R.pad, ne, len_new=ln_new, pad_new=pad_new,
-                                       width_new=width, err=err, workspace=R.ws)
-        else:
-            R.sv.spec_realign_kv(R.kv, R.ln, R.pad, ne, len_new=ln_new, pad_new=pad_new, width_new=width, err=err,
-                                 workspace=R.ws)
-        R.sv.spec_rebuild_pos_mask(pad_new, R.pos, R.mask, pad_old=R.pad)
-        h_res.copy_(blocks[1 - cur], non_blocking=True)
+            enqueue(cur)
         e1.record(st)
         torch.cuda.synchronize(dev)
         if step >= args.warmup:
@@ -576,7 +604,7 @@ def run_e2e(args, R, st, dev, pg, world, seed):
         cur = 1 - cur
     R.ln, R.pad = views(blocks[cur])[3].clone(), views(blocks[cur])[4].clone()
     total = max_over_ranks(total, pg, dev)
-    h2d = hx.numel() * hx.element_size() + hd.numel() * 4 + sum(t.numel() * 4 for t in extra)
+    h2d = sum(n for (_, n, _, _) in offs.values())
     return {"value": round(aggregate(steps, total, world), 3), "unit": "rounds/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": n_out * 4, "steps": steps}
 

@@ -340,6 +340,39 @@ SPEC_API int spec_unpad_scatter(const void *batch, void *pool, spec_dtype dt, in
                        int32_t *pool_len, int32_t *err, void *workspace, size_t workspace_bytes,
                        void *cuda_stream);
 
+/*
+ * One whole round in one call: spec_verify_greedy (or spec_verify_sample /
+ * spec_verify_sample_filtered), then spec_realign_kv_multi over `caches` with
+ * the n_emit the verification produced, then spec_rebuild_pos_mask with
+ * pad_old = pad.  The definitions, layouts, outputs and errors are those of
+ * the three calls; each argument means what it means there.  Every argument
+ * is checked before anything is launched (a non-zero return launches
+ * nothing); the launches follow one another on the stream, so the
+ * realignment reads n_emit on the device and the caller needs no
+ * synchronisation inside a round (the whole round can be captured in a CUDA
+ * graph).  pad_new must not alias pad.  One workspace serves all three
+ * stages: spec_workspace_bytes(B, k, V).
+ */
+SPEC_API int spec_round_greedy(const void *target_logits, spec_dtype dt, int B, int k, int V,
+                      const int32_t *draft_tokens, const int32_t *draft_len, int32_t eos_id,
+                      const int32_t *remaining, const spec_kv_cache *caches, int n_caches, int S,
+                      const int32_t *len, const int32_t *pad, int32_t *pos, uint8_t *mask,
+                      int32_t *out_tokens, int32_t *n_accept, int32_t *n_emit, int32_t *len_new,
+                      int32_t *pad_new, int32_t *width_new, int32_t *err, void *workspace,
+                      size_t workspace_bytes, void *cuda_stream);
+
+/* The stochastic round; top_k / top_p may be NULL (see
+ * spec_verify_sample_filtered). */
+SPEC_API int spec_round_sample(const void *target_logits, spec_dtype dt, float temperature,
+                      const int32_t *top_k, const float *top_p, const float *draft_probs,
+                      const int32_t *draft_tokens, const float *uniforms, int B, int k, int V,
+                      const int32_t *draft_len, int32_t eos_id, const int32_t *remaining,
+                      const spec_kv_cache *caches, int n_caches, int S, const int32_t *len,
+                      const int32_t *pad, int32_t *pos, uint8_t *mask, int32_t *out_tokens,
+                      int32_t *n_accept, int32_t *n_emit, float *out_residual, uint32_t *flags,
+                      int32_t *len_new, int32_t *pad_new, int32_t *width_new, int32_t *err,
+                      void *workspace, size_t workspace_bytes, void *cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

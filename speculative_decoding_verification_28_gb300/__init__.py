@@ -29,6 +29,8 @@ from .api import (  # noqa: F401
     spec_realign_kv_multi,
     MAX_CACHES,
     spec_rebuild_pos_mask,
+    spec_round_greedy,
+    spec_round_sample,
     spec_verify_greedy,
     spec_verify_greedy_static,
     STATIC_SCRATCH_BYTES,
@@ -36,3 +38,4 @@ from .api import (  # noqa: F401
     spec_verify_sample_filtered,
     spec_workspace_bytes,
 )
+from .graph import RoundGraph  # noqa: F401,E402

@@ -39,6 +39,11 @@ class KVCacheDesc(ctypes.Structure):
 
 SIGNATURES["spec_realign_kv_multi"] = ([_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
                                        _i32)
+SIGNATURES["spec_round_greedy"] = ([_vp, _i32, _i32, _i32, _i32, _vp, _vp, ctypes.c_int32, _vp, _vp, _i32, _i32,
+                                    _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32)
+SIGNATURES["spec_round_sample"] = ([_vp, _i32, _f32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, ctypes.c_int32,
+                                    _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                    _vp, _vp, _vp, _sz, _vp], _i32)
 
 SIGNATURES["spec_commit_ragged"] = ([_i32, _vp, _i32, _vp, _vp, _i32, _vp, _vp], _i32)
 SIGNATURES["spec_repad_gather"] = ([_vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp,

@@ -281,6 +281,108 @@ def spec_realign_kv_multi(caches, length, pad, n_emit, len_new=None, pad_new=Non
     return len_new, pad_new, width_new, err
 
 
+def _cache_descs(caches, dev, B, S):
+    if not 1 <= len(caches) <= MAX_CACHES:
+        raise ValueError(f"1..{MAX_CACHES} caches")
+    descs = (_lib.KVCacheDesc * len(caches))()
+    for i, kv in enumerate(caches):
+        L, two, Bc, H, Sc, D = kv.shape
+        if two != 2 or Bc != B or Sc != S:
+            raise ValueError("every cache must be [L, 2, B, H, S, D] with the same B and S")
+        _need(kv, None, f"caches[{i}]", dev)
+        if kv.dtype not in _DT:
+            raise ValueError(f"unsupported kv dtype {kv.dtype}")
+        descs[i] = _lib.KVCacheDesc(kv.data_ptr(), _DT[kv.dtype], L, H, D)
+    return descs
+
+
+def _round_outputs(B, k, dev, out_tokens, n_accept, n_emit, len_new, pad_new, width_new, err):
+    e = lambda n: torch.empty(n, dtype=torch.int32, device=dev)  # noqa: E731
+    return (e((B, k + 1)) if out_tokens is None else out_tokens, e(B) if n_accept is None else n_accept,
+            e(B) if n_emit is None else n_emit, e(B) if len_new is None else len_new,
+            e(B) if pad_new is None else pad_new, e(1) if width_new is None else width_new,
+            e(1) if err is None else err)
+
+
+def spec_round_greedy(target_logits, draft_tokens, caches, length, pad, pos, mask, draft_len=None, eos_id=-1,
+                      remaining=None, out_tokens=None, n_accept=None, n_emit=None, len_new=None, pad_new=None,
+                      width_new=None, err=None, workspace=None, stream=None):
+    """One greedy round in one call: verify, realign every cache by one plan,
+    rebuild pos / mask (pad_new must not alias pad).
+    -> (out_tokens, n_accept, n_emit, len_new, pad_new, width_new, err)."""
+    lib = _lib.load()
+    B, k1, V = target_logits.shape
+    k = k1 - 1
+    dev = target_logits.device
+    S = caches[0].shape[4]
+    _need(target_logits, None, "target_logits", dev)
+    if target_logits.dtype not in _DT:
+        raise ValueError(f"unsupported logits dtype {target_logits.dtype}")
+    _need(draft_tokens, torch.int32, "draft_tokens", dev, (B, k))
+    _need(draft_len, torch.int32, "draft_len", dev, (B,))
+    _need(remaining, torch.int32, "remaining", dev, (B,))
+    descs = _cache_descs(caches, dev, B, S)
+    for t, nm in ((length, "len"), (pad, "pad")):
+        _need(t, torch.int32, nm, dev, (B,))
+    _need(pos, torch.int32, "pos", dev, (B, S))
+    _need(mask, torch.uint8, "mask", dev, (B, S))
+    outs = _round_outputs(B, k, dev, out_tokens, n_accept, n_emit, len_new, pad_new, width_new, err)
+    st = _stream(stream, dev)
+    ws = _workspace(workspace, B, k, V, dev, st)
+    o, na, ne, ln2, pd2, w2, er = outs
+    _check(lib.spec_round_greedy(_p(target_logits), _DT[target_logits.dtype], B, k, V, _p(draft_tokens),
+                                 _p(draft_len), int(eos_id), _p(remaining), ctypes.cast(descs, ctypes.c_void_p),
+                                 len(caches), S, _p(length), _p(pad), _p(pos), _p(mask), _p(o), _p(na), _p(ne),
+                                 _p(ln2), _p(pd2), _p(w2), _p(er), ws.ptr(), ws.nbytes, st))
+    return outs
+
+
+def spec_round_sample(target_logits, draft_probs, draft_tokens, uniforms, caches, length, pad, pos, mask,
+                      temperature=1.0, top_k=None, top_p=None, draft_len=None, eos_id=-1, remaining=None,
+                      out_tokens=None, n_accept=None, n_emit=None, out_residual=None, flags=None, len_new=None,
+                      pad_new=None, width_new=None, err=None, workspace=None, stream=None):
+    """One stochastic round in one call (top_k / top_p: None, a scalar or [B]
+    device arrays, as in spec_verify_sample_filtered).
+    -> (out_tokens, n_accept, n_emit, len_new, pad_new, width_new, err, flags, out_residual)."""
+    lib = _lib.load()
+    B, k1, V = target_logits.shape
+    k = k1 - 1
+    dev = target_logits.device
+    S = caches[0].shape[4]
+    _need(target_logits, None, "target_logits", dev)
+    if target_logits.dtype not in _DT:
+        raise ValueError(f"unsupported logits dtype {target_logits.dtype}")
+    if top_k is not None and not torch.is_tensor(top_k):
+        top_k = torch.full((B,), int(top_k), dtype=torch.int32, device=dev)
+    if top_p is not None and not torch.is_tensor(top_p):
+        top_p = torch.full((B,), float(top_p), dtype=torch.float32, device=dev)
+    _need(top_k, torch.int32, "top_k", dev, (B,))
+    _need(top_p, torch.float32, "top_p", dev, (B,))
+    _need(draft_probs, torch.float32, "draft_probs", dev, (B, k, V))
+    _need(draft_tokens, torch.int32, "draft_tokens", dev, (B, k))
+    _need(uniforms, torch.float32, "uniforms", dev, (B, k + 1))
+    _need(draft_len, torch.int32, "draft_len", dev, (B,))
+    _need(remaining, torch.int32, "remaining", dev, (B,))
+    descs = _cache_descs(caches, dev, B, S)
+    for t, nm in ((length, "len"), (pad, "pad")):
+        _need(t, torch.int32, nm, dev, (B,))
+    _need(pos, torch.int32, "pos", dev, (B, S))
+    _need(mask, torch.uint8, "mask", dev, (B, S))
+    outs = _round_outputs(B, k, dev, out_tokens, n_accept, n_emit, len_new, pad_new, width_new, err)
+    flags = torch.empty(B, dtype=torch.int32, device=dev) if flags is None else flags
+    _need(flags, torch.int32, "flags", dev, (B,))
+    _need(out_residual, torch.float32, "out_residual", dev, (B, V))
+    st = _stream(stream, dev)
+    ws = _workspace(workspace, B, k, V, dev, st)
+    o, na, ne, ln2, pd2, w2, er = outs
+    _check(lib.spec_round_sample(_p(target_logits), _DT[target_logits.dtype], float(temperature), _p(top_k),
+                                 _p(top_p), _p(draft_probs), _p(draft_tokens), _p(uniforms), B, k, V, _p(draft_len),
+                                 int(eos_id), _p(remaining), ctypes.cast(descs, ctypes.c_void_p), len(caches), S,
+                                 _p(length), _p(pad), _p(pos), _p(mask), _p(o), _p(na), _p(ne), _p(out_residual),
+                                 _p(flags), _p(ln2), _p(pd2), _p(w2), _p(er), ws.ptr(), ws.nbytes, st))
+    return outs + (flags, out_residual)
+
+
 def spec_rebuild_pos_mask(pad_new, pos, mask, pad_old=None, stream=None):
     """pos [B, S] int32 and mask [B, S] uint8 rewritten in place from pad_new."""
     lib = _lib.load()

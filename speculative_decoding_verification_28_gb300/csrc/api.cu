@@ -44,6 +44,91 @@ int check_verify_common(const void *logits, int dt, int B, int k, int V, const i
     return SPEC_OK;
 }
 
+// ---- verification: checks and arguments ----------------------------------
+int check_greedy(const void *logits, int dt, int B, int k, int V, const int32_t *draft, const int32_t *out_tokens,
+                 const int32_t *n_accept, const int32_t *n_emit, void *workspace, size_t workspace_bytes)
+{
+    const int rc = check_verify_common(logits, dt, B, k, V, draft, out_tokens, n_accept, n_emit);
+    if (rc != SPEC_OK || B == 0)
+        return rc;
+    return check_workspace(workspace, workspace_bytes, spec_workspace_bytes(B, k, V));
+}
+
+int check_sample(const void *logits, int dt, float temperature, const int32_t *top_k, const float *top_p,
+                 const float *draft_probs, const int32_t *draft, const float *uniforms, int B, int k, int V,
+                 const int32_t *out_tokens, const int32_t *n_accept, const int32_t *n_emit,
+                 const float *out_residual, const uint32_t *flags, void *workspace, size_t workspace_bytes)
+{
+    const int rc = check_verify_common(logits, dt, B, k, V, draft, out_tokens, n_accept, n_emit);
+    if (rc != SPEC_OK || B == 0)
+        return rc;
+    if (!(temperature > 0.0f) || !(temperature <= 3.0e38f) || !uniforms || (k > 0 && !draft_probs))
+        return SPEC_EINVAL;
+    if ((top_k || top_p) && V > SPEC_MAX_FILTER_V)
+        return SPEC_EINVAL;
+    if (!aligned(uniforms, 4) || (draft_probs && !aligned(draft_probs, 4)) ||
+        (out_residual && !aligned(out_residual, 4)) || (flags && !aligned(flags, 4)) ||
+        (top_k && !aligned(top_k, 4)) || (top_p && !aligned(top_p, 4)))
+        return SPEC_EALIGN;
+    return check_workspace(workspace, workspace_bytes, spec_workspace_bytes(B, k, V));
+}
+
+VerifyArgs verify_args(const void *logits, int B, int k, int V, const int32_t *draft, const int32_t *draft_len,
+                       int32_t eos_id, const int32_t *remaining, int32_t *out_tokens, int32_t *n_accept,
+                       int32_t *n_emit, void *workspace)
+{
+    VerifyArgs a{};
+    a.logits = logits;
+    a.B = B;
+    a.k = k;
+    a.V = V;
+    a.draft = draft;
+    a.draft_len = draft_len;
+    a.eos = eos_id;
+    a.remaining = remaining;
+    a.out_tokens = out_tokens;
+    a.n_accept = n_accept;
+    a.n_emit = n_emit;
+    a.ws = workspace;
+    return a;
+}
+
+VerifyArgs sample_args(const void *logits, float temperature, const int32_t *top_k, const float *top_p,
+                       const float *draft_probs, const int32_t *draft, const float *uniforms, int B, int k, int V,
+                       const int32_t *draft_len, int32_t eos_id, const int32_t *remaining, int32_t *out_tokens,
+                       int32_t *n_accept, int32_t *n_emit, float *out_residual, uint32_t *flags, void *workspace)
+{
+    VerifyArgs a = verify_args(logits, B, k, V, draft, draft_len, eos_id, remaining, out_tokens, n_accept, n_emit,
+                               workspace);
+    a.inv_temp = 1.0f / temperature;
+    a.unit_temp = temperature == 1.0f ? 1 : 0;
+    a.q = draft_probs;
+    a.u = uniforms;
+    a.out_residual = out_residual;
+    a.flags = flags;
+    a.filtered = (top_k || top_p) ? 1 : 0;
+    a.top_k = top_k;
+    a.top_p = top_p;
+    a.dec_scale = (float)(1.44269504088896340736 / (double)temperature);
+    return a;
+}
+
+int run_sample(const void *logits, spec_dtype dt, float temperature, const int32_t *top_k, const float *top_p,
+               const float *draft_probs, const int32_t *draft, const float *uniforms, int B, int k, int V,
+               const int32_t *draft_len, int32_t eos_id, const int32_t *remaining, int32_t *out_tokens,
+               int32_t *n_accept, int32_t *n_emit, float *out_residual, uint32_t *flags, void *workspace,
+               size_t workspace_bytes, void *cuda_stream)
+{
+    const int rc = check_sample(logits, dt, temperature, top_k, top_p, draft_probs, draft, uniforms, B, k, V,
+                                out_tokens, n_accept, n_emit, out_residual, flags, workspace, workspace_bytes);
+    if (rc != SPEC_OK || B == 0)
+        return rc;
+    return launched(launch_verify_sample(sample_args(logits, temperature, top_k, top_p, draft_probs, draft, uniforms, B,
+                                                     k, V, draft_len, eos_id, remaining, out_tokens, n_accept,
+                                                     n_emit, out_residual, flags, workspace),
+                                         dt, (cudaStream_t)cuda_stream));
+}
+
 }  // namespace
 
 extern "C" {
@@ -93,73 +178,13 @@ int spec_verify_greedy(const void *target_logits, spec_dtype dt, int B, int k, i
                        const int32_t *remaining, int32_t *out_tokens, int32_t *n_accept, int32_t *n_emit,
                        void *workspace, size_t workspace_bytes, void *cuda_stream)
 {
-    int rc = check_verify_common(target_logits, dt, B, k, V, draft_tokens, out_tokens, n_accept, n_emit);
+    const int rc = check_greedy(target_logits, dt, B, k, V, draft_tokens, out_tokens, n_accept, n_emit, workspace,
+                                workspace_bytes);
     if (rc != SPEC_OK || B == 0)
         return rc;
-    rc = check_workspace(workspace, workspace_bytes, spec_workspace_bytes(B, k, V));
-    if (rc != SPEC_OK)
-        return rc;
-    VerifyArgs a{};
-    a.logits = target_logits;
-    a.B = B;
-    a.k = k;
-    a.V = V;
-    a.draft = draft_tokens;
-    a.draft_len = draft_len;
-    a.eos = eos_id;
-    a.remaining = remaining;
-    a.out_tokens = out_tokens;
-    a.n_accept = n_accept;
-    a.n_emit = n_emit;
-    a.ws = workspace;
-    return launched(launch_verify_greedy(a, dt, (cudaStream_t)cuda_stream));
-}
-
-static int verify_sample_impl(const void *target_logits, spec_dtype dt, float temperature, const int32_t *top_k,
-                              const float *top_p, const float *draft_probs, const int32_t *draft_tokens,
-                              const float *uniforms, int B, int k, int V, const int32_t *draft_len, int32_t eos_id,
-                              const int32_t *remaining, int32_t *out_tokens, int32_t *n_accept, int32_t *n_emit,
-                              float *out_residual, uint32_t *flags, void *workspace, size_t workspace_bytes,
-                              void *cuda_stream)
-{
-    int rc = check_verify_common(target_logits, dt, B, k, V, draft_tokens, out_tokens, n_accept, n_emit);
-    if (rc != SPEC_OK || B == 0)
-        return rc;
-    if (!(temperature > 0.0f) || !(temperature <= 3.0e38f) || !uniforms || (k > 0 && !draft_probs))
-        return SPEC_EINVAL;
-    if ((top_k || top_p) && V > SPEC_MAX_FILTER_V)
-        return SPEC_EINVAL;
-    if (!aligned(uniforms, 4) || (draft_probs && !aligned(draft_probs, 4)) ||
-        (out_residual && !aligned(out_residual, 4)) || (flags && !aligned(flags, 4)) ||
-        (top_k && !aligned(top_k, 4)) || (top_p && !aligned(top_p, 4)))
-        return SPEC_EALIGN;
-    rc = check_workspace(workspace, workspace_bytes, spec_workspace_bytes(B, k, V));
-    if (rc != SPEC_OK)
-        return rc;
-    VerifyArgs a{};
-    a.logits = target_logits;
-    a.B = B;
-    a.k = k;
-    a.V = V;
-    a.draft = draft_tokens;
-    a.draft_len = draft_len;
-    a.eos = eos_id;
-    a.remaining = remaining;
-    a.out_tokens = out_tokens;
-    a.n_accept = n_accept;
-    a.n_emit = n_emit;
-    a.ws = workspace;
-    a.inv_temp = 1.0f / temperature;
-    a.unit_temp = temperature == 1.0f ? 1 : 0;
-    a.q = draft_probs;
-    a.u = uniforms;
-    a.out_residual = out_residual;
-    a.flags = flags;
-    a.filtered = (top_k || top_p) ? 1 : 0;
-    a.top_k = top_k;
-    a.top_p = top_p;
-    a.dec_scale = (float)(1.44269504088896340736 / (double)temperature);
-    return launched(launch_verify_sample(a, dt, (cudaStream_t)cuda_stream));
+    return launched(launch_verify_greedy(verify_args(target_logits, B, k, V, draft_tokens, draft_len, eos_id, remaining,
+                                                     out_tokens, n_accept, n_emit, workspace),
+                                         dt, (cudaStream_t)cuda_stream));
 }
 
 int spec_verify_sample(const void *target_logits, spec_dtype dt, float temperature, const float *draft_probs,
@@ -168,7 +193,7 @@ int spec_verify_sample(const void *target_logits, spec_dtype dt, float temperatu
                        int32_t *n_accept, int32_t *n_emit, float *out_residual, uint32_t *flags,
                        void *workspace, size_t workspace_bytes, void *cuda_stream)
 {
-    return verify_sample_impl(target_logits, dt, temperature, nullptr, nullptr, draft_probs, draft_tokens, uniforms,
+    return run_sample(target_logits, dt, temperature, nullptr, nullptr, draft_probs, draft_tokens, uniforms,
                               B, k, V, draft_len, eos_id, remaining, out_tokens, n_accept, n_emit, out_residual,
                               flags, workspace, workspace_bytes, cuda_stream);
 }
@@ -180,15 +205,19 @@ int spec_verify_sample_filtered(const void *target_logits, spec_dtype dt, float 
                                 int32_t *n_emit, float *out_residual, uint32_t *flags, void *workspace,
                                 size_t workspace_bytes, void *cuda_stream)
 {
-    return verify_sample_impl(target_logits, dt, temperature, top_k, top_p, draft_probs, draft_tokens, uniforms, B,
+    return run_sample(target_logits, dt, temperature, top_k, top_p, draft_probs, draft_tokens, uniforms, B,
                               k, V, draft_len, eos_id, remaining, out_tokens, n_accept, n_emit, out_residual, flags,
                               workspace, workspace_bytes, cuda_stream);
 }
 
-int spec_realign_kv_multi(const spec_kv_cache *caches, int n_caches, int B, int S, const int32_t *len,
-                          const int32_t *pad, const int32_t *n_emit, int32_t *len_new, int32_t *pad_new,
-                          int32_t *width_new, int32_t *err, void *workspace, size_t workspace_bytes,
-                          void *cuda_stream)
+}  // extern "C"
+
+namespace {
+
+// argument checks of a realignment over `caches` (nothing launched)
+int check_realign(const spec_kv_cache *caches, int n_caches, int B, int S, const int32_t *len, const int32_t *pad,
+                  const int32_t *n_emit, const int32_t *len_new, const int32_t *pad_new, const int32_t *width_new,
+                  const int32_t *err, void *workspace, size_t workspace_bytes)
 {
     if (!caches || n_caches < 1 || n_caches > SPEC_MAX_CACHES || B < 0 || S < 1)
         return SPEC_EINVAL;
@@ -214,9 +243,13 @@ int spec_realign_kv_multi(const spec_kv_cache *caches, int n_caches, int B, int 
     if (!aligned(len, 4) || !aligned(pad, 4) || !aligned(n_emit, 4) || !aligned(len_new, 4) || !aligned(pad_new, 4) ||
         !aligned(width_new, 4) || !aligned(err, 4))
         return SPEC_EALIGN;
-    const int rc = check_workspace(workspace, workspace_bytes, spec_workspace_bytes(B, 0, 1));
-    if (rc != SPEC_OK)
-        return rc;
+    return check_workspace(workspace, workspace_bytes, spec_workspace_bytes(B, 0, 1));
+}
+
+cudaError_t start_realign(const spec_kv_cache *caches, int n_caches, int B, int S, const int32_t *len,
+                          const int32_t *pad, const int32_t *n_emit, int32_t *len_new, int32_t *pad_new,
+                          int32_t *width_new, int32_t *err, void *workspace, cudaStream_t st)
+{
     RealignArgs a{};
     for (int c = 0; c < n_caches; ++c)
         a.cache[c] = CacheDesc{caches[c].kv, dtype_bytes(caches[c].dt), caches[c].L, caches[c].H, caches[c].D};
@@ -231,7 +264,38 @@ int spec_realign_kv_multi(const spec_kv_cache *caches, int n_caches, int B, int 
     a.width_new = width_new;
     a.err = err;
     a.ws = workspace;
-    return launched(launch_realign(a, (cudaStream_t)cuda_stream));
+    return launch_realign(a, st);
+}
+
+int check_pos_mask(int B, int S, const int32_t *pad_old, const int32_t *pad_new, const int32_t *pos,
+                   const uint8_t *mask)
+{
+    if (B < 0 || S < 0 || B > 65535)
+        return SPEC_EINVAL;
+    if (B == 0 || S == 0)
+        return SPEC_OK;
+    if (!pad_new || !pos || !mask || (pad_old && pad_old == pad_new))
+        return SPEC_EINVAL;
+    if (!aligned(pad_new, 4) || !aligned(pos, 4) || (pad_old && !aligned(pad_old, 4)))
+        return SPEC_EALIGN;
+    return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_realign_kv_multi(const spec_kv_cache *caches, int n_caches, int B, int S, const int32_t *len,
+                          const int32_t *pad, const int32_t *n_emit, int32_t *len_new, int32_t *pad_new,
+                          int32_t *width_new, int32_t *err, void *workspace, size_t workspace_bytes,
+                          void *cuda_stream)
+{
+    const int rc = check_realign(caches, n_caches, B, S, len, pad, n_emit, len_new, pad_new, width_new, err,
+                                 workspace, workspace_bytes);
+    if (rc != SPEC_OK || B == 0)
+        return rc;
+    return launched(start_realign(caches, n_caches, B, S, len, pad, n_emit, len_new, pad_new, width_new, err,
+                                  workspace, (cudaStream_t)cuda_stream));
 }
 
 int spec_realign_kv(void *kv, spec_dtype dt, int L, int B, int H, int S, int D, const int32_t *len,
@@ -254,14 +318,9 @@ int spec_realign_kv(void *kv, spec_dtype dt, int L, int B, int H, int S, int D, 
 int spec_rebuild_pos_mask(int B, int S, const int32_t *pad_old, const int32_t *pad_new, int32_t *pos,
                           uint8_t *mask, void *cuda_stream)
 {
-    if (B < 0 || S < 0 || B > 65535)
-        return SPEC_EINVAL;
-    if (B == 0 || S == 0)
-        return SPEC_OK;
-    if (!pad_new || !pos || !mask || (pad_old && pad_old == pad_new))
-        return SPEC_EINVAL;
-    if (!aligned(pad_new, 4) || !aligned(pos, 4) || (pad_old && !aligned(pad_old, 4)))
-        return SPEC_EALIGN;
+    const int rc = check_pos_mask(B, S, pad_old, pad_new, pos, mask);
+    if (rc != SPEC_OK || B == 0 || S == 0)
+        return rc;
     return launched(launch_pos_mask(B, S, pad_old, pad_new, pos, mask, (cudaStream_t)cuda_stream));
 }
 
@@ -372,6 +431,65 @@ int spec_unpad_scatter(const void *batch, void *pool, spec_dtype dt, int L, int 
     a.err = err;
     a.ws = workspace;
     return launched(launch_pool_copy(a, (cudaStream_t)cuda_stream));
+}
+
+// ---- one whole round ------------------------------------------------------
+// verify, realign every cache by one plan, rebuild positions and mask: every
+// argument is checked before the first launch; the launches follow one
+// another on the stream (the realignment reads n_emit on the device).
+int spec_round_greedy(const void *target_logits, spec_dtype dt, int B, int k, int V, const int32_t *draft_tokens,
+                      const int32_t *draft_len, int32_t eos_id, const int32_t *remaining, const spec_kv_cache *caches,
+                      int n_caches, int S, const int32_t *len, const int32_t *pad, int32_t *pos, uint8_t *mask,
+                      int32_t *out_tokens, int32_t *n_accept, int32_t *n_emit, int32_t *len_new, int32_t *pad_new,
+                      int32_t *width_new, int32_t *err, void *workspace, size_t workspace_bytes, void *cuda_stream)
+{
+    int rc = check_greedy(target_logits, dt, B, k, V, draft_tokens, out_tokens, n_accept, n_emit, workspace,
+                          workspace_bytes);
+    if (rc == SPEC_OK)
+        rc = check_realign(caches, n_caches, B, S, len, pad, n_emit, len_new, pad_new, width_new, err, workspace,
+                           workspace_bytes);
+    if (rc == SPEC_OK)
+        rc = check_pos_mask(B, S, pad, pad_new, pos, mask);
+    if (rc != SPEC_OK || B == 0)
+        return rc;
+    const cudaStream_t st = (cudaStream_t)cuda_stream;
+    cudaError_t e = launch_verify_greedy(verify_args(target_logits, B, k, V, draft_tokens, draft_len, eos_id,
+                                                     remaining, out_tokens, n_accept, n_emit, workspace),
+                                         dt, st);
+    if (e == cudaSuccess)
+        e = start_realign(caches, n_caches, B, S, len, pad, n_emit, len_new, pad_new, width_new, err, workspace, st);
+    if (e == cudaSuccess)
+        e = launch_pos_mask(B, S, pad, pad_new, pos, mask, st);
+    return launched(e);
+}
+
+int spec_round_sample(const void *target_logits, spec_dtype dt, float temperature, const int32_t *top_k,
+                      const float *top_p, const float *draft_probs, const int32_t *draft_tokens,
+                      const float *uniforms, int B, int k, int V, const int32_t *draft_len, int32_t eos_id,
+                      const int32_t *remaining, const spec_kv_cache *caches, int n_caches, int S, const int32_t *len,
+                      const int32_t *pad, int32_t *pos, uint8_t *mask, int32_t *out_tokens, int32_t *n_accept,
+                      int32_t *n_emit, float *out_residual, uint32_t *flags, int32_t *len_new, int32_t *pad_new,
+                      int32_t *width_new, int32_t *err, void *workspace, size_t workspace_bytes, void *cuda_stream)
+{
+    int rc = check_sample(target_logits, dt, temperature, top_k, top_p, draft_probs, draft_tokens, uniforms, B, k, V,
+                          out_tokens, n_accept, n_emit, out_residual, flags, workspace, workspace_bytes);
+    if (rc == SPEC_OK)
+        rc = check_realign(caches, n_caches, B, S, len, pad, n_emit, len_new, pad_new, width_new, err, workspace,
+                           workspace_bytes);
+    if (rc == SPEC_OK)
+        rc = check_pos_mask(B, S, pad, pad_new, pos, mask);
+    if (rc != SPEC_OK || B == 0)
+        return rc;
+    const cudaStream_t st = (cudaStream_t)cuda_stream;
+    cudaError_t e = launch_verify_sample(sample_args(target_logits, temperature, top_k, top_p, draft_probs, draft_tokens,
+                                                     uniforms, B, k, V, draft_len, eos_id, remaining, out_tokens,
+                                                     n_accept, n_emit, out_residual, flags, workspace),
+                                         dt, st);
+    if (e == cudaSuccess)
+        e = start_realign(caches, n_caches, B, S, len, pad, n_emit, len_new, pad_new, width_new, err, workspace, st);
+    if (e == cudaSuccess)
+        e = launch_pos_mask(B, S, pad, pad_new, pos, mask, st);
+    return launched(e);
 }
 
 }  // extern "C"

@@ -206,3 +206,32 @@ def test_pool_argument_errors(lib):
     assert repad(ws=None) == -3 and repad(batch=FAKE_ODD) == -5
     assert lib.spec_unpad_scatter(FAKE, FAKE, 1, 2, 8, 2, 2, 64, 8, FAKE, None, FAKE, FAKE, FAKE, FAKE, 1 << 20,
                                   None) == -1
+
+
+def test_round_entry_points_check_everything_before_launching(lib):
+    from speculative_decoding_verification_28_gb300._lib import KVCacheDesc
+
+    one = (KVCacheDesc * 1)(KVCacheDesc(0x10000, 1, 2, 2, 8))
+    P = ctypes.cast(one, ctypes.c_void_p)
+
+    def greedy(B=2, S=64, pad=FAKE, pad_new=ctypes.c_void_p(0x20000), pos=FAKE, n_caches=1, caches=P, ws=FAKE):
+        return lib.spec_round_greedy(FAKE, 1, B, 3, 100, FAKE, None, -1, None, caches, n_caches, S, FAKE, pad, pos,
+                                     FAKE, FAKE, FAKE, FAKE, FAKE, pad_new, FAKE, FAKE, ws, 1 << 30, None)
+
+    assert greedy(B=-1) == -1
+    assert greedy(pad_new=FAKE) == -1           # pad_new aliases pad
+    assert greedy(pos=None) == -1
+    assert greedy(n_caches=0) == -1
+    assert greedy(caches=None) == -1
+    assert greedy(pos=FAKE_ODD) == -5
+    assert greedy(ws=FAKE_ODD) == -3
+    assert greedy(B=0) == 0
+
+    def sample(T=1.0, tk=None, u=FAKE):
+        return lib.spec_round_sample(FAKE, 0, T, tk, None, FAKE, FAKE, u, 2, 3, 100, None, -1, None, P, 1, 64,
+                                     FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE,
+                                     ctypes.c_void_p(0x20000), FAKE, FAKE, FAKE, 1 << 30, None)
+
+    assert sample(T=0.0) == -1
+    assert sample(u=None) == -1
+    assert sample(tk=FAKE_ODD) == -5

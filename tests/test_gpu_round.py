@@ -1,0 +1,158 @@
+"""One whole round per call (spec_round_greedy / spec_round_sample): the
+fused entry points against the oracle (greedy: verification, the
+realignment of every cache byte for byte, positions and mask) and against
+the separate entry points (stochastic, which are themselves checked against
+the oracle in test_gpu_verify_sample.py / test_gpu_verify_filter.py)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_verification_28_gb300 as sv
+from gpu_util import dev, logits_to_dev, to_dev
+from specgen import greedy_round_inputs, prompt_lengths, sample_round_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _state(B, S, k, seed):
+    ln = prompt_lengths(B, 4, 60, seed)
+    W = int(ln.max())
+    assert W + k + 1 <= S
+    return ln, (W - ln).astype(np.int32)
+
+
+@pytest.mark.parametrize("two_caches", [False, True])
+def test_greedy_round_equals_oracle_over_chained_rounds(two_caches):
+    rng = np.random.default_rng(7 + two_caches)
+    B, k, V, S = 9, 4, 3000, 128
+    kv = rng.integers(0, 65535, size=(2, 2, B, 3, S, 16), dtype=np.uint16).view(np.float16)
+    dkv = rng.standard_normal((1, 2, B, 2, S, 8)).astype(np.float32)
+    kv_t, dkv_t = torch.from_numpy(kv.copy()).to(dev()), torch.from_numpy(dkv.copy()).to(dev())
+    caches = [kv_t, dkv_t] if two_caches else [kv_t]
+    ln, pad = _state(B, S, k, seed=11)
+    pos = torch.zeros((B, S), dtype=torch.int32, device=dev())
+    mask = torch.zeros((B, S), dtype=torch.uint8, device=dev())
+    opos, omask = oracle.rebuild_pos_mask(S, pad)
+    pos.copy_(torch.from_numpy(opos))
+    mask.copy_(torch.from_numpy(omask))
+    for r in range(10):
+        if int(ln[0] + pad[0]) + k + 1 > S:
+            break
+        x, d = greedy_round_inputs(B, k, V, 0.6, 1.0, seed=100 + r, dtype="f32")
+        o_out, o_na, o_ne = oracle.verify_greedy(x, oracle.DT_F32, d)
+        out, na, ne, ln2, pd2, w2, err = sv.spec_round_greedy(to_dev(x), to_dev(d), caches, to_dev(ln), to_dev(pad),
+                                                              pos, mask)
+        st, o_ln, o_pd, o_w = oracle.realign_kv(kv, ln, pad, o_ne)
+        if two_caches:
+            st2, _, _, _ = oracle.realign_kv(dkv, ln, pad, o_ne)
+            assert st2 == 0
+        oracle.rebuild_pos_mask(S, o_pd, opos, omask)
+        assert st == 0 and int(err.item()) == 0
+        assert np.array_equal(out.cpu().numpy(), o_out) and np.array_equal(na.cpu().numpy(), o_na)
+        assert np.array_equal(ne.cpu().numpy(), o_ne)
+        assert np.array_equal(ln2.cpu().numpy(), o_ln) and np.array_equal(pd2.cpu().numpy(), o_pd)
+        assert int(w2.item()) == o_w
+        assert np.array_equal(kv_t.cpu().numpy().view(np.uint16), kv.view(np.uint16)), r
+        if two_caches:
+            assert np.array_equal(dkv_t.cpu().numpy(), dkv), r
+        assert np.array_equal(pos.cpu().numpy(), opos) and np.array_equal(mask.cpu().numpy(), omask)
+        ln, pad = o_ln, o_pd
+
+
+@pytest.mark.parametrize("filtered", [False, True])
+def test_sample_round_equals_separate_calls(filtered):
+    rng = np.random.default_rng(3 + filtered)
+    B, k, V, S = 12, 3, 5000, 96
+    kv = rng.standard_normal((2, 2, B, 2, S, 8)).astype(np.float32)
+    kv_a, kv_b = torch.from_numpy(kv.copy()).to(dev()), torch.from_numpy(kv.copy()).to(dev())
+    ln, pad = _state(B, S, k, seed=5)
+    x, q, d, u = sample_round_inputs(B, k, V, 0.5, seed=9, dtype="bf16")
+    xt, qt, dt_, ut = logits_to_dev(x, oracle.DT_BF16), to_dev(q), to_dev(d), to_dev(u)
+    tk = to_dev(rng.integers(0, 60, size=B).astype(np.int32)) if filtered else None
+    tp = to_dev(rng.choice([0.5, 0.9, 1.0], size=B).astype(np.float32)) if filtered else None
+    pos_a = torch.zeros((B, S), dtype=torch.int32, device=dev())
+    mask_a = torch.zeros((B, S), dtype=torch.uint8, device=dev())
+    pos_b, mask_b = pos_a.clone(), mask_a.clone()
+    res = torch.empty((B, V), dtype=torch.float32, device=dev())
+    g = sv.spec_round_sample(xt, qt, dt_, ut, [kv_a], to_dev(ln), to_dev(pad), pos_a, mask_a, top_k=tk, top_p=tp,
+                             out_residual=res)
+    if filtered:
+        s = sv.spec_verify_sample_filtered(xt, qt, dt_, ut, top_k=tk, top_p=tp, want_residual=True)
+    else:
+        s = sv.spec_verify_sample(xt, qt, dt_, ut, want_residual=True)
+    ln2, pd2, w2, err = sv.spec_realign_kv(kv_b, to_dev(ln), to_dev(pad), s[2])
+    sv.spec_rebuild_pos_mask(pd2, pos_b, mask_b, pad_old=to_dev(pad))
+    for a, b in zip(g[:3], s[:3]):
+        assert torch.equal(a, b)
+    assert torch.equal(g[7], s[3]) and torch.equal(g[8], s[4])
+    assert torch.equal(g[3], ln2) and torch.equal(g[4], pd2) and torch.equal(g[5], w2) and int(g[6].item()) == 0
+    assert torch.equal(kv_a, kv_b) and torch.equal(pos_a, pos_b) and torch.equal(mask_a, mask_b)
+
+
+def test_round_rejects_aliased_padding_and_launches_nothing():
+    B, k, V, S = 4, 2, 100, 32
+    x, d = greedy_round_inputs(B, k, V, 0.5, 1.0, seed=1, dtype="f32")
+    kv = torch.zeros((1, 2, B, 1, S, 8), dtype=torch.float32, device=dev())
+    ln = to_dev(np.full(B, 5, np.int32))
+    pad = to_dev(np.zeros(B, np.int32))
+    pos = torch.zeros((B, S), dtype=torch.int32, device=dev())
+    mask = torch.zeros((B, S), dtype=torch.uint8, device=dev())
+    out = torch.full((B, k + 1), -9, dtype=torch.int32, device=dev())
+    with pytest.raises(sv.SpecError):
+        sv.spec_round_greedy(to_dev(x), to_dev(d), [kv], ln, pad, pos, mask, out_tokens=out, pad_new=pad)
+    torch.cuda.synchronize()
+    assert (out == -9).all()
+
+
+def test_round_replayed_from_a_cuda_graph_equals_oracle():
+    """spec_round_greedy captured once per buffer parity (RoundGraph) and
+    replayed over chained rounds: same results as the oracle, byte for byte."""
+    rng = np.random.default_rng(17)
+    B, k, V, S = 8, 3, 2000, 96
+    kv = rng.standard_normal((2, 2, B, 2, S, 16)).astype(np.float32)
+    kv_t = torch.from_numpy(kv.copy()).to(dev())
+    ln, pad = _state(B, S, k, seed=21)
+    pos = torch.from_numpy(oracle.rebuild_pos_mask(S, pad)[0]).to(dev())
+    mask = torch.from_numpy(oracle.rebuild_pos_mask(S, pad)[1]).to(dev())
+    opos, omask = oracle.rebuild_pos_mask(S, pad)
+    x_d = torch.empty((B, k + 1, V), dtype=torch.float32, device=dev())
+    d_d = torch.empty((B, k), dtype=torch.int32, device=dev())
+    blocks = [torch.empty(B * (k + 1) + 4 * B + 2, dtype=torch.int32, device=dev()) for _ in range(2)]
+    ws = sv.Workspace(B, k, V, dev())
+
+    def views(blk):
+        o = B * (k + 1)
+        return (blk[:o].view(B, k + 1), blk[o:o + B], blk[o + B:o + 2 * B], blk[o + 2 * B:o + 3 * B],
+                blk[o + 3 * B:o + 4 * B], blk[o + 4 * B:o + 4 * B + 1], blk[o + 4 * B + 1:])
+
+    def enqueue(par):
+        out, na, ne, _, _, w, err = views(blocks[1 - par])
+        _, _, _, ln_in, pad_in, _, _ = views(blocks[par])
+        _, _, _, ln_out, pad_out, _, _ = views(blocks[1 - par])
+        sv.spec_round_greedy(x_d, d_d, [kv_t], ln_in, pad_in, pos, mask, out_tokens=out, n_accept=na, n_emit=ne,
+                             len_new=ln_out, pad_new=pad_out, width_new=w, err=err, workspace=ws)
+
+    graphs = [sv.RoundGraph(lambda p=p: enqueue(p), dev()) for p in (0, 1)]
+    views(blocks[0])[3].copy_(to_dev(ln))
+    views(blocks[0])[4].copy_(to_dev(pad))
+    cur = 0
+    for r in range(8):
+        if int(ln[0] + pad[0]) + k + 1 > S:
+            break
+        x, d = greedy_round_inputs(B, k, V, 0.6, 1.0, seed=300 + r, dtype="f32")
+        x_d.copy_(torch.from_numpy(x))
+        d_d.copy_(torch.from_numpy(d))
+        graphs[cur].replay()
+        torch.cuda.synchronize()
+        out, na, ne, ln2, pd2, w2, err = (t.cpu().numpy() for t in views(blocks[1 - cur]))
+        o_out, o_na, o_ne = oracle.verify_greedy(x, oracle.DT_F32, d)
+        st, o_ln, o_pd, o_w = oracle.realign_kv(kv, ln, pad, o_ne)
+        oracle.rebuild_pos_mask(S, o_pd, opos, omask)
+        assert st == 0 and int(err[0]) == 0
+        assert np.array_equal(out, o_out) and np.array_equal(na, o_na) and np.array_equal(ne, o_ne)
+        assert np.array_equal(ln2, o_ln) and np.array_equal(pd2, o_pd) and int(w2[0]) == o_w
+        assert np.array_equal(kv_t.cpu().numpy(), kv), r
+        assert np.array_equal(pos.cpu().numpy(), opos) and np.array_equal(mask.cpu().numpy(), omask)
+        ln, pad = o_ln, o_pd
+        cur = 1 - cur
