@@ -692,9 +692,11 @@ def run_exspec_bench(args, c, rank, local_rank, world):
     """EXSPEC rounds over a ragged pool: each round the largest same-length
     group in the window is verified in place (grouped round: verify + commit,
     no KV moves), or the chosen sequences take the unpad-append-repad
-    fallback (repad, verify, realign, pos/mask, unpad).  Timed: the library
-    calls only -- the selection, then the round -- with the synthetic target
-    forward between them untimed and an L2 flush before each timed part."""
+    fallback (repad + pos/mask, verify, unpad straight from the extended
+    batch: the realignment a batch would need for its next round is skipped,
+    the batch is unpadded right away).  Timed: the library calls only -- the
+    selection, then the round -- with the synthetic target forward between
+    them untimed and an L2 flush before each timed part."""
     import torch
 
     import speculative_decoding_verification_28_gb300 as sv
@@ -774,21 +776,20 @@ def run_exspec_bench(args, c, rank, local_rank, world):
             mask = mask_flat[: Bb * S].view(Bb, S)
             flush.zero_()
 
-            def repad():
-                return sv.spec_repad_gather(pool, batch, idx, pool_len, workspace=ws)
+            def repad():  # the batch and its positions / mask for the forward
+                r = sv.spec_repad_gather(pool, batch, idx, pool_len, workspace=ws)
+                sv.spec_rebuild_pos_mask(r[1], pos, mask)
+                return r
             (ln, pd, w, err0), t_repad = timed(repad)
             assert int(err0.item()) == 0
-            sv.spec_rebuild_pos_mask(pd, pos, mask)
             W = int(w.item())
             torch_gen.kv_write_query(batch, qtok, pos, W)
             flush.zero_()
             moved = int(((ln - 1).sum()).item())
 
-            def rest():
+            def rest():  # verify, then unpad straight from the extended batch (no realignment)
                 _, _, ne = sv.spec_verify_greedy(x, d, workspace=ws)
-                ln2, pd2, w2, err1 = sv.spec_realign_kv(batch, ln, pd, ne, workspace=ws)
-                sv.spec_rebuild_pos_mask(pd2, pos, mask, pad_old=pd)
-                err = sv.spec_unpad_scatter(batch, pool, idx, ln2, pd2, pool_len, workspace=ws)
+                err = sv.spec_unpad_scatter(batch, pool, idx, ln, pd, pool_len, n_emit=ne, workspace=ws)
                 return ne, err
             (ne, err), t_round = timed(rest)
             t_parts = (t_sel, t_repad, t_round)
@@ -843,7 +844,7 @@ def run_exspec_bench(args, c, rank, local_rank, world):
         "selection_us": round(float(np.mean([r[1][0] for r in rounds])) * 1e6, 2) if rounds else None,
         "roofline": roof,
         "tokens_per_round": round(sum(r[3] for r in rounds) / max(n, 1) / B, 4),
-        "gpu_launches": sum(3 if r[0] else 9 for r in rounds),
+        "gpu_launches": sum(3 if r[0] else 7 for r in rounds),
         "clocks": clk.summary(),
     }
     if pg:

@@ -334,11 +334,19 @@ SPEC_API int spec_repad_gather(const void *pool, void *batch, spec_dtype dt, int
 /* Unpad: batch row b's rows pad[b] .. pad[b] + len[b] - 2 go back to slot 0 of
  * pool sequence idx[b], and pool_len[idx[b]] = len[b]; no other pool byte
  * changes.  err [1]: SPEC_REALIGN_OK or SPEC_REALIGN_LAYOUT (bad or repeated
- * index, len < 1, pad < 0 or a run past S; nothing written). */
+ * index, len < 1, pad < 0, n_emit < 0 or a run past S; nothing written).
+ * n_emit [B] int32 or NULL: when given, the lengths written back are
+ * len + n_emit, read from a batch that a round has just extended without
+ * realigning it.  After a round on a left-padded batch of width W the
+ * verification forward wrote the last token and the proposals at slots
+ * W - 1 .. = pad + len - 1 .., so rows pad .. pad + len + n_emit - 2 hold
+ * positions 0 .. len + n_emit - 2: unpadding them needs no realignment first
+ * (the pool ends byte for byte as after spec_realign_kv and an unpad with the
+ * new lengths and paddings). */
 SPEC_API int spec_unpad_scatter(const void *batch, void *pool, spec_dtype dt, int L, int N, int B, int H, int S,
                        int D, const int32_t *idx, const int32_t *len, const int32_t *pad,
-                       int32_t *pool_len, int32_t *err, void *workspace, size_t workspace_bytes,
-                       void *cuda_stream);
+                       const int32_t *n_emit, int32_t *pool_len, int32_t *err, void *workspace,
+                       size_t workspace_bytes, void *cuda_stream);
 
 /*
  * One whole round in one call: spec_verify_greedy (or spec_verify_sample /

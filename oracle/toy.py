@@ -219,7 +219,8 @@ def exspec_select(lens, active, window, B, group):
     return picks, ce == B and len(picks) == B
 
 
-def run_exspec(pair: ToyPair, prompts, n_new, k, S, B, window, ops, eos_id=-1, max_rounds=2000):
+def run_exspec(pair: ToyPair, prompts, n_new, k, S, B, window, ops, eos_id=-1, max_rounds=2000,
+               fallback_realign=True, result=None):
     """EXSPEC-style decoding of the toy pair over a ragged pool: each round the
     window's largest same-length group is verified in place (grouped round, no
     realignment: the commit is a length update); when no full group forms the
@@ -232,7 +233,14 @@ def run_exspec(pair: ToyPair, prompts, n_new, k, S, B, window, ops, eos_id=-1, m
       commit(pool_len, idx, n_emit, S) -> status            (pool_len in place)
       repad(pool, batch, idx, pool_len) -> (status, len, pad, width)
       realign(kv, len, pad, n_emit) -> (status, len_new, pad_new, width)
-      unpad(batch, pool, idx, len, pad, pool_len) -> status  (pool_len in place)
+      unpad(batch, pool, idx, len, pad, pool_len, n_emit=None) -> status
+                                                   (pool_len in place; with n_emit the
+                                                    lengths written back are len + n_emit)
+    fallback_realign=False unpads a fallback round straight from the extended
+    batch (lengths len + n_emit at the old paddings) instead of realigning
+    the batch first: the rows pad .. pad + len + n_emit - 2 already hold
+    positions 0 .. len + n_emit - 2, so the pool must end byte for byte the
+    same.  result (a dict, optional) receives the final pool and lengths.
     Returns (generated tokens per sequence, rounds, grouped rounds)."""
     N = len(prompts)
     L, H, D = pair.L, pair.H, pair.D
@@ -284,13 +292,19 @@ def run_exspec(pair: ToyPair, prompts, n_new, k, S, B, window, ops, eos_id=-1, m
                     pair.write_query_kv_seq(batch, pos, i, n, W - 1 + j, t)
                 logits[i] = pair.batched_logits(batch, pos, mask, i, W - 1, k + 1)
             out, _, ne = ops["verify"](logits, draft, remaining, eos_id)
-            st, ln2, pad2, _ = ops["realign"](batch, ln, pad, ne)
-            assert st == 0
-            assert ops["unpad"](batch, pool, np.array(picks, np.int32), ln2, pad2, pool_len) == 0
+            if fallback_realign:
+                st, ln2, pad2, _ = ops["realign"](batch, ln, pad, ne)
+                assert st == 0
+                assert ops["unpad"](batch, pool, np.array(picks, np.int32), ln2, pad2, pool_len) == 0
+            else:
+                assert ops["unpad"](batch, pool, np.array(picks, np.int32), ln, pad, pool_len,
+                                    np.asarray(ne, np.int32)) == 0
         for i, n in enumerate(picks):
             toks = [int(t) for t in out[i, : ne[i]]]
             gen[n] += toks
             hist[n] += toks
             if len(gen[n]) >= n_new or (eos_id >= 0 and eos_id in toks):
                 active[n] = False
+    if result is not None:
+        result["pool"], result["pool_len"] = pool, pool_len
     return gen, rounds, grouped

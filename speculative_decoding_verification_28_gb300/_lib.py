@@ -49,7 +49,7 @@ SIGNATURES["spec_commit_ragged"] = ([_i32, _vp, _i32, _vp, _vp, _i32, _vp, _vp],
 SIGNATURES["spec_repad_gather"] = ([_vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
                                     _vp, _sz, _vp], _i32)
 SIGNATURES["spec_unpad_scatter"] = ([_vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
-                                     _vp, _sz, _vp], _i32)
+                                     _vp, _vp, _sz, _vp], _i32)
 
 _lib = None
 

@@ -456,9 +456,11 @@ def spec_repad_gather(pool, batch, idx, pool_len, len_out=None, pad_out=None, wi
     return len_out, pad_out, width_out, err
 
 
-def spec_unpad_scatter(batch, pool, idx, length, pad, pool_len, err=None, workspace=None, stream=None):
+def spec_unpad_scatter(batch, pool, idx, length, pad, pool_len, n_emit=None, err=None, workspace=None, stream=None):
     """batch [L,2,B,H,S,D] -> pool [L,2,N,H,S,D]; pool_len [N] updated in
-    place. -> err [1] int32."""
+    place.  n_emit [B] (optional): write back len + n_emit rows from a batch
+    a round has just extended, without realigning it first.
+    -> err [1] int32."""
     lib = _lib.load()
     L, two, N, H, S, D = pool.shape
     B = batch.shape[2]
@@ -471,9 +473,10 @@ def spec_unpad_scatter(batch, pool, idx, length, pad, pool_len, err=None, worksp
     for t, nm in ((length, "len"), (pad, "pad")):
         _need(t, torch.int32, nm, dev, (B,))
     _need(pool_len, torch.int32, "pool_len", dev, (N,))
+    _need(n_emit, torch.int32, "n_emit", dev, (B,))
     err = torch.empty(1, dtype=torch.int32, device=dev) if err is None else err
     st = _stream(stream, dev)
     ws = _workspace(workspace, B, 0, 1, dev, st)
     _check(lib.spec_unpad_scatter(_p(batch), _p(pool), _DT[pool.dtype], L, N, B, H, S, D, _p(idx), _p(length),
-                                  _p(pad), _p(pool_len), _p(err), ws.ptr(), ws.nbytes, st))
+                                  _p(pad), _p(n_emit), _p(pool_len), _p(err), ws.ptr(), ws.nbytes, st))
     return err

@@ -403,15 +403,15 @@ int spec_repad_gather(const void *pool, void *batch, spec_dtype dt, int L, int N
 }
 
 int spec_unpad_scatter(const void *batch, void *pool, spec_dtype dt, int L, int N, int B, int H, int S, int D,
-                       const int32_t *idx, const int32_t *len, const int32_t *pad, int32_t *pool_len, int32_t *err,
-                       void *workspace, size_t workspace_bytes, void *cuda_stream)
+                       const int32_t *idx, const int32_t *len, const int32_t *pad, const int32_t *n_emit,
+                       int32_t *pool_len, int32_t *err, void *workspace, size_t workspace_bytes, void *cuda_stream)
 {
     int rc = pool_common(batch, pool, dt, L, N, B, H, S, D, idx, err, workspace, workspace_bytes);
     if (rc != SPEC_OK || B == 0)
         return rc;
     if (!len || !pad || !pool_len)
         return SPEC_EINVAL;
-    if (!aligned(len, 4) || !aligned(pad, 4) || !aligned(pool_len, 4))
+    if (!aligned(len, 4) || !aligned(pad, 4) || !aligned(pool_len, 4) || (n_emit && !aligned(n_emit, 4)))
         return SPEC_EALIGN;
     PoolArgs a{};
     a.src = batch;
@@ -427,6 +427,7 @@ int spec_unpad_scatter(const void *batch, void *pool, spec_dtype dt, int L, int 
     a.idx = idx;
     a.len = len;
     a.pad = pad;
+    a.n_emit = n_emit;
     a.pool_len_out = pool_len;
     a.err = err;
     a.ws = workspace;

@@ -10,7 +10,9 @@
 //            §2) is that length update: their KV rows lie past the new length;
 //   repad  : pool -> left-padded batch (the chosen sequences' rows
 //            0 .. len - 2 at slot W - len, W the longest), for a fallback round;
-//   unpad  : batch -> pool (rows pad .. pad + len - 2 back to slot 0) after it.
+//   unpad  : batch -> pool (rows pad .. pad + len - 2 back to slot 0) after it;
+//            with n_emit the lengths are len + n_emit, straight from the batch a
+//            round has extended (no realignment needed before unpadding).
 // repad / unpad are out-of-place copies of every slab's run, done by the same
 // bulk-copy engine as the realignment shift.  Roofline: HBM-bound,
 // 2 * (len - 1) * D * elt bytes per slab.
@@ -67,8 +69,10 @@ __global__ void __launch_bounds__(kPoolPlanThreads) pool_plan_kernel(PoolArgs a)
             if (ok)
                 atomicMax(&s_W, l);
         } else if (ok) {
-            const int l = a.len[b], p = a.pad[b];
-            ok = l >= 1 && p >= 0 && (long long)p + l - 1 <= a.S;
+            const int e = a.n_emit ? a.n_emit[b] : 0;
+            const long long l = (long long)a.len[b] + e;
+            const int p = a.pad[b];
+            ok = e >= 0 && l >= 1 && p >= 0 && p + l - 1 <= a.S;
         }
         if (!ok)
             atomicOr(&s_bad, 1);
@@ -94,7 +98,7 @@ __global__ void __launch_bounds__(kPoolPlanThreads) pool_plan_kernel(PoolArgs a)
             a.len_out[b] = l;
             a.pad_out[b] = W - l;
         } else {
-            const int l = a.len[b];
+            const int l = a.len[b] + (a.n_emit ? a.n_emit[b] : 0);
             pp.seq_src[b] = b;
             pp.src_off[b] = a.pad[b];
             pp.seq_dst[b] = n;

@@ -76,6 +76,7 @@ struct PoolArgs {
     const int32_t *idx;       // [B] pool index of each batch row
     const int32_t *pool_len;  // repad: [N] lengths in the pool
     const int32_t *len, *pad; // unpad: [B] batch lengths and paddings
+    const int32_t *n_emit;    // unpad: [B] commits added to len, or null
     int32_t *len_out, *pad_out, *width_out;  // repad outputs
     int32_t *pool_len_out;    // unpad: [N] lengths written back
     int32_t *err;

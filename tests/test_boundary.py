@@ -204,8 +204,10 @@ def test_pool_argument_errors(lib):
     assert repad(L=0) == -1 and repad(N=70000) == -1 and repad(dt=7) == -2
     assert repad(B=0) == 0 and repad(pool=None) == -1 and repad(pl=None) == -1
     assert repad(ws=None) == -3 and repad(batch=FAKE_ODD) == -5
-    assert lib.spec_unpad_scatter(FAKE, FAKE, 1, 2, 8, 2, 2, 64, 8, FAKE, None, FAKE, FAKE, FAKE, FAKE, 1 << 20,
-                                  None) == -1
+    assert lib.spec_unpad_scatter(FAKE, FAKE, 1, 2, 8, 2, 2, 64, 8, FAKE, None, FAKE, None, FAKE, FAKE, FAKE,
+                                  1 << 20, None) == -1
+    assert lib.spec_unpad_scatter(FAKE, FAKE, 1, 2, 8, 2, 2, 64, 8, FAKE, FAKE, FAKE, FAKE_ODD, FAKE, FAKE, FAKE,
+                                  1 << 20, None) == -5
 
 
 def test_round_entry_points_check_everything_before_launching(lib):

@@ -133,10 +133,11 @@ def device_ops():
         kv[...] = kv_t.cpu().numpy()
         return int(err.item()), l2.cpu().numpy(), p2.cpu().numpy(), int(w2.item())
 
-    def unpad(batch, pool, idx, ln, pad, pl):
+    def unpad(batch, pool, idx, ln, pad, pl, ne=None):
         p_t, b_t = torch.from_numpy(pool).to(dev()), torch.from_numpy(batch).to(dev())
         g = to_dev(pl.copy())
-        err = sv.spec_unpad_scatter(b_t, p_t, to_dev(np.asarray(idx, np.int32)), to_dev(ln), to_dev(pad), g)
+        err = sv.spec_unpad_scatter(b_t, p_t, to_dev(np.asarray(idx, np.int32)), to_dev(ln), to_dev(pad), g,
+                                    n_emit=None if ne is None else to_dev(np.asarray(ne, np.int32)))
         pool[...] = p_t.cpu().numpy()
         pl[...] = g.cpu().numpy()
         return int(err.item())
@@ -148,7 +149,8 @@ def oracle_ops():
     return dict(group=lambda lens, B: oracle.group_by_length(lens, B),
                 verify=lambda x, d, rem, eos: oracle.verify_greedy(x, DT_F32, d, None, eos, rem),
                 commit=oracle.commit_ragged, repad=oracle.repad_gather, realign=oracle.realign_kv,
-                unpad=oracle.unpad_scatter)
+                unpad=lambda b, p, i, ln, pad, pl, ne=None: oracle.unpad_scatter(
+                    b, p, i, ln if ne is None else np.asarray(ln, np.int32) + ne, pad, pl))
 
 
 @pytest.mark.parametrize("N,B,window,k,alpha,n_new,eos,lens", [
@@ -156,17 +158,45 @@ def oracle_ops():
     (10, 3, 6, 3, 0.5, 14, -1, [4, 4, 4, 2, 7, 7, 1, 5, 5, 3]),
     (6, 2, 2, 2, 0.9, 10, 4, [2, 5, 5, 3, 2, 6]),
 ])
-def test_exspec_on_device_equals_single_sequence_greedy(N, B, window, k, alpha, n_new, eos, lens):
+@pytest.mark.parametrize("fallback_realign", [True, False])
+def test_exspec_on_device_equals_single_sequence_greedy(N, B, window, k, alpha, n_new, eos, lens, fallback_realign):
     pair = ToyPair(V=11, L=2, H=2, D=4, alpha=alpha, seed=N * 7 + B)
     rng = np.random.default_rng(N + B)
     prompts = [list(rng.integers(0, 11, size=n)) for n in lens]
     S = max(lens) + n_new + 2 * (k + 1) + 8
-    gen, rounds, grouped = run_exspec(pair, prompts, n_new, k, S, B, window, device_ops(), eos_id=eos)
+    a, b = {}, {}
+    gen, rounds, grouped = run_exspec(pair, prompts, n_new, k, S, B, window, device_ops(), eos_id=eos,
+                                      fallback_realign=fallback_realign, result=a)
     for n in range(N):
         assert gen[n] == pair.ref_generate(n, prompts[n], n_new, eos_id=eos), n
-    # and the same sequence of round kinds as the oracle's run
-    _, r2, g2 = run_exspec(pair, prompts, n_new, k, S, B, window, oracle_ops(), eos_id=eos)
+    # and the same rounds and the same final pool as the oracle's run (which realigns)
+    _, r2, g2 = run_exspec(pair, prompts, n_new, k, S, B, window, oracle_ops(), eos_id=eos, result=b)
     assert (rounds, grouped) == (r2, g2)
+    assert np.array_equal(a["pool"].view(np.uint32), b["pool"].view(np.uint32))
+    assert np.array_equal(a["pool_len"], b["pool_len"])
+
+
+def test_unpad_with_commits_matches_oracle_and_refuses_negative_counts():
+    rng = np.random.default_rng(41)
+    L, N, H, S, D, B = 2, 30, 2, 200, 16, 7
+    pool = rng.standard_normal((L, 2, N, H, S, D)).astype(np.float32)
+    batch = rng.standard_normal((L, 2, B, H, S, D)).astype(np.float32)
+    idx = rng.choice(N, size=B, replace=False).astype(np.int32)
+    ln = rng.integers(1, 120, size=B).astype(np.int32)
+    pad = (int(ln.max()) - ln).astype(np.int32)
+    ne = rng.integers(0, 6, size=B).astype(np.int32)
+    pl = rng.integers(1, 150, size=N).astype(np.int32)
+    pool_t, pl_t = torch.from_numpy(pool.copy()).to(dev()), to_dev(pl.copy())
+    err = sv.spec_unpad_scatter(torch.from_numpy(batch).to(dev()), pool_t, to_dev(idx), to_dev(ln), to_dev(pad),
+                                pl_t, n_emit=to_dev(ne))
+    ref_pl = pl.copy()
+    assert oracle.unpad_scatter(batch, pool, idx, ln + ne, pad, ref_pl) == 0 and int(err.item()) == 0
+    assert np.array_equal(pool_t.cpu().numpy(), pool) and np.array_equal(pl_t.cpu().numpy(), ref_pl)
+    bad = ne.copy()
+    bad[3] = -1
+    err = sv.spec_unpad_scatter(torch.from_numpy(batch).to(dev()), pool_t, to_dev(idx), to_dev(ln), to_dev(pad),
+                                pl_t, n_emit=to_dev(bad))
+    assert int(err.item()) == sv.REALIGN_LAYOUT and np.array_equal(pool_t.cpu().numpy(), pool)
 
 
 @pytest.mark.parametrize("N,B,window,vals", [(512, 64, 512, 8), (512, 64, 96, 8), (300, 16, 40, 900),

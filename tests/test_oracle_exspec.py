@@ -88,7 +88,8 @@ def oracle_ops():
         commit=oracle.commit_ragged,
         repad=oracle.repad_gather,
         realign=oracle.realign_kv,
-        unpad=oracle.unpad_scatter,
+        unpad=lambda b, p, i, ln, pad, pl, ne=None: oracle.unpad_scatter(
+            b, p, i, ln if ne is None else np.asarray(ln, np.int32) + ne, pad, pl),
     )
 
 
@@ -116,3 +117,20 @@ def test_both_round_kinds_occur_and_planted_mistakes_diverge():
     ops["commit"] = lambda pl, idx, ne, S: oracle.commit_ragged(pl, idx, np.maximum(ne - 1, 0), S)
     bad, _, _ = run_exspec(pair, prompts, 14, k, S, B, window, ops)
     assert any(bad[n] != pair.ref_generate(n, prompts[n], 14) for n in range(N))
+
+
+@pytest.mark.parametrize("N,B,window,k,alpha,n_new,eos,lens", CASES)
+def test_fallback_without_realignment_leaves_the_same_pool(N, B, window, k, alpha, n_new, eos, lens):
+    """A fallback round unpadded straight from the extended batch (lengths
+    len + n_emit at the old paddings) leaves the pool byte for byte as
+    realign-then-unpad does, round after round."""
+    pair = ToyPair(V=11, L=2, H=2, D=4, alpha=alpha, seed=N * 7 + B)
+    rng = np.random.default_rng(N + B)
+    prompts = [list(rng.integers(0, 11, size=n)) for n in lens]
+    S = max(lens) + n_new + 2 * (k + 1) + 8
+    a, b = {}, {}
+    r1 = run_exspec(pair, prompts, n_new, k, S, B, window, oracle_ops(), eos_id=eos, result=a)
+    r2 = run_exspec(pair, prompts, n_new, k, S, B, window, oracle_ops(), eos_id=eos, fallback_realign=False, result=b)
+    assert r1 == r2
+    assert np.array_equal(a["pool_len"], b["pool_len"])
+    assert np.array_equal(a["pool"].view(np.uint32), b["pool"].view(np.uint32))
