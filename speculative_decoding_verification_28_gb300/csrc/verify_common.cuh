@@ -112,6 +112,31 @@ __device__ __forceinline__ float vec_max<__half>(const uint4 &u)
     return max_nan(f.x, f.y);
 }
 
+// NaN-propagating element-wise maximum of two 16-byte vectors (32-bit words
+// holding one fp32 or two bf16 / fp16 values)
+template <typename T>
+__device__ __forceinline__ uint32_t max_word(uint32_t a, uint32_t b);
+template <>
+__device__ __forceinline__ uint32_t max_word<float>(uint32_t a, uint32_t b)
+{
+    return __float_as_uint(max_nan(__uint_as_float(a), __uint_as_float(b)));
+}
+template <>
+__device__ __forceinline__ uint32_t max_word<__nv_bfloat16>(uint32_t a, uint32_t b)
+{
+    return max_nan_bf16x2(a, b);
+}
+template <>
+__device__ __forceinline__ uint32_t max_word<__half>(uint32_t a, uint32_t b)
+{
+    return max_nan_f16x2(a, b);
+}
+template <typename T>
+__device__ __forceinline__ uint4 max_vec(const uint4 &a, const uint4 &b)
+{
+    return make_uint4(max_word<T>(a.x, b.x), max_word<T>(a.y, b.y), max_word<T>(a.z, b.z), max_word<T>(a.w, b.w));
+}
+
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e): e^x = 2^(x log2 e)
 
 // Per-warp re-check, between load batches, that the unit's row is still

@@ -27,6 +27,8 @@
 // V * (sizeof(T) + 4) for one row per drawing sequence.
 #include <float.h>
 
+#include <type_traits>
+
 #include "bulk_copy.cuh"
 #include "sample_final.cuh"
 
@@ -64,7 +66,73 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
     if (lo + t < cs.head_end)
         add1(Storage<T>::at(row, lo + t));
     const T *body = row + cs.head_end;
-    for (int base = 0; base < cs.nvec; base += UNROLL * NT) {  // warp-uniform trip count
+    // Full batches (every thread has all its vectors in range): one packed
+    // maximum over the batch, one NaN / +inf test and one rescale test per
+    // batch, and a lazy reference: sums are kept relative to `m`, which is
+    // moved only when the batch maximum exceeds it by more than 8 (terms up
+    // to 2^8 lose nothing in fp32); `mt` tracks the exact maximum and the sum
+    // is brought to it once at the end.  Four partial sums break the add
+    // chain.  What remains after the full batches takes the guarded loop.
+    float mt = m;                              // the head element, if any, is already in (m, s)
+    float sa[4] = {s, 0.0f, 0.0f, 0.0f};
+    int base = 0;
+    bool dropped = false;
+    // one full batch of NB vectors per thread starting at vector `base`
+    auto batch = [&](auto nb) {
+        constexpr int NB = decltype(nb)::value;
+        uint4 r[NB];
+#pragma unroll
+        for (int u = 0; u < NB; ++u)
+            r[u] = ld_stream16(body + (size_t)(base + t + u * NT) * VEC);
+        uint4 mx = r[0];
+#pragma unroll
+        for (int u = 1; u < NB; ++u)
+            mx = max_vec<T>(mx, r[u]);
+        const float vraw = vec_max<T>(mx);
+        if (kRaw)
+            xr = max_nan(xr, vraw);
+        const float vm = vraw * c;  // c > 0: the maximum commutes with the scale
+        bad |= !(vm < INFINITY);    // NaN or +inf in the batch
+        mt = fmaxf(mt, vm);
+        if (vm > m + 8.0f || m == -INFINITY) {
+            const float scale = (m > -INFINITY) ? exp2f(m - vm) : 0.0f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                sa[q] *= scale;
+            m = vm;
+        }
+        if (m > -INFINITY) {
+#pragma unroll
+            for (int u = 0; u < NB; ++u) {
+                float f[VEC];
+                Storage<T>::unpack(r[u], f);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e)
+                    sa[e & 3] += exp2_sfu(fmaf(f[e], c, -m));
+            }
+        }
+    };
+    // batches of 8 vectors (128 bytes in flight per thread), then of 4
+    for (; base + 8 * NT <= cs.nvec; base += 8 * NT) {  // warp-uniform trip count
+        if (base > 0 && probe.dropped()) {
+            dropped = true;
+            break;
+        }
+        batch(std::integral_constant<int, 8>());
+    }
+    for (; !dropped && base + UNROLL * NT <= cs.nvec; base += UNROLL * NT) {
+        if (base > 0 && probe.dropped()) {
+            dropped = true;
+            break;
+        }
+        batch(std::integral_constant<int, UNROLL>());
+    }
+    s = (sa[0] + sa[1]) + (sa[2] + sa[3]);
+    if (m > -INFINITY && mt > m) {  // bring the sum to the exact maximum
+        s *= exp2f(m - mt);
+        m = mt;
+    }
+    for (; !dropped && base < cs.nvec; base += UNROLL * NT) {  // the rest, in guarded batches of UNROLL
         if (base > 0 && probe.dropped())
             break;
         const int i = base + t;
