@@ -135,25 +135,39 @@ def aggregate(units_per_rank, max_time_s, n_ranks):
 # clocks
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle samples every 50 ms into a temporary file.
+    Started before the warm-up so that it is already sampling when the timed
+    region begins; begin() / end() mark that region (wall clock) and the
+    summary keeps the samples stamped inside it (the nearest one if the
+    region was shorter than the sampling period)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index):
+        import tempfile
+
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
         return self
+
+    def begin(self):
+        self.t0 = time.time()
+
+    def end(self):
+        self.t1 = time.time()
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -165,24 +179,32 @@ class ClockSampler:
             self.f.close()
 
     def summary(self):
+        import datetime
+
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in open(self.path):
             p = [x.strip() for x in line.split(",")]
-            if len(p) < 9:
+            if len(p) < 10:
                 continue
             try:
-                sm.append(float(p[1]))
-                smax = float(p[2])
+                ts = datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(p[2]), float(p[3]), p[6:10]))
             except ValueError:
                 continue
-            for n, v in zip(names, p[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        t0 = self.t0 if self.t0 is not None else rows[0][0]
+        t1 = self.t1 if self.t1 is not None else rows[-1][0]
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        if not inside:
+            inside = [min(rows, key=lambda r: abs(r[0] - (t0 + t1) / 2))]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in inside for n, v in zip(names, r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": float(np.median([r[1] for r in inside])), "sm_max_mhz": inside[-1][2], "reasons": reasons,
+                "samples": len(inside), "window_ms": round((t1 - t0) * 1e3, 1)}
 
 
 # ---------------------------------------------------------------------------
@@ -414,22 +436,25 @@ def run_ours(args, c, rank, local_rank, world):
 
     dump = open(args.dump_steps, "w") if args.dump_steps else None
 
-    for _ in range(args.warmup):
-        one_step(False)
-    if pg:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
     per = []
     moved_rows = []
     verify_bytes = []
     emitted = 0
-    with ClockSampler(local_rank) as clk:
+    with ClockSampler(local_rank) as clk:  # sampling already runs when the timed region starts
+        for _ in range(args.warmup):
+            one_step(False)
+        if pg:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        clk.begin()
         for _ in range(args.steps):
             t, m, e, vb = one_step(True)
             per.append(t)
             moved_rows.append(m)
             verify_bytes.append(vb)
             emitted += e
+        torch.cuda.synchronize(dev)
+        clk.end()
     torch.cuda.synchronize(dev)
     if pg:
         dist.barrier()
@@ -798,17 +823,20 @@ def run_exspec_bench(args, c, rank, local_rank, world):
         active[done] = False
         return full, t_parts, moved, int(ne.sum().item())
 
-    for _ in range(args.warmup):
-        one_round()
-    torch.cuda.synchronize(dev)
-    if pg:
-        dist.barrier()
     rounds = []
-    with ClockSampler(local_rank) as clk:
+    with ClockSampler(local_rank) as clk:  # sampling already runs when the timed region starts
+        for _ in range(args.warmup):
+            one_round()
+        torch.cuda.synchronize(dev)
+        if pg:
+            dist.barrier()
+        clk.begin()
         for _ in range(args.steps):
             r = one_round()
             if r is not None:
                 rounds.append(r)
+        torch.cuda.synchronize(dev)
+        clk.end()
     if pg:
         dist.barrier()
     total = sum(sum(r[1]) for r in rounds)

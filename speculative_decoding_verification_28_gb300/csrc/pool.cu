@@ -48,7 +48,7 @@ __device__ __forceinline__ bool mark_index(uint32_t *bits, int n, int N)
 __global__ void __launch_bounds__(kPoolPlanThreads) pool_plan_kernel(PoolArgs a)
 {
     __shared__ uint32_t s_bits[kMaxPool / 32];
-    __shared__ int s_bad, s_W, s_count;
+    __shared__ int s_bad, s_W;
     dep_release();  // the copy kernel may be scheduled; it waits for this grid
     const PoolPlan pp = pool_plan(a.ws, a.B);
     const int t = threadIdx.x, nt = blockDim.x;
@@ -57,7 +57,6 @@ __global__ void __launch_bounds__(kPoolPlanThreads) pool_plan_kernel(PoolArgs a)
     if (t == 0) {
         s_bad = 0;
         s_W = 0;
-        s_count = 0;
     }
     __syncthreads();
     for (int b = t; b < a.B; b += nt) {
