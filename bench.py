@@ -686,7 +686,7 @@ def run_cpu_baseline(c, args, R, budget_s=10.0, max_rounds=400):
         t, kv = oracle_rounds(c, 1, args.seed + 1 + n, kv_host=kv, R=R if kv is None else None)
         spent += t
         n += 1
-    return {"value": round(n / spent, 4), "unit": "rounds/s", "cores": 1, "kind": "oracle",
+    return {"value": round(n / spent, 4), "unit": "rounds/s", "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{n} full rounds of the same workload ({spent:.1f} s of oracle time: verify + realign "
                       f"of a host copy of the cache + pos/mask), single-threaded C, inputs generated outside "
                       f"the timing"}
@@ -708,7 +708,8 @@ def run_reference(args, c):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 oracle",
             "data": "synthetic", "config": {"workload": f"{args.workload}: " + describe(c)},
-            "cpu_baseline": {"value": round(v, 4), "unit": "rounds/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": round(v, 4), "unit": "rounds/s", "cores": 1, "host_cores": os.cpu_count(),
+                             "kind": "oracle",
                              "sample": "each step one full round of the workload on the host"},
             "e2e": {"value": round(v, 4), "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
