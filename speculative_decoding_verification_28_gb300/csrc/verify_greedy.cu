@@ -23,7 +23,7 @@ template <typename T>
 __device__ uint64_t chunk_argmax(const T *row, int lo, int hi, uint64_t *s_red, const StopProbe &probe)
 {
     constexpr int VEC = Storage<T>::kVec;
-    constexpr int UNROLL = 4;
+    constexpr int UNROLL = 8;  // 16-byte loads in flight per thread
     const ChunkSplit<T> cs(row, lo, hi);
     float best = -INFINITY;
     uint32_t bidx = 0xFFFFFFFFu;

@@ -45,7 +45,6 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
                                     bool &bad_out, float *s_f, const StopProbe &probe, float *xmax_out)
 {
     constexpr int VEC = Storage<T>::kVec;
-    constexpr int UNROLL = 4;
     const ChunkSplit<T> cs(row, lo, hi);
     float m = -INFINITY, s = 0.0f, xr = -INFINITY;
     bool bad = false;
@@ -112,7 +111,7 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
             }
         }
     };
-    // batches of 8 vectors (128 bytes in flight per thread), then of 4
+    // full batches of 8 vectors (128 bytes in flight per thread)
     for (; base + 8 * NT <= cs.nvec; base += 8 * NT) {  // warp-uniform trip count
         if (base > 0 && probe.dropped()) {
             dropped = true;
@@ -120,31 +119,27 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
         }
         batch(std::integral_constant<int, 8>());
     }
-    for (; !dropped && base + UNROLL * NT <= cs.nvec; base += UNROLL * NT) {
-        if (base > 0 && probe.dropped()) {
-            dropped = true;
-            break;
-        }
-        batch(std::integral_constant<int, UNROLL>());
-    }
     s = (sa[0] + sa[1]) + (sa[2] + sa[3]);
     if (m > -INFINITY && mt > m) {  // bring the sum to the exact maximum
         s *= exp2f(m - mt);
         m = mt;
     }
-    for (; !dropped && base < cs.nvec; base += UNROLL * NT) {  // the rest, in guarded batches of UNROLL
+    // the rest (fewer than 8 vectors per thread): one guarded round, all of
+    // its loads in flight together
+    constexpr int GU = 8;
+    for (; !dropped && base < cs.nvec; base += GU * NT) {
         if (base > 0 && probe.dropped())
             break;
         const int i = base + t;
-        uint4 r[UNROLL];
+        uint4 r[GU];
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
+        for (int u = 0; u < GU; ++u) {
             const int vi = i + u * NT;
             if (vi < cs.nvec)
                 r[u] = ld_stream16(body + (size_t)vi * VEC);
         }
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
+        for (int u = 0; u < GU; ++u) {
             const int vi = i + u * NT;
             if (vi < cs.nvec) {
                 const float vraw = vec_max<T>(r[u]);
