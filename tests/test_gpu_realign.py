@@ -149,10 +149,11 @@ def _full_size_rounds(name, alpha, rounds, sample_slabs):
     every round the invariant checker scans the whole cache and the oracle
     checks sampled slabs bit for bit."""
     c = CONFIGS[name]
-    L, B, H, S, D, k, V = c["L"], c["B"], c["H"], c["S"], c["D"], c["k"], c["V"]
+    L, B, H, S, D, V = c["L"], c["B"], c["H"], c["S"], c["D"], c["V"]
+    k = c["k"] if "k" in c else max(c["ks"])
     g = torch.Generator(device=dev()).manual_seed(2000 + int(alpha * 10))
     rng = np.random.default_rng(2000)
-    ln = prompt_lengths(B, *c["prompt"], seed=2000 + B)
+    ln = prompt_lengths(B, *(c["prompt"] if "prompt" in c else c["pool_len"]), seed=2000 + B)
     W = int(ln.max())
     pad = (W - ln).astype(np.int32)
     kv = torch.empty((L, 2, B, H, S, D), dtype=torch.bfloat16, device=dev())
@@ -201,6 +202,19 @@ def _full_size_rounds(name, alpha, rounds, sample_slabs):
 @pytest.mark.parametrize("alpha", [0.5, 0.8])
 def test_config2_full_size(alpha):
     _full_size_rounds("c2", alpha, rounds=6, sample_slabs=24)
+
+
+def test_config3_full_size():
+    """8 GiB cache (32 x 2 x 32 x 8 x 2048 x 128 bf16); the commits come from
+    greedy verification at alpha 0.8 (the realignment does not depend on how
+    n_emit was decided)."""
+    _full_size_rounds("c3", 0.8, rounds=5, sample_slabs=24)
+
+
+def test_config4_full_size_batch():
+    """A 64-sequence batch of config 4's cache (28 x 2 x 64 x 4 x 2048 x 128
+    bf16, 7 GiB), k = 8, lengths U[128, 1024]."""
+    _full_size_rounds("c4", 0.7, rounds=5, sample_slabs=24)
 
 
 def test_config5_full_size():
