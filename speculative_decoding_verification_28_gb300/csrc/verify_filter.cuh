@@ -273,6 +273,50 @@ __device__ void hist_select(const FilterHist &h, int nb, unsigned int need, unsi
     }
 }
 
+// Maximum of a whole row (NaN-propagating: a NaN anywhere gives NaN) for
+// every thread of the block; 8 loads in flight per thread.  s_f: NT / 32
+// floats of scratch.
+template <typename T, int NT>
+__device__ float row_max_pass(const T *row, int V, float *s_f)
+{
+    constexpr int VEC = Storage<T>::kVec;
+    constexpr int U = 8;
+    const ChunkSplit<T> cs(row, 0, V);
+    const int t = threadIdx.x;
+    float mx = -INFINITY;
+    for (int v = t; v < cs.head_end; v += NT)
+        mx = max_nan(mx, Storage<T>::at(row, v));
+    const T *body = row + cs.head_end;
+    for (int base = 0; base < cs.nvec; base += U * NT) {
+        uint4 r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int vi = base + t + u * NT;
+            if (vi < cs.nvec)
+                r[u] = ld_stream16(body + (size_t)vi * VEC);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int vi = base + t + u * NT;
+            if (vi < cs.nvec)
+                mx = max_nan(mx, vec_max<T>(r[u]));
+        }
+    }
+    for (int v = cs.tail_beg + t; v < V; v += NT)
+        mx = max_nan(mx, Storage<T>::at(row, v));
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1)
+        mx = max_nan(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, k));
+    if ((t & 31) == 0)
+        s_f[t >> 5] = mx;
+    __syncthreads();
+    float r = -INFINITY;
+    for (int i = 0; i < NT / 32; ++i)
+        r = max_nan(r, s_f[i]);
+    __syncthreads();
+    return r;
+}
+
 template <typename T, int NT>
 __global__ void __launch_bounds__(NT) verify_filter_kernel(VerifyArgs a)
 {
@@ -293,19 +337,34 @@ __global__ void __launch_bounds__(NT) verify_filter_kernel(VerifyArgs a)
     __syncthreads();
     float cut = -INFINITY, s_kept = 0.0f;
     if (!s_skip) {
-        float m, s;
-        bool bad;
-        chunk_softmax_stats<T, true, NT>(row, 0, a.V, c, m, s, bad, s_f, StopProbe{a.stop_enc, u.b, u.j}, &s_xmax);
-        if (t == 0) {
-            s_m = m;
-            s_s = s;
-            s_bad = (bad || !(s > 0.0f) || !(s <= FLT_MAX)) ? 1 : 0;
-            s_skip = stopped_before(a.stop_enc, u.b, u.j) ? 1 : 0;
-        }
-        __syncthreads();
         const int tk = a.top_k ? a.top_k[u.b] : 0;
         const float tp = a.top_p ? a.top_p[u.b] : 1.0f;
         const bool use_k = tk > 0 && tk < a.V, use_p = tp < 1.0f;
+        if (use_k || use_p) {
+            // the kept sum comes from the fixed-point masses: pass 1 needs only
+            // the maximum (a NaN or +inf gives a non-finite maximum; so does a
+            // row of -inf only)
+            const float xm = row_max_pass<T, NT>(row, a.V, s_f);
+            if (t == 0) {
+                s_xmax = xm;
+                s_m = xm * c;
+                s_s = 0.0f;
+                s_bad = (xm > -INFINITY && xm < INFINITY) ? 0 : 1;
+                s_skip = stopped_before(a.stop_enc, u.b, u.j) ? 1 : 0;
+            }
+        } else {
+            float m, s;
+            bool bad;
+            chunk_softmax_stats<T, true, NT>(row, 0, a.V, c, m, s, bad, s_f, StopProbe{a.stop_enc, u.b, u.j},
+                                             &s_xmax);
+            if (t == 0) {
+                s_m = m;
+                s_s = s;
+                s_bad = (bad || !(s > 0.0f) || !(s <= FLT_MAX)) ? 1 : 0;
+                s_skip = stopped_before(a.stop_enc, u.b, u.j) ? 1 : 0;
+            }
+        }
+        __syncthreads();
         s_kept = s_s;
         if (!s_skip && !s_bad && (use_k || use_p)) {
             const float xmax = s_xmax, cdec = a.dec_scale;
