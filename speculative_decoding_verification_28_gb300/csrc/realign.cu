@@ -10,7 +10,8 @@
 //       sequences that move, longest run first (so the long slabs start early
 //       and the tail of the shift is short).
 // shift (persistent, one thread per CTA drives the bulk-copy engine): each
-//       (layer, K/V, sequence, head) slab of a moving sequence is an in-place
+//       (layer, K/V, sequence, head) slab of a moving sequence, in every cache
+//       the call realigns (e.g. target and draft, by the one plan), is an in-place
 //       memmove of run * D * elt contiguous bytes by delta rows.  Tiles are
 //       staged global -> shared -> global with cp.async.bulk; they are taken
 //       from the end the run moves towards (descending for delta > 0), so a

@@ -21,15 +21,19 @@
 // as the unfiltered path.
 //
 // One CTA per target row (rows j-major, skipped once an earlier stop of the
-// sequence is known, as in the statistics kernel).  Pass 1 reads the row
-// from HBM: maximum, softmax sum, flags.  The cuts are radix selections on an
-// order-preserving 32-bit key of the logit, 11-bit digits (two levels for
+// sequence is known, as in the statistics kernel); 1024 threads when the
+// batch has at most two rows per SM, else 256.  Pass 1 reads the row from
+// HBM: its maximum when the row is filtered (the kept sum then comes from the
+// Q masses), else the softmax statistics.  The cuts are radix selections on
+// an order-preserving 32-bit key of the logit, 11-bit digits (two levels for
 // 16-bit logits, whose keys carry at most 22 significant bits; three for
 // fp32): each level is one more pass over the row (now in L2) building
 // per-digit counts and Q masses in shared memory (32-bit atomics on three
 // parts of each mass), then a block scan from the top digit finds the digit
-// holding the k-th largest key (counts) or the top-p boundary (masses).  Roofline: HBM reads V * sizeof(T) per needed row;
-// the later passes are L2 reads plus shared-memory atomics.
+// holding the k-th largest key (counts) or the top-p boundary (masses).
+// Roofline: HBM reads V * sizeof(T) per needed row; the later passes are L2
+// reads, a fixed-point weight per logit and shared-memory atomics, which
+// make the kernel instruction-bound.
 #pragma once
 
 #include "sample_final.cuh"

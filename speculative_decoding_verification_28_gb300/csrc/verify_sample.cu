@@ -14,14 +14,20 @@
 // the row as undefined.
 //
 // Three kernels, stream-ordered:
-//   stats  : per (b, j, chunk) online max / sum of 2^(x c - m) (lazy rows, as
-//            in the greedy kernel); the row's last CTA gathers x[y] and q[y]
-//            and runs the ratio test; the sequence's last row runs the
-//            first-stop ballot and decides which row (if any) is drawn from;
+//   stats  : per (b, j, chunk) max / sum of 2^(x c - m) (lazy rows, as in the
+//            greedy kernel; 8 loads in flight per thread, one packed maximum
+//            and one rescale test per batch of vectors); the row's last CTA
+//            gathers x[y] and q[y] and runs the ratio test; the sequence's
+//            last row runs the first-stop ballot and decides which row (if
+//            any) is drawn from.  With top-k / top-p the filter kernel of
+//            verify_filter.cuh takes this place (one CTA per row, and the
+//            row's cut goes to the draw kernel);
 //   draw   : per (b, chunk) of the drawn row, one vectorised pass summing the
 //            residual and p; the row's last CTA picks the mode, finds the chunk
 //            holding u * total from the chunk sums, stages that chunk's weights
-//            in shared memory and scans them for the inverse-CDF index;
+//            in shared memory and scans them for the inverse-CDF index; it is
+//            launched programmatically and waits for the first kernel on the
+//            device;
 //   resid  : optional, writes the normalised distribution of the draw.
 // Roofline: HBM-bound; stats reads V * sizeof(T) per needed row; draw reads
 // V * (sizeof(T) + 4) for one row per drawing sequence.
