@@ -1,5 +1,6 @@
 // bulk_copy.cuh -- inline PTX for mbarriers and 1-D bulk copies
-// (cp.async.bulk, the non-tensor TMA path) on sm_103a, used by the KV shift.
+// (cp.async.bulk, the non-tensor TMA path) on sm_103a, used by the KV shift
+// and the pool copies.
 #pragma once
 
 #include <stdint.h>

@@ -22,28 +22,52 @@ struct RowStats {
 
 __device__ __forceinline__ float scale_of(const VerifyArgs &a) { return a.unit_temp ? kLog2e : a.inv_temp * kLog2e; }
 
-// Lane 0 only: ratio test of row u.row and its results.  m, s: the row's
-// base-2 maximum and kept sum; cut: the smallest kept logit (-inf: all kept);
-// bad: the row's softmax is undefined.
+// The loaded inputs of one row's ratio test.
+struct RowInputs {
+    int y;        // the proposal (-1: none, the bonus row or a stopped budget)
+    float xy;     // its target logit
+    float qy;     // its draft probability
+    float u;      // the row's uniform
+};
+
+// One lane: the draft token of row u.row (first load round).
+__device__ __forceinline__ int row_proposal(const VerifyArgs &a, const Unit &u)
+{
+    return (u.j < u.kb) ? a.draft[(size_t)u.b * a.k + u.j] : -1;
+}
+
+// One lane: the rest of the row's inputs, given its proposal y (second round).
 template <typename T>
-__device__ void sample_row_decide(const VerifyArgs &a, const Unit &u, const T *row, float m, float s, float cut,
-                                  bool bad)
+__device__ __forceinline__ RowInputs row_inputs(const VerifyArgs &a, const Unit &u, const T *row, int y)
+{
+    RowInputs in{y, 0.0f, 1.0f, 0.0f};
+    if (u.j < u.kb && y >= 0 && y < a.V) {
+        in.xy = Storage<T>::at(row, y);
+        in.qy = a.q[((size_t)u.b * a.k + u.j) * a.V + y];
+        in.u = a.u[(size_t)u.b * (a.k + 1) + u.j];
+    }
+    return in;
+}
+
+// One lane: ratio test of row u.row from its loaded inputs, and its results.
+// m, s: the row's base-2 maximum and kept sum; cut: the smallest kept logit
+// (-inf: all kept); bad: the row's softmax is undefined.
+__device__ __forceinline__ void row_decide(const VerifyArgs &a, const Unit &u, const RowInputs &in, float m, float s,
+                                           float cut, bool bad)
 {
     const float c = scale_of(a);
     uint32_t fl = (bad || !(s <= FLT_MAX) || !(s > 0.0f)) ? SPEC_FLAG_NONFINITE : 0u;
     int acc = 0;
     bool stop;
     if (u.j < u.kb) {
-        const int y = a.draft[(size_t)u.b * a.k + u.j];
+        const int y = in.y;
         if (y < 0 || y >= a.V) {
             fl |= SPEC_FLAG_BAD_TOKEN;
         } else {
-            const float xy = Storage<T>::at(row, y);
-            const float py = (xy >= cut) ? exp2f(fmaf(xy, c, -m)) / s : 0.0f;
-            const float qy = a.q[((size_t)u.b * a.k + u.j) * a.V + y];
-            if (qy == 0.0f)
+            const float py = (in.xy >= cut) ? exp2f(fmaf(in.xy, c, -m)) / s : 0.0f;
+            if (in.qy == 0.0f)
                 fl |= SPEC_FLAG_Q_ZERO;
-            acc = (a.u[(size_t)u.b * (a.k + 1) + u.j] < py / qy) ? 1 : 0;
+            acc = (in.u < py / in.qy) ? 1 : 0;
         }
         stop = !acc || (a.eos >= 0 && y == a.eos) || (u.j + 1 == u.rem);
     } else {
@@ -58,28 +82,38 @@ __device__ void sample_row_decide(const VerifyArgs &a, const Unit &u, const T *r
         atomicMax(a.stop_enc + u.b, kStopBase - u.j);
 }
 
-// Warp 0 (all 32 lanes) after a row of sequence u.b is done: counts the row;
-// the sequence's last row runs the first-stop scan and writes the outputs.
-__device__ __forceinline__ void sample_seq_finish(const VerifyArgs &a, const Unit &u)
+// One lane: loads the row's inputs and runs the ratio test.
+template <typename T>
+__device__ void sample_row_decide(const VerifyArgs &a, const Unit &u, const T *row, float m, float s, float cut,
+                                  bool bad)
 {
-    const int lane = threadIdx.x & 31;
-    int last_row = 0;
-    if (lane == 0) {
-        __threadfence();
-        last_row = (atomicAdd(a.seq_cnt + u.b, 1) == a.k) ? 1 : 0;
-    }
-    last_row = __shfl_sync(0xFFFFFFFFu, last_row, 0);
-    if (!last_row)
-        return;
-    __threadfence();
+    row_decide(a, u, row_inputs<T>(a, u, row, row_proposal(a, u)), m, s, cut, bad);
+}
 
-    const int b = u.b, kb = u.kb, rem = u.rem, j = lane;
+// One lane, after row u.row's results are stored: counts the row for its
+// sequence; true for the sequence's last row (whose warp then writes the
+// outputs with sample_seq_outputs).
+__device__ __forceinline__ bool sample_seq_count(const VerifyArgs &a, int b)
+{
+    __threadfence();
+    return atomicAdd(a.seq_cnt + b, 1) == a.k;
+}
+
+// One warp (all 32 lanes), after every row of sequence b was counted: the
+// first stop by one ballot (lane j = row j), the accepted prefix committed,
+// the draw (correction or bonus) handed to the draw kernel, the sequence's
+// counters reset.  Row results written by other CTAs are read through L2.
+__device__ __forceinline__ void sample_seq_outputs(const VerifyArgs &a, int b, int kb, int rem)
+{
+    __threadfence();
+    const int lane = threadIdx.x & 31;
+    const int j = lane;
     int acc = 0, d = -1;
     uint32_t fl = 0;
     bool stop = false;
     if (j <= a.k && rem > 0) {
-        acc = a.row_tok[b * (a.k + 1) + j];
-        fl = a.row_flag[b * (a.k + 1) + j];
+        acc = __ldcg(a.row_tok + b * (a.k + 1) + j);
+        fl = __ldcg(a.row_flag + b * (a.k + 1) + j);
         if (j < kb) {
             d = a.draft[(size_t)b * a.k + j];
             stop = !acc || (a.eos >= 0 && d == a.eos) || (j + 1 == rem);
@@ -110,6 +144,17 @@ __device__ __forceinline__ void sample_seq_finish(const VerifyArgs &a, const Uni
         a.seq_cnt[b] = 0;
         a.stop_enc[b] = 0;
     }
+}
+
+// Warp 0 (all 32 lanes) after a row of sequence u.b is done: counts the row;
+// the sequence's last row writes the outputs.
+__device__ __forceinline__ void sample_seq_finish(const VerifyArgs &a, const Unit &u)
+{
+    int last_row = 0;
+    if ((threadIdx.x & 31) == 0)
+        last_row = sample_seq_count(a, u.b) ? 1 : 0;
+    if (__shfl_sync(0xFFFFFFFFu, last_row, 0))
+        sample_seq_outputs(a, u.b, u.kb, u.rem);
 }
 
 }  // namespace spec

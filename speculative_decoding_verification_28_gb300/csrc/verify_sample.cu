@@ -216,72 +216,89 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
     }
 }
 
+// (max, sum) of two base-2 softmax partials
+__device__ __forceinline__ void merge_ms(float &ma, float &sa, float mb, float sb)
+{
+    const float mx = fmaxf(ma, mb);
+    const float x = (ma > -INFINITY) ? sa * exp2f(ma - mx) : 0.0f;
+    const float y = (mb > -INFINITY) ? sb * exp2f(mb - mx) : 0.0f;
+    ma = mx;
+    sa = x + y;
+}
+
+// One lane, after the last unit of row u.row was counted: unless an earlier
+// stop is known, merges the row's chunk partials (read through L2: other
+// CTAs wrote them) and runs the ratio test; resets the row's counter.  y is
+// the row's proposal (row_proposal), loaded by the caller ahead of time.
+// The stop word, the partials and the test's inputs are loaded together.
+template <typename T>
+__device__ void stats_row_finish(const VerifyArgs &a, const Unit &u, int y)
+{
+    if (u.needed) {
+        const bool stopped = stopped_before(a.stop_enc, u.b, u.j);
+        const T *row = reinterpret_cast<const T *>(a.logits) + (size_t)u.row * a.V;
+        const RowInputs in = row_inputs<T>(a, u, row, y);
+        const float4 *part = static_cast<const float4 *>(a.part) + (size_t)u.row * a.C;
+        float m = -INFINITY, s = 0.0f;
+        bool bad = false;
+#pragma unroll 8
+        for (int cc = 0; cc < a.C; ++cc) {
+            const float4 p = __ldcg(part + cc);
+            merge_ms(m, s, p.x, p.y);
+            bad |= p.z > 0.0f;
+        }
+        if (!stopped)
+            row_decide(a, u, in, m, s, -INFINITY, bad);
+    }
+    a.row_cnt[u.row] = 0;
+}
+
+// One lane, after unit u's chunk statistics (m, s, bad: the base-2 maximum,
+// the sum relative to it and the non-finite flag; m = -inf and s = 0 for a
+// chunk that was not read): stores the partial and counts it; the row's last
+// unit finishes the row and counts it for the sequence.  True when that was
+// the sequence's last row.  The row's proposal is loaded before the counter
+// round trip, in case this unit is the last.
+template <typename T>
+__device__ bool stats_unit_count(const VerifyArgs &a, const Unit &u, float m_c, float s_c, bool bad_c)
+{
+    const int y = u.needed ? row_proposal(a, u) : -1;
+    static_cast<float4 *>(a.part)[(size_t)u.row * a.C + u.c] = make_float4(m_c, s_c, bad_c ? 1.0f : 0.0f, 0.0f);
+    if (a.C > 1) {
+        __threadfence();
+        if (atomicAdd(a.row_cnt + u.row, 1) != a.C - 1)
+            return false;
+        __threadfence();
+    }
+    stats_row_finish<T>(a, u, y);
+    return sample_seq_count(a, u.b);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) verify_stats_kernel(VerifyArgs a)
 {
     __shared__ float s_f[3 * kThreads / 32];
-    __shared__ int s_skip, s_last;  // written once each: no read/write race between them
-    int *stop_enc = a.stop_enc, *row_cnt = a.row_cnt;
-    float4 *part = static_cast<float4 *>(a.part);
+    __shared__ int s_skip;
     const float c = scale_of(a);
-
     const Unit u = decode_unit(a);
     const T *row = reinterpret_cast<const T *>(a.logits) + (size_t)u.row * a.V;
     if (threadIdx.x == 0)
-        s_skip = (!u.needed || stopped_before(stop_enc, u.b, u.j)) ? 1 : 0;
+        s_skip = (!u.needed || stopped_before(a.stop_enc, u.b, u.j)) ? 1 : 0;
     __syncthreads();
+    float m = -INFINITY, s = 0.0f;
+    bool bad = false;
     if (!s_skip) {
         const int lo = u.c * a.chunk;
         const int hi = min(a.V, lo + a.chunk);
-        float m, s;
-        bool bad;
-        chunk_softmax_stats<T, false>(row, lo, hi, c, m, s, bad, s_f, StopProbe{stop_enc, u.b, u.j}, nullptr);
+        chunk_softmax_stats<T, false>(row, lo, hi, c, m, s, bad, s_f, StopProbe{a.stop_enc, u.b, u.j}, nullptr);
+    }
+    if (threadIdx.x < 32) {
+        int seq_last = 0;
         if (threadIdx.x == 0)
-            part[(size_t)u.row * a.C + u.c] = make_float4(m, s, bad ? 1.0f : 0.0f, 0.0f);
+            seq_last = stats_unit_count<T>(a, u, m, s, bad) ? 1 : 0;
+        if (__shfl_sync(0xFFFFFFFFu, seq_last, 0))
+            sample_seq_outputs(a, u.b, u.kb, u.rem);
     }
-    if (threadIdx.x == 0) {
-        if (a.C > 1) {
-            __threadfence();
-            s_last = (atomicAdd(row_cnt + u.row, 1) == a.C - 1) ? 1 : 0;
-        } else {
-            s_last = 1;  // a single-chunk row is finalised by its only CTA
-        }
-    }
-    __syncthreads();
-    if (!s_last || threadIdx.x >= 32)
-        return;
-    __threadfence();
-    const int lane = threadIdx.x;
-    int eval = 0;
-    if (lane == 0)
-        eval = (u.needed && !stopped_before(stop_enc, u.b, u.j)) ? 1 : 0;
-    eval = __shfl_sync(0xFFFFFFFFu, eval, 0);
-    if (eval) {
-        // merge the chunk statistics of the row
-        float m = -INFINITY;
-        for (int cc = lane; cc < a.C; cc += 32)
-            m = fmaxf(m, part[(size_t)u.row * a.C + cc].x);
-#pragma unroll
-        for (int k = 16; k > 0; k >>= 1)
-            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, k));
-        float s = 0.0f, bad = 0.0f;
-        for (int cc = lane; cc < a.C; cc += 32) {
-            const float4 p = part[(size_t)u.row * a.C + cc];
-            if (p.x > -INFINITY)
-                s += p.y * exp2f(p.x - m);
-            bad = fmaxf(bad, p.z);
-        }
-#pragma unroll
-        for (int k = 16; k > 0; k >>= 1) {
-            s += __shfl_xor_sync(0xFFFFFFFFu, s, k);
-            bad = fmaxf(bad, __shfl_xor_sync(0xFFFFFFFFu, bad, k));
-        }
-        if (lane == 0)
-            sample_row_decide<T>(a, u, row, m, s, -INFINITY, bad > 0.0f);
-    }
-    if (lane == 0)
-        row_cnt[u.row] = 0;
-    sample_seq_finish(a, u);
 }
 
 }  // namespace spec
@@ -649,14 +666,13 @@ static cudaError_t launch_sample_t(const VerifyArgs &args, cudaStream_t st)
 {
     VerifyArgs a = args;
     resolve_verify_args(a);
-    const unsigned g1 = (unsigned)(a.B * (a.k + 1) * a.C);
     const unsigned g2 = (unsigned)(a.B * draw_chunks(a.V));
     if (a.filtered) {
         const cudaError_t ef = launch_filter_rows<T>(a, st);
         if (ef != cudaSuccess)
             return ef;
     } else {
-        verify_stats_kernel<T><<<g1, kThreads, 0, st>>>(a);
+        verify_stats_kernel<T><<<a.B * (a.k + 1) * a.C, kThreads, 0, st>>>(a);
     }
     // the draw kernel becomes resident while the stats kernel drains and
     // waits for it on the device (griddepcontrol.wait)
