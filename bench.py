@@ -506,7 +506,7 @@ def run_ours(args, c, rank, local_rank, world):
         "roofline": roofline,
         "verify_roofline": {"bound": "hbm", "kernels": ("verify_greedy_kernel" if c["mode"] == "greedy" else
                                                         ("verify_filter_kernel" if R.filtered() else
-                                                         "verify_stats_kernel") + " + verify_draw_kernel"),
+                                                         "verify_stats_kernel") + " + verify_draw_sums_kernel + verify_draw_pick_kernel"),
                             "achieved": round(float(np.sum(verify_bytes) / (per[:, 1].sum() / 1e3) / 1e9), 1),
                             "peak": peak, "unit": "GB/s",
                             "frac": round(float(np.sum(verify_bytes) / (per[:, 1].sum() / 1e3) / 1e9) / peak, 4),
@@ -518,7 +518,7 @@ def run_ours(args, c, rank, local_rank, world):
                                                                              / 1e9), 1),
                                             "pos_mask": round(float(brk[:, 2].mean()) * 1e3, 2)}},
         "tokens_per_round": round(emitted / args.steps / c["B"], 4),
-        "gpu_launches": args.steps * (4 if c["mode"] == "greedy" else 5),
+        "gpu_launches": args.steps * (4 if c["mode"] == "greedy" else 6),
         "clocks": clk.summary(),
     }
     if not args.no_e2e:

@@ -21,7 +21,7 @@ constexpr int kMinChunk = 4096;        // smallest vocabulary chunk of a verify 
 #define SPEC_TARGET_UNITS 2432
 #endif
 constexpr int kTargetUnits = SPEC_TARGET_UNITS;  // ~two waves of 8 CTAs on 152 SMs
-constexpr int kDrawChunk = 8192;       // elements per CTA in the draw kernel (its scan stages one in smem)
+constexpr int kDrawChunk = 8192;       // elements per CTA of the draw sums kernel (one 1024-element segment per warp)
 constexpr int kMaxRows = SPEC_MAX_K + 1;
 constexpr int kStopBase = 1024;        // stop row j is stored as kStopBase - j
 
@@ -52,6 +52,8 @@ __host__ __device__ inline Split verify_split(int B, int k, int V)
 }
 __host__ __device__ inline int verify_chunks(int B, int k, int V) { return verify_split(B, k, V).C; }
 __host__ __device__ inline int draw_chunks(int V) { return (V + kDrawChunk - 1) / kDrawChunk; }
+constexpr int kDrawSeg = 1024;  // elements per draw segment: one warp's sums, the pick's final scan
+__host__ __device__ inline int draw_segs(int V) { return (V + kDrawSeg - 1) / kDrawSeg; }
 
 // ---------------------------------------------------------------------------
 // workspace layout (byte offsets; every array 256-byte aligned)
@@ -63,7 +65,7 @@ struct Layout {
     // realignment plan
     size_t order, delta, src_pad, run, seq_src, seq_dst, misc;
     // counters that every verify call leaves at zero
-    size_t zero_begin, seq_cnt, stop_enc, res_cnt, row_cnt, zero_end;
+    size_t zero_begin, seq_cnt, stop_enc, row_cnt, zero_end;
     // verify scratch
     size_t row_tok, row_ms, row_flag, row_cut, part, draw_row, rpart, rtot;
     size_t total;
@@ -93,7 +95,6 @@ __host__ __device__ inline Layout make_layout(int B, int k, int V)
     L.zero_begin = o;
     L.seq_cnt = take(b * 4);
     L.stop_enc = take(b * 4);
-    L.res_cnt = take(b * 4);
     L.row_cnt = take(b * kMaxRows * 4);  // sized for the largest k
     L.zero_end = o;
     L.row_tok = take(rows * 4);
@@ -102,7 +103,7 @@ __host__ __device__ inline Layout make_layout(int B, int k, int V)
     L.row_cut = take(rows * 4);
     L.part = take(rows * C * 16);
     L.draw_row = take(b * 4);
-    L.rpart = take(b * (size_t)draw_chunks(V > 0 ? V : 1) * 8);
+    L.rpart = take(b * (size_t)draw_segs(V > 0 ? V : 1) * 8);  // two floats per draw segment
     L.rtot = take(b * 8);
     L.total = o;
     return L;

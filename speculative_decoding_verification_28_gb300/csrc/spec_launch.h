@@ -22,7 +22,7 @@ struct VerifyArgs {
     int32_t *n_emit;
     void *ws;
     // workspace arrays, resolved on the host by the launcher from ws
-    int *stop_enc, *row_cnt, *seq_cnt, *res_cnt, *row_tok, *draw_row;
+    int *stop_enc, *row_cnt, *seq_cnt, *row_tok, *draw_row;
     float2 *row_ms;
     uint32_t *row_flag;
     void *part;

@@ -202,7 +202,6 @@ void resolve_verify_args(VerifyArgs &a)
     a.stop_enc = ws_at<int>(a.ws, lay.stop_enc);
     a.row_cnt = ws_at<int>(a.ws, lay.row_cnt);
     a.seq_cnt = ws_at<int>(a.ws, lay.seq_cnt);
-    a.res_cnt = ws_at<int>(a.ws, lay.res_cnt);
     a.row_tok = ws_at<int>(a.ws, lay.row_tok);
     a.draw_row = ws_at<int>(a.ws, lay.draw_row);
     a.row_ms = ws_at<float2>(a.ws, lay.row_ms);

@@ -13,7 +13,7 @@
 // token (probability 0); NaN / +inf, or a row without a finite logit, flags
 // the row as undefined.
 //
-// Three kernels, stream-ordered:
+// Four kernels, stream-ordered:
 //   stats  : per (b, j, chunk) max / sum of 2^(x c - m) (lazy rows, as in the
 //            greedy kernel; 8 loads in flight per thread, one packed maximum
 //            and one rescale test per batch of vectors); the row's last CTA
@@ -22,12 +22,14 @@
 //            any) is drawn from.  With top-k / top-p the filter kernel of
 //            verify_filter.cuh takes this place (one CTA per row, and the
 //            row's cut goes to the draw kernel);
-//   draw   : per (b, chunk) of the drawn row, one vectorised pass summing the
-//            residual and p; the row's last CTA picks the mode, finds the chunk
-//            holding u * total from the chunk sums, stages that chunk's weights
-//            in shared memory and scans them for the inverse-CDF index; it is
-//            launched programmatically and waits for the first kernel on the
-//            device;
+//   sums   : per (b, 1024-element segment) of the drawn row, one warp sums
+//            the residual and p in a vectorised pass;
+//   pick   : one warp per drawing sequence picks the mode, finds the segment
+//            holding u * total from the segment sums, loads that segment
+//            into registers and scans it for the inverse-CDF index, all
+//            prefix sums in exact 64-bit fixed point.  Sums and
+//            pick are launched programmatically and wait for the kernel
+//            before them on the device;
 //   resid  : optional, writes the normalised distribution of the draw.
 // Roofline: HBM-bound; stats reads V * sizeof(T) per needed row; draw reads
 // V * (sizeof(T) + 4) for one row per drawing sequence.
@@ -340,302 +342,316 @@ __device__ DrawRow<T> draw_row_of(const VerifyArgs &a, int b, int r, int kb)
     return d;
 }
 
-// two block sums for thread 0: warp shuffles, one barrier, warp 0 finishes
-__device__ __forceinline__ void block_sum2_to0(float &a, float &b, float *s_f)
+// Segments: the drawn row is cut into segments of kDrawSeg elements; a warp
+// of the sums kernel sums one segment, and the pick scans one segment.
+constexpr int kSegPerLane = kDrawSeg / 32;  // contiguous elements per lane in the pick
+static_assert(kDrawChunk == kDrawSeg * (kThreads / 32), "a sums CTA covers one segment per warp");
+
+__device__ __forceinline__ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// q bits of element e (0 .. VEC-1) of a 16-byte logits vector, from its VEC/4 q vectors
+__device__ __forceinline__ float q_elem(const uint4 *qq, int e)
 {
-#pragma unroll
-    for (int k = 16; k > 0; k >>= 1) {
-        a += __shfl_xor_sync(0xFFFFFFFFu, a, k);
-        b += __shfl_xor_sync(0xFFFFFFFFu, b, k);
-    }
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    if (l == 0) {
-        s_f[w] = a;
-        s_f[kThreads / 32 + w] = b;
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        a = (l < kThreads / 32) ? s_f[l] : 0.0f;
-        b = (l < kThreads / 32) ? s_f[kThreads / 32 + l] : 0.0f;
-#pragma unroll
-        for (int k = 16; k > 0; k >>= 1) {
-            a += __shfl_xor_sync(0xFFFFFFFFu, a, k);
-            b += __shfl_xor_sync(0xFFFFFFFFu, b, k);
-        }
-    }
+    const uint4 &w4 = qq[e / 4];
+    const uint32_t qb = (e & 3) == 0 ? w4.x : (e & 3) == 1 ? w4.y : (e & 3) == 2 ? w4.z : w4.w;
+    return __uint_as_float(qb);
 }
 
-__device__ __forceinline__ float block_sum(float v, float *s_f)
-{
-#pragma unroll
-    for (int k = 16; k > 0; k >>= 1)
-        v += __shfl_xor_sync(0xFFFFFFFFu, v, k);
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
-    if (l == 0)
-        s_f[w] = v;
-    __syncthreads();
-    float t = 0.0f;
-    for (int i = 0; i < kThreads / 32; ++i)
-        t += s_f[i];
-    return t;
-}
-
-// sums of max(0, p - q) and of p over elements [lo, hi) of the drawn row:
-// 16-byte loads of the logits and of q where both rows allow it
+// One warp: sums of max(0, p - q) and of p over elements [lo, hi) of the
+// drawn row, for every lane.  A full aligned segment is read with 16-byte
+// loads, lane l taking vectors l, l + 32, ... (all of a batch in flight).
 template <typename T>
-__device__ void draw_chunk_sums(const DrawRow<T> &dr, bool residual, int lo, int hi, float &sr, float &sp)
+__device__ void draw_segment_sums(const DrawRow<T> &dr, bool residual, int lo, int hi, float &sr, float &sp)
 {
     constexpr int VEC = Storage<T>::kVec;
-    const bool vec_ok = ((reinterpret_cast<uintptr_t>(dr.x + lo) & 15) == 0) &&
-                        (!residual || (reinterpret_cast<uintptr_t>(dr.q + lo) & 15) == 0);
-    int v0 = lo;
-    if (vec_ok) {
-        constexpr int UNROLL = 4;
-        constexpr int QV = VEC / 4;  // 16-byte q vectors per logits vector
-        const int nvec = (hi - lo) / VEC;
-        for (int i = threadIdx.x; i < nvec; i += UNROLL * kThreads) {
-            uint4 r[UNROLL], qq[UNROLL][QV];
+    constexpr int QV = VEC / 4;                 // 16-byte q vectors per logits vector
+    constexpr int NV = kDrawSeg / VEC / 32;     // logits vectors per lane: 4 (16-bit types) or 8 (fp32)
+    constexpr int NB = NV > 4 ? 4 : NV;         // vectors per batch
+    const int l = threadIdx.x & 31;
+    sr = 0.0f;
+    sp = 0.0f;
+    if (hi - lo == kDrawSeg && aligned16(dr.x + lo) && (!residual || aligned16(dr.q + lo))) {
 #pragma unroll
-            for (int u = 0; u < UNROLL; ++u) {
-                const int vi = i + u * kThreads;
-                if (vi < nvec) {
-                    r[u] = ld_stream16(dr.x + lo + (size_t)vi * VEC);
-                    if (residual) {
+        for (int b0 = 0; b0 < NV; b0 += NB) {
+            uint4 r[NB], qq[NB][QV];
 #pragma unroll
-                        for (int h = 0; h < QV; ++h)
-                            qq[u][h] = ld_stream16(dr.q + lo + (size_t)vi * VEC + 4 * h);
-                    }
+            for (int u = 0; u < NB; ++u) {
+                const int vi = (b0 + u) * 32 + l;
+                r[u] = ld_stream16(dr.x + lo + (size_t)vi * VEC);
+                if (residual) {
+#pragma unroll
+                    for (int h = 0; h < QV; ++h)
+                        qq[u][h] = ld_stream16(dr.q + lo + (size_t)vi * VEC + 4 * h);
                 }
             }
 #pragma unroll
-            for (int u = 0; u < UNROLL; ++u) {
-                const int vi = i + u * kThreads;
-                if (vi < nvec) {
-                    float f[VEC];
-                    Storage<T>::unpack(r[u], f);
+            for (int u = 0; u < NB; ++u) {
+                float f[VEC];
+                Storage<T>::unpack(r[u], f);
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) {
-                        const float p = dr.p(f[e]);
-                        sp += p;
-                        if (residual) {
-                            const uint4 &w4 = qq[u][e / 4];
-                            const uint32_t qb = (e & 3) == 0 ? w4.x : (e & 3) == 1 ? w4.y : (e & 3) == 2 ? w4.z : w4.w;
-                            sr += fmaxf(p - __uint_as_float(qb), 0.0f);
-                        }
-                    }
+                for (int e = 0; e < VEC; ++e) {
+                    const float p = dr.p(f[e]);
+                    sp += p;
+                    if (residual)
+                        sr += fmaxf(p - q_elem(qq[u], e), 0.0f);
                 }
             }
         }
-        v0 = lo + nvec * VEC;
+    } else {
+        for (int v = lo + l; v < hi; v += 32) {
+            const float p = dr.pv(v);
+            sp += p;
+            if (residual)
+                sr += fmaxf(p - __ldg(dr.q + v), 0.0f);
+        }
     }
-    for (int v = v0 + threadIdx.x; v < hi; v += kThreads) {
-        const float p = dr.pv(v);
-        sp += p;
-        if (residual)
-            sr += fmaxf(p - __ldg(dr.q + v), 0.0f);
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1) {
+        sr += __shfl_xor_sync(0xFFFFFFFFu, sr, k);
+        sp += __shfl_xor_sync(0xFFFFFFFFu, sp, k);
     }
 }
 
-constexpr int kSeg = kDrawChunk / kThreads;  // contiguous elements per thread in the final scan
-constexpr int kPadded = kDrawChunk + kDrawChunk / 32;
-
+// draw, pass 1: per (b, segment) of the drawn row, the sums of the residual
+// and of p, one warp per segment.  Launched programmatically behind the
+// statistics kernel; no barrier, no counter: a warp retires once its sums
+// are out.
 template <typename T>
-__global__ void __launch_bounds__(kThreads) verify_draw_kernel(VerifyArgs a)
+__global__ void __launch_bounds__(kThreads) verify_draw_sums_kernel(VerifyArgs a)
 {
-    __shared__ float s_w[kPadded];  // weights of the chosen chunk, one pad word per 32
-    __shared__ float s_f[2 * kThreads / 32];
-    __shared__ double s_d[kThreads / 32];
-    __shared__ int s_flag, s_pick, s_lastpos, s_chunk, s_use_res;
-    __shared__ double s_base, s_target;
-    dep_wait();  // launched programmatically: the stats grid's results are complete
-    const int Cd = draw_chunks(a.V);
+    dep_wait();  // the statistics grid's results are complete
+    const int Cd = draw_chunks(a.V), Ns = draw_segs(a.V);
     const int b = blockIdx.x / Cd, c = blockIdx.x % Cd;
     const int r = a.draw_row[b];
     if (r < 0)
         return;
+    const int sg = c * (kThreads / 32) + (threadIdx.x >> 5);
+    if (sg >= Ns)
+        return;  // warps past the end of the row
     int kb = a.draft_len ? a.draft_len[b] : a.k;
     kb = kb < 0 ? 0 : (kb > a.k ? a.k : kb);
     const bool residual = r < kb;
     const DrawRow<T> dr = draw_row_of<T>(a, b, r, kb);
-    float *rpart = a.rpart;
-    int *res_cnt = a.res_cnt;
-    double *rtot = a.rtot;
-
-    // one pass over this chunk: sum of the residual and sum of p
-    const int lo = c * kDrawChunk, hi = min(a.V, lo + kDrawChunk);
-    float sr = 0.0f, sp = 0.0f;
-    draw_chunk_sums<T>(dr, residual, lo, hi, sr, sp);
-    block_sum2_to0(sr, sp, s_f);
-    if (threadIdx.x == 0) {
-        rpart[((size_t)b * Cd + c) * 2 + 0] = sr;
-        rpart[((size_t)b * Cd + c) * 2 + 1] = sp;
-        __threadfence();
-        s_flag = (atomicAdd(res_cnt + b, 1) == Cd - 1) ? 1 : 0;
+    const int lo = sg * kDrawSeg, hi = min(a.V, lo + kDrawSeg);
+    float sr, sp;
+    draw_segment_sums<T>(dr, residual, lo, hi, sr, sp);
+    if ((threadIdx.x & 31) == 0) {
+        a.rpart[((size_t)b * Ns + sg) * 2 + 0] = sr;
+        a.rpart[((size_t)b * Ns + sg) * 2 + 1] = sp;
     }
-    __syncthreads();
-    if (!s_flag)
+}
+
+// x * 2^60 as an unsigned integer, truncated (the fixed point of the pick:
+// weights are probabilities, below 2).  0 for x <= 0 and for x below 2^-60;
+// x >= 2, inf and NaN (rows already flagged non-finite) saturate at 2^62.
+// Integer operations only: FP64 is slow on this part.
+__device__ __forceinline__ unsigned long long fixed60(float x)
+{
+    const uint32_t bits = __float_as_uint(x);
+    if ((int32_t)bits <= 0)
+        return 0ull;                               // +-0, negatives, negative NaN
+    const int sh = (int)(bits >> 23) - 127 + 37;  // x = mant * 2^(e - 23), x * 2^60 = mant * 2^(e + 37)
+    const unsigned long long mant = (bits & 0x7FFFFFu) | 0x800000u;
+    if (sh >= 38)
+        return 1ull << 62;
+    if (sh >= 0)
+        return mant << sh;
+    return sh <= -24 ? 0ull : (mant >> -sh);
+}
+
+constexpr int kPickSegs = 8;   // segment sums per lane and block: a block covers 256 segments (V <= 262144)
+constexpr int kPickWarps = 2;  // sequences per CTA of the pick kernel
+
+// draw, pass 2: one warp per drawing sequence (kPickWarps per CTA), launched
+// programmatically behind the sums.  The weights are the residual when it has
+// positive mass, else p (the bonus row always draws from p).  Prefix sums
+// over segments and lanes are exact unsigned 64-bit fixed point (fixed60), so
+// the target u * total (u * 2^64 times the total, high half) lies in exactly
+// one segment.
+// Segment sums are read a block of 256 at a time, lane l holding segments
+// 8 l .. 8 l + 7 of the block, in the same round as the sequence's draw row,
+// budget and uniform; a prefix over the lanes finds the lane, the lane finds
+// the segment.  That segment is loaded with lane l holding its elements
+// 32 l .. 32 l + 31 in registers; the lanes' fp32 sums, in fixed point, give
+// an exact prefix that finds the lane, and the lane walks its 32 weights in
+// fp32 against the remaining distance.  The pick is the first index whose
+// cumulative weight exceeds the target.  The segment sums come from the sums
+// kernel's fp32 arithmetic and the lane weights are re-summed here, so at
+// the last few ulps the two can disagree: if the lane's walk ends short of
+// the target, the lane's last index of positive weight is taken, and if no
+// lane of the segment holds the target, the segment's.
+template <typename T>
+__global__ void __launch_bounds__(kPickWarps * 32) verify_draw_pick_kernel(VerifyArgs a)
+{
+    typedef unsigned long long u64;
+    dep_wait();  // the sums grid's results are complete
+    const int l = threadIdx.x & 31;
+    const int b = blockIdx.x * kPickWarps + (threadIdx.x >> 5);
+    if (b >= a.B)
         return;
-    __threadfence();
+    const int Ns = draw_segs(a.V);
+    const float *rs = a.rpart + (size_t)b * Ns * 2;
+    // one round: the draw row, the budget, the uniform, the first block of segment sums
+    const int r = a.draw_row[b];
+    int kb = a.draft_len ? a.draft_len[b] : a.k;
+    const float uu = a.u[(size_t)b * (a.k + 1) + a.k];
+    float bR[kPickSegs], bP[kPickSegs];
+    auto load_block = [&](int s0) {
+#pragma unroll
+        for (int j = 0; j < kPickSegs; ++j) {
+            const int i = s0 + l * kPickSegs + j;
+            bR[j] = i < Ns ? __ldcg(rs + 2 * i) : 0.0f;
+            bP[j] = i < Ns ? __ldcg(rs + 2 * i + 1) : 0.0f;
+        }
+    };
+    load_block(0);
+    if (r < 0)
+        return;
+    kb = kb < 0 ? 0 : (kb > a.k ? a.k : kb);
+    const bool residual = r < kb;
+    const DrawRow<T> dr = draw_row_of<T>(a, b, r, kb);
+    constexpr int kBlock = 32 * kPickSegs;
 
-    // last CTA of the row: choose the weights, find the chunk, scan it.
-    // Warp 0 loads the chunk sums in parallel (32 chunks per pass) and scans
-    // them in fp64 with shuffles; a ballot finds the chunk holding u * total.
-    if (threadIdx.x < 32) {
-        const int l = threadIdx.x;
-        double R = 0.0, P = 0.0;
-        for (int i0 = 0; i0 < Cd; i0 += 32) {
-            const int i = i0 + l;
-            if (i < Cd) {
-                R += (double)rpart[((size_t)b * Cd + i) * 2 + 0];
-                P += (double)rpart[((size_t)b * Cd + i) * 2 + 1];
-            }
-        }
+    // totals
+    u64 R = 0, P = 0;
+    for (int s0 = 0; s0 < Ns; s0 += kBlock) {
+        if (s0 > 0)
+            load_block(s0);
 #pragma unroll
-        for (int k = 16; k > 0; k >>= 1) {
-            R += __shfl_xor_sync(0xFFFFFFFFu, R, k);
-            P += __shfl_xor_sync(0xFFFFFFFFu, P, k);
-        }
-        const bool use_res = residual && R > 0.0;
-        const int sel = use_res ? 0 : 1;
-        const double W = use_res ? R : P;
-        const double target = (double)a.u[(size_t)b * (a.k + 1) + a.k] * W;
-        double before = 0.0;  // sum of the chunks of earlier passes
-        int cs = -1, lastpos = -1;
-        double cs_base = 0.0;
-        for (int i0 = 0; i0 < Cd && cs < 0; i0 += 32) {
-            const int i = i0 + l;
-            const double pc = (i < Cd) ? (double)rpart[((size_t)b * Cd + i) * 2 + sel] : 0.0;
-            double incl = pc;
-#pragma unroll
-            for (int k = 1; k < 32; k <<= 1) {
-                const double o = __shfl_up_sync(0xFFFFFFFFu, incl, k);
-                if (l >= k)
-                    incl += o;
-            }
-            const unsigned pos = __ballot_sync(0xFFFFFFFFu, pc > 0.0);
-            if (pos)
-                lastpos = i0 + 31 - __clz((int)pos);
-            const unsigned hit = __ballot_sync(0xFFFFFFFFu, i < Cd && before + incl > target);
-            if (hit) {
-                const int f = __ffs(hit) - 1;
-                cs = i0 + f;
-                cs_base = before + __shfl_sync(0xFFFFFFFFu, incl - pc, f);
-            }
-            before += __shfl_sync(0xFFFFFFFFu, incl, 31);
-        }
-        if (l == 0) {
-            if (cs < 0) {  // rounding left u * W at or past the total: last positive chunk
-                cs = lastpos >= 0 ? lastpos : Cd - 1;
-                cs_base = -1.0;  // take the last positive index of that chunk
-            }
-            s_base = cs_base;
-            s_chunk = cs;
-            s_use_res = use_res ? 1 : 0;
-            s_target = target;
-            s_pick = 0x7FFFFFFF;
-            s_lastpos = -1;
-            rtot[b] = use_res ? W : -W;  // sign records the mode for the residual writer
-            if (residual && !use_res && a.flags)
-                a.flags[b] |= SPEC_FLAG_ZERO_RESIDUAL;
-            res_cnt[b] = 0;
+        for (int j = 0; j < kPickSegs; ++j) {
+            R += fixed60(bR[j]);
+            P += fixed60(bP[j]);
         }
     }
-    __syncthreads();
-    const bool use_res = s_use_res != 0;
-    const double target = s_target, base = s_base;
-    const int clo = s_chunk * kDrawChunk, n = min(a.V, clo + kDrawChunk) - clo;
-    // stage the chunk's weights: every thread issues all of its 16-byte loads
-    // (logits and q) before using any, then writes weights to shared memory
-    {
-        constexpr int VEC = Storage<T>::kVec;
-        constexpr int NV = kDrawChunk / VEC / kThreads;  // vectors per thread
-        const bool vec_ok = (n == kDrawChunk) && ((reinterpret_cast<uintptr_t>(dr.x + clo) & 15) == 0) &&
-                            (!use_res || (reinterpret_cast<uintptr_t>(dr.q + clo) & 15) == 0);
-        if (vec_ok) {
-            constexpr int NH = NV / 2;  // two halves keep the register count down
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-            uint4 xr[NH], qr[NH][VEC / 4];
 #pragma unroll
-            for (int v = 0; v < NH; ++v) {
-                const int i = (threadIdx.x + (half * NH + v) * kThreads) * VEC;
-                xr[v] = ld_stream16(dr.x + clo + i);
-                if (use_res) {
+    for (int k = 16; k > 0; k >>= 1) {
+        R += __shfl_xor_sync(0xFFFFFFFFu, R, k);
+        P += __shfl_xor_sync(0xFFFFFFFFu, P, k);
+    }
+    const bool use_res = residual && R > 0;
+    const u64 W = use_res ? R : P;
+    const u64 target = __umul64hi(fixed60(uu) << 4, W);  // u in [0, 1): u * 2^64 fits; target < W when W > 0
+    if (l == 0) {
+        const double Wd = (double)W * 0x1p-60;
+        a.rtot[b] = use_res ? Wd : -Wd;  // sign records the mode for the residual writer
+        if (residual && !use_res && a.flags)
+            a.flags[b] |= SPEC_FLAG_ZERO_RESIDUAL;
+    }
+
+    // the segment holding the target
+    u64 before = 0, cs_base = 0;
+    int cs = -1;
+    for (int s0 = 0; s0 < Ns && cs < 0 && W > 0; s0 += kBlock) {
+        if (s0 > 0 || Ns > kBlock)
+            load_block(s0);  // block 0 is still in registers when it is the only one
+        u64 f[kPickSegs], tot = 0;
 #pragma unroll
-                    for (int h = 0; h < VEC / 4; ++h)
-                        qr[v][h] = ld_stream16(dr.q + clo + i + 4 * h);
+        for (int j = 0; j < kPickSegs; ++j) {
+            f[j] = fixed60(use_res ? bR[j] : bP[j]);
+            tot += f[j];
+        }
+        u64 incl = tot;
+#pragma unroll
+        for (int k = 1; k < 32; k <<= 1) {
+            const u64 o = __shfl_up_sync(0xFFFFFFFFu, incl, k);
+            if (l >= k)
+                incl += o;
+        }
+        const u64 lo_l = before + incl - tot;
+        int my = -1;
+        u64 my_base = 0;
+        if (lo_l <= target && target - lo_l < tot) {
+            u64 run = lo_l;
+#pragma unroll
+            for (int j = 0; j < kPickSegs; ++j) {
+                if (my < 0 && target - run < f[j]) {
+                    my = s0 + l * kPickSegs + j;
+                    my_base = run;
                 }
+                run += f[j];
             }
-#pragma unroll
-            for (int v = 0; v < NH; ++v) {
-                const int i = (threadIdx.x + (half * NH + v) * kThreads) * VEC;
-                float f[VEC];
-                Storage<T>::unpack(xr[v], f);
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float p = dr.p(f[e]);
-                    float wv = p;
-                    if (use_res) {
-                        const uint4 &w4 = qr[v][e / 4];
-                        const uint32_t qb = (e & 3) == 0 ? w4.x : (e & 3) == 1 ? w4.y : (e & 3) == 2 ? w4.z : w4.w;
-                        wv = fmaxf(p - __uint_as_float(qb), 0.0f);
-                    }
-                    s_w[(i + e) + ((i + e) >> 5)] = wv;
-                }
-            }
-            }
-        } else {
-            for (int i = threadIdx.x; i < n; i += kThreads)
-                s_w[i + (i >> 5)] = dr.w(clo + i, use_res);
         }
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, my >= 0);
+        if (hit) {
+            const int h = __ffs(hit) - 1;
+            cs = __shfl_sync(0xFFFFFFFFu, my, h);
+            cs_base = __shfl_sync(0xFFFFFFFFu, my_base, h);
+        }
+        before += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
-    __syncthreads();
-    const int slo = threadIdx.x * kSeg, shi = min(n, slo + kSeg);
-    float seg = 0.0f;
-    int seg_last = -1;
-    for (int i = slo; i < shi; ++i) {
-        const float wv = s_w[i + (i >> 5)];
-        seg += wv;
-        if (wv > 0.0f)
-            seg_last = clo + i;
+    const bool take_last = cs < 0;  // no positive weight at all (W = 0)
+    if (take_last)
+        cs = Ns - 1;
+
+    // the segment's weights, 32 contiguous ones per lane
+    const int slo = cs * kDrawSeg, shi = min(a.V, slo + kDrawSeg);
+    const int e0 = slo + l * kSegPerLane;
+    float w[kSegPerLane];
+    constexpr int VEC = Storage<T>::kVec;
+    if (shi - slo == kDrawSeg && aligned16(dr.x + slo) && (!use_res || aligned16(dr.q + slo))) {
+        uint4 xr[kSegPerLane / VEC], qr[kSegPerLane / 4];
+#pragma unroll
+        for (int v = 0; v < kSegPerLane / VEC; ++v)
+            xr[v] = ld_stream16(dr.x + e0 + v * VEC);
+        if (use_res) {
+#pragma unroll
+            for (int v = 0; v < kSegPerLane / 4; ++v)
+                qr[v] = ld_stream16(dr.q + e0 + v * 4);
+        }
+#pragma unroll
+        for (int v = 0; v < kSegPerLane / VEC; ++v) {
+            float f[VEC];
+            Storage<T>::unpack(xr[v], f);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const float p = dr.p(f[e]);
+                w[v * VEC + e] = use_res ? fmaxf(p - q_elem(qr + (v * VEC) / 4, e), 0.0f) : p;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < kSegPerLane; ++i)
+            w[i] = (e0 + i < shi) ? dr.w(e0 + i, use_res) : 0.0f;
     }
-    // exclusive scan of the segment sums (fp64)
-    double incl = (double)seg;
-    const int l = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    // lane sums in fp32 (four partial sums), their prefix exact in fixed point
+    float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    int lane_last = -1;
+#pragma unroll
+    for (int i = 0; i < kSegPerLane; ++i) {
+        ls[i & 3] += w[i];
+        if (w[i] > 0.0f)
+            lane_last = e0 + i;
+    }
+    const u64 lane_sum = fixed60((ls[0] + ls[1]) + (ls[2] + ls[3]));
+    u64 incl = lane_sum;
 #pragma unroll
     for (int k = 1; k < 32; k <<= 1) {
-        const double o = __shfl_up_sync(0xFFFFFFFFu, incl, k);
+        const u64 o = __shfl_up_sync(0xFFFFFFFFu, incl, k);
         if (l >= k)
             incl += o;
     }
-    if (l == 31)
-        s_d[wid] = incl;
-    __syncthreads();
-    double warp_off = 0.0;
-    for (int i = 0; i < wid; ++i)
-        warp_off += s_d[i];
-    // the segment holding the target: its start offset in fp64, the walk
-    // within it in fp32 against the remaining distance
-    const double seg_start = base + warp_off + incl - (double)seg;
-    if (base >= 0.0 && seg_start + (double)seg > target) {
-        const float rem = (float)(target - seg_start);
+    const u64 start = cs_base + incl - lane_sum;
+    int cand = 0x7FFFFFFF;
+    if (!take_last && start <= target && target - start < lane_sum) {
+        // the lane's walk in fp32 against the remaining distance
+        const float rem = (float)(target - start) * 0x1p-60f;
         float run = 0.0f;
-        for (int i = slo; i < shi; ++i) {
-            run += s_w[i + (i >> 5)];
-            if (run > rem) {
-                atomicMin(&s_pick, clo + i);
-                break;
-            }
+#pragma unroll
+        for (int i = 0; i < kSegPerLane; ++i) {
+            run += w[i];
+            if (cand == 0x7FFFFFFF && run > rem && w[i] > 0.0f)
+                cand = e0 + i;
         }
+        if (cand == 0x7FFFFFFF)
+            cand = lane_last;  // rounding: the lane's own last positive weight
     }
-    if (seg_last >= 0)
-        atomicMax(&s_lastpos, seg_last);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int tok = s_pick;
-        if (tok == 0x7FFFFFFF)
-            tok = s_lastpos >= 0 ? s_lastpos : clo + n - 1;
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1) {
+        cand = min(cand, __shfl_xor_sync(0xFFFFFFFFu, cand, k));
+        lane_last = max(lane_last, __shfl_xor_sync(0xFFFFFFFFu, lane_last, k));
+    }
+    if (l == 0) {
+        const int tok = cand != 0x7FFFFFFF ? cand : (lane_last >= 0 ? lane_last : shi - 1);
         a.out_tokens[(size_t)b * (a.k + 1) + r] = tok;
     }
 }
@@ -674,8 +690,8 @@ static cudaError_t launch_sample_t(const VerifyArgs &args, cudaStream_t st)
     } else {
         verify_stats_kernel<T><<<a.B * (a.k + 1) * a.C, kThreads, 0, st>>>(a);
     }
-    // the draw kernel becomes resident while the stats kernel drains and
-    // waits for it on the device (griddepcontrol.wait)
+    // the two draw kernels become resident while the kernel before each
+    // drains, and wait for it on the device (griddepcontrol.wait)
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr.val.programmaticStreamSerializationAllowed = 1;
@@ -685,7 +701,12 @@ static cudaError_t launch_sample_t(const VerifyArgs &args, cudaStream_t st)
     cfg.stream = st;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, verify_draw_kernel<T>, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, verify_draw_sums_kernel<T>, a);
+    if (e != cudaSuccess)
+        return e;
+    cfg.gridDim = dim3((unsigned)((a.B + kPickWarps - 1) / kPickWarps));
+    cfg.blockDim = dim3(kPickWarps * 32);
+    e = cudaLaunchKernelEx(&cfg, verify_draw_pick_kernel<T>, a);
     if (e != cudaSuccess)
         return e;
     if (a.out_residual)
