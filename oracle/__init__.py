@@ -22,6 +22,9 @@ from .core import (  # noqa: F401
     unpad_scatter,
     group_by_length,
     mutant,
+    set_threads,
+    threads,
+    threads_available,
     realign_kv,
     realign_plan,
     rebuild_pos_mask,

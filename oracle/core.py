@@ -42,13 +42,15 @@ _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile oracle.c into liboracle.so with gcc (IEEE arithmetic, no fast-math)."""
+    """Compile oracle.c into liboracle.so with gcc (IEEE arithmetic, no fast-math),
+    with OpenMP for the loops over sequences and slabs when the compiler has it."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(
-            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math", "-ffp-contract=off", "-o", tmp, _SRC,
-             "-lm"]
-        )
+        base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math", "-ffp-contract=off", "-o", tmp, _SRC]
+        try:
+            subprocess.check_call(base + ["-fopenmp", "-lm"], stderr=subprocess.DEVNULL)
+        except subprocess.CalledProcessError:
+            subprocess.check_call(base + ["-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -61,6 +63,8 @@ def _load():
             lib = ctypes.CDLL(_LIB)
             vp, i32, i64, f64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
             lib.oracle_set_mutant.argtypes = [i32]
+            lib.oracle_set_threads.argtypes = [i32]
+            lib.oracle_threads_available.restype = i32
             lib.oracle_verify_greedy.argtypes = [vp, i32, i32, i32, i32, vp, vp, ctypes.c_int32, vp, vp, vp, vp]
             f32 = ctypes.c_float
             lib.oracle_verify_sample.argtypes = [
@@ -117,6 +121,27 @@ def mutant(name: str):
         yield
     finally:
         lib.oracle_set_mutant(0)
+
+
+def set_threads(n: int) -> None:
+    """Threads for the oracle's loops over sequences and cache slabs (1 by
+    default); results do not depend on it."""
+    _load().oracle_set_threads(int(n))
+
+
+def threads_available() -> int:
+    """Processors OpenMP sees (1 when the oracle was built without it)."""
+    return int(_load().oracle_threads_available())
+
+
+@contextlib.contextmanager
+def threads(n: int):
+    """set_threads(n) for the duration of a block."""
+    set_threads(n)
+    try:
+        yield
+    finally:
+        set_threads(1)
 
 
 def verify_greedy(logits, dt, draft_tokens, draft_len=None, eos_id=-1, remaining=None):

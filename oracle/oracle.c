@@ -15,7 +15,9 @@
  *   [AL]  "Speculative decoding: proposals and verified output" (Atlas lesson)
  *
  * Arithmetic: probabilities in fp64 (double); logits are read exactly from
- * their storage type (fp32, bf16 or fp16 bit patterns) into double.
+ * their storage type (fp32, bf16 or fp16 bit patterns) into double.  The
+ * loops over sequences and cache slabs may run on several threads
+ * (oracle_set_threads), with results identical to one thread.
  *
  * Pins: every function here is checked in tests/test_oracle_*.py against
  * values the pages print, closed forms, brute force on tiny inputs and planted
@@ -29,6 +31,24 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Threads for the loops over sequences and cache slabs (OpenMP when built
+   with it; 1 by default).  Every sequence and every slab is computed exactly
+   as on one thread -- nothing is reduced across them -- so the results do
+   not depend on the thread count. */
+static int g_threads = 1;
+void oracle_set_threads(int n) { g_threads = n > 0 ? n : 1; }
+int oracle_threads_available(void)
+{
+#ifdef _OPENMP
+    return omp_get_num_procs();
+#else
+    return 1;
+#endif
+}
 
 /* ------------------------------------------------------------------ */
 /* storage types of the logits                                         */
@@ -150,6 +170,7 @@ void oracle_verify_greedy(const void *logits, int dtype, int B, int k, int V,
                           int32_t eos_id, const int32_t *remaining,
                           int32_t *out_tokens, int32_t *n_accept, int32_t *n_emit)
 {
+#pragma omp parallel for num_threads(g_threads) schedule(dynamic, 1)
     for (int b = 0; b < B; ++b) {
         int kb = draft_len ? draft_len[b] : k;
         int64_t rem = remaining ? remaining[b] : INT64_MAX;
@@ -421,20 +442,17 @@ static int inverse_cdf(const double *w, int V, double u)
  * came from (residual, or p on zero residual, or the bonus row's p); rows of
  * sequences that drew nothing are left untouched.
  */
-void oracle_verify_sample(const void *logits, int dtype, double temperature,
-                          const float *draft_probs, const int32_t *draft_tokens,
-                          const float *uniforms, int B, int k, int V,
-                          const int32_t *draft_len, int32_t eos_id,
-                          const int32_t *remaining, int32_t *out_tokens,
-                          int32_t *n_accept, int32_t *n_emit, double *out_residual,
-                          uint32_t *flags, const int32_t *top_k, const float *top_p)
+/* sequence b of oracle_verify_sample; p, w, praw, vals: V-sized scratch */
+static void sample_sequence(int b, const void *logits, int dtype, double temperature,
+                            const float *draft_probs, const int32_t *draft_tokens,
+                            const float *uniforms, int k, int V,
+                            const int32_t *draft_len, int32_t eos_id,
+                            const int32_t *remaining, int32_t *out_tokens,
+                            int32_t *n_accept, int32_t *n_emit, double *out_residual,
+                            uint32_t *flags, const int32_t *top_k, const float *top_p,
+                            double *p, double *w, double *praw, ValIdx *vals)
 {
-    size_t nv = (size_t)(V > 0 ? V : 1);
-    double *p = (double *)malloc(sizeof(double) * nv);
-    double *w = (double *)malloc(sizeof(double) * nv);
-    double *praw = (double *)malloc(sizeof(double) * nv);
-    ValIdx *vals = (ValIdx *)malloc(sizeof(ValIdx) * nv);
-    for (int b = 0; b < B; ++b) {
+    {
         int tk = top_k ? top_k[b] : 0;
         float tp = top_p ? top_p[b] : 1.0f;
         int kb = draft_len ? draft_len[b] : k;
@@ -521,10 +539,33 @@ void oracle_verify_sample(const void *logits, int dtype, double temperature,
         if (flags)
             flags[b] = fl;
     }
-    free(p);
-    free(w);
-    free(praw);
-    free(vals);
+}
+
+void oracle_verify_sample(const void *logits, int dtype, double temperature,
+                          const float *draft_probs, const int32_t *draft_tokens,
+                          const float *uniforms, int B, int k, int V,
+                          const int32_t *draft_len, int32_t eos_id,
+                          const int32_t *remaining, int32_t *out_tokens,
+                          int32_t *n_accept, int32_t *n_emit, double *out_residual,
+                          uint32_t *flags, const int32_t *top_k, const float *top_p)
+{
+    size_t nv = (size_t)(V > 0 ? V : 1);
+#pragma omp parallel num_threads(g_threads)
+    {
+        double *p = (double *)malloc(sizeof(double) * nv);
+        double *w = (double *)malloc(sizeof(double) * nv);
+        double *praw = (double *)malloc(sizeof(double) * nv);
+        ValIdx *vals = (ValIdx *)malloc(sizeof(ValIdx) * nv);
+#pragma omp for schedule(dynamic, 1)
+        for (int b = 0; b < B; ++b)
+            sample_sequence(b, logits, dtype, temperature, draft_probs, draft_tokens, uniforms, k, V, draft_len,
+                            eos_id, remaining, out_tokens, n_accept, n_emit, out_residual, flags, top_k, top_p, p, w,
+                            praw, vals);
+        free(p);
+        free(w);
+        free(praw);
+        free(vals);
+    }
 }
 
 /* fp64 processed distribution of one logits row (top_k <= 0 and top_p >= 1:
@@ -640,14 +681,13 @@ int oracle_realign_kv(void *kv, int elt_bytes, int L, int B, int H, int S, int D
     if (st == 0) {
         int64_t row_bytes = (int64_t)D * elt_bytes;
         int64_t slab_bytes = row_bytes * S;
-        for (int l = 0; l < L; ++l)
-            for (int c = 0; c < 2; ++c)
-                for (int b = 0; b < B; ++b)
-                    for (int h = 0; h < H; ++h) {
-                        int64_t slab = (((int64_t)l * 2 + c) * B + b) * H + h;
-                        oracle_shift_slab((uint8_t *)kv + slab * slab_bytes, row_bytes, po[b],
-                                          pn[b], ln[b] - 1);
-                    }
+        int64_t n_slabs = (int64_t)L * 2 * B * H;
+        /* slabs are disjoint: each is moved exactly as on one thread */
+#pragma omp parallel for num_threads(g_threads) schedule(dynamic, 16)
+        for (int64_t slab = 0; slab < n_slabs; ++slab) {
+            int b = (int)((slab / H) % B);
+            oracle_shift_slab((uint8_t *)kv + slab * slab_bytes, row_bytes, po[b], pn[b], ln[b] - 1);
+        }
         memcpy(len_new, ln, sizeof(int32_t) * (size_t)B);
         memcpy(pad_new, pn, sizeof(int32_t) * (size_t)B);
         *width_new = wn;
