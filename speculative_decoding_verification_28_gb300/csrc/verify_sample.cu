@@ -16,7 +16,8 @@
 // Four kernels, stream-ordered:
 //   stats  : per (b, j, chunk) max / sum of 2^(x c - m) (lazy rows, as in the
 //            greedy kernel; 8 loads in flight per thread, one packed maximum
-//            and one rescale test per batch of vectors); the row's last CTA
+//            and one rescale test per batch of vectors, the last batch padded
+//            with -inf); the row's last CTA
 //            gathers x[y] and q[y] and runs the ratio test; the sequence's
 //            last row runs the first-stop ballot and decides which row (if
 //            any) is drawn from.  With top-k / top-p the filter kernel of
@@ -48,6 +49,25 @@ namespace spec {
 // ---------------------------------------------------------------------------
 // kRaw: also the unscaled maximum of the logits (to xmax_out of warp 0;
 // s_f then needs 4 * NT / 32 floats); NT = threads of the block
+// -inf in every element of a 16-byte vector (padding past a chunk's end)
+template <typename T>
+__device__ __forceinline__ uint4 neg_inf_vec();
+template <>
+__device__ __forceinline__ uint4 neg_inf_vec<float>()
+{
+    return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+}
+template <>
+__device__ __forceinline__ uint4 neg_inf_vec<__nv_bfloat16>()
+{
+    return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+}
+template <>
+__device__ __forceinline__ uint4 neg_inf_vec<__half>()
+{
+    return make_uint4(0xFC00FC00u, 0xFC00FC00u, 0xFC00FC00u, 0xFC00FC00u);
+}
+
 template <typename T, bool kRaw, int NT = kThreads>
 __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float &m_out, float &s_out,
                                     bool &bad_out, float *s_f, const StopProbe &probe, float *xmax_out)
@@ -79,18 +99,22 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
     // moved only when the batch maximum exceeds it by more than 8 (terms up
     // to 2^8 lose nothing in fp32); `mt` tracks the exact maximum and the sum
     // is brought to it once at the end.  Four partial sums break the add
-    // chain.  What remains after the full batches takes the guarded loop.
+    // chain.  What remains after the full batches is one guarded batch.
     float mt = m;                              // the head element, if any, is already in (m, s)
     float sa[4] = {s, 0.0f, 0.0f, 0.0f};
     int base = 0;
     bool dropped = false;
-    // one full batch of NB vectors per thread starting at vector `base`
-    auto batch = [&](auto nb) {
+    // one batch of NB vectors per thread starting at vector `base`; guarded
+    // (the last, partial batch): vectors past the chunk's end read as -inf
+    auto batch = [&](auto nb, auto guard) {
         constexpr int NB = decltype(nb)::value;
+        constexpr bool kGuard = decltype(guard)::value;
         uint4 r[NB];
 #pragma unroll
-        for (int u = 0; u < NB; ++u)
-            r[u] = ld_stream16(body + (size_t)(base + t + u * NT) * VEC);
+        for (int u = 0; u < NB; ++u) {
+            const int vi = base + t + u * NT;
+            r[u] = (!kGuard || vi < cs.nvec) ? ld_stream16(body + (size_t)vi * VEC) : neg_inf_vec<T>();
+        }
         uint4 mx = r[0];
 #pragma unroll
         for (int u = 1; u < NB; ++u)
@@ -125,49 +149,16 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
             dropped = true;
             break;
         }
-        batch(std::integral_constant<int, 8>());
+        batch(std::integral_constant<int, 8>(), std::false_type());
     }
+    // the rest (fewer than 8 vectors per thread): one guarded batch, with the
+    // same single packed maximum and lazy rescale test
+    if (!dropped && base < cs.nvec && (base == 0 || !probe.dropped()))
+        batch(std::integral_constant<int, 8>(), std::true_type());
     s = (sa[0] + sa[1]) + (sa[2] + sa[3]);
     if (m > -INFINITY && mt > m) {  // bring the sum to the exact maximum
         s *= exp2f(m - mt);
         m = mt;
-    }
-    // the rest (fewer than 8 vectors per thread): one guarded round, all of
-    // its loads in flight together
-    constexpr int GU = 8;
-    for (; !dropped && base < cs.nvec; base += GU * NT) {
-        if (base > 0 && probe.dropped())
-            break;
-        const int i = base + t;
-        uint4 r[GU];
-#pragma unroll
-        for (int u = 0; u < GU; ++u) {
-            const int vi = i + u * NT;
-            if (vi < cs.nvec)
-                r[u] = ld_stream16(body + (size_t)vi * VEC);
-        }
-#pragma unroll
-        for (int u = 0; u < GU; ++u) {
-            const int vi = i + u * NT;
-            if (vi < cs.nvec) {
-                const float vraw = vec_max<T>(r[u]);
-                if (kRaw)
-                    xr = max_nan(xr, vraw);
-                const float vm = vraw * c;  // c > 0: the maximum commutes with the scale
-                bad |= !(vm < INFINITY);                // NaN or +inf in the vector
-                if (vm > m) {
-                    s = (m > -INFINITY) ? s * exp2f(m - vm) : 0.0f;
-                    m = vm;
-                }
-                if (m > -INFINITY) {
-                    float f[VEC];
-                    Storage<T>::unpack(r[u], f);
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e)
-                        s += exp2_sfu(fmaf(f[e], c, -m));
-                }
-            }
-        }
     }
     if (cs.tail_beg + t < hi)
         add1(Storage<T>::at(row, cs.tail_beg + t));
