@@ -100,8 +100,11 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
     // to 2^8 lose nothing in fp32); `mt` tracks the exact maximum and the sum
     // is brought to it once at the end.  Four partial sums break the add
     // chain.  What remains after the full batches is one guarded batch.
-    float mt = m;                              // the head element, if any, is already in (m, s)
-    float sa[4] = {s, 0.0f, 0.0f, 0.0f};
+    float mt = m;  // the head element, if any, is already in (m, s)
+    // partial sums (0, 1) and (2, 3) as pairs: element e of a vector goes to
+    // partial sum e mod 4; paired fp32 instructions (FFMA2 / FADD2 / FMUL2,
+    // each lane rounded to nearest) do two elements at a time
+    float2 sa[2] = {make_float2(s, 0.0f), make_float2(0.0f, 0.0f)};
     int base = 0;
     bool dropped = false;
     // one batch of NB vectors per thread starting at vector `base`; guarded
@@ -127,19 +130,21 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
         mt = fmaxf(mt, vm);
         if (vm > m + 8.0f || m == -INFINITY) {
             const float scale = (m > -INFINITY) ? exp2f(m - vm) : 0.0f;
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                sa[q] *= scale;
+            sa[0] = __fmul2_rn(sa[0], make_float2(scale, scale));
+            sa[1] = __fmul2_rn(sa[1], make_float2(scale, scale));
             m = vm;
         }
         if (m > -INFINITY) {
+            const float2 c2 = make_float2(c, c), nm2 = make_float2(-m, -m);
 #pragma unroll
             for (int u = 0; u < NB; ++u) {
                 float f[VEC];
                 Storage<T>::unpack(r[u], f);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e)
-                    sa[e & 3] += exp2_sfu(fmaf(f[e], c, -m));
+                for (int e = 0; e < VEC; e += 2) {
+                    const float2 z = __ffma2_rn(make_float2(f[e], f[e + 1]), c2, nm2);
+                    sa[(e >> 1) & 1] = __fadd2_rn(sa[(e >> 1) & 1], make_float2(exp2_sfu(z.x), exp2_sfu(z.y)));
+                }
             }
         }
     };
@@ -155,7 +160,7 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
     // same single packed maximum and lazy rescale test
     if (!dropped && base < cs.nvec && (base == 0 || !probe.dropped()))
         batch(std::integral_constant<int, 8>(), std::true_type());
-    s = (sa[0] + sa[1]) + (sa[2] + sa[3]);
+    s = (sa[0].x + sa[0].y) + (sa[1].x + sa[1].y);
     if (m > -INFINITY && mt > m) {  // bring the sum to the exact maximum
         s *= exp2f(m - mt);
         m = mt;
