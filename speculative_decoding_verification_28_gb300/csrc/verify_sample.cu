@@ -367,6 +367,11 @@ __device__ void draw_segment_sums(const DrawRow<T> &dr, bool residual, int lo, i
     sr = 0.0f;
     sp = 0.0f;
     if (hi - lo == kDrawSeg && aligned16(dr.x + lo) && (!residual || aligned16(dr.q + lo))) {
+        // two elements per paired fp32 instruction (FFMA2 / FMUL2 / FADD2):
+        // p as DrawRow::p computes it, sums in two lanes each
+        const float2 c2 = make_float2(dr.c, dr.c), nm2 = make_float2(-dr.m, -dr.m);
+        const float2 is2 = make_float2(dr.inv_s, dr.inv_s), neg1 = make_float2(-1.0f, -1.0f);
+        float2 sp2 = make_float2(0.0f, 0.0f), sr2 = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int b0 = 0; b0 < NV; b0 += NB) {
             uint4 r[NB], qq[NB][QV];
@@ -385,14 +390,21 @@ __device__ void draw_segment_sums(const DrawRow<T> &dr, bool residual, int lo, i
                 float f[VEC];
                 Storage<T>::unpack(r[u], f);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float p = dr.p(f[e]);
-                    sp += p;
-                    if (residual)
-                        sr += fmaxf(p - q_elem(qq[u], e), 0.0f);
+                for (int e = 0; e < VEC; e += 2) {
+                    const float2 z = __ffma2_rn(make_float2(f[e], f[e + 1]), c2, nm2);
+                    float2 p = __fmul2_rn(make_float2(exp2_sfu(z.x), exp2_sfu(z.y)), is2);
+                    p.x = f[e] >= dr.cut ? p.x : 0.0f;
+                    p.y = f[e + 1] >= dr.cut ? p.y : 0.0f;
+                    sp2 = __fadd2_rn(sp2, p);
+                    if (residual) {
+                        const float2 d = __ffma2_rn(make_float2(q_elem(qq[u], e), q_elem(qq[u], e + 1)), neg1, p);
+                        sr2 = __fadd2_rn(sr2, make_float2(fmaxf(d.x, 0.0f), fmaxf(d.y, 0.0f)));
+                    }
                 }
             }
         }
+        sp = sp2.x + sp2.y;
+        sr = sr2.x + sr2.y;
     } else {
         for (int v = lo + l; v < hi; v += 32) {
             const float p = dr.pv(v);
