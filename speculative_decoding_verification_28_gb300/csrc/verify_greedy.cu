@@ -19,8 +19,15 @@ namespace spec {
 // elements are looked at one by one only when that maximum beats the running
 // best, which happens O(log n) times per thread.  A chunk holding a NaN is
 // recomputed exactly (NaN counts as larger than every number; first NaN wins).
+// y: the row's proposal (-1: none).  As soon as this thread block has seen
+// a finite element strictly above x[y] anywhere in its chunk, the row's
+// argmax cannot be y: the row rejects, and its stop is posted at once
+// (atomicMax(stop_word, stop_val)) so that later rows of the sequence can be
+// skipped before the row is finalised.  (A NaN anywhere would be the argmax,
+// which is not y either; x[y] NaN or y outside [0, V): no early test.)
 template <typename T>
-__device__ uint64_t chunk_argmax(const T *row, int lo, int hi, uint64_t *s_red, const StopProbe &probe)
+__device__ uint64_t chunk_argmax(const T *row, int V, int lo, int hi, uint64_t *s_red, const StopProbe &probe, int y,
+                                 int *stop_word, int stop_val)
 {
     constexpr int VEC = Storage<T>::kVec;
     constexpr int UNROLL = 8;  // 16-byte loads in flight per thread
@@ -45,6 +52,8 @@ __device__ uint64_t chunk_argmax(const T *row, int lo, int hi, uint64_t *s_red, 
     const T *body = row + cs.head_end;
     if (t < cs.nvec)
         first = first == 0xFFFFFFFFu ? (uint32_t)(cs.head_end + t * VEC) : first;
+    bool signalled = y < 0 || y >= V;  // warp-uniform
+    float xy = INFINITY;
     for (int base = 0; base < cs.nvec; base += UNROLL * kThreads) {  // warp-uniform trip count
         if (base > 0 && probe.dropped())
             break;
@@ -56,6 +65,8 @@ __device__ uint64_t chunk_argmax(const T *row, int lo, int hi, uint64_t *s_red, 
             if (vi < cs.nvec)
                 r[u] = ld_stream16(body + (size_t)vi * VEC);
         }
+        if (base == 0 && !signalled)
+            xy = Storage<T>::at(row, y);  // after the batch's loads are in flight
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int vi = i + u * kThreads;
@@ -73,6 +84,11 @@ __device__ uint64_t chunk_argmax(const T *row, int lo, int hi, uint64_t *s_red, 
                     bidx = (uint32_t)(cs.head_end + vi * VEC + e);
                 }
             }
+        }
+        if (!signalled && __any_sync(0xFFFFFFFFu, best > xy)) {
+            if ((t & 31) == 0)
+                atomicMax(stop_word, stop_val);
+            signalled = true;
         }
     }
     if (cs.tail_beg + t < hi)
@@ -100,6 +116,7 @@ __global__ void __launch_bounds__(kThreads) verify_greedy_kernel(VerifyArgs a)
     uint64_t *part = static_cast<uint64_t *>(a.part);
 
     const Unit u = decode_unit(a);
+    const int y = u.j < u.kb ? a.draft[(size_t)u.b * a.k + u.j] : -1;  // used after the first batch is issued
     if (threadIdx.x == 0)
         s_skip = (!u.needed || stopped_before(stop_enc, u.b, u.j)) ? 1 : 0;
     __syncthreads();
@@ -107,7 +124,8 @@ __global__ void __launch_bounds__(kThreads) verify_greedy_kernel(VerifyArgs a)
         const T *row = reinterpret_cast<const T *>(a.logits) + (size_t)u.row * a.V;
         const int lo = u.c * a.chunk;
         const int hi = min(a.V, lo + a.chunk);
-        const uint64_t key = chunk_argmax<T>(row, lo, hi, s_red, StopProbe{stop_enc, u.b, u.j});
+        const uint64_t key = chunk_argmax<T>(row, a.V, lo, hi, s_red, StopProbe{stop_enc, u.b, u.j}, y,
+                                             stop_enc + u.b, kStopBase - u.j);
         if (threadIdx.x == 0)
             part[((size_t)u.row * a.C + u.c) * 2] = key;
     }
