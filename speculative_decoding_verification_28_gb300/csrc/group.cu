@@ -5,8 +5,12 @@
 // library's: L* = most frequent active length (ties to the smaller), members of
 // length L* by ascending index (at most B), then other active sequences by
 // ascending (|len - L*|, index); -1 beyond the active count.
-// One CTA: bitonic sort of (length, index) keys in shared memory, run lengths
-// by binary search, best run by a max-reduction, second sort for the fill.
+// One CTA: bitonic sort of (length, index) keys, run lengths by binary
+// search, best run by a max-reduction, second sort for the fill.  Pools of
+// up to 1024 sequences keep one key per thread in a register: compare-exchange
+// stages with strides below 32 go through warp shuffles, the wider ones
+// through shared memory with one barrier each (15 of the network's 55
+// stages); larger pools sort in shared memory.
 #include "spec_common.cuh"
 #include "spec_launch.h"
 
@@ -125,10 +129,97 @@ __global__ void __launch_bounds__(kGroupThreads)
     }
 }
 
+// Bitonic network over the 1024 keys held one per thread (thread i ends with
+// the i-th smallest).  buf: 2 x 1024 keys of shared memory, alternated so that
+// one barrier per shared-memory stage suffices.
+__device__ uint64_t bitonic_sort_reg(uint64_t x, uint64_t *buf)
+{
+    const int i = threadIdx.x;
+    int flip = 0;
+    for (int size = 2; size <= kGroupThreads; size <<= 1)
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            uint64_t y;
+            if (stride >= 32) {
+                uint64_t *b = buf + flip * kGroupThreads;
+                b[i] = x;
+                __syncthreads();
+                y = b[i ^ stride];
+                flip ^= 1;
+            } else {
+                y = shfl_xor_u64(x, stride);
+            }
+            const bool asc = (i & size) == 0, lower = (i & stride) == 0;
+            x = (lower == asc) ? (x < y ? x : y) : (x > y ? x : y);
+        }
+    return x;
+}
+
+// N <= kGroupThreads: the same policy with one key per thread
+__global__ void __launch_bounds__(kGroupThreads)
+    group_kernel_reg(int N, const int32_t *len, const uint8_t *active, int B, int32_t *out_idx,
+                     int32_t *out_count_equal, int32_t *out_group_len)
+{
+    __shared__ uint64_t buf[2 * kGroupThreads];
+    __shared__ unsigned long long s_best;
+    const uint64_t NONE = ~0ull;
+    const int i = threadIdx.x;
+    if (i == 0)
+        s_best = 0;
+    uint64_t x = NONE;
+    if (i < N && (!active || active[i]))
+        x = ((uint64_t)((uint32_t)len[i] ^ 0x80000000u) << 32) | (uint32_t)i;
+    x = bitonic_sort_reg(x, buf);
+    const int nact = __syncthreads_count(x != NONE);  // the sorted keys: the active ones first
+    uint64_t *key = buf;  // the sorted keys, for neighbours and the binary search
+    key[i] = x;
+    __syncthreads();
+    if (i < nact) {
+        const uint32_t li = (uint32_t)(x >> 32);
+        if (i == 0 || (uint32_t)(key[i - 1] >> 32) != li) {  // a run starts here
+            int lo = i, hi = nact;  // first position with a larger length
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if ((uint32_t)(key[mid] >> 32) > li)
+                    hi = mid;
+                else
+                    lo = mid + 1;
+            }
+            atomicMax(&s_best, ((unsigned long long)(lo - i) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)i));
+        }
+    }
+    __syncthreads();
+    const unsigned long long best = s_best;
+    const int start = nact > 0 ? (int)(0xFFFFFFFFu - (uint32_t)best) : 0;
+    const int cnt = nact > 0 ? (int)(best >> 32) : 0;
+    const int ce = cnt < B ? cnt : B;
+    const int lstar = nact > 0 ? (int)((uint32_t)(key[start] >> 32) ^ 0x80000000u) : 0;
+    if (i < ce)
+        out_idx[i] = (int)(uint32_t)key[start + i];
+    // fill: the other active sequences by (|len - L*|, index)
+    uint64_t x2 = NONE;
+    if (i < nact && !(i >= start && i < start + ce)) {
+        const long long dist = (long long)(int)((uint32_t)(x >> 32) ^ 0x80000000u) - lstar;
+        x2 = ((uint64_t)(uint32_t)(dist < 0 ? -dist : dist) << 32) | (uint32_t)x;
+    }
+    __syncthreads();  // every read of key[] (buf) is done before the second sort reuses it
+    x2 = bitonic_sort_reg(x2, buf);
+    if (ce + i < B)
+        out_idx[ce + i] = x2 != NONE ? (int)(uint32_t)x2 : -1;
+    for (int s = kGroupThreads + ce + i; s < B; s += kGroupThreads)  // B beyond the pool: -1
+        out_idx[s] = -1;
+    if (i == 0) {
+        *out_count_equal = ce;
+        *out_group_len = nact > 0 ? lstar : -1;
+    }
+}
+
 cudaError_t launch_group(int N, const int32_t *len, const uint8_t *active, int B, int32_t *out_idx,
                          int32_t *out_count_equal, int32_t *out_group_len, cudaStream_t st)
 {
-    group_kernel<<<1, kGroupThreads, 0, st>>>(N, len, active, B, out_idx, out_count_equal, out_group_len);
+    if (N <= kGroupThreads)
+        group_kernel_reg<<<1, kGroupThreads, 0, st>>>(N, len, active, B, out_idx, out_count_equal, out_group_len);
+    else
+        group_kernel<<<1, kGroupThreads, 0, st>>>(N, len, active, B, out_idx, out_count_equal, out_group_len);
     return cudaGetLastError();
 }
 

@@ -39,9 +39,11 @@ class ExspecScheduler:
         dev = pool_len.device
         self._mask_h = torch.zeros(self.N, dtype=torch.uint8).pin_memory()
         self._mask_d = torch.zeros(self.N, dtype=torch.uint8, device=dev)
-        self.idx = torch.empty(self.B, dtype=torch.int32, device=dev)
-        self.count_equal = torch.empty(1, dtype=torch.int32, device=dev)
-        self.group_len = torch.empty(1, dtype=torch.int32, device=dev)
+        # the kernel's three outputs side by side: one copy brings them back
+        self._out_d = torch.empty(self.B + 2, dtype=torch.int32, device=dev)
+        self.idx = self._out_d[: self.B]
+        self.count_equal = self._out_d[self.B:self.B + 1]
+        self.group_len = self._out_d[self.B + 1:]
         self._out_h = torch.empty(self.B + 2, dtype=torch.int32).pin_memory()
 
     def select_async(self, active: np.ndarray, stream=None):
@@ -53,9 +55,7 @@ class ExspecScheduler:
         self._mask_d.copy_(self._mask_h, non_blocking=True)
         api.spec_group_by_length(self.pool_len, self.B, active=self._mask_d, out_idx=self.idx,
                                  out_count_equal=self.count_equal, out_group_len=self.group_len, stream=stream)
-        self._out_h[: self.B].copy_(self.idx, non_blocking=True)
-        self._out_h[self.B:self.B + 1].copy_(self.count_equal, non_blocking=True)
-        self._out_h[self.B + 1:].copy_(self.group_len, non_blocking=True)
+        self._out_h.copy_(self._out_d, non_blocking=True)
 
     def selection(self):
         """After the stream reached select_async's copies: (pool indices of

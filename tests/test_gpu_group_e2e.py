@@ -40,7 +40,7 @@ def test_config4_pools(variant):
 
 def test_small_pools_and_degenerate_cases():
     rng = np.random.default_rng(0)
-    for N in list(range(0, 12)) + [1000, 4096]:
+    for N in list(range(0, 12)) + [1000, 1024, 1025, 4096]:
         for trial in range(5):
             lens = rng.integers(-3, 6, size=N).astype(np.int32)
             act = (rng.random(N) < 0.7).astype(np.uint8)
