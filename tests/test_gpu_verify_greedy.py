@@ -107,6 +107,37 @@ def test_ties_nan_inf_and_signed_zero():
     run_both(x, oracle.DT_F32, d, repeat=2)
 
 
+def test_early_rejection_declines_when_unsure():
+    """A row's rejection is posted early only when a finite element lies
+    strictly above the proposal's logit.  These rows must reach the oracle's
+    answer through the full argmax instead: a NaN proposal logit (the only
+    NaN: the proposal is the argmax), a proposal outside [0, V), a proposal
+    tied with the maximum at a lower index (rejected by the tie rule), a +inf
+    proposal (accepted), a -inf proposal (rejected early), a NaN elsewhere in
+    the row (the NaN is the argmax), and a row where the proposal is beaten
+    only in its last chunk."""
+    rng = np.random.default_rng(91)
+    B, k, V = 8, 4, 5 * 8192 + 37
+    x = rng.standard_normal((B, k + 1, V)).astype(np.float32)
+    d = rng.integers(0, V, (B, k)).astype(np.int32)
+    # make every proposal the argmax of its row first (accepted), then break some
+    for b in range(B):
+        for j in range(k):
+            x[b, j, d[b, j]] = 10.0
+    x[0, 0, d[0, 0]] = np.nan                      # the only NaN: accepted
+    d[1, 0] = V + 3                                # outside the vocabulary: rejected
+    x[2, 1, 7] = 10.0                              # tie with the maximum at a lower index
+    d[2, 1] = max(int(d[2, 1]), 8)
+    x[2, 1, d[2, 1]] = 10.0
+    x[3, 0, d[3, 0]] = np.inf                      # +inf: accepted
+    x[4, 0, d[4, 0]] = -np.inf                     # -inf: rejected
+    x[5, 0, (d[5, 0] + 100) % V] = np.nan          # a NaN elsewhere is the argmax
+    x[6, 0, :] = -5.0                              # beaten only near the row's end
+    x[6, 0, d[6, 0]] = 1.0
+    x[6, 0, V - 2] = 2.0
+    run_both(x, oracle.DT_F32, d, repeat=2)
+
+
 def test_empty_batch_is_a_noop():
     x = torch.zeros((0, 3, 100), dtype=torch.float32, device=dev())
     d = torch.zeros((0, 2), dtype=torch.int32, device=dev())
