@@ -171,6 +171,14 @@ def test_small_vocabularies_many_draws(V, dtype):
     check(x, DT_OF[dtype], q, d, u)
 
 
+@pytest.mark.parametrize("V,dtype", [(262144, "bf16"), (300007, "f32"), (600000, "bf16")])
+def test_large_vocabularies(V, dtype):
+    """Rows longer than 256 segments of 1024 (the draw's pick walks its
+    segment sums in several blocks), one of them with a ragged tail."""
+    x, q, d, u = sample_round_inputs(6, 2, V, 0.5, seed=V % 1000, dtype=dtype)
+    check(x, DT_OF[dtype], q, d, u)
+
+
 @pytest.mark.parametrize("T", [0.5, 0.7, 1.5, 3.0])
 def test_temperature(T):
     x, q, d, u = sample_round_inputs(256, 4, 5000, 0.5, seed=int(T * 10), dtype="f32")
