@@ -272,10 +272,13 @@ __device__ bool stats_unit_count(const VerifyArgs &a, const Unit &u, float m_c, 
     return sample_seq_count(a, u.b);
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kThreads) verify_stats_kernel(VerifyArgs a)
+// NT threads per CTA: 128 when a unit would give 256 threads at most one
+// batch of 8 vectors each (twice the CTAs per SM, two batches per thread),
+// else kThreads
+template <typename T, int NT>
+__global__ void __launch_bounds__(NT) verify_stats_kernel(VerifyArgs a)
 {
-    __shared__ float s_f[3 * kThreads / 32];
+    __shared__ float s_f[3 * NT / 32];
     __shared__ int s_skip;
     const float c = scale_of(a);
     const Unit u = decode_unit(a);
@@ -288,7 +291,7 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(VerifyArgs a)
     if (!s_skip) {
         const int lo = u.c * a.chunk;
         const int hi = min(a.V, lo + a.chunk);
-        chunk_softmax_stats<T, false>(row, lo, hi, c, m, s, bad, s_f, StopProbe{a.stop_enc, u.b, u.j}, nullptr);
+        chunk_softmax_stats<T, false, NT>(row, lo, hi, c, m, s, bad, s_f, StopProbe{a.stop_enc, u.b, u.j}, nullptr);
     }
     if (threadIdx.x < 32) {
         int seq_last = 0;
@@ -696,7 +699,11 @@ static cudaError_t launch_sample_t(const VerifyArgs &args, cudaStream_t st)
         if (ef != cudaSuccess)
             return ef;
     } else {
-        verify_stats_kernel<T><<<a.B * (a.k + 1) * a.C, kThreads, 0, st>>>(a);
+        const long long vec_per_unit = (long long)a.chunk * (long long)sizeof(T) / 16;
+        if (vec_per_unit <= 8LL * kThreads)
+            verify_stats_kernel<T, 128><<<a.B * (a.k + 1) * a.C, 128, 0, st>>>(a);
+        else
+            verify_stats_kernel<T, kThreads><<<a.B * (a.k + 1) * a.C, kThreads, 0, st>>>(a);
     }
     // the two draw kernels become resident while the kernel before each
     // drains, and wait for it on the device (griddepcontrol.wait)
