@@ -20,14 +20,15 @@ constexpr int kMinChunk = 4096;        // smallest vocabulary chunk of a verify 
 #ifndef SPEC_TARGET_UNITS
 #define SPEC_TARGET_UNITS 2432
 #endif
-constexpr int kTargetUnits = SPEC_TARGET_UNITS;  // ~two waves of 8 CTAs on 152 SMs
+constexpr int kTargetUnits = SPEC_TARGET_UNITS;  // the best of a sweep over 608 .. 19456 units
 constexpr int kDrawChunk = 8192;       // elements per CTA of the draw sums kernel (one 1024-element segment per warp)
 constexpr int kMaxRows = SPEC_MAX_K + 1;
 constexpr int kStopBase = 1024;        // stop row j is stored as kStopBase - j
 
-// Split of each logits row into work units: enough units for about two waves
-// over the whole batch, each at least kMinChunk elements, lengths a multiple of
-// 64 elements (16-byte aligned starts whenever the row start is).
+// Split of each logits row into work units: about kTargetUnits units over the
+// whole batch (four waves of four 256-thread CTAs per SM), each at least
+// kMinChunk elements, lengths a multiple of 64 elements (16-byte aligned
+// starts whenever the row start is).
 struct Split {
     int C;    // chunks per row
     int len;  // elements per chunk (the last one may be shorter)

@@ -17,20 +17,22 @@
 //   stats  : per (b, j, chunk) max / sum of 2^(x c - m) (lazy rows, as in the
 //            greedy kernel; 8 loads in flight per thread, one packed maximum
 //            and one rescale test per batch of vectors, the last batch padded
-//            with -inf); the row's last CTA
-//            gathers x[y] and q[y] and runs the ratio test; the sequence's
-//            last row runs the first-stop ballot and decides which row (if
-//            any) is drawn from.  With top-k / top-p the filter kernel of
-//            verify_filter.cuh takes this place (one CTA per row, and the
-//            row's cut goes to the draw kernel);
+//            with -inf, two elements per paired fp32 instruction; 128-thread
+//            CTAs when a chunk is short); the row's last CTA gathers x[y] and
+//            q[y] and runs the ratio test; the sequence's last row runs the
+//            first-stop ballot and decides which row (if any) is drawn from.
+//            With top-k / top-p the filter kernel of verify_filter.cuh takes
+//            this place (one CTA per row, and the row's cut goes to the draw
+//            kernels);
 //   sums   : per (b, 1024-element segment) of the drawn row, one warp sums
 //            the residual and p in a vectorised pass;
 //   pick   : one warp per drawing sequence picks the mode, finds the segment
 //            holding u * total from the segment sums, loads that segment
-//            into registers and scans it for the inverse-CDF index, all
-//            prefix sums in exact 64-bit fixed point.  Sums and
-//            pick are launched programmatically and wait for the kernel
-//            before them on the device;
+//            into registers and scans it for the inverse-CDF index: prefix
+//            sums over segments and lanes in exact 64-bit fixed point, the
+//            walk within a lane in fp32.  Sums and pick are launched
+//            programmatically and wait for the kernel before them on the
+//            device;
 //   resid  : optional, writes the normalised distribution of the draw.
 // Roofline: HBM-bound; stats reads V * sizeof(T) per needed row; draw reads
 // V * (sizeof(T) + 4) for one row per drawing sequence.
