@@ -110,6 +110,29 @@ __device__ __forceinline__ unsigned long long q40_weight(float d, float c)
     return __float2ull_rz(__fmul_rn(p, scale));
 }
 
+// q40_weight of two logits at once with paired fp32 instructions (FMUL2,
+// FADD2, FFMA2; every lane rounded to nearest, so each result is bit for bit
+// q40_weight's).  t is clamped at -65 before the integer scale is formed, so
+// an out-of-range t never reaches the conversion; such a t gives 0 anyway.
+__device__ __forceinline__ void q40_weight2(float2 d, float c, unsigned long long &q0, unsigned long long &q1)
+{
+    const float2 t = __fmul2_rn(d, make_float2(c, c));
+    const float i0 = rintf(fmaxf(t.x, -65.0f)), i1 = rintf(fmaxf(t.y, -65.0f));
+    const float2 f = __fadd2_rn(t, make_float2(-i0, -i1));
+    float2 p = make_float2(0x1.ffcbfcp-17f, 0x1.ffcbfcp-17f);
+    p = __ffma2_rn(p, f, make_float2(0x1.430912p-13f, 0x1.430912p-13f));
+    p = __ffma2_rn(p, f, make_float2(0x1.5d87fep-10f, 0x1.5d87fep-10f));
+    p = __ffma2_rn(p, f, make_float2(0x1.3b2ab6p-7f, 0x1.3b2ab6p-7f));
+    p = __ffma2_rn(p, f, make_float2(0x1.c6b08ep-5f, 0x1.c6b08ep-5f));
+    p = __ffma2_rn(p, f, make_float2(0x1.ebfbe0p-3f, 0x1.ebfbe0p-3f));
+    p = __ffma2_rn(p, f, make_float2(0x1.62e430p-1f, 0x1.62e430p-1f));
+    p = __ffma2_rn(p, f, make_float2(1.0f, 1.0f));
+    const float2 sc = make_float2(__int_as_float(((int)i0 + 40 + 127) << 23), __int_as_float(((int)i1 + 40 + 127) << 23));
+    const float2 r = __fmul2_rn(p, sc);
+    q0 = (t.x >= -64.0f) ? __float2ull_rz(r.x) : 0ull;
+    q1 = (t.y >= -64.0f) ? __float2ull_rz(r.y) : 0ull;
+}
+
 // f(x) for every logit of the row: 16-byte vectors, scalar head and tail
 template <typename T, int NT, typename F>
 __device__ __forceinline__ void row_for_each(const T *row, int V, F &f)
@@ -138,6 +161,42 @@ __device__ __forceinline__ void row_for_each(const T *row, int V, F &f)
 #pragma unroll
                 for (int q = 0; q < VEC; ++q)
                     f(e[q]);
+            }
+        }
+    }
+    for (int v = cs.tail_beg + t; v < V; v += NT)
+        f(Storage<T>::at(row, v));
+}
+
+// f2(x0, x1) for the element pairs of every 16-byte vector of the row, f(x)
+// for the scalar head and tail
+template <typename T, int NT, typename F, typename F2>
+__device__ __forceinline__ void row_for_each_pair(const T *row, int V, F &f, F2 &f2)
+{
+    constexpr int VEC = Storage<T>::kVec;
+    constexpr int UNROLL = 4;
+    const ChunkSplit<T> cs(row, 0, V);
+    const int t = threadIdx.x;
+    for (int v = t; v < cs.head_end; v += NT)
+        f(Storage<T>::at(row, v));
+    const T *body = row + cs.head_end;
+    for (int base = 0; base < cs.nvec; base += UNROLL * NT) {
+        uint4 r[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int vi = base + t + u * NT;
+            if (vi < cs.nvec)
+                r[u] = ld_stream16(body + (size_t)vi * VEC);
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int vi = base + t + u * NT;
+            if (vi < cs.nvec) {
+                float e[VEC];
+                Storage<T>::unpack(r[u], e);
+#pragma unroll
+                for (int q = 0; q < VEC; q += 2)
+                    f2(e[q], e[q + 1]);
             }
         }
     }
@@ -175,7 +234,37 @@ __device__ void hist_pass(const T *row, int V, int l, uint32_t prefix, uint32_t 
             atomicAdd(&h.mhi[dg], (unsigned int)(q >> 28));
         }
     };
-    row_for_each<T, NT>(row, V, add);
+    // Level 0: every logit at or above lo_key is in, so weights go two at a
+    // time -- in the 256-thread form; the 1024-thread form is held to 64
+    // registers, where the pairs' extra live values cost more than they save.
+    if constexpr (kMass && NT < 1024) {
+        if (l != 0) {
+            row_for_each<T, NT>(row, V, add);
+            return;
+        }
+        auto add2 = [&](float x0, float x1) {
+            const uint32_t k0 = order_key(x0), k1 = order_key(x1);
+            unsigned long long q0, q1;
+            q40_weight2(__fadd2_rn(make_float2(x0, x1), make_float2(-xmax, -xmax)), cdec, q0, q1);
+            if (k0 >= lo_key) {
+                const int dg = (int)(k0 >> sh);
+                atomicAdd(&h.cnt[dg], 1u);
+                atomicAdd(&h.mlo[dg], (unsigned int)(q0 & 0x3FFFull));
+                atomicAdd(&h.mmid[dg], (unsigned int)((q0 >> 14) & 0x3FFFull));
+                atomicAdd(&h.mhi[dg], (unsigned int)(q0 >> 28));
+            }
+            if (k1 >= lo_key) {
+                const int dg = (int)(k1 >> sh);
+                atomicAdd(&h.cnt[dg], 1u);
+                atomicAdd(&h.mlo[dg], (unsigned int)(q1 & 0x3FFFull));
+                atomicAdd(&h.mmid[dg], (unsigned int)((q1 >> 14) & 0x3FFFull));
+                atomicAdd(&h.mhi[dg], (unsigned int)(q1 >> 28));
+            }
+        };
+        row_for_each_pair<T, NT>(row, V, add, add2);
+    } else {
+        row_for_each<T, NT>(row, V, add);
+    }
 }
 
 // First digit from the top whose inclusive cumulative count reaches `need`
@@ -322,7 +411,7 @@ __device__ float row_max_pass(const T *row, int V, float *s_f)
 }
 
 template <typename T, int NT>
-__global__ void __launch_bounds__(NT) verify_filter_kernel(VerifyArgs a)
+__global__ void __launch_bounds__(NT, NT >= 1024 ? 1 : 3) verify_filter_kernel(VerifyArgs a)
 {
     constexpr int L = KeyLevels<T>::kLevels;
     __shared__ FilterHist h;
