@@ -156,3 +156,70 @@ def test_round_replayed_from_a_cuda_graph_equals_oracle():
         assert np.array_equal(pos.cpu().numpy(), opos) and np.array_equal(mask.cpu().numpy(), omask)
         ln, pad = o_ln, o_pd
         cur = 1 - cur
+
+
+@pytest.mark.parametrize("filtered", [False, True])
+def test_sample_round_replayed_from_a_cuda_graph_equals_direct_calls(filtered):
+    """spec_round_sample captured once per buffer parity (RoundGraph: the
+    statistics or filter kernel, the two programmatically launched draw
+    kernels, the realignment and the positions / mask) and replayed over
+    chained rounds gives, round after round, exactly what direct calls give
+    on a twin state: tokens, counts, lengths, paddings, width, flags, cache,
+    positions and mask."""
+    rng = np.random.default_rng(23 + filtered)
+    B, k, V, S = 8, 3, 3000, 128
+    kv = rng.standard_normal((2, 2, B, 2, S, 16)).astype(np.float32)
+    kv_g, kv_e = torch.from_numpy(kv.copy()).to(dev()), torch.from_numpy(kv.copy()).to(dev())
+    ln, pad = _state(B, S, k, seed=29)
+    p0, m0 = oracle.rebuild_pos_mask(S, pad)
+    pos_g, mask_g = torch.from_numpy(p0).to(dev()), torch.from_numpy(m0).to(dev())
+    pos_e, mask_e = pos_g.clone(), mask_g.clone()
+    x_d = torch.empty((B, k + 1, V), dtype=torch.bfloat16, device=dev())
+    q_d = torch.empty((B, k, V), dtype=torch.float32, device=dev())
+    d_d = torch.empty((B, k), dtype=torch.int32, device=dev())
+    u_d = torch.empty((B, k + 1), dtype=torch.float32, device=dev())
+    tk = to_dev(rng.integers(0, 40, size=B).astype(np.int32)) if filtered else None
+    tp = to_dev(rng.choice([0.6, 0.9, 1.0], size=B).astype(np.float32)) if filtered else None
+    n = B * (k + 1) + 5 * B + 2
+    blocks = [torch.zeros(n, dtype=torch.int32, device=dev()) for _ in range(2)]
+    ws = sv.Workspace(B, k, V, dev())
+
+    def views(blk):
+        o = B * (k + 1)
+        return (blk[:o].view(B, k + 1), blk[o:o + B], blk[o + B:o + 2 * B], blk[o + 2 * B:o + 3 * B],
+                blk[o + 3 * B:o + 4 * B], blk[o + 4 * B:o + 4 * B + 1], blk[o + 4 * B + 1:o + 4 * B + 2],
+                blk[o + 4 * B + 2:o + 5 * B + 2])
+
+    def enqueue(par):
+        out, na, ne, ln_out, pad_out, w, err, fl = views(blocks[1 - par])
+        ln_in, pad_in = views(blocks[par])[3], views(blocks[par])[4]
+        sv.spec_round_sample(x_d, q_d, d_d, u_d, [kv_g], ln_in, pad_in, pos_g, mask_g, top_k=tk, top_p=tp,
+                             out_tokens=out, n_accept=na, n_emit=ne, flags=fl, len_new=ln_out, pad_new=pad_out,
+                             width_new=w, err=err, workspace=ws)
+
+    graphs = [sv.RoundGraph(lambda p=p: enqueue(p), dev()) for p in (0, 1)]
+    views(blocks[0])[3].copy_(to_dev(ln))
+    views(blocks[0])[4].copy_(to_dev(pad))
+    ln_e, pad_e = to_dev(ln), to_dev(pad)
+    cur, rounds = 0, 0
+    for r in range(8):
+        if int(views(blocks[cur])[3][0].item() + views(blocks[cur])[4][0].item()) + k + 1 > S:
+            break
+        x, q, d, u = sample_round_inputs(B, k, V, 0.5, seed=400 + r, dtype="bf16")
+        x_d.copy_(logits_to_dev(x, oracle.DT_BF16))
+        q_d.copy_(to_dev(q))
+        d_d.copy_(to_dev(d))
+        u_d.copy_(to_dev(u))
+        graphs[cur].replay()
+        e = sv.spec_round_sample(x_d, q_d, d_d, u_d, [kv_e], ln_e, pad_e, pos_e, mask_e, top_k=tk, top_p=tp)
+        torch.cuda.synchronize()
+        out, na, ne, ln2, pd2, w2, err, fl = views(blocks[1 - cur])
+        assert torch.equal(out, e[0]) and torch.equal(na, e[1]) and torch.equal(ne, e[2]), r
+        assert torch.equal(ln2, e[3]) and torch.equal(pd2, e[4]) and torch.equal(w2, e[5].view(1)), r
+        assert int(err.item()) == 0 and int(e[6].item()) == 0
+        assert torch.equal(fl, e[7].view(-1)), r
+        assert torch.equal(kv_g, kv_e) and torch.equal(pos_g, pos_e) and torch.equal(mask_g, mask_e), r
+        ln_e, pad_e = e[3].clone(), e[4].clone()
+        cur = 1 - cur
+        rounds += 1
+    assert rounds >= 4
