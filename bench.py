@@ -59,6 +59,7 @@ def parse():
     ap.add_argument("--pool-lengths", choices=["a", "b"], default="a",
                     help="c4x pool lengths: a = U[128,1024] (as configured), b = uniform over {128, 256, ..., 1024}")
     ap.add_argument("--window", type=int, default=None, help="c4x: sliding window (default: the whole pool)")
+    ap.add_argument("--batch", type=int, default=None, help="c4x: sequences gathered per round (default: 64)")
     ap.add_argument("--top-k", type=int, default=None, help="stochastic workloads: top-k on the target distribution")
     ap.add_argument("--top-p", type=float, default=None, help="stochastic workloads: top-p on the target distribution")
     ap.add_argument("--layers", type=int, default=None,
@@ -786,6 +787,8 @@ def run_exspec_bench(args, c, rank, local_rank, world):
     seed = rank_seed(args.seed, rank)
     g = torch.Generator(device=dev).manual_seed(seed)
     rng = np.random.default_rng(seed)
+    if args.batch:
+        c["B"] = int(args.batch)
     N, B, k, V = c["N"], c["B"], c["k"], c["V"]
     L, H, S, D = c["L"], c["H"], c["S"], c["D"]
     lo, hi = c["pool_len"]
