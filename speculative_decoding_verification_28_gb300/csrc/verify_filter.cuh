@@ -235,9 +235,10 @@ __device__ void hist_pass(const T *row, int V, int l, uint32_t prefix, uint32_t 
         }
     };
     // Level 0: every logit at or above lo_key is in, so weights go two at a
-    // time -- in the 256-thread form; the 1024-thread form is held to 64
-    // registers, where the pairs' extra live values cost more than they save.
-    if constexpr (kMass && NT < 1024) {
+    // time -- in the 256-thread form; the 512- and 1024-thread forms are held
+    // to 64 registers, where the pairs' extra live values cost more than they
+    // save.
+    if constexpr (kMass && NT <= 256) {
         if (l != 0) {
             row_for_each<T, NT>(row, V, add);
             return;
@@ -411,7 +412,7 @@ __device__ float row_max_pass(const T *row, int V, float *s_f)
 }
 
 template <typename T, int NT>
-__global__ void __launch_bounds__(NT, NT >= 1024 ? 1 : 3) verify_filter_kernel(VerifyArgs a)
+__global__ void __launch_bounds__(NT, NT >= 1024 ? 1 : (NT >= 512 ? 2 : 3)) verify_filter_kernel(VerifyArgs a)
 {
     constexpr int L = KeyLevels<T>::kLevels;
     __shared__ FilterHist h;
@@ -521,15 +522,32 @@ __global__ void __launch_bounds__(NT, NT >= 1024 ? 1 : 3) verify_filter_kernel(V
     sample_seq_finish(a, u);
 }
 
-// Block size: 1024 threads when the batch has at most two rows per SM (a
-// row is one CTA, so a few rows would otherwise leave the GPU idle), else 256.
+// Block size by the number of rows (one CTA per row): a row per SM at most
+// -> 1024 threads; two rows per SM at most -> 512 for top-p alone (two CTAs
+// fit on an SM, so every row runs in the first wave; measured faster), 1024
+// with top-k (its count-only passes are issue-bound: two CTAs sharing an SM
+// gain nothing over a second wave); more rows -> 256.
 template <typename T>
 cudaError_t launch_filter_rows(const VerifyArgs &args, cudaStream_t st)
 {
+    static int sm_count[64];
     VerifyArgs f = args;
     f.C = 1;  // one CTA per row
-    const unsigned rows = (unsigned)(f.B * (f.k + 1));
-    if (rows <= 2u * 152u)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (sm_count[dev & 63] == 0) {
+        e = cudaDeviceGetAttribute(&sm_count[dev & 63], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return e;
+    }
+    const unsigned rows = (unsigned)(f.B * (f.k + 1)), sms = (unsigned)sm_count[dev & 63];
+    if (rows <= sms)
+        verify_filter_kernel<T, 1024><<<rows, 1024, 0, st>>>(f);
+    else if (rows <= 2u * sms && f.top_k == nullptr)
+        verify_filter_kernel<T, 512><<<rows, 512, 0, st>>>(f);
+    else if (rows <= 2u * sms)
         verify_filter_kernel<T, 1024><<<rows, 1024, 0, st>>>(f);
     else
         verify_filter_kernel<T, kThreads><<<rows, kThreads, 0, st>>>(f);
