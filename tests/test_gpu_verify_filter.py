@@ -118,6 +118,18 @@ def test_config3_shape_typical_settings():
               top_k=tk, top_p=tp)
 
 
+@pytest.mark.parametrize("B,dtype", [(32, "f32"), (40, "bf16")])
+def test_top_p_alone_between_one_and_two_rows_per_sm(B, dtype):
+    """Top-p without a top-k array on 160 / 200 rows: the filter's 512-thread
+    form (every row in the first wave)."""
+    c = CONFIGS["c3"]
+    k, V = c["k"], c["V"] if dtype == "f32" else 30000
+    rng = np.random.default_rng(B)
+    x, q, d, u = sample_round_inputs(B, k, V, c["noise"], seed=B + 11, dtype=dtype)
+    tp = rng.choice([0.5, 0.8, 0.9, 0.95, 1.0], size=B).astype(np.float32)
+    check(x, DT_OF[dtype], q, d, u, top_k=None, top_p=tp)
+
+
 def test_config5_shape_bf16():
     """B=64 of config 5's rows (k=8, V=128256 bf16), top_p = 0.95."""
     c = CONFIGS["c5"]
