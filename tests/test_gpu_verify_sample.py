@@ -179,6 +179,16 @@ def test_large_vocabularies(V, dtype):
     check(x, DT_OF[dtype], q, d, u)
 
 
+@pytest.mark.parametrize("V,dtype", [(70001, "bf16"), (40003, "f32"), (65536, "f16")])
+def test_long_chunks(V, dtype):
+    """1500 target rows of two chunks each, every chunk 4096 or more 16-byte
+    vectors (several full batches per thread of the 256-thread statistics
+    form); rows of odd length start unaligned, so chunks have scalar heads
+    and tails."""
+    x, q, d, u = sample_round_inputs(300, 4, V, 0.5, seed=V % 997, dtype=dtype)
+    check(x, DT_OF[dtype], q, d, u)
+
+
 @pytest.mark.parametrize("T", [0.5, 0.7, 1.5, 3.0])
 def test_temperature(T):
     x, q, d, u = sample_round_inputs(256, 4, 5000, 0.5, seed=int(T * 10), dtype="f32")
