@@ -36,6 +36,8 @@
 // make the kernel instruction-bound.
 #pragma once
 
+#include <type_traits>
+
 #include "sample_final.cuh"
 
 namespace spec {
@@ -411,10 +413,68 @@ __device__ float row_max_pass(const T *row, int V, float *s_f)
     return r;
 }
 
+// Radix selection of a filtered row's cut (all NT threads; ends with a
+// barrier): the k-th largest logit, then the top-p boundary among the logits
+// at or above it.  Returns the smallest kept logit; kept_mass: the Q mass of
+// the kept logits.
+template <typename T, int NT>
+__device__ __forceinline__ float radix_cut(const T *row, int V, float xmax, float cdec, int tk, float tp, bool use_k,
+                                           bool use_p, FilterHist &h, FilterSel &sel, unsigned int *s_wc,
+                                           unsigned long long *s_wm, unsigned long long &kept_mass)
+{
+    constexpr int L = KeyLevels<T>::kLevels;
+    uint32_t K = 0u;
+    kept_mass = 0ull;
+    if (use_k) {
+        uint32_t prefix = 0u;
+        unsigned int need = (unsigned int)tk;
+        unsigned long long above = 0ull;
+        for (int l = 0; l < L; ++l) {
+            const int nb = lvl_bins(l);
+            hist_clear<NT>(h, nb);
+            __syncthreads();
+            if (use_p)
+                hist_pass<T, false, NT>(row, V, l, prefix, 0u, xmax, cdec, h);
+            else
+                hist_pass<T, true, NT>(row, V, l, prefix, 0u, xmax, cdec, h);
+            __syncthreads();
+            hist_select<false, NT>(h, nb, need, 0ull, 0.0f, false, sel, s_wc, s_wm);
+            const int bin = sel.bin < 0 ? 0 : sel.bin;  // a digit is always found
+            need -= sel.cnt_above;
+            above += sel.mass_above;
+            if (l == L - 1)
+                kept_mass = above + h.mass(bin);
+            prefix = (l == 0) ? (uint32_t)bin : ((prefix << (lvl_shift(l - 1) - lvl_shift(l))) | (uint32_t)bin);
+            __syncthreads();
+        }
+        K = prefix << lvl_shift(L - 1);
+    }
+    if (use_p) {
+        uint32_t prefix = 0u;
+        unsigned long long A = 0ull;
+        for (int l = 0; l < L; ++l) {
+            const int nb = lvl_bins(l);
+            hist_clear<NT>(h, nb);
+            __syncthreads();
+            hist_pass<T, true, NT>(row, V, l, prefix, K, xmax, cdec, h);
+            __syncthreads();
+            hist_select<true, NT>(h, nb, 0u, A, tp, l == 0, sel, s_wc, s_wm);
+            const int bin = sel.bin < 0 ? 0 : sel.bin;  // a digit is always found
+            A += sel.mass_above;
+            if (l == L - 1)
+                kept_mass = A + h.mass(bin);
+            prefix = (l == 0) ? (uint32_t)bin : ((prefix << (lvl_shift(l - 1) - lvl_shift(l))) | (uint32_t)bin);
+            __syncthreads();
+        }
+        K = prefix << lvl_shift(L - 1);
+    }
+    const uint32_t low = (1u << lvl_shift(L - 1)) - 1u;  // key bits below the last digit
+    return key_value(K | ((K & 0x80000000u) ? 0u : low));
+}
+
 template <typename T, int NT>
 __global__ void __launch_bounds__(NT, NT >= 1024 ? 1 : (NT >= 512 ? 2 : 3)) verify_filter_kernel(VerifyArgs a)
 {
-    constexpr int L = KeyLevels<T>::kLevels;
     __shared__ FilterHist h;
     __shared__ float s_f[4 * NT / 32];
     __shared__ unsigned int s_wc[NT / 32];
@@ -461,54 +521,8 @@ __global__ void __launch_bounds__(NT, NT >= 1024 ? 1 : (NT >= 512 ? 2 : 3)) veri
         __syncthreads();
         s_kept = s_s;
         if (!s_skip && !s_bad && (use_k || use_p)) {
-            const float xmax = s_xmax, cdec = a.dec_scale;
-            uint32_t K = 0u;
-            unsigned long long kept_mass = 0ull;
-            if (use_k) {
-                uint32_t prefix = 0u;
-                unsigned int need = (unsigned int)tk;
-                unsigned long long above = 0ull;
-                for (int l = 0; l < L; ++l) {
-                    const int nb = lvl_bins(l);
-                    hist_clear<NT>(h, nb);
-                    __syncthreads();
-                    if (use_p)
-                        hist_pass<T, false, NT>(row, a.V, l, prefix, 0u, xmax, cdec, h);
-                    else
-                        hist_pass<T, true, NT>(row, a.V, l, prefix, 0u, xmax, cdec, h);
-                    __syncthreads();
-                    hist_select<false, NT>(h, nb, need, 0ull, 0.0f, false, sel, s_wc, s_wm);
-                    const int bin = sel.bin < 0 ? 0 : sel.bin;  // a digit is always found
-                    need -= sel.cnt_above;
-                    above += sel.mass_above;
-                    if (l == L - 1)
-                        kept_mass = above + h.mass(bin);
-                    prefix = (l == 0) ? (uint32_t)bin : ((prefix << (lvl_shift(l - 1) - lvl_shift(l))) | (uint32_t)bin);
-                    __syncthreads();
-                }
-                K = prefix << lvl_shift(L - 1);
-            }
-            if (use_p) {
-                uint32_t prefix = 0u;
-                unsigned long long A = 0ull;
-                for (int l = 0; l < L; ++l) {
-                    const int nb = lvl_bins(l);
-                    hist_clear<NT>(h, nb);
-                    __syncthreads();
-                    hist_pass<T, true, NT>(row, a.V, l, prefix, K, xmax, cdec, h);
-                    __syncthreads();
-                    hist_select<true, NT>(h, nb, 0u, A, tp, l == 0, sel, s_wc, s_wm);
-                    const int bin = sel.bin < 0 ? 0 : sel.bin;  // a digit is always found
-                    A += sel.mass_above;
-                    if (l == L - 1)
-                        kept_mass = A + h.mass(bin);
-                    prefix = (l == 0) ? (uint32_t)bin : ((prefix << (lvl_shift(l - 1) - lvl_shift(l))) | (uint32_t)bin);
-                    __syncthreads();
-                }
-                K = prefix << lvl_shift(L - 1);
-            }
-            const uint32_t low = (1u << lvl_shift(L - 1)) - 1u;  // key bits below the last digit
-            cut = key_value(K | ((K & 0x80000000u) ? 0u : low));
+            unsigned long long kept_mass;
+            cut = radix_cut<T, NT>(row, a.V, s_xmax, a.dec_scale, tk, tp, use_k, use_p, h, sel, s_wc, s_wm, kept_mass);
             s_kept = (float)((double)kept_mass * 0x1p-40);
         }
     }
@@ -519,6 +533,404 @@ __global__ void __launch_bounds__(NT, NT >= 1024 ? 1 : (NT >= 512 ? 2 : 3)) veri
         eval = (u.needed && !stopped_before(a.stop_enc, u.b, u.j)) ? 1 : 0;
     if (eval)
         sample_row_decide<T>(a, u, row, s_m, s_kept, cut, s_bad != 0);
+    sample_seq_finish(a, u);
+}
+
+// ---------------------------------------------------------------------------
+// 16-bit logits (bf16 / fp16): the cut from a table of value counts.
+//
+// A 16-bit logit takes at most 65536 values, so one pass over the row counts
+// each bit pattern (16-bit counters, two per shared word; one shared atomic
+// per logit) and the rest works on the table: the row maximum is its highest
+// non-empty value, and the Q mass of a value is its count times the value's
+// weight q40_weight(x - x_max) -- the same weights and the same exact
+// integer sums as the radix selection, with one weight per distinct value
+// instead of one per logit per pass.  A block scan in descending value order
+// gives the k-th largest value and the top-p boundary; the thread range that
+// holds either one is then walked by one warp.  A counter that wraps (more
+// than 65535 equal logits) shows as a total count below V; the row then
+// takes the radix selection, on the same shared memory.
+// ---------------------------------------------------------------------------
+constexpr int kTabThreads = 1024;
+constexpr int kTabWords = 32768;  // 65536 16-bit counters
+constexpr int kTabMinV = 32768;   // rows at least this long take the table form
+constexpr int kTabSmem = kTabWords * 4;
+
+template <typename T>
+struct Tab16;
+template <>
+struct Tab16<__nv_bfloat16> {
+    static constexpr uint32_t kPinfKey = 0xFF80u, kNinfKey = 0x007Fu;  // order keys of +inf and -inf
+    __device__ static float value(uint32_t h) { return __uint_as_float(h << 16); }
+};
+template <>
+struct Tab16<__half> {
+    static constexpr uint32_t kPinfKey = 0xFC00u, kNinfKey = 0x03FFu;
+    __device__ static float value(uint32_t h) { return __half2float(__ushort_as_half((unsigned short)h)); }
+};
+
+// order key of a 16-bit pattern and back (-0 has its own key, 0x7FFF, below
+// +0's 0x8000; the table merges -0 into +0 before any key is formed)
+__device__ __forceinline__ uint32_t pat_key(uint32_t h) { return (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u); }
+__device__ __forceinline__ uint32_t key_pat(uint32_t k) { return (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu); }
+
+// Thread t owns the 64 keys 65535 - 64 t (rank 0) down to 65472 - 64 t (rank
+// 63): non-negative patterns 0x7FFF - 64 t - r for t < 512, negative ones
+// 64 t + r above; either way the 32 table words from tab_base(t).
+__device__ __forceinline__ uint32_t rank_pat(int t, int r)
+{
+    return t < 512 ? 0x7FFFu - 64u * (uint32_t)t - (uint32_t)r : 64u * (uint32_t)t + (uint32_t)r;
+}
+__device__ __forceinline__ int tab_base(int t) { return t < 512 ? 0x3FE0 - 32 * t : 32 * t; }
+__device__ __forceinline__ uint32_t tab_half(uint32_t x, uint32_t h) { return (h & 1u) ? (x >> 16) : (x & 0xFFFFu); }
+
+// all threads: counts every logit of the row into the table (cleared before)
+template <typename T>
+__device__ __forceinline__ void tab_count(const T *row, int V, unsigned int *tab)
+{
+    constexpr int NT = kTabThreads;
+    const ChunkSplit<T> cs(row, 0, V);
+    const int t = threadIdx.x;
+    auto add = [&](uint32_t h) { atomicAdd(tab + (h >> 1), (h & 1u) ? 0x10000u : 1u); };
+    for (int v = t; v < cs.head_end; v += NT)
+        add(__ldg(reinterpret_cast<const unsigned short *>(row) + v));
+    const T *body = row + cs.head_end;
+    constexpr int U = 8;  // 128 KB of loads in flight per CTA (one CTA per SM)
+    for (int base = 0; base < cs.nvec; base += U * NT) {
+        uint4 r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int vi = base + t + u * NT;
+            if (vi < cs.nvec)
+                r[u] = ld_stream16(body + (size_t)vi * 8);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int vi = base + t + u * NT;
+            if (vi < cs.nvec) {
+                const uint32_t w[4] = {r[u].x, r[u].y, r[u].z, r[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    add(w[e] & 0xFFFFu);
+                    add(w[e] >> 16);
+                }
+            }
+        }
+    }
+    for (int v = cs.tail_beg + t; v < V; v += NT)
+        add(__ldg(reinterpret_cast<const unsigned short *>(row) + v));
+}
+
+// Block-wide exclusive prefix (thread order) of a count and a mass, with the
+// mass total; ends with a barrier.  s_wc / s_wm: one slot per warp.
+__device__ __forceinline__ void tab_scan(uint32_t c, unsigned long long m, uint32_t &c_ex, unsigned long long &m_ex,
+                                         unsigned long long &m_tot, unsigned int *s_wc, unsigned long long *s_wm)
+{
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    uint32_t ic = c;
+    unsigned long long im = m;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t oc = __shfl_up_sync(0xFFFFFFFFu, ic, o);
+        const unsigned long long om = __shfl_up_sync(0xFFFFFFFFu, im, o);
+        if (lane >= o) {
+            ic += oc;
+            im += om;
+        }
+    }
+    __syncthreads();  // earlier readers of s_wc / s_wm are done
+    if (lane == 31) {
+        s_wc[w] = ic;
+        s_wm[w] = im;
+    }
+    __syncthreads();
+    c_ex = ic - c;
+    m_ex = im - m;
+    m_tot = 0;
+    for (int i = 0; i < kTabThreads / 32; ++i) {
+        if (i < w) {
+            c_ex += s_wc[i];
+            m_ex += s_wm[i];
+        }
+        m_tot += s_wm[i];
+    }
+}
+
+// Warp 0 (all lanes): walks the 64 keys of thread tc in descending order,
+// lane l taking ranks 2 l and 2 l + 1 (one table word).  Keys below kk count
+// as empty.  Finds the first non-empty key where the running count from the
+// top (c0 + counts) reaches `need` (kCount) or the running mass (m0 +
+// masses) reaches `bound` as a double; writes that key and the running mass
+// at it to *key_out / *mass_out (untouched when there is none).
+template <typename T, bool kCount>
+__device__ __forceinline__ void tab_walk(const unsigned int *tab, int tc, uint32_t kk, float xmax, float cdec,
+                                         uint32_t c0, uint32_t need, unsigned long long m0, double bound,
+                                         int *key_out, unsigned long long *mass_out)
+{
+    const int lane = threadIdx.x & 31;
+    const uint32_t ha = rank_pat(tc, 2 * lane), hb = rank_pat(tc, 2 * lane + 1);
+    const uint32_t x = tab[ha >> 1];
+    const uint32_t ka = pat_key(ha), kb = pat_key(hb);
+    const uint32_t na = ka >= kk ? tab_half(x, ha) : 0u, nb = kb >= kk ? tab_half(x, hb) : 0u;
+    // an empty key's weight is not needed: x_max stands in (no inf or NaN)
+    const float va = na ? Tab16<T>::value(ha) : xmax, vb = nb ? Tab16<T>::value(hb) : xmax;
+    unsigned long long qa, qb;
+    q40_weight2(__fadd2_rn(make_float2(va, vb), make_float2(-xmax, -xmax)), cdec, qa, qb);
+    const unsigned long long ma = (unsigned long long)na * qa, mb = (unsigned long long)nb * qb;
+    uint32_t ic = na + nb;
+    unsigned long long im = ma + mb;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t oc = __shfl_up_sync(0xFFFFFFFFu, ic, o);
+        const unsigned long long om = __shfl_up_sync(0xFFFFFFFFu, im, o);
+        if (lane >= o) {
+            ic += oc;
+            im += om;
+        }
+    }
+    const uint32_t ce = c0 + ic - (na + nb);
+    const unsigned long long me = m0 + im - (ma + mb);
+    bool hit_a, hit_b;
+    if (kCount) {
+        hit_a = na > 0u && ce + na >= need;
+        hit_b = nb > 0u && ce + na + nb >= need;
+    } else {
+        hit_a = na > 0u && (double)(me + ma) >= bound;
+        hit_b = nb > 0u && (double)(me + ma + mb) >= bound;
+    }
+    const unsigned hits = __ballot_sync(0xFFFFFFFFu, hit_a || hit_b);
+    if (hits && lane == __ffs(hits) - 1) {
+        *key_out = (int)(hit_a ? ka : kb);
+        *mass_out = hit_a ? me + ma : me + ma + mb;
+    }
+}
+
+// Table selection (all threads, after tab_count and a barrier).  Returns
+// false when the table is unusable (a wrapped counter: the caller runs the
+// radix selection); else the row's maximum, its non-finite flag and, when
+// the row is filtered and finite, the cut and the kept Q mass.  s_i: 9 ints,
+// s_u: 4 u64 of shared scratch (every slot written once per row).
+template <typename T>
+__device__ bool tab_select(unsigned int *tab, int V, float cdec, int tk, float tp, bool use_k, bool use_p,
+                           float &xmax_out, bool &bad_out, float &cut_out, unsigned long long &kept_out,
+                           unsigned int *s_wc, unsigned long long *s_wm, int *s_i, unsigned long long *s_u)
+{
+    const int t = threadIdx.x, lane = t & 31;
+    const unsigned int *mine = tab + tab_base(t);
+    if (t == 0) {  // -0 (pattern 0x8000) joins +0 (pattern 0)
+        const uint32_t nz = tab[0x4000] & 0xFFFFu, pz = tab[0] & 0xFFFFu;
+        s_i[0] = (nz + pz > 0xFFFFu) ? 1 : 0;  // would wrap
+        tab[0x4000] -= nz;
+        tab[0] += nz;
+        s_i[1] = -1;     // highest non-empty key
+        s_i[2] = 0;      // total count
+        s_i[3] = -1;     // thread holding the k-th largest key
+        s_i[5] = -1;     // the k-th largest key
+        s_i[6] = 65536;  // lowest non-empty key
+        s_i[7] = -1;     // thread holding the top-p boundary
+        s_i[8] = -1;     // the top-p boundary key
+    }
+    __syncthreads();
+    // pass 1: count, highest and lowest non-empty key (words read in an order
+    // rotated by the lane: no bank conflicts)
+    const uint32_t pbase = 2u * (uint32_t)tab_base(t);
+    uint32_t cl = 0;
+    int top = -1, bot = 65536;
+    for (int i = 0; i < 32; ++i) {
+        const int j = (i + lane) & 31;
+        const uint32_t x = mine[j];
+        if (x) {
+            const uint32_t n0 = x & 0xFFFFu, n1 = x >> 16;
+            cl += n0 + n1;
+            const uint32_t h = pbase + 2u * (uint32_t)j;
+            if (n0) {
+                const int k = (int)pat_key(h);
+                top = max(top, k);
+                bot = min(bot, k);
+            }
+            if (n1) {
+                const int k = (int)pat_key(h + 1u);
+                top = max(top, k);
+                bot = min(bot, k);
+            }
+        }
+    }
+    const uint32_t cw = __reduce_add_sync(0xFFFFFFFFu, cl);
+    top = __reduce_max_sync(0xFFFFFFFFu, top);
+    bot = __reduce_min_sync(0xFFFFFFFFu, bot);
+    if (lane == 0) {
+        atomicAdd(s_i + 2, (int)cw);
+        atomicMax(s_i + 1, top);
+        atomicMin(s_i + 6, bot);
+    }
+    __syncthreads();
+    if (s_i[0] || s_i[2] != V)
+        return false;  // a counter wrapped (or would have)
+    const uint32_t kmax = (uint32_t)s_i[1], kmin = (uint32_t)s_i[6];
+    const float xmax = Tab16<T>::value(key_pat(kmax));
+    xmax_out = xmax;
+    // +inf or a NaN at the top, a NaN at the bottom, or nothing above -inf
+    bad_out = kmax >= Tab16<T>::kPinfKey || kmin < Tab16<T>::kNinfKey || kmax <= Tab16<T>::kNinfKey;
+    if (bad_out || !(use_k || use_p))
+        return true;
+    // pass 2: Q masses, two values per word with paired weights
+    unsigned long long ml = 0;
+#pragma unroll 4
+    for (int i = 0; i < 32; ++i) {
+        const int j = (i + lane) & 31;
+        const uint32_t x = mine[j];
+        if (x) {
+            const uint32_t h = pbase + 2u * (uint32_t)j;
+            const float v0 = (x & 0xFFFFu) ? Tab16<T>::value(h) : xmax, v1 = (x >> 16) ? Tab16<T>::value(h + 1u) : xmax;
+            unsigned long long q0, q1;
+            q40_weight2(__fadd2_rn(make_float2(v0, v1), make_float2(-xmax, -xmax)), cdec, q0, q1);
+            ml += (unsigned long long)(x & 0xFFFFu) * q0 + (unsigned long long)(x >> 16) * q1;
+        }
+    }
+    uint32_t c_ex;
+    unsigned long long m_ex, m_tot;
+    tab_scan(cl, ml, c_ex, m_ex, m_tot, s_wc, s_wm);
+    // top-k: the key where the count from the top reaches tk (ties kept)
+    uint32_t kk = 0u;                  // lowest key top-k keeps
+    unsigned long long tot_p = m_tot;  // Q mass of the logits top-k keeps
+    int tck = 1024;                    // thread holding kk
+    if (use_k) {
+        const uint32_t need = (uint32_t)tk;
+        if (c_ex < need && need <= c_ex + cl) {  // exactly one thread
+            s_i[3] = t;
+            s_i[4] = (int)c_ex;
+            s_u[2] = m_ex;
+        }
+        __syncthreads();
+        tck = s_i[3];
+        if (t < 32)
+            tab_walk<T, true>(tab, tck, 0u, xmax, cdec, (uint32_t)s_i[4], need, s_u[2], 0.0, s_i + 5, s_u);
+        __syncthreads();
+        kk = (uint32_t)s_i[5];
+        tot_p = s_u[0];
+    }
+    if (!use_p) {
+        cut_out = Tab16<T>::value(key_pat(kk));
+        kept_out = tot_p;
+        return true;
+    }
+    // top-p among the keys >= kk: the first non-empty key from the top at
+    // which double(mass above + its mass) >= double(tp) * double(tot_p).  The
+    // running mass only grows, so that key lies in the one thread whose
+    // kept range holds a key, has double(mass above) < bound (or nothing
+    // non-empty above) and reaches the bound within the range.
+    const double bound = (double)tp * (double)tot_p;
+    if (t <= tck) {
+        const uint32_t cl_r = (t == tck) ? 1u : cl;  // thread tck keeps kk at least
+        const unsigned long long ml_r = (t == tck) ? tot_p - m_ex : ml;
+        if (cl_r > 0u && (c_ex == 0u || (double)m_ex < bound) && (double)(m_ex + ml_r) >= bound) {
+            s_i[7] = t;
+            s_u[3] = m_ex;
+        }
+    }
+    __syncthreads();
+    const int tcp = s_i[7];
+    if (tcp >= 0 && t < 32)
+        tab_walk<T, false>(tab, tcp, kk, xmax, cdec, 0u, 0u, s_u[3], bound, s_i + 8, s_u + 1);
+    __syncthreads();
+    if (s_i[8] < 0) {  // no key reached the bound: the lowest key kept
+        cut_out = Tab16<T>::value(key_pat(use_k ? kk : kmin));
+        kept_out = tot_p;
+    } else {
+        cut_out = Tab16<T>::value(key_pat((uint32_t)s_i[8]));
+        kept_out = s_u[1];
+    }
+    return true;
+}
+
+// One CTA of kTabThreads per target row of 16-bit logits, V >= kTabMinV;
+// dynamic shared memory: kTabSmem bytes (the table, or the radix
+// histograms when a counter wrapped)
+template <typename T>
+__global__ void __launch_bounds__(kTabThreads, 1) verify_filter_tab_kernel(VerifyArgs a)
+{
+    constexpr int NT = kTabThreads;
+    extern __shared__ __align__(16) unsigned int tab[];
+    __shared__ float s_f[4 * NT / 32];
+    __shared__ unsigned int s_wc[NT / 32];
+    __shared__ unsigned long long s_wm[NT / 32];
+    __shared__ FilterSel sel;
+    __shared__ int s_i[9];
+    __shared__ unsigned long long s_u[4];
+    __shared__ float s_m, s_s, s_xmax, s_cut;
+    __shared__ int s_bad, s_skip;
+    const float c = scale_of(a);
+    const Unit u = decode_unit(a);
+    const T *row = reinterpret_cast<const T *>(a.logits) + (size_t)u.row * a.V;
+    const int t = threadIdx.x;
+    if (t == 0) {
+        s_skip = (!u.needed || stopped_before(a.stop_enc, u.b, u.j)) ? 1 : 0;
+        s_cut = -INFINITY;
+    }
+    __syncthreads();
+    if (!s_skip) {
+        const int tk = a.top_k ? a.top_k[u.b] : 0;
+        const float tp = a.top_p ? a.top_p[u.b] : 1.0f;
+        const bool use_k = tk > 0 && tk < a.V, use_p = tp < 1.0f;
+        if (use_k || use_p) {
+            for (int i = t; i < kTabWords / 4; i += NT)
+                reinterpret_cast<uint4 *>(tab)[i] = make_uint4(0u, 0u, 0u, 0u);  // 8 stores per thread
+            __syncthreads();
+            tab_count<T>(row, a.V, tab);
+            if (t == 0)
+                s_skip = stopped_before(a.stop_enc, u.b, u.j) ? 1 : 0;
+            __syncthreads();
+            if (!s_skip) {
+                float xmax, cutv;
+                bool bad;
+                unsigned long long kept;
+                // block-uniform result (it derives from shared values only)
+                if (tab_select<T>(tab, a.V, a.dec_scale, tk, tp, use_k, use_p, xmax, bad, cutv, kept, s_wc, s_wm,
+                                  s_i, s_u)) {
+                    if (t == 0) {
+                        s_m = xmax * c;
+                        s_bad = bad ? 1 : 0;
+                        s_s = bad ? 0.0f : (float)((double)kept * 0x1p-40);
+                        s_cut = bad ? -INFINITY : cutv;
+                    }
+                } else {  // a counter wrapped: the radix selection on the same memory
+                    __syncthreads();
+                    const float xm = row_max_pass<T, NT>(row, a.V, s_f);
+                    const bool badm = !(xm > -INFINITY && xm < INFINITY);
+                    float cr = -INFINITY;
+                    unsigned long long km = 0ull;
+                    if (!badm)
+                        cr = radix_cut<T, NT>(row, a.V, xm, a.dec_scale, tk, tp, use_k, use_p,
+                                              *reinterpret_cast<FilterHist *>(tab), sel, s_wc, s_wm, km);
+                    if (t == 0) {
+                        s_m = xm * c;
+                        s_bad = badm ? 1 : 0;
+                        s_s = (float)((double)km * 0x1p-40);
+                        s_cut = cr;
+                    }
+                }
+            }
+        } else {
+            float m, s;
+            bool bad;
+            chunk_softmax_stats<T, true, NT>(row, 0, a.V, c, m, s, bad, s_f, StopProbe{a.stop_enc, u.b, u.j},
+                                             &s_xmax);
+            if (t == 0) {
+                s_m = m;
+                s_s = s;
+                s_bad = (bad || !(s > 0.0f) || !(s <= FLT_MAX)) ? 1 : 0;
+                s_skip = stopped_before(a.stop_enc, u.b, u.j) ? 1 : 0;
+            }
+        }
+        __syncthreads();
+    }
+    if (t >= 32)
+        return;
+    int eval = 0;
+    if (t == 0)
+        eval = (u.needed && !stopped_before(a.stop_enc, u.b, u.j)) ? 1 : 0;
+    if (eval)
+        sample_row_decide<T>(a, u, row, s_m, s_s, s_cut, s_bad != 0);
     sample_seq_finish(a, u);
 }
 
@@ -543,6 +955,20 @@ cudaError_t launch_filter_rows(const VerifyArgs &args, cudaStream_t st)
             return e;
     }
     const unsigned rows = (unsigned)(f.B * (f.k + 1)), sms = (unsigned)sm_count[dev & 63];
+    if constexpr (sizeof(T) == 2) {
+        if (f.V >= kTabMinV) {
+            static bool attr_set[64];
+            if (!attr_set[dev & 63]) {
+                e = cudaFuncSetAttribute(verify_filter_tab_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kTabSmem);
+                if (e != cudaSuccess)
+                    return e;
+                attr_set[dev & 63] = true;
+            }
+            verify_filter_tab_kernel<T><<<rows, kTabThreads, kTabSmem, st>>>(f);
+            return cudaGetLastError();
+        }
+    }
     if (rows <= sms)
         verify_filter_kernel<T, 1024><<<rows, 1024, 0, st>>>(f);
     else if (rows <= 2u * sms && f.top_k == nullptr)

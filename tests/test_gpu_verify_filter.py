@@ -139,6 +139,69 @@ def test_config5_shape_bf16():
           top_k=None, top_p=np.full(64, 0.95, np.float32))
 
 
+@pytest.mark.parametrize("V,dtype", [(32768, "bf16"), (50001, "f16"), (128256, "bf16"), (262144, "f16")])
+def test_table_form_16bit(V, dtype):
+    """16-bit rows of at least 32768 logits: the cut from the table of value
+    counts (mixed per-sequence settings, off values and extremes)."""
+    B = 48 if V <= 50001 else 16
+    rng = np.random.default_rng(V + 3)
+    x, q, d, u = sample_round_inputs(B, 3, V, 0.5, seed=V % 991, dtype=dtype)
+    tk, tp = _params(rng, B, V)
+    check(x, DT_OF[dtype], q, d, u, top_k=tk, top_p=tp)
+
+
+def _bits16(x):
+    return x.view(np.uint16) if x.dtype == np.float16 else x
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_table_form_ties_and_signed_zeros(dtype):
+    """Logits quantised to quarters (many tokens per value, -0 and +0 both
+    present and equal): the k-th value and the top-p boundary fall inside
+    groups of equal logits, some at zero."""
+    rng = np.random.default_rng(61)
+    B, k, V = 64, 3, 40000
+    x, q, d, u = sample_round_inputs(B, k, V, 0.5, seed=62, dtype=dtype)
+    xf = np.round(rng.standard_normal(x.shape).astype(np.float32) * 4) / 4
+    xf[xf == 0] = np.where(rng.random(np.count_nonzero(xf == 0)) < 0.5, -0.0, 0.0)
+    if dtype == "bf16":
+        xs = (xf.view(np.uint32) >> 16).astype(np.uint16)
+    else:
+        xs = xf.astype(np.float16)
+    assert (_bits16(xs) == 0x8000).any() and (_bits16(xs) == 0).any()
+    tk, tp = _params(rng, B, V)
+    check(xs, DT_OF[dtype], q, d, u, top_k=tk, top_p=tp)
+    check(xs, DT_OF[dtype], q, d, u, top_k=np.full(B, 5000, np.int32), top_p=np.full(B, 0.6, np.float32))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_table_form_counter_wrap_and_bad_rows(dtype):
+    """Rows where more than 65535 logits share one value (a 16-bit counter
+    wraps, or would when -0 joins +0): the row takes the radix selection and
+    matches all the same.  Rows with a NaN (either sign) or +inf are flagged."""
+    rng = np.random.default_rng(71)
+    B, k, V = 12, 2, 140000
+    x, q, d, u = sample_round_inputs(B, k, V, 0.5, seed=72, dtype=dtype)
+    xb = _bits16(x)
+    one = 0x3F80 if dtype == "bf16" else 0x3C00
+    pinf = 0x7F80 if dtype == "bf16" else 0x7C00
+    for b in range(0, B, 3):  # 70000 logits equal to 1.0 in every row of these sequences
+        for j in range(k + 1):
+            xb[b, j, rng.choice(V, 70000, replace=False)] = one
+    for b in range(1, B, 3):  # 40000 +0 and 30000 -0
+        for j in range(k + 1):
+            idx = rng.choice(V, 70000, replace=False)
+            xb[b, j, idx[:40000]] = 0x0000
+            xb[b, j, idx[40000:]] = 0x8000
+    xb[2, 0, 17] = 0xFFC1 if dtype == "bf16" else 0xFE01   # negative NaN
+    xb[5, 1, 99] = pinf                                     # +inf
+    xb[8, 0, 1234] = 0x7FC1 if dtype == "bf16" else 0x7E01  # positive NaN
+    d[2, 0] = d[2, 0] if d[2, 0] != 17 else 18
+    tk = rng.choice([0, 3, 80000, V - 1], size=B).astype(np.int32)
+    tp = rng.choice([0.5, 0.9, 0.99, 1.0], size=B).astype(np.float32)
+    check(x, DT_OF[dtype], q, d, u, top_k=tk, top_p=tp)
+
+
 def test_zz_filter_statistics():
     assert STATS.get("kept_sets", 0) > 500, STATS
     assert STATS["boundary"] < 1e-4 * max(STATS["decisions"], 1) + 1, STATS
