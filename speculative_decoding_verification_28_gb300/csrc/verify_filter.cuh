@@ -622,7 +622,9 @@ __device__ __forceinline__ void tab_count(const T *row, int V, unsigned int *tab
 }
 
 // Block-wide exclusive prefix (thread order) of a count and a mass, with the
-// mass total; ends with a barrier.  s_wc / s_wm: one slot per warp.
+// mass total; ends with a barrier.  s_wc: one slot per warp, s_wm: one per
+// warp and the total (warp 0 turns the warp totals into their exclusive
+// prefix by shuffles).
 __device__ __forceinline__ void tab_scan(uint32_t c, unsigned long long m, uint32_t &c_ex, unsigned long long &m_ex,
                                          unsigned long long &m_tot, unsigned int *s_wc, unsigned long long *s_wm)
 {
@@ -644,16 +646,31 @@ __device__ __forceinline__ void tab_scan(uint32_t c, unsigned long long m, uint3
         s_wm[w] = im;
     }
     __syncthreads();
-    c_ex = ic - c;
-    m_ex = im - m;
-    m_tot = 0;
-    for (int i = 0; i < kTabThreads / 32; ++i) {
-        if (i < w) {
-            c_ex += s_wc[i];
-            m_ex += s_wm[i];
+    static_assert(kTabThreads == 1024, "one warp total per lane of warp 0");
+    if (w == 0) {  // inclusive prefix of the 32 warp totals, stored exclusive
+        uint32_t wc = s_wc[lane];
+        unsigned long long wm = s_wm[lane];
+        const uint32_t wc0 = wc;
+        const unsigned long long wm0 = wm;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t oc = __shfl_up_sync(0xFFFFFFFFu, wc, o);
+            const unsigned long long om = __shfl_up_sync(0xFFFFFFFFu, wm, o);
+            if (lane >= o) {
+                wc += oc;
+                wm += om;
+            }
         }
-        m_tot += s_wm[i];
+        __syncwarp();
+        s_wc[lane] = wc - wc0;
+        s_wm[lane] = wm - wm0;
+        if (lane == 31)
+            s_wm[32] = wm;  // the block total
     }
+    __syncthreads();
+    c_ex = ic - c + s_wc[w];
+    m_ex = im - m + s_wm[w];
+    m_tot = s_wm[32];
 }
 
 // Warp 0 (all lanes): walks the 64 keys of thread tc in descending order,
@@ -736,24 +753,16 @@ __device__ bool tab_select(unsigned int *tab, int V, float cdec, int tk, float t
     const uint32_t pbase = 2u * (uint32_t)tab_base(t);
     uint32_t cl = 0;
     int top = -1, bot = 65536;
-    for (int i = 0; i < 32; ++i) {
+#pragma unroll 8
+    for (int i = 0; i < 32; ++i) {  // branch-free: the loads and tests overlap
         const int j = (i + lane) & 31;
         const uint32_t x = mine[j];
-        if (x) {
-            const uint32_t n0 = x & 0xFFFFu, n1 = x >> 16;
-            cl += n0 + n1;
-            const uint32_t h = pbase + 2u * (uint32_t)j;
-            if (n0) {
-                const int k = (int)pat_key(h);
-                top = max(top, k);
-                bot = min(bot, k);
-            }
-            if (n1) {
-                const int k = (int)pat_key(h + 1u);
-                top = max(top, k);
-                bot = min(bot, k);
-            }
-        }
+        const uint32_t n0 = x & 0xFFFFu, n1 = x >> 16;
+        cl += n0 + n1;
+        const uint32_t h = pbase + 2u * (uint32_t)j;
+        const int k0 = (int)pat_key(h), k1 = (int)pat_key(h + 1u);
+        top = max(top, max(n0 ? k0 : -1, n1 ? k1 : -1));
+        bot = min(bot, min(n0 ? k0 : 65536, n1 ? k1 : 65536));
     }
     const uint32_t cw = __reduce_add_sync(0xFFFFFFFFu, cl);
     top = __reduce_max_sync(0xFFFFFFFFu, top);
@@ -773,13 +782,14 @@ __device__ bool tab_select(unsigned int *tab, int V, float cdec, int tk, float t
     bad_out = kmax >= Tab16<T>::kPinfKey || kmin < Tab16<T>::kNinfKey || kmax <= Tab16<T>::kNinfKey;
     if (bad_out || !(use_k || use_p))
         return true;
-    // pass 2: Q masses, two values per word with paired weights
+    // pass 2: Q masses, two values per word with paired weights (warps
+    // whose keys are all empty skip it)
     unsigned long long ml = 0;
-#pragma unroll 4
-    for (int i = 0; i < 32; ++i) {
-        const int j = (i + lane) & 31;
-        const uint32_t x = mine[j];
-        if (x) {
+    if (__any_sync(0xFFFFFFFFu, cl != 0u)) {
+#pragma unroll 8
+        for (int i = 0; i < 32; ++i) {  // branch-free: independent weights overlap
+            const int j = (i + lane) & 31;
+            const uint32_t x = mine[j];
             const uint32_t h = pbase + 2u * (uint32_t)j;
             const float v0 = (x & 0xFFFFu) ? Tab16<T>::value(h) : xmax, v1 = (x >> 16) ? Tab16<T>::value(h + 1u) : xmax;
             unsigned long long q0, q1;
@@ -853,7 +863,7 @@ __global__ void __launch_bounds__(kTabThreads, 1) verify_filter_tab_kernel(Verif
     extern __shared__ __align__(16) unsigned int tab[];
     __shared__ float s_f[4 * NT / 32];
     __shared__ unsigned int s_wc[NT / 32];
-    __shared__ unsigned long long s_wm[NT / 32];
+    __shared__ unsigned long long s_wm[NT / 32 + 1];
     __shared__ FilterSel sel;
     __shared__ int s_i[9];
     __shared__ unsigned long long s_u[4];
