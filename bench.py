@@ -506,7 +506,8 @@ def run_ours(args, c, rank, local_rank, world):
                    "parallelism": f"independent batch per GPU x{world}"},
         "roofline": roofline,
         "verify_roofline": {"bound": "hbm", "kernels": ("verify_greedy_kernel" if c["mode"] == "greedy" else
-                                                        ("verify_filter_kernel" if R.filtered() else
+                                                        (("verify_filter_tab_kernel" if c["logit_dtype"] != "f32" and c["V"] >= 32768
+                                                          else "verify_filter_kernel") if R.filtered() else
                                                          "verify_stats_kernel") + " + verify_draw_sums_kernel + verify_draw_pick_kernel"),
                             "achieved": round(float(np.sum(verify_bytes) / (per[:, 1].sum() / 1e3) / 1e9), 1),
                             "peak": peak, "unit": "GB/s",
