@@ -112,10 +112,26 @@ __device__ __forceinline__ unsigned long long q40_weight(float d, float c)
     return __float2ull_rz(__fmul_rn(p, scale));
 }
 
+// floor(p * 2^(i + 40)) for p in [0.5, 2) and i in [-65, 0] from integer
+// instructions only: the product is exact (a power-of-two scale of a normal
+// float), so it is p's 24-bit significand shifted by the product's exponent
+__device__ __forceinline__ unsigned long long q40_bits(float p, int i)
+{
+    const uint32_t b = __float_as_uint(p);
+    const uint32_t m = (b & 0x7FFFFFu) | 0x800000u;
+    const int s = (int)(b >> 23) - 127 + i + 40 - 23;  // weight of the significand's lowest bit
+    if (s >= 0)
+        return (unsigned long long)m << s;
+    return s > -24 ? (unsigned long long)(m >> -s) : 0ull;
+}
+
 // q40_weight of two logits at once with paired fp32 instructions (FMUL2,
 // FADD2, FFMA2; every lane rounded to nearest, so each result is bit for bit
 // q40_weight's).  t is clamped at -65 before the integer scale is formed, so
 // an out-of-range t never reaches the conversion; such a t gives 0 anyway.
+// kBits: the last step by q40_bits instead of the float product and its
+// conversion to 64 bits (same result; no conversion unit).
+template <bool kBits = false>
 __device__ __forceinline__ void q40_weight2(float2 d, float c, unsigned long long &q0, unsigned long long &q1)
 {
     const float2 t = __fmul2_rn(d, make_float2(c, c));
@@ -129,10 +145,15 @@ __device__ __forceinline__ void q40_weight2(float2 d, float c, unsigned long lon
     p = __ffma2_rn(p, f, make_float2(0x1.ebfbe0p-3f, 0x1.ebfbe0p-3f));
     p = __ffma2_rn(p, f, make_float2(0x1.62e430p-1f, 0x1.62e430p-1f));
     p = __ffma2_rn(p, f, make_float2(1.0f, 1.0f));
-    const float2 sc = make_float2(__int_as_float(((int)i0 + 40 + 127) << 23), __int_as_float(((int)i1 + 40 + 127) << 23));
-    const float2 r = __fmul2_rn(p, sc);
-    q0 = (t.x >= -64.0f) ? __float2ull_rz(r.x) : 0ull;
-    q1 = (t.y >= -64.0f) ? __float2ull_rz(r.y) : 0ull;
+    if constexpr (kBits) {
+        q0 = (t.x >= -64.0f) ? q40_bits(p.x, (int)i0) : 0ull;
+        q1 = (t.y >= -64.0f) ? q40_bits(p.y, (int)i1) : 0ull;
+    } else {
+        const float2 sc = make_float2(__int_as_float(((int)i0 + 40 + 127) << 23), __int_as_float(((int)i1 + 40 + 127) << 23));
+        const float2 r = __fmul2_rn(p, sc);
+        q0 = (t.x >= -64.0f) ? __float2ull_rz(r.x) : 0ull;
+        q1 = (t.y >= -64.0f) ? __float2ull_rz(r.y) : 0ull;
+    }
 }
 
 // f(x) for every logit of the row: 16-byte vectors, scalar head and tail
@@ -673,15 +694,35 @@ __device__ __forceinline__ void tab_scan(uint32_t c, unsigned long long m, uint3
     m_tot = s_wm[32];
 }
 
+// The smallest integer A with double(A) >= bound (0 < bound < 2^63), so that
+// double(A) >= bound becomes A >= threshold.  floor(bound) lies within one
+// ulp of bound (at most 2^10 above 2^53), and rounding is monotonic: a
+// binary search over [floor - 1024, floor + 1].
+__device__ __forceinline__ unsigned long long u64_threshold(double bound)
+{
+    if (!(bound > 0.0))
+        return 0ull;
+    const unsigned long long a = (unsigned long long)bound;
+    unsigned long long lo = a > 1024ull ? a - 1024ull : 0ull, hi = a + 1ull;
+    while (lo < hi) {
+        const unsigned long long mid = lo + (hi - lo) / 2;
+        if ((double)mid >= bound)
+            hi = mid;
+        else
+            lo = mid + 1ull;
+    }
+    return hi;
+}
+
 // Warp 0 (all lanes): walks the 64 keys of thread tc in descending order,
 // lane l taking ranks 2 l and 2 l + 1 (one table word).  Keys below kk count
 // as empty.  Finds the first non-empty key where the running count from the
 // top (c0 + counts) reaches `need` (kCount) or the running mass (m0 +
-// masses) reaches `bound` as a double; writes that key and the running mass
+// masses) reaches the threshold `athr`; writes that key and the running mass
 // at it to *key_out / *mass_out (untouched when there is none).
 template <typename T, bool kCount>
 __device__ __forceinline__ void tab_walk(const unsigned int *tab, int tc, uint32_t kk, float xmax, float cdec,
-                                         uint32_t c0, uint32_t need, unsigned long long m0, double bound,
+                                         uint32_t c0, uint32_t need, unsigned long long m0, unsigned long long athr,
                                          int *key_out, unsigned long long *mass_out)
 {
     const int lane = threadIdx.x & 31;
@@ -692,7 +733,7 @@ __device__ __forceinline__ void tab_walk(const unsigned int *tab, int tc, uint32
     // an empty key's weight is not needed: x_max stands in (no inf or NaN)
     const float va = na ? Tab16<T>::value(ha) : xmax, vb = nb ? Tab16<T>::value(hb) : xmax;
     unsigned long long qa, qb;
-    q40_weight2(__fadd2_rn(make_float2(va, vb), make_float2(-xmax, -xmax)), cdec, qa, qb);
+    q40_weight2<true>(__fadd2_rn(make_float2(va, vb), make_float2(-xmax, -xmax)), cdec, qa, qb);
     const unsigned long long ma = (unsigned long long)na * qa, mb = (unsigned long long)nb * qb;
     uint32_t ic = na + nb;
     unsigned long long im = ma + mb;
@@ -712,8 +753,8 @@ __device__ __forceinline__ void tab_walk(const unsigned int *tab, int tc, uint32
         hit_a = na > 0u && ce + na >= need;
         hit_b = nb > 0u && ce + na + nb >= need;
     } else {
-        hit_a = na > 0u && (double)(me + ma) >= bound;
-        hit_b = nb > 0u && (double)(me + ma + mb) >= bound;
+        hit_a = na > 0u && me + ma >= athr;
+        hit_b = nb > 0u && me + ma + mb >= athr;
     }
     const unsigned hits = __ballot_sync(0xFFFFFFFFu, hit_a || hit_b);
     if (hits && lane == __ffs(hits) - 1) {
@@ -726,7 +767,7 @@ __device__ __forceinline__ void tab_walk(const unsigned int *tab, int tc, uint32
 // false when the table is unusable (a wrapped counter: the caller runs the
 // radix selection); else the row's maximum, its non-finite flag and, when
 // the row is filtered and finite, the cut and the kept Q mass.  s_i: 9 ints,
-// s_u: 4 u64 of shared scratch (every slot written once per row).
+// s_u: 5 u64 of shared scratch (every slot written once per row).
 template <typename T>
 __device__ bool tab_select(unsigned int *tab, int V, float cdec, int tk, float tp, bool use_k, bool use_p,
                            float &xmax_out, bool &bad_out, float &cut_out, unsigned long long &kept_out,
@@ -793,7 +834,7 @@ __device__ bool tab_select(unsigned int *tab, int V, float cdec, int tk, float t
             const uint32_t h = pbase + 2u * (uint32_t)j;
             const float v0 = (x & 0xFFFFu) ? Tab16<T>::value(h) : xmax, v1 = (x >> 16) ? Tab16<T>::value(h + 1u) : xmax;
             unsigned long long q0, q1;
-            q40_weight2(__fadd2_rn(make_float2(v0, v1), make_float2(-xmax, -xmax)), cdec, q0, q1);
+            q40_weight2<true>(__fadd2_rn(make_float2(v0, v1), make_float2(-xmax, -xmax)), cdec, q0, q1);
             ml += (unsigned long long)(x & 0xFFFFu) * q0 + (unsigned long long)(x >> 16) * q1;
         }
     }
@@ -814,7 +855,7 @@ __device__ bool tab_select(unsigned int *tab, int V, float cdec, int tk, float t
         __syncthreads();
         tck = s_i[3];
         if (t < 32)
-            tab_walk<T, true>(tab, tck, 0u, xmax, cdec, (uint32_t)s_i[4], need, s_u[2], 0.0, s_i + 5, s_u);
+            tab_walk<T, true>(tab, tck, 0u, xmax, cdec, (uint32_t)s_i[4], need, s_u[2], 0ull, s_i + 5, s_u);
         __syncthreads();
         kk = (uint32_t)s_i[5];
         tot_p = s_u[0];
@@ -827,13 +868,16 @@ __device__ bool tab_select(unsigned int *tab, int V, float cdec, int tk, float t
     // top-p among the keys >= kk: the first non-empty key from the top at
     // which double(mass above + its mass) >= double(tp) * double(tot_p).  The
     // running mass only grows, so that key lies in the one thread whose
-    // kept range holds a key, has double(mass above) < bound (or nothing
+    // kept range holds a key, has its mass above below the bound (or nothing
     // non-empty above) and reaches the bound within the range.
-    const double bound = (double)tp * (double)tot_p;
+    if (t == 0)  // double(A) >= double(tp) * double(tot_p) as an integer test
+        s_u[4] = u64_threshold((double)tp * (double)tot_p);
+    __syncthreads();
+    const unsigned long long athr = s_u[4];
     if (t <= tck) {
         const uint32_t cl_r = (t == tck) ? 1u : cl;  // thread tck keeps kk at least
         const unsigned long long ml_r = (t == tck) ? tot_p - m_ex : ml;
-        if (cl_r > 0u && (c_ex == 0u || (double)m_ex < bound) && (double)(m_ex + ml_r) >= bound) {
+        if (cl_r > 0u && (c_ex == 0u || m_ex < athr) && m_ex + ml_r >= athr) {
             s_i[7] = t;
             s_u[3] = m_ex;
         }
@@ -841,7 +885,7 @@ __device__ bool tab_select(unsigned int *tab, int V, float cdec, int tk, float t
     __syncthreads();
     const int tcp = s_i[7];
     if (tcp >= 0 && t < 32)
-        tab_walk<T, false>(tab, tcp, kk, xmax, cdec, 0u, 0u, s_u[3], bound, s_i + 8, s_u + 1);
+        tab_walk<T, false>(tab, tcp, kk, xmax, cdec, 0u, 0u, s_u[3], athr, s_i + 8, s_u + 1);
     __syncthreads();
     if (s_i[8] < 0) {  // no key reached the bound: the lowest key kept
         cut_out = Tab16<T>::value(key_pat(use_k ? kk : kmin));
@@ -866,7 +910,7 @@ __global__ void __launch_bounds__(kTabThreads, 1) verify_filter_tab_kernel(Verif
     __shared__ unsigned long long s_wm[NT / 32 + 1];
     __shared__ FilterSel sel;
     __shared__ int s_i[9];
-    __shared__ unsigned long long s_u[4];
+    __shared__ unsigned long long s_u[5];
     __shared__ float s_m, s_s, s_xmax, s_cut;
     __shared__ int s_bad, s_skip;
     const float c = scale_of(a);
