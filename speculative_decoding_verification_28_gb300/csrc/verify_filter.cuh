@@ -20,9 +20,12 @@
 // reproducible; the kept token probabilities use the same ex2-based softmax
 // as the unfiltered path.
 //
-// One CTA per target row (rows j-major, skipped once an earlier stop of the
-// sequence is known, as in the statistics kernel); 1024 threads when the
-// batch has at most two rows per SM, else 256.  Pass 1 reads the row from
+// Two kernels, one CTA per target row each (rows j-major, skipped once an
+// earlier stop of the sequence is known, as in the statistics kernel).
+// 16-bit rows of at least kTabMinV logits take the table form further down
+// (a count per bit pattern, one weight per distinct value).  Every other row
+// takes the radix form: 1024, 512 or 256 threads by the number of rows
+// (launch_filter_rows).  Its pass 1 reads the row from
 // HBM: its maximum when the row is filtered (the kept sum then comes from the
 // Q masses), else the softmax statistics.  The cuts are radix selections on
 // an order-preserving 32-bit key of the logit, 11-bit digits (two levels for
@@ -31,9 +34,10 @@
 // per-digit counts and Q masses in shared memory (32-bit atomics on three
 // parts of each mass), then a block scan from the top digit finds the digit
 // holding the k-th largest key (counts) or the top-p boundary (masses).
-// Roofline: HBM reads V * sizeof(T) per needed row; the later passes are L2
-// reads, a fixed-point weight per logit and shared-memory atomics, which
-// make the kernel instruction-bound.
+// Roofline: HBM reads V * sizeof(T) per needed row; the radix form's later
+// passes are L2 reads, a fixed-point weight per logit and shared-memory
+// atomics, which make it instruction-bound; the table form is bound by its
+// one shared atomic per logit and by the selection's latency.
 #pragma once
 
 #include <type_traits>
