@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--batch", type=int, default=None, help="c4x: sequences gathered per round (default: 64)")
     ap.add_argument("--top-k", type=int, default=None, help="stochastic workloads: top-k on the target distribution")
     ap.add_argument("--top-p", type=float, default=None, help="stochastic workloads: top-p on the target distribution")
+    ap.add_argument("--logit-dtype", choices=["bf16", "f32"], default=None,
+                    help="override the workload's logits storage type (a variant, not a configured workload)")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the cache's layer count (small profiling captures only)")
     return ap.parse_args()
@@ -80,6 +82,8 @@ def workload_params(args):
         c["k"] = args.k
     if args.layers:
         c["L"] = args.layers
+    if args.logit_dtype:
+        c["logit_dtype"] = args.logit_dtype
     c["draft"] = tuple(int(x) for x in args.draft_cache.split(",")) if args.draft_cache else None
     c["top_k"], c["top_p"] = args.top_k, args.top_p
     if (args.top_k is not None or args.top_p is not None) and c["mode"] != "sample":
