@@ -15,6 +15,7 @@ step 1) without defining the transforms.  Pinned here:
   - the committed token's distribution equals the processed distribution
     (midpoint grid over the uniforms), and acceptance = sum min(p', q);
   - the fixed-point weight of the nucleus decision against 2^t;
+  - -0 and +0 are one value at the cut, in every storage type;
   - five planted mistakes each fail at least one of these.
 """
 from fractions import Fraction
@@ -95,6 +96,37 @@ def test_brute_force_tiny_rows():
         assert list(p > 0) == keep, (x, top_k, top_p, p)
         w = np.where(keep, 2.0 ** x.astype(np.float64), 0.0)
         assert np.allclose(p, w / w.sum(), atol=1e-7)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
+def test_signed_zeros_are_one_value(dt):
+    """-0 and +0 are one logit value: neither is strictly larger than the
+    other, so top-k and top-p keep both or neither (brute force on tiny rows
+    drawn from {-2, -1, -0, +0, 1}, in each storage type)."""
+    rng = np.random.default_rng(19)
+    vals = np.array([-2.0, -1.0, -0.0, 0.0, 1.0], np.float32)
+    code = {"f32": DT_F32, "bf16": oracle.DT_BF16, "f16": oracle.DT_F16}[dt]
+    both = 0
+    for _ in range(1500):
+        V = int(rng.integers(2, 8))
+        x = vals[rng.integers(0, 5, size=V)]
+        top_k = int(rng.integers(0, V + 1))
+        top_p = float(np.float32(rng.choice([1.0, 0.0, rng.integers(1, 16) / 16, rng.random()])))
+        if dt == "bf16":
+            xs = (x.view(np.uint32) >> 16).astype(np.uint16)
+        elif dt == "f16":
+            xs = x.astype(np.float16)
+        else:
+            xs = x
+        p, bad = oracle.softmax_row(xs[None], code, 0, T_UNIT, top_k, top_p)
+        keep = _brute_kept(list(x), top_k, top_p)
+        assert not bad
+        assert list(p > 0) == keep, (x, top_k, top_p, p)
+        zs = np.flatnonzero(x == 0)
+        if np.signbit(x[zs]).any() and not np.signbit(x[zs]).all():
+            both += 1
+            assert len(set((p[zs] > 0).tolist())) == 1
+    assert both > 300  # rows holding both zeros were drawn
 
 
 def _round_inputs(rng, B, k, V, sigma=2.0):
