@@ -249,3 +249,20 @@ def test_negative_infinity_is_a_masked_token():
     x[0, 0, :] = -np.inf
     _, bad = oracle.softmax_row(x[0], DT_F32, 0)
     assert bad
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_sixteen_bit_nan_of_either_sign_is_undefined(dt):
+    """In 16-bit storage a NaN of either sign, or +inf, makes the row's
+    distribution undefined, filtered or not; -inf alone does not."""
+    code = {"bf16": oracle.DT_BF16, "f16": oracle.DT_F16}[dt]
+    pats = {"bf16": dict(pnan=0x7FC1, nnan=0xFFC1, pinf=0x7F80, ninf=0xFF80, one=0x3F80),
+            "f16": dict(pnan=0x7E01, nnan=0xFE01, pinf=0x7C00, ninf=0xFC00, one=0x3C00)}[dt]
+    for kind, expect_bad in (("pnan", True), ("nnan", True), ("pinf", True), ("ninf", False)):
+        row = np.full((1, 8), pats["one"], np.uint16)
+        row[0, 3] = 0  # a smaller logit, so filters have something to cut
+        row[0, 5] = pats[kind]
+        xs = row if dt == "bf16" else row.view(np.float16)
+        for top_k, top_p in ((0, 1.0), (2, 1.0), (0, 0.5), (3, 0.9)):
+            _, bad = oracle.softmax_row(xs, code, 0, 1.0, top_k, top_p)
+            assert bad == expect_bad, (kind, top_k, top_p)
