@@ -35,6 +35,7 @@ MUTANTS = {
     "ratio_unfiltered": 13,
     "resid_unfiltered": 14,
     "topp_first": 15,
+    "zero_sign_order": 16,
 }
 
 _lock = threading.Lock()

@@ -27,6 +27,7 @@
  * parity is UNPINNED by the pages (it is only checked against an independent
  * brute-force restatement of the same policy).
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -111,7 +112,8 @@ enum {
     MUT_TOPP_BELOW = 12,      /* nucleus = largest top set of mass <= top_p */
     MUT_RATIO_UNFILTERED = 13,/* ratio test on p before the transforms      */
     MUT_RESID_UNFILTERED = 14,/* residual built from p before the transforms*/
-    MUT_TOPP_FIRST = 15       /* top-p applied before top-k                 */
+    MUT_TOPP_FIRST = 15,      /* top-p applied before top-k                 */
+    MUT_ZERO_SIGN_ORDER = 16  /* cut compares -0 as smaller than +0         */
 };
 static int g_mutant = MUT_NONE;
 void oracle_set_mutant(int m) { g_mutant = m; }
@@ -308,6 +310,13 @@ static int cmp_desc(const void *a, const void *b)
     return (p->v > q->v) - (p->v < q->v);
 }
 
+/* the value the cut compares: the logit itself (the planted mistake orders
+   -0 below +0, as a comparison of bit patterns would) */
+static double cut_value(double x)
+{
+    return (g_mutant == MUT_ZERO_SIGN_ORDER && x == 0.0 && signbit(x)) ? -DBL_MIN : x;
+}
+
 /* Smallest kept logit (the keep test is x >= cut) of a row after top-k and
    top-p; -inf when nothing is filtered.  vals is scratch of V entries. */
 static double filter_cut(const void *x, int dtype, int64_t off, int V, float T, int top_k, float top_p,
@@ -318,7 +327,7 @@ static double filter_cut(const void *x, int dtype, int64_t off, int V, float T, 
     if (!use_k && !use_p)
         return -INFINITY;
     for (int v = 0; v < V; ++v) {
-        vals[v].x = logit_at(x, dtype, off + v);
+        vals[v].x = cut_value(logit_at(x, dtype, off + v));
         vals[v].v = v;
     }
     qsort(vals, (size_t)V, sizeof *vals, cmp_desc);
@@ -382,7 +391,7 @@ static int processed_row(const void *x, int dtype, int64_t off, int V, double T,
         return 0;
     double s = 0.0;
     for (int v = 0; v < V; ++v) {
-        if (!(logit_at(x, dtype, off + v) >= cut))
+        if (!(cut_value(logit_at(x, dtype, off + v)) >= cut))
             p[v] = 0.0;
         s += p[v];
     }

@@ -16,7 +16,7 @@ step 1) without defining the transforms.  Pinned here:
     (midpoint grid over the uniforms), and acceptance = sum min(p', q);
   - the fixed-point weight of the nucleus decision against 2^t;
   - -0 and +0 are one value at the cut, in every storage type;
-  - five planted mistakes each fail at least one of these.
+  - six planted mistakes each fail at least one of these.
 """
 from fractions import Fraction
 
@@ -210,9 +210,10 @@ def test_q40_weight_against_powers_of_two():
 
 
 @pytest.mark.parametrize("mut", ["topk_strict", "topp_below", "ratio_unfiltered", "resid_unfiltered",
-                                 "topp_first"])
+                                 "topp_first", "zero_sign_order"])
 def test_planted_mistakes_fail_a_pin(mut):
     checks = [test_worked_example, test_top_k_one_is_greedy, test_brute_force_tiny_rows,
+              lambda: test_signed_zeros_are_one_value("bf16"),
               lambda: [test_output_distribution_is_the_processed_target(n)
                        for n in ("k2", "k3", "p0625", "p0875", "k3p05625")]]
     failed = 0
