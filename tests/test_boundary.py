@@ -154,6 +154,37 @@ def test_product_path_has_no_fallback():
         _lib.LIB_PATH, _lib._lib = saved
 
 
+def test_host_tensors_are_refused_not_computed():
+    """Every entry point of the binding refuses CPU tensors before any call:
+    there is no host path to fall back to."""
+    import torch
+
+    import speculative_decoding_verification_28_gb300 as sv
+
+    x = torch.zeros((2, 3, 64), dtype=torch.float32)
+    d = torch.zeros((2, 2), dtype=torch.int32)
+    q = torch.full((2, 2, 64), 1.0 / 64)
+    u = torch.zeros((2, 3))
+    kv = torch.zeros((1, 2, 2, 1, 16, 8))
+    ln = torch.tensor([3, 5], dtype=torch.int32)
+    pad = torch.tensor([2, 0], dtype=torch.int32)
+    ne = torch.tensor([1, 2], dtype=torch.int32)
+    pos = torch.zeros((2, 16), dtype=torch.int32)
+    mask = torch.zeros((2, 16), dtype=torch.uint8)
+    pool_len = torch.tensor([3, 5, 4], dtype=torch.int32)
+    idx = torch.tensor([0, 2], dtype=torch.int32)
+    calls = [lambda: sv.spec_verify_greedy(x, d),
+             lambda: sv.spec_verify_sample(x, q, d, u),
+             lambda: sv.spec_verify_sample_filtered(x, q, d, u, top_k=5, top_p=0.9),
+             lambda: sv.spec_realign_kv(kv, ln, pad, ne),
+             lambda: sv.spec_rebuild_pos_mask(pad, pos, mask),
+             lambda: sv.spec_group_by_length(pool_len, 2),
+             lambda: sv.spec_commit_ragged(pool_len, idx, ne, 16)]
+    for call in calls:
+        with pytest.raises(ValueError, match="CUDA"):
+            call()
+
+
 def test_static_entry_point_rejects_oversized_batches_before_any_launch(lib):
     """The allocation-free variant has a fixed scratch: sizes beyond it are a
     clear error (-6) found on the host."""
