@@ -286,9 +286,11 @@ SPEC_API int spec_group_by_length(int N, const int32_t *len, const uint8_t *acti
  * scratch (spec_workspace_bytes(B, k, V)) exceeds SPEC_STATIC_SCRATCH_BYTES
  * are rejected with SPEC_ESCRATCH before anything is launched.
  *
- * The first call on each device looks up the device address of the array
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  Every call also clears the array's counters
+ * The array used is the current device's: cuda_stream must belong to the
+ * current device (or be a default stream), else SPEC_EINVAL is returned and
+ * nothing is enqueued.  The first call on each device looks up the device
+ * address of the array (cudaGetSymbolAddress, with that device current);
+ * make that first call before any stream capture.  Every call also clears the array's counters
  * with an asynchronous memset on the caller's stream.  All calls on a device
  * share the one array and it keeps the last call's contents, so calls that
  * overlap on the GPU (different streams without ordering) race: order them.

@@ -89,9 +89,11 @@ __global__ void fill_kernel(void *kv, int elt, Shape sh, const int32_t *tokens, 
 }
 
 // the synthetic forward's KV write for the k+1 query slots W-1 .. W+k1-2
+// (W from the host, or read on the device from W_dev when it is given)
 __global__ void write_query_kernel(void *kv, int elt, Shape sh, const int32_t *qtok, int k1, const int32_t *pos,
-                                   int W)
+                                   int W_host, const int32_t *W_dev)
 {
+    const int W = W_dev ? *W_dev : W_host;
     const long long rows = (long long)sh.L * 2 * sh.B * sh.H * k1;
     const int lane = threadIdx.x & 31;
     const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
@@ -204,7 +206,18 @@ int specgen_kv_write_query(void *kv, int elt, int L, int B, int H, int S, int D,
 {
     Shape sh{L, B, H, S, D};
     write_query_kernel<<<grid_for((long long)L * 2 * B * H * k1), 256, 0, (cudaStream_t)stream>>>(kv, elt, sh, qtok,
-                                                                                                 k1, pos, W);
+                                                                                                 k1, pos, W, nullptr);
+    return (int)cudaGetLastError();
+}
+
+// as specgen_kv_write_query, with the width read on the device (no host
+// round trip between a round and the next forward)
+int specgen_kv_write_query_dev(void *kv, int elt, int L, int B, int H, int S, int D, const int32_t *qtok, int k1,
+                               const int32_t *pos, const int32_t *W_dev, void *stream)
+{
+    Shape sh{L, B, H, S, D};
+    write_query_kernel<<<grid_for((long long)L * 2 * B * H * k1), 256, 0, (cudaStream_t)stream>>>(kv, elt, sh, qtok,
+                                                                                                 k1, pos, 0, W_dev);
     return (int)cudaGetLastError();
 }
 

@@ -38,8 +38,9 @@ def _load():
         lib.specgen_kv_write_query.argtypes = [vp, i, i, i, i, i, i, vp, i, vp, i, vp]
         lib.specgen_kv_check.argtypes = [vp, i, i, i, i, i, i, vp, vp, vp, vp, vp]
         lib.specgen_kv_write_query_pool.argtypes = [vp, i, i, i, i, i, i, vp, i, i, vp, vp, vp]
+        lib.specgen_kv_write_query_dev.argtypes = [vp, i, i, i, i, i, i, vp, i, vp, vp, vp]
         for f in (lib.specgen_kv_fill, lib.specgen_kv_write_query, lib.specgen_kv_check,
-                  lib.specgen_kv_write_query_pool):
+                  lib.specgen_kv_write_query_pool, lib.specgen_kv_write_query_dev):
             f.restype = i
         _lib = lib
     return _lib
@@ -68,6 +69,24 @@ def kv_write_query(kv, qtok, pos, W):
     L, _, B, H, S, D = kv.shape
     rc = _load().specgen_kv_write_query(_p(kv), _ELT[kv.dtype], L, B, H, S, D, _p(qtok), qtok.shape[1], _p(pos),
                                         int(W), _s())
+    assert rc == 0, rc
+
+
+def kv_write_query_dev(kv, qtok, pos, W):
+    """kv_write_query with the width W a [1] int32 device tensor (read on the
+    device: nothing waits for the host)."""
+    L, _, B, H, S, D = kv.shape
+    rc = _load().specgen_kv_write_query_dev(_p(kv), _ELT[kv.dtype], L, B, H, S, D, _p(qtok), qtok.shape[1], _p(pos),
+                                            _p(W), _s())
+    assert rc == 0, rc
+
+
+def kv_check_async(kv, tokens, pad_new, len_new, bad):
+    """Adds to `bad` ([1] int64 on the device) the number of KV elements that
+    break I2, without waiting for the result."""
+    L, _, B, H, S, D = kv.shape
+    rc = _load().specgen_kv_check(_p(kv), _ELT[kv.dtype], L, B, H, S, D, _p(tokens), _p(pad_new), _p(len_new),
+                                  _p(bad), _s())
     assert rc == 0, rc
 
 

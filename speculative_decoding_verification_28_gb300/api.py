@@ -146,9 +146,10 @@ def spec_verify_greedy_static(target_logits, draft_tokens, draft_len=None, eos_i
                        (n_emit, "n_emit", (B,))):
         _need(t, torch.int32, nm, dev, shp)
     st = _stream(stream, dev)
-    _check(lib.spec_verify_greedy_static(_p(target_logits), _DT[target_logits.dtype], B, k, V, _p(draft_tokens),
-                                         _p(draft_len), int(eos_id), _p(remaining), _p(out_tokens), _p(n_accept),
-                                         _p(n_emit), st))
+    with torch.cuda.device(dev):  # the library uses the current device's array
+        _check(lib.spec_verify_greedy_static(_p(target_logits), _DT[target_logits.dtype], B, k, V, _p(draft_tokens),
+                                             _p(draft_len), int(eos_id), _p(remaining), _p(out_tokens),
+                                             _p(n_accept), _p(n_emit), st))
     return out_tokens, n_accept, n_emit
 
 

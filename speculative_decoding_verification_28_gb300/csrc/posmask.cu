@@ -5,6 +5,19 @@
 //   mask[b, s] = s >= pad'_b;   pos[b, s] = s - pad'_b there, 0 in the padding
 // (cumsum(mask) - 1 clamped at 0).  Rows whose padding did not change are
 // skipped.  Roofline: write-only, 5 bytes per slot of a changed row.
+//
+// Ordering.  The kernel is launched programmatically, so after a
+// realignment it runs alongside the KV shift.  Two rules keep that safe:
+//  * it reads pad_new, which the plan kernel wrote.  The shift lets its
+//    dependents launch only after its own griddepcontrol.wait has returned
+//    (the plan grid complete, its writes performed), so this kernel never
+//    starts before those writes.
+//  * every CTA ends with griddepcontrol.wait, so this grid cannot complete
+//    before the grid it follows (the shift) has completed and its writes
+//    are visible.  Work the caller enqueues after the round -- the next
+//    forward reading the cache, a copy of the error word the shift may set
+//    -- follows this grid in ordinary stream order, hence the shift too.
+#include "bulk_copy.cuh"
 #include "spec_common.cuh"
 #include "spec_launch.h"
 
@@ -13,16 +26,8 @@ namespace spec {
 constexpr int kPmThreads = 256;
 constexpr int kPmSlots = 8;  // slots per thread on the vector path
 
-__global__ void __launch_bounds__(kPmThreads)
-    pos_mask_kernel(int B, int S, const int32_t *pad_old, const int32_t *pad_new, int32_t *pos, uint8_t *mask,
-                    int vec)
+__device__ __forceinline__ void pos_mask_row(int S, int pn, int32_t *prow, uint8_t *mrow, int vec)
 {
-    const int b = blockIdx.y;
-    const int pn = pad_new[b];
-    if (pad_old && pad_old[b] == pn)
-        return;
-    int32_t *prow = pos + (size_t)b * S;
-    uint8_t *mrow = mask + (size_t)b * S;
     if (vec) {
         const int s0 = (blockIdx.x * kPmThreads + threadIdx.x) * kPmSlots;
         if (s0 >= S)
@@ -48,6 +53,19 @@ __global__ void __launch_bounds__(kPmThreads)
     }
 }
 
+__global__ void __launch_bounds__(kPmThreads)
+    pos_mask_kernel(int B, int S, const int32_t *pad_old, const int32_t *pad_new, int32_t *pos, uint8_t *mask,
+                    int vec)
+{
+    const int b = blockIdx.y;
+    const int pn = pad_new[b];
+    if (!(pad_old && pad_old[b] == pn))
+        pos_mask_row(S, pn, pos + (size_t)b * S, mask + (size_t)b * S, vec);
+    // no CTA completes before the grid this one follows has completed
+    if (threadIdx.x == 0)
+        dep_wait();
+}
+
 cudaError_t launch_pos_mask(int B, int S, const int32_t *pad_old, const int32_t *pad_new, int32_t *pos,
                             uint8_t *mask, cudaStream_t st)
 {
@@ -59,6 +77,8 @@ cudaError_t launch_pos_mask(int B, int S, const int32_t *pad_old, const int32_t 
     // allows it only after the plan that wrote pad_new is complete, and it
     // never touches pos or mask; a kernel that does not release dependents
     // early (any other kernel) completes first, as in an ordinary launch.
+    // Either way the grid's final griddepcontrol.wait keeps it from completing
+    // before that kernel.
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr.val.programmaticStreamSerializationAllowed = 1;

@@ -23,12 +23,21 @@ constexpr int kMaxDevices = 64;
 void *g_scratch_addr[kMaxDevices];
 std::mutex g_setup_mutex;
 
-// device address of the scratch on the current device (looked up once)
-int scratch_on_current_device(void **out)
+// device address of the scratch on the current device (looked up once); a
+// stream of another device is refused: the clear and the launch would run
+// there against this device's array
+int scratch_on_current_device(cudaStream_t st, void **out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return SPEC_ECUDA;
+    if (st != nullptr && st != cudaStreamLegacy && st != cudaStreamPerThread) {
+        int sdev = -1;
+        if (cudaStreamGetDevice(st, &sdev) != cudaSuccess)
+            return SPEC_ECUDA;
+        if (sdev != dev)
+            return SPEC_EINVAL;
+    }
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     if (!g_scratch_addr[dev]) {
         void *p = nullptr;
@@ -65,11 +74,11 @@ extern "C" int spec_verify_greedy_static(const void *target_logits, spec_dtype d
     const Layout lay = make_layout(B, k, V);
     if (lay.total > SPEC_STATIC_SCRATCH_BYTES)
         return SPEC_ESCRATCH;
+    cudaStream_t st = (cudaStream_t)cuda_stream;
     void *scratch = nullptr;
-    const int rc = scratch_on_current_device(&scratch);
+    const int rc = scratch_on_current_device(st, &scratch);
     if (rc != SPEC_OK)
         return rc;
-    cudaStream_t st = (cudaStream_t)cuda_stream;
     if (cudaMemsetAsync(static_cast<char *>(scratch) + lay.zero_begin, 0, lay.zero_end - lay.zero_begin, st) !=
         cudaSuccess)
         return SPEC_ECUDA;

@@ -223,3 +223,127 @@ def test_sample_round_replayed_from_a_cuda_graph_equals_direct_calls(filtered):
         cur = 1 - cur
         rounds += 1
     assert rounds >= 4
+
+
+# ---------------------------------------------------------------------------
+# work enqueued right after a round, with no host synchronisation
+# ---------------------------------------------------------------------------
+def _chain_without_host_sync(mode, via, seed):
+    """Chained rounds on one stream with nothing waiting for the host.  After
+    each round, at once: the committed tokens are written into the token
+    table, a device kernel checks invariant I2 over the whole cache (slot
+    pad'_b + p holds f(b, tok_p, p) for every p < len'_b - 1) and the round's
+    error word is copied on the device; the next round's forward writes its
+    query slots at the width the round left on the device.  Any of these
+    running before the KV shift completed would see (or clobber) rows in
+    flight.  Shapes: greedy = config 2's cache and logits (B=8, k=5,
+    V=32000 bf16, alpha=0.8, KV 32x2x8x32x1024x128 bf16) with prompts
+    U[64,256]; sample = config 3's (B=32, k=4, V=128256 fp32, KV
+    32x2x32x8x2048x128 bf16) with prompts U[128,512], so that the width
+    stays within the cache for every round of the chain."""
+    from specgen import torch_gen
+
+    d_ = dev()
+    if mode == "greedy":
+        B, k, V, L, H, S, D, lo, hi, ldt = 8, 5, 32000, 32, 32, 1024, 128, 64, 256, torch.bfloat16
+    else:
+        B, k, V, L, H, S, D, lo, hi, ldt = 32, 4, 128256, 32, 8, 2048, 128, 128, 512, torch.float32
+    g = torch.Generator(device=d_).manual_seed(seed)
+    kv = torch.empty((L, 2, B, H, S, D), dtype=torch.bfloat16, device=d_)
+    tokens = torch.randint(0, V, (B, S), device=d_, dtype=torch.int32, generator=g)
+    ln0 = prompt_lengths(B, lo, hi, seed)
+    W0 = int(ln0.max())
+    pad0 = (W0 - ln0).astype(np.int32)
+    R = (S - W0 - (k + 1)) // (k + 1)  # the width grows by at most k + 1 per round
+    lens = [to_dev(ln0), torch.empty(B, dtype=torch.int32, device=d_)]
+    pads = [to_dev(pad0), torch.empty(B, dtype=torch.int32, device=d_)]
+    widths = [torch.tensor([W0], dtype=torch.int32, device=d_), torch.empty(1, dtype=torch.int32, device=d_)]
+    torch_gen.kv_fill(kv, tokens, pads[0], lens[0] - 1, junk=True)
+    pos = torch.empty((B, S), dtype=torch.int32, device=d_)
+    mask = torch.empty((B, S), dtype=torch.uint8, device=d_)
+    sv.spec_rebuild_pos_mask(pads[0], pos, mask)
+    x_d = torch.empty((B, k + 1, V), dtype=ldt, device=d_)
+    d_d = torch.empty((B, k), dtype=torch.int32, device=d_)
+    q_d = torch.empty((B, k, V), dtype=torch.float32, device=d_)
+    u_d = torch.empty((B, k + 1), dtype=torch.float32, device=d_)
+    out = torch.empty((B, k + 1), dtype=torch.int32, device=d_)
+    na = torch.empty(B, dtype=torch.int32, device=d_)
+    ne = torch.empty(B, dtype=torch.int32, device=d_)
+    err = torch.empty(1, dtype=torch.int32, device=d_)
+    ws = sv.Workspace(B, k, V, d_)
+    bad = torch.zeros(1, dtype=torch.int64, device=d_)
+    errs = torch.full((R,), -99, dtype=torch.int32, device=d_)
+    ne_log = torch.zeros((R, B), dtype=torch.int32, device=d_)
+    cols = torch.arange(k + 1, device=d_)
+
+    def enqueue(par):
+        ln_in, pad_in, ln_out, pad_out = lens[par], pads[par], lens[1 - par], pads[1 - par]
+        w_out = widths[1 - par]
+        if via == "calls":
+            if mode == "greedy":
+                sv.spec_verify_greedy(x_d, d_d, out_tokens=out, n_accept=na, n_emit=ne, workspace=ws)
+            else:
+                sv.spec_verify_sample(x_d, q_d, d_d, u_d, out_tokens=out, n_accept=na, n_emit=ne, workspace=ws)
+            sv.spec_realign_kv(kv, ln_in, pad_in, ne, len_new=ln_out, pad_new=pad_out, width_new=w_out, err=err,
+                               workspace=ws)
+            sv.spec_rebuild_pos_mask(pad_out, pos, mask, pad_old=pad_in)
+        elif mode == "greedy":
+            sv.spec_round_greedy(x_d, d_d, [kv], ln_in, pad_in, pos, mask, out_tokens=out, n_accept=na, n_emit=ne,
+                                 len_new=ln_out, pad_new=pad_out, width_new=w_out, err=err, workspace=ws)
+        else:
+            sv.spec_round_sample(x_d, q_d, d_d, u_d, [kv], ln_in, pad_in, pos, mask, out_tokens=out, n_accept=na,
+                                 n_emit=ne, len_new=ln_out, pad_new=pad_out, width_new=w_out, err=err, workspace=ws)
+
+    graphs = [sv.RoundGraph(lambda p=p: enqueue(p), d_) for p in (0, 1)] if via == "graph" else None
+    torch.cuda.synchronize()
+    cur = 0
+    for r in range(R):
+        if mode == "greedy":
+            x, d = torch_gen.greedy_round_inputs(B, k, V, 0.8, 2.0, g, ldt, d_)
+        else:
+            x, q, d, u = torch_gen.sample_round_inputs(B, k, V, 0.5, g, ldt, d_)
+            q_d.copy_(q)
+            u_d.copy_(u)
+        x_d.copy_(x)
+        d_d.copy_(d)
+        # the forward: KV of the last token and the k proposals at the width on the device
+        last = torch.gather(tokens, 1, (lens[cur].long() - 1).unsqueeze(1))
+        torch_gen.kv_write_query_dev(kv, torch.cat([last, d_d], 1).contiguous(), pos, widths[cur])
+        if graphs is not None:
+            graphs[cur].replay()
+        else:
+            enqueue(cur)
+        # straight after the round, on the same stream: the token table, the I2 check, the error word
+        at = (lens[cur].long().unsqueeze(1) + cols).clamp(max=S - 1)
+        keep = cols.unsqueeze(0) < ne.unsqueeze(1)
+        tokens.scatter_(1, at, torch.where(keep, out, torch.gather(tokens, 1, at)))
+        torch_gen.kv_check_async(kv, tokens, pads[1 - cur], lens[1 - cur], bad)
+        errs[r:r + 1].copy_(err)
+        ne_log[r].copy_(ne)
+        cur = 1 - cur
+    torch.cuda.synchronize()
+    assert R >= 100
+    assert int(bad.item()) == 0
+    assert (errs == 0).all(), errs
+    # the metadata the device ended with, replayed on the host from the commits
+    ln_h, pad_h = ln0.astype(np.int64), pad0.astype(np.int64)
+    moved = 0
+    for n in ne_log.cpu().numpy():
+        ln_n = ln_h + n
+        pad_n = ln_n.max() - ln_n
+        moved += int((pad_n != pad_h).sum())
+        ln_h, pad_h = ln_n, pad_n
+    assert np.array_equal(lens[cur].cpu().numpy(), ln_h) and np.array_equal(pads[cur].cpu().numpy(), pad_h)
+    opos, omask = oracle.rebuild_pos_mask(S, pad_h.astype(np.int32))
+    assert np.array_equal(pos.cpu().numpy(), opos) and np.array_equal(mask.cpu().numpy(), omask)
+    assert moved > R  # sequences moved in most rounds
+
+
+@pytest.mark.parametrize("via", ["round", "graph", "calls"])
+def test_greedy_work_after_a_round_needs_no_host_sync(via):
+    _chain_without_host_sync("greedy", via, seed=61)
+
+
+@pytest.mark.parametrize("via", ["round", "calls"])
+def test_sample_work_after_a_round_needs_no_host_sync(via):
+    _chain_without_host_sync("sample", via, seed=67)

@@ -237,13 +237,6 @@ def test_workspace_reuse_across_kinds():
         assert np.array_equal(gg[0].cpu().numpy(), og[0])
 
 
-def test_zz_boundary_rate():
-    """All files above: boundary cases stay below 1e-4 of the decisions."""
-    assert STATS["decisions"] > 50_000
-    assert STATS["boundary"] < 1e-4 * STATS["decisions"], STATS
-    print("sampling parity statistics:", STATS)
-
-
 def test_masked_vocabulary_rows():
     """Rows with -inf logits (masked tokens, e.g. after top-k filtering) are
     ordinary distributions: masked tokens have probability 0."""
@@ -257,3 +250,10 @@ def test_masked_vocabulary_rows():
     check(x, oracle.DT_F32, q, d, u)
     xb = (x.view(np.uint32) >> 16).astype(np.uint16)  # -inf survives bf16 truncation
     check(xb, oracle.DT_BF16, q, d, u)
+
+
+def test_zz_boundary_rate():
+    """All files above: boundary cases stay below 1e-4 of the decisions."""
+    assert STATS["decisions"] > 50_000
+    assert STATS["boundary"] < 1e-4 * STATS["decisions"], STATS
+    print("sampling parity statistics:", STATS)

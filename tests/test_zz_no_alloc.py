@@ -59,3 +59,46 @@ def test_rejects_sizes_beyond_the_scratch():
     assert rc == -6
     torch.cuda.synchronize()
     assert (buf == 7).all()
+
+
+def test_on_a_side_stream_of_the_current_device():
+    """A caller's own stream (not the default one) on the current device is
+    accepted; results as with the workspace entry point."""
+    B, k, V = 16, 4, 5000
+    x, d = greedy_round_inputs(B, k, V, 0.7, 1.0, seed=77, dtype="f32")
+    xt, dtd = _dev_logits(x, False), torch.from_numpy(d).cuda()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        a = sv.spec_verify_greedy_static(xt, dtd, stream=s)
+    s.synchronize()
+    b = sv.spec_verify_greedy(xt, dtd)
+    for ga, gb in zip(a, b):
+        assert torch.equal(ga, gb)
+
+
+@pytest.mark.skipif(torch.cuda.device_count() < 2, reason="needs two GPUs")
+def test_tensors_on_another_device_than_the_current_one():
+    """Tensors on cuda:1 while cuda:0 is current: the binding makes their
+    device current, so the array of the right device is used; a raw call
+    with a stream of another device is refused with SPEC_EINVAL (-1)."""
+    import ctypes
+
+    from speculative_decoding_verification_28_gb300 import _lib
+
+    B, k, V = 8, 3, 3000
+    x, d = greedy_round_inputs(B, k, V, 0.6, 1.0, seed=78, dtype="f32")
+    with torch.cuda.device(0):
+        xt, dtd = torch.from_numpy(x).to("cuda:1"), torch.from_numpy(d).to("cuda:1")
+        a = sv.spec_verify_greedy_static(xt, dtd)
+    b = sv.spec_verify_greedy(xt, dtd)
+    for ga, gb in zip(a, b):
+        assert torch.equal(ga, gb)
+    lib = _lib.load()
+    p = ctypes.c_void_p(xt.data_ptr())
+    s1 = ctypes.c_void_p(torch.cuda.current_stream(1).cuda_stream)
+    with torch.cuda.device(0):
+        rc = lib.spec_verify_greedy_static(p, 0, B, k, V, ctypes.c_void_p(dtd.data_ptr()), None, -1, None,
+                                           ctypes.c_void_p(a[0].data_ptr()), ctypes.c_void_p(a[1].data_ptr()),
+                                           ctypes.c_void_p(a[2].data_ptr()), s1)
+    assert rc == -1
