@@ -45,11 +45,13 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c2")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c5")
     ap.add_argument("--alpha", type=float, default=None)
     ap.add_argument("--k", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="c5: skip the stochastic leg (c5s on the same cache) reported under the key 'c5s'")
     ap.add_argument("--seed", type=int, default=1002)
     ap.add_argument("--dump-steps", default=None,
                     help="write each step's algorithmic bytes and call times (JSON lines) to this file")
@@ -89,7 +91,9 @@ def workload_params(args):
     if (args.top_k is not None or args.top_p is not None) and c["mode"] != "sample":
         raise SystemExit("--top-k / --top-p apply to the stochastic workloads (c3, c5s)")
     if c["mode"] in ("greedy", "exspec"):
-        c["alpha"] = args.alpha if args.alpha is not None else max(c["alphas"])
+        # config 5: the middle of its sweep; elsewhere the heaviest realignment
+        default = 0.6 if w["cfg"] == "c5" else max(c["alphas"])
+        c["alpha"] = args.alpha if args.alpha is not None else default
     else:
         c["alpha"] = None
     return c
@@ -105,6 +109,40 @@ def describe(c):
         s += f", target top_k={c.get('top_k')} top_p={c.get('top_p')}"
     s += f", alpha={c['alpha']}" if c["alpha"] is not None else f", draft=target+N(0,{c['noise']})"
     return s + f"; KV {kv}; prompts U{list(c['prompt'])}"
+
+
+# the CPU legs (cpu_baseline and --impl reference) realign a host copy of the
+# first CPU_LAYERS layers of caches larger than this, and scale that time to
+# every layer (each (layer, K/V, head) slab is an independent move of the
+# same rows)
+CPU_FULL_CACHE_BYTES = 8 << 30
+CPU_LAYERS = 1
+
+
+def kv_bytes(c):
+    return c["L"] * 2 * c["B"] * c["H"] * c["S"] * c["D"] * (2 if c["kv_dtype"] == "bf16" else 4)
+
+
+def cpu_layers(c):
+    """Layers of the cache the CPU legs realign (all of them when it fits)."""
+    return c["L"] if kv_bytes(c) <= CPU_FULL_CACHE_BYTES else CPU_LAYERS
+
+
+def cpu_sample_text(c):
+    lc = cpu_layers(c)
+    if lc == c["L"]:
+        return "full rounds: verification, realignment of a host copy of the whole cache, positions / mask"
+    return (f"verification of the whole batch and positions / mask per round; realignment timed on a host copy "
+            f"of the first {lc} of {c['L']} layers ({lc * 2 * c['B'] * c['H']} of {c['L'] * 2 * c['B'] * c['H']} "
+            f"(layer, K/V, sequence, head) slabs) and scaled by {c['L'] // lc} to the whole cache")
+
+
+def bench_config(args, c, world):
+    """The `config` object of the JSON line, the same for both arms."""
+    return {"workload": f"{args.workload}: " + describe(c),
+            "l2": "GPU arm: flushed between steps (256 MiB write, outside the timed events)",
+            "cpu_sample": cpu_sample_text(c),
+            "parallelism": f"independent batch per GPU x{world}"}
 
 
 # ---------------------------------------------------------------------------
@@ -240,10 +278,13 @@ def kernel_source_digest():
     return h.hexdigest()[:16]
 
 
-def ncu_traffic_ratio(workload):
-    """DRAM bytes / algorithmic bytes of the shift kernel from the committed
-    ncu summary, if it was taken on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", f"kv_shift_{workload}.txt")
+def ncu_shift_record(workload):
+    """The shift kernel's DRAM traffic from the committed ncu summary of this
+    workload's cache (config 5's for both of its modes), if it was taken on
+    the current kernel source: traffic / algorithmic bytes, reads /
+    algorithmic read bytes, and which capture they come from."""
+    name = {"c5s": "c5"}.get(workload, workload)
+    p = os.path.join(ROOT, "profiles", f"kv_shift_{name}.txt")
     if not os.path.exists(p):
         return None
     rec = {}
@@ -254,7 +295,9 @@ def ncu_traffic_ratio(workload):
     if (rec.get("source digest", "").split() or [""])[0] != kernel_source_digest():
         return None
     try:
-        return float(rec["dram bytes / algorithmic bytes"])
+        return {"traffic_ratio": float(rec["dram bytes / algorithmic bytes"].split()[0]),
+                "read_ratio": float(rec["reads / algorithmic read half"].split()[0]),
+                "source": f"profiles/kv_shift_{name}.txt ({rec.get('capture', 'reduced cache').split(';')[0]})"}
     except (KeyError, ValueError):
         return None
 
@@ -266,7 +309,9 @@ class Round:
     """State of one left-padded batch on the device plus the harness that
     plays the target model between rounds."""
 
-    def __init__(self, c, seed, device):
+    def __init__(self, c, seed, device, kv=None):
+        """kv: an existing cache of this workload's shape to reuse (it is
+        refilled), e.g. config 5's 128 GiB cache for its second mode."""
         import torch
 
         import speculative_decoding_verification_28_gb300 as sv
@@ -279,7 +324,12 @@ class Round:
         B, S, k = c["B"], c["S"], c["k"]
         self.g = torch.Generator(device=device).manual_seed(seed)
         self.rng = np.random.default_rng(seed)
-        self.kv = torch.empty((c["L"], 2, B, c["H"], S, c["D"]), dtype=self.kv_dt, device=device)
+        shape = (c["L"], 2, B, c["H"], S, c["D"])
+        if kv is not None:
+            assert tuple(kv.shape) == shape and kv.dtype == self.kv_dt
+            self.kv = kv
+        else:
+            self.kv = torch.empty(shape, dtype=self.kv_dt, device=device)
         self.draft = None
         if c.get("draft"):
             Ld, Hd, Dd = c["draft"]
@@ -405,6 +455,8 @@ class Round:
 
 
 def run_ours(args, c, rank, local_rank, world):
+    import argparse
+
     import torch
 
     dev = torch.device(f"cuda:{local_rank}")
@@ -415,7 +467,41 @@ def run_ours(args, c, rank, local_rank, world):
 
         dist.init_process_group("nccl", device_id=dev)
     st = torch.cuda.current_stream(dev)
-    R = Round(c, rank_seed(args.seed, rank), dev)
+    seed = rank_seed(args.seed, rank)
+    R = Round(c, seed, dev)
+    m = measure(args, c, R, st, dev, pg, world, rank, seed)
+    line = {
+        "metric": METRIC, "value": m.pop("value"), "unit": "rounds/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": m.pop("ms_per_step"), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": m.pop("dtype"),
+        "data": "synthetic (seeded; stands in for SpecBench/Multi30k-shaped rounds)",
+        "config": bench_config(args, c, world),
+        "timed": "library calls only (device time: each step is enqueued behind an untimed GPU gate); "
+                 "the harness target forward runs between steps",
+    }
+    line.update(m)
+    if args.workload == "c5" and not args.no_extra:
+        # the stochastic mode of config 5 on the same cache (refilled), after the greedy leg
+        a2 = argparse.Namespace(**{**vars(args), "workload": "c5s", "alpha": None})
+        c2 = workload_params(a2)
+        kv = R.kv
+        del R
+        torch.cuda.empty_cache()
+        R2 = Round(c2, seed + 1, dev, kv=kv)
+        m2 = measure(a2, c2, R2, st, dev, pg, world, rank, seed + 1)
+        m2["rounds_per_s"] = m2.pop("value")
+        line["c5s"] = {"config": {"workload": "c5s: " + describe(c2), "cpu_sample": cpu_sample_text(c2)}, **m2}
+        del R2, kv
+    if pg:
+        dist.destroy_process_group()
+    return line
+
+
+def measure(args, c, R, st, dev, pg, world, rank, seed):
+    """Warm-up, K timed rounds, untimed breakdown rounds, the end-to-end
+    replay and the oracle baseline for one workload; returns the fields of
+    its JSON line."""
+    import torch
 
     def one_step(timed, breakdown=False):
         """One round; returns [step, verify, realign + pos/mask] device ms (or,
@@ -447,16 +533,18 @@ def run_ours(args, c, rank, local_rank, world):
                                    "verify_alg_bytes": vbytes, "emitted": emitted, "call_ms": times}) + "\n")
         return times, moved, emitted, vbytes
 
-    dump = open(args.dump_steps, "w") if args.dump_steps else None
+    dump = open(args.dump_steps, "a") if args.dump_steps else None
 
     per = []
     moved_rows = []
     verify_bytes = []
     emitted = 0
-    with ClockSampler(local_rank) as clk:  # sampling already runs when the timed region starts
+    with ClockSampler(dev.index) as clk:  # sampling already runs when the timed region starts
         for _ in range(args.warmup):
             one_step(False)
         if pg:
+            import torch.distributed as dist
+
             dist.barrier()
         torch.cuda.synchronize(dev)
         clk.begin()
@@ -479,6 +567,8 @@ def run_ours(args, c, rank, local_rank, world):
     brk_steps = [one_step(False, breakdown=True) for _ in range(min(10, max(3, args.steps // 5)))]
     brk = np.array([b[0] for b in brk_steps])
     brk_bytes = np.array([b[1] for b in brk_steps], dtype=np.float64) * R.row_bytes_all_slabs() * 2
+    if dump is not None:
+        dump.close()
 
     # roofline of the dominant kernel: the KV shift, timed over the realign
     # call and the position/mask rebuild that may overlap it (plan kernel and
@@ -489,33 +579,25 @@ def run_ours(args, c, rank, local_rank, world):
     mean_alg = float(alg_bytes.mean())
     achieved = float(alg_bytes.sum() / (realign_ms.sum() / 1e3) / 1e9)
     peak, peak_src = hbm_peak()
-    ratio = ncu_traffic_ratio(args.workload)
+    prof = ncu_shift_record(args.workload)
     roofline = {"bound": "hbm",
                 "kernel": "kv_shift_bulk_kernel (timed with realign_plan_kernel and pos_mask_kernel: lower bound)",
                 "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
-                "traffic": None if ratio is None else round(ratio * mean_alg),
+                "traffic": None if prof is None else round(prof["traffic_ratio"] * mean_alg),
+                "read_ratio": None if prof is None else prof["read_ratio"],
+                "traffic_source": None if prof is None else prof["source"],
                 "algorithmic_bytes_per_launch": round(mean_alg)}
-
-    line = {
-        "metric": METRIC, "value": round(value, 3), "unit": "rounds/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(float(per[:, 0].mean()), 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None,
+    v_ach = float(np.sum(verify_bytes) / (per[:, 1].sum() / 1e3) / 1e9)
+    out = {
+        "value": round(value, 3), "ms_per_step": round(float(per[:, 0].mean()), 4),
         "dtype": c["logit_dtype"] if c["mode"] == "greedy" else "f32 arithmetic on " + c["logit_dtype"] + " logits",
-        "data": "synthetic (seeded; stands in for SpecBench/Multi30k-shaped rounds)",
-        "config": {"workload": f"{args.workload}: " + describe(c),
-                   "l2": "flushed between steps (256 MiB write, outside the timed events)",
-                   "timed": "library calls only (device time: each step is enqueued behind an untimed GPU gate); "
-                   "the harness target forward runs between steps",
-                   "parallelism": f"independent batch per GPU x{world}"},
         "roofline": roofline,
         "verify_roofline": {"bound": "hbm", "kernels": ("verify_greedy_kernel" if c["mode"] == "greedy" else
                                                         (("verify_filter_tab_kernel" if c["logit_dtype"] != "f32" and c["V"] >= 32768
                                                           else "verify_filter_kernel") if R.filtered() else
                                                          "verify_stats_kernel") + " + verify_draw_sums_kernel + verify_draw_pick_kernel"),
-                            "achieved": round(float(np.sum(verify_bytes) / (per[:, 1].sum() / 1e3) / 1e9), 1),
-                            "peak": peak, "unit": "GB/s",
-                            "frac": round(float(np.sum(verify_bytes) / (per[:, 1].sum() / 1e3) / 1e9) / peak, 4),
+                            "achieved": round(v_ach, 1), "peak": peak, "unit": "GB/s", "frac": round(v_ach / peak, 4),
                             "algorithmic_bytes_per_launch": round(float(np.mean(verify_bytes)))},
         "per_call_us": {"verify": round(float(per[:, 1].mean()) * 1e3, 2),
                         "realign_and_pos_mask": round(float(per[:, 2].mean()) * 1e3, 2),
@@ -523,17 +605,17 @@ def run_ours(args, c, rank, local_rank, world):
                                             "realign_alone_gbs": round(float(brk_bytes.sum() / (brk[:, 1].sum() / 1e3)
                                                                              / 1e9), 1),
                                             "pos_mask": round(float(brk[:, 2].mean()) * 1e3, 2)}},
+        # the realignment's share of a round (the pages: ~13% at batch 1 to ~40% at batch 32 end to end)
+        "realign_share": round(float(per[:, 2].sum() / per[:, 0].sum()), 4),
         "tokens_per_round": round(emitted / args.steps / c["B"], 4),
         "gpu_launches": args.steps * (4 if c["mode"] == "greedy" else 6),
         "clocks": clk.summary(),
     }
     if not args.no_e2e:
-        line["e2e"] = run_e2e(args, R, st, dev, pg, world, rank_seed(args.seed, rank))
+        out["e2e"] = run_e2e(args, R, st, dev, pg, world, seed)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = run_cpu_baseline(c, args, R)
-    if pg:
-        dist.destroy_process_group()
-    return line
+        out["cpu_baseline"] = run_cpu_baseline(c, args, R)
+    return out
 
 
 def run_e2e(args, R, st, dev, pg, world, seed):
@@ -651,27 +733,55 @@ def e2e_pass(args, R, st, dev, pg, world, seed, use_graph):
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
-def oracle_rounds(c, n_rounds, seed, kv_host=None, state=None, R=None):
-    """n_rounds full rounds of the CPU oracle on the host (on the threads
-    oracle.set_threads gave it): verification on the round's logits,
-    realignment of the host copy of the cache, position/mask rebuild.
-    Returns (seconds in oracle calls, kv)."""
+def host_inputs(c, seed):
+    """One round's inputs made on the host (NumPy), for the reference arm:
+    one generator for small batches, blocks of sequences on every host core
+    for large ones."""
+    from specgen import greedy_round_inputs, round_inputs_blocked, sample_round_inputs
+
+    B, k, V = c["B"], c["k"], c["V"]
+    if B * (k + 1) * V >= (1 << 24):
+        return round_inputs_blocked(c["mode"], B, k, V, seed, c["logit_dtype"], alpha=c.get("alpha"),
+                                    sigma=c.get("sigma", 1.0), noise=c.get("noise"), threads=os.cpu_count())
+    if c["mode"] == "greedy":
+        return greedy_round_inputs(B, k, V, c["alpha"], c["sigma"], seed=seed, dtype=c["logit_dtype"])
+    return sample_round_inputs(B, k, V, c["noise"], seed=seed, dtype=c["logit_dtype"])
+
+
+def device_inputs(c, R, seed):
+    """One round's inputs drawn on the GPU by the bench's own generator (the
+    same recipe as its timed rounds) and copied to the host, for the oracle
+    baseline of our arm."""
+    import torch
+
+    g = torch.Generator(device=R.dev).manual_seed(int(seed))
+    B, k, V = c["B"], c["k"], c["V"]
+    if c["mode"] == "greedy":
+        t = R.tg.greedy_round_inputs(B, k, V, c["alpha"], c["sigma"], g, R.lg_dt, R.dev)
+    else:
+        t = R.tg.sample_round_inputs(B, k, V, c["noise"], g, R.lg_dt, R.dev)
+    x = t[0].view(torch.int16).cpu().numpy().view(np.uint16) if t[0].dtype == torch.bfloat16 else t[0].cpu().numpy()
+    return (x,) + tuple(a.cpu().numpy() for a in t[1:])
+
+
+def oracle_rounds(c, n_rounds, seed, kv_host, make_inputs, state=None):
+    """n_rounds rounds of the CPU oracle on the host (on the threads
+    oracle.set_threads gave it): verification of the round's logits,
+    realignment of the host cache `kv_host` (the first cpu_layers(c) layers),
+    position/mask rebuild.  The realignment time is scaled to every layer.
+    Returns (seconds, state) with state = (lengths, paddings) to continue."""
     import oracle
-    from specgen import greedy_round_inputs, prompt_lengths, sample_round_inputs
+    from specgen import prompt_lengths
 
     rng = np.random.default_rng(seed)
-    B, k, V, S = c["B"], c["k"], c["V"], c["S"]
+    B, k, S = c["B"], c["k"], c["S"]
+    scale = c["L"] / kv_host.shape[0]
     dt = {"bf16": oracle.DT_BF16, "f32": oracle.DT_F32}[c["logit_dtype"]]
-    if kv_host is None:
-        if R is not None:
-            kv_host = R.kv.view(-1).view(__import__("torch").int16).cpu().numpy().view(np.uint16)
-            kv_host = kv_host.reshape(tuple(R.kv.shape)) if c["kv_dtype"] == "bf16" else R.kv.cpu().numpy()
-        else:
-            kv_host = np.zeros((c["L"], 2, B, c["H"], S, c["D"]),
-                               np.uint16 if c["kv_dtype"] == "bf16" else np.float32)
-            kv_host.fill(0)  # touch every page now, not inside the timed oracle calls
-    ln = prompt_lengths(B, *c["prompt"], seed=rng)
-    pad = (int(ln.max()) - ln).astype(np.int32)
+    if state is None:
+        ln = prompt_lengths(B, *c["prompt"], seed=rng)
+        pad = (int(ln.max()) - ln).astype(np.int32)
+    else:
+        ln, pad = state
     pos = np.zeros((B, S), np.int32)
     mask = np.zeros((B, S), np.uint8)
     spent = 0.0
@@ -679,20 +789,22 @@ def oracle_rounds(c, n_rounds, seed, kv_host=None, state=None, R=None):
         if int(ln[0] + pad[0]) + k + 1 > S:
             ln = prompt_lengths(B, *c["prompt"], seed=rng)
             pad = (int(ln.max()) - ln).astype(np.int32)
+        inp = make_inputs(int(rng.integers(1 << 30)))
+        t0 = time.perf_counter()
         if c["mode"] == "greedy":
-            x, d = greedy_round_inputs(B, k, V, c["alpha"], c["sigma"], seed=rng, dtype=c["logit_dtype"])
-            t0 = time.perf_counter()
-            _, _, ne = oracle.verify_greedy(x, dt, d)
+            _, _, ne = oracle.verify_greedy(inp[0], dt, inp[1])
         else:
-            x, q, d, u = sample_round_inputs(B, k, V, c["noise"], seed=rng, dtype=c["logit_dtype"])
-            t0 = time.perf_counter()
+            x, q, d, u = inp
             _, _, ne, _, _ = oracle.verify_sample(x, dt, q, d, u, top_k=c.get("top_k"), top_p=c.get("top_p"))
+        t1 = time.perf_counter()
         st, ln, pad2, w = oracle.realign_kv(kv_host, ln, pad, ne)
+        t2 = time.perf_counter()
         oracle.rebuild_pos_mask(S, pad2, pos, mask)
-        spent += time.perf_counter() - t0
+        t3 = time.perf_counter()
+        spent += (t1 - t0) + scale * (t2 - t1) + (t3 - t2)
         assert st == 0
         pad = pad2
-    return spent, kv_host
+    return spent, (ln, pad)
 
 
 def warm_oracle_threads():
@@ -705,17 +817,35 @@ def warm_oracle_threads():
     oracle.verify_greedy(x, oracle.DT_F32, d)
 
 
-def run_cpu_baseline(c, args, R, budget_s=8.0, max_rounds=400):
-    """Rounds of the oracle until ~budget_s seconds of oracle time, on every
-    host core (OpenMP over sequences and cache slabs) and on one thread."""
+def host_cache(c, R=None):
+    """The host cache the oracle realigns: a copy of the device cache's first
+    cpu_layers(c) layers (our arm), or zeros of that shape (reference arm)."""
+    lc = cpu_layers(c)
+    if R is not None:
+        import torch
+
+        sub = R.kv[:lc]
+        if sub.dtype == torch.bfloat16:
+            return sub.view(torch.int16).cpu().numpy().view(np.uint16)
+        return sub.cpu().numpy()
+    kv = np.zeros((lc, 2, c["B"], c["H"], c["S"], c["D"]), np.uint16 if c["kv_dtype"] == "bf16" else np.float32)
+    kv.fill(0)  # touch every page now, not inside the timed oracle calls
+    return kv
+
+
+def run_cpu_baseline(c, args, R, budget_s=8.0, max_rounds=400, min_rounds=3):
+    """Rounds of the oracle until ~budget_s seconds of oracle time (at least
+    min_rounds), on every host core (OpenMP over sequences and cache slabs)
+    and on one thread; inputs from the bench's own generator."""
     import oracle
 
     def timed(threads):
-        spent, n, kv = 0.0, 0, None
+        spent, n, state = 0.0, 0, None
+        kv = host_cache(c, R)
         with oracle.threads(threads):
             warm_oracle_threads()
-            while spent < budget_s and n < max_rounds:
-                t, kv = oracle_rounds(c, 1, args.seed + 1 + n, kv_host=kv, R=R if kv is None else None)
+            while (spent < budget_s or n < min_rounds) and n < max_rounds:
+                t, state = oracle_rounds(c, 1, args.seed + 1 + n, kv, lambda sd: device_inputs(c, R, sd), state)
                 spent += t
                 n += 1
         return n, spent
@@ -727,10 +857,9 @@ def run_cpu_baseline(c, args, R, budget_s=8.0, max_rounds=400):
     best_cores, best = (cores, v_all) if v_all >= v_one else (1, v_one)
     return {"value": round(best, 4), "unit": "rounds/s", "cores": best_cores, "host_cores": os.cpu_count(),
             "kind": "oracle",
-            "sample": f"full rounds of the same workload (verify + realign of a host copy of the cache + pos/mask) "
-                      f"in C, OpenMP over sequences and cache slabs; the faster of {cores} threads ({n_all} rounds, "
-                      f"{t_all:.1f} s) and one thread ({n_one} rounds, {t_one:.1f} s); inputs generated outside "
-                      f"the timing",
+            "sample": f"{cpu_sample_text(c)}; the oracle (C, OpenMP over sequences and cache slabs), the faster of "
+                      f"{cores} threads ({n_all} rounds, {t_all:.1f} s) and one thread ({n_one} rounds, {t_one:.1f} s); "
+                      f"inputs generated outside the timing",
             "all_cores": {"value": round(v_all, 4), "cores": cores},
             "single_thread": {"value": round(v_one, 4), "cores": 1}}
 
@@ -742,15 +871,21 @@ def run_reference(args, c):
     import oracle
 
     per = []
-    kv = None
+    kv = host_cache(c)
+    state = None
     # every host core when the round moves a large cache; one thread for the
     # tiny workloads, where a parallel region costs more than the round
-    kv_bytes = c["L"] * 2 * c["B"] * c["H"] * c["S"] * c["D"] * (2 if c["kv_dtype"] == "bf16" else 4)
-    cores = oracle.threads_available() if kv_bytes >= (64 << 20) else 1
+    cores = oracle.threads_available() if kv_bytes(c) >= (64 << 20) else 1
+    warm = None
     with oracle.threads(cores):
         warm_oracle_threads()
         for i in range(args.warmup + args.steps):
-            spent, kv = oracle_rounds(c, 1, args.seed + 31 * i, kv_host=kv)
+            if i < args.warmup:  # warm-up rounds share one input set
+                warm = warm if warm is not None else host_inputs(c, args.seed + 31 * i)
+                make = (lambda w: (lambda sd: w))(warm)
+            else:
+                make = lambda sd: host_inputs(c, sd)
+            spent, state = oracle_rounds(c, 1, args.seed + 31 * i, kv, make, state)
             if i >= args.warmup:
                 per.append(spent)
     total = float(np.sum(per))
@@ -758,11 +893,12 @@ def run_reference(args, c):
     return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "rounds/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 oracle",
-            "data": "synthetic", "config": {"workload": f"{args.workload}: " + describe(c)},
+            "data": "synthetic", "config": bench_config(args, c, world),
+            "timed": "each step one round of the CPU oracle on the host (inputs generated outside the timing)",
             "cpu_baseline": {"value": round(v, 4), "unit": "rounds/s", "cores": cores, "host_cores": os.cpu_count(),
                              "kind": "oracle",
-                             "sample": "each step one full round of the workload on the host, OpenMP over "
-                                       f"sequences and cache slabs on {cores} threads"},
+                             "sample": f"{cpu_sample_text(c)}; OpenMP over sequences and cache slabs on {cores} "
+                                       f"threads"},
             "e2e": {"value": round(v, 4), "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

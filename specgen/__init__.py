@@ -17,6 +17,7 @@ from .np_gen import (  # noqa: F401
     greedy_round_inputs,
     kv_row_values,
     prompt_lengths,
+    round_inputs_blocked,
     sample_round_inputs,
     splitmix64,
 )

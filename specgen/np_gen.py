@@ -144,3 +144,24 @@ def sample_round_inputs(B, k, V, noise, seed, dtype="f32", sigma=1.0):
             d[b, j] = t
     u = rng.random((B, k + 1), dtype=np.float32)
     return xs, q, d, u
+
+
+def round_inputs_blocked(mode, B, k, V, seed, dtype, alpha=None, sigma=1.0, noise=None, threads=8, block=32):
+    """greedy_round_inputs / sample_round_inputs for large batches, made on
+    host threads: sequences in blocks of `block`, block i drawn from the
+    generator seeded with [seed, i].  The same recipe per sequence; the
+    random stream differs from the single-generator form."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    starts = list(range(0, B, block))
+
+    def part(i):
+        nb = min(block, B - starts[i])
+        rng = np.random.default_rng([int(seed), i])
+        if mode == "greedy":
+            return greedy_round_inputs(nb, k, V, alpha, sigma, rng, dtype=dtype)
+        return sample_round_inputs(nb, k, V, noise, rng, dtype=dtype, sigma=sigma)
+
+    with ThreadPoolExecutor(max(1, int(threads))) as ex:
+        parts = list(ex.map(part, range(len(starts))))
+    return tuple(np.concatenate([p[j] for p in parts]) for j in range(len(parts[0])))
