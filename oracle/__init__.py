@@ -16,7 +16,7 @@ from .core import (  # noqa: F401
     MUTANTS,
     build,
     filter_cut,
-    q40_weight,
+    filter_info,
     commit_ragged,
     repad_gather,
     unpad_scatter,

@@ -73,10 +73,8 @@ def _load():
             ]
             lib.oracle_softmax_row.argtypes = [vp, i32, i64, i32, f64, i32, f32, vp]
             lib.oracle_softmax_row.restype = i32
-            lib.oracle_filter_cut.argtypes = [vp, i32, i64, i32, f32, i32, f32]
+            lib.oracle_filter_cut.argtypes = [vp, i32, i64, i32, f32, i32, f32, vp]
             lib.oracle_filter_cut.restype = f64
-            lib.oracle_q40_weight.argtypes = [f32, f32]
-            lib.oracle_q40_weight.restype = ctypes.c_uint64
             lib.oracle_realign_plan.argtypes = [i32, i32, vp, vp, vp, vp, vp, vp]
             lib.oracle_realign_plan.restype = i32
             lib.oracle_shift_slab.argtypes = [vp, i64, i32, i32, i32]
@@ -208,15 +206,21 @@ def softmax_row(logits, dt, row, temperature=1.0, top_k=0, top_p=1.0):
 
 def filter_cut(logits, dt, row, temperature=1.0, top_k=0, top_p=1.0):
     """Smallest logit top-k / top-p keep in row ``row`` (-inf: no filter)."""
+    return filter_info(logits, dt, row, temperature, top_k, top_p)[0]
+
+
+def filter_info(logits, dt, row, temperature=1.0, top_k=0, top_p=1.0):
+    """(cut, margin, total, undecided) of row ``row``: the smallest kept
+    logit; min |A - top_p M| over the two top-p decisions next to the cut and
+    the kept total M, both in units of the top token's mass (margin +inf
+    without top-p); whether a decision fell inside the oracle's fp64 error
+    band."""
     lib = _load()
     x = _logits(logits, dt)
-    return lib.oracle_filter_cut(_ptr(x), dt, int(row), x.shape[-1], float(temperature), int(top_k), float(top_p))
-
-
-def q40_weight(d, c):
-    """The nucleus decision's fixed-point weight of a logit difference d <= 0
-    at scale c (both fp32)."""
-    return int(_load().oracle_q40_weight(float(d), float(c)))
+    info = np.zeros(3, np.float64)
+    cut = lib.oracle_filter_cut(_ptr(x), dt, int(row), x.shape[-1], float(temperature), int(top_k), float(top_p),
+                                _ptr(info))
+    return cut, float(info[0]), float(info[1]), bool(info[2])
 
 
 def realign_plan(S, length, pad, n_emit):

@@ -256,43 +256,37 @@ static int softmax_row(const void *x, int dtype, int64_t off, int V, double T, d
  *     is always kept (so top_p <= 0 keeps only it);
  *   then p = softmax(x / T) renormalised over the kept tokens (fp64).
  *
- * The top-p boundary is a floating-point decision: at V ~ 1e5 the masses of
- * neighbouring tokens differ by ~1e-6 of the total, below the error of any
- * fp32 sum.  It is therefore taken in a stated precision, the same on every
- * side that claims this definition:
- *   c = fp32(log2(e) / T)        (T the fp32 temperature, quotient in double)
- *   t = fp32(fp32(x_v - x_max) * c)
- *   w = 2^t by range reduction (t = i + f, i = rint(t), |f| <= 1/2; Cody and
- *       Waite) and the degree-7 Taylor polynomial of 2^f = e^(f ln 2)
- *       evaluated in fp32 by Horner's rule with fused multiply-adds;
- *   Q = floor(w * 2^40) as an unsigned 64-bit integer (0 for t < -64), and
- *       every mass in the decision is an exact integer sum of Q;
- *   keep v iff x_v = x_max or double(A(v)) < double(top_p) * double(T_Q),
- *       A(v) = sum of Q over kept-by-top-k tokens with a larger logit, T_Q the
- *       sum over all kept-by-top-k tokens.
- * Exact integer sums make the decision independent of summation order.
+ * The top-p decision is taken on that definition in real arithmetic.  The
+ * masses are m_v = e^{(x_v - x_max) / T} (x_max the largest kept logit, so
+ * the top mass is exactly 1), computed in fp64: x_v - x_max and the division
+ * by T are rounded once each (|a| u of relative error for the exponent a,
+ * u = 2^-53), exp within one ulp, so each mass is within (2 + |a|) u of its
+ * exact value relative, and |a| e^a <= 1/e bounds the second part by u/e in
+ * absolute terms.  Sums are compensated (Neumaier), within 2u of the exact
+ * sum of their terms.  A partial mass A and the total M are therefore
+ * within 4u M + n u / e of their exact values (n kept tokens), and the
+ * comparison A < top_p * M (top_p the fp32 value as given, the product
+ * rounded once) is exact whenever |A - top_p M| exceeds
+ *   eps = (10 M + n) u.
+ * A decision inside that band is taken as computed and reported (the
+ * "undecided" output of oracle_filter_cut); at the sizes used here the band
+ * is ~1e-15 of the total.
  */
 
-/* (ln 2)^n / n!, n = 0..7, rounded to fp32 */
-static const float kExp2Taylor[8] = {
-    0x1p+0f, 0x1.62e430p-1f, 0x1.ebfbe0p-3f, 0x1.c6b08ep-5f,
-    0x1.3b2ab6p-7f, 0x1.5d87fep-10f, 0x1.430912p-13f, 0x1.ffcbfcp-17f,
-};
-
-/* Q40 weight of a logit whose difference to the row maximum is d (<= 0). */
-uint64_t oracle_q40_weight(float d, float c)
+/* compensated (Neumaier) running sum */
+typedef struct {
+    double s, c;
+} CSum;
+static void csum_add(CSum *a, double v)
 {
-    float t = d * c;
-    if (!(t >= -64.0f))
-        return 0; /* also -inf */
-    float i = rintf(t);
-    float f = t - i;
-    float poly = kExp2Taylor[7];
-    for (int n = 6; n >= 0; --n)
-        poly = fmaf(poly, f, kExp2Taylor[n]);
-    float w = ldexpf(poly, (int)i + 40);
-    return (uint64_t)w;
+    double t = a->s + v;
+    if (fabs(a->s) >= fabs(v))
+        a->c += (a->s - t) + v;
+    else
+        a->c += (v - t) + a->s;
+    a->s = t;
 }
+static double csum_val(const CSum *a) { return a->s + a->c; }
 
 typedef struct {
     double x;
@@ -318,12 +312,22 @@ static double cut_value(double x)
 }
 
 /* Smallest kept logit (the keep test is x >= cut) of a row after top-k and
-   top-p; -inf when nothing is filtered.  vals is scratch of V entries. */
+   top-p; -inf when nothing is filtered.  vals is scratch of V entries.
+   Optional outputs: *margin = min |A - top_p M| over the two top-p decisions
+   next to the cut (masses in units of the top mass; +inf without top-p),
+   *total = M, *undecided = 1 when a decision of the row fell inside the
+   error band eps. */
 static double filter_cut(const void *x, int dtype, int64_t off, int V, float T, int top_k, float top_p,
-                         ValIdx *vals)
+                         ValIdx *vals, double *margin, double *total_out, int *undecided)
 {
     int use_k = top_k > 0 && top_k < V;
     int use_p = top_p < 1.0f;
+    if (margin)
+        *margin = INFINITY;
+    if (total_out)
+        *total_out = 0.0;
+    if (undecided)
+        *undecided = 0;
     if (!use_k && !use_p)
         return -INFINITY;
     for (int v = 0; v < V; ++v) {
@@ -343,31 +347,48 @@ static double filter_cut(const void *x, int dtype, int64_t off, int V, float T, 
             return INFINITY;
         return vals[nk - 1].x;
     }
-    const float c = (float)(1.44269504088896340736 / (double)T);
-    const float xmax = (float)vals[0].x;
-    uint64_t total = 0;
+    const double Td = (double)T;
+    const double xmax = vals[0].x;
+    CSum tot = {0.0, 0.0};
     for (int i = 0; i < nk; ++i)
-        total += oracle_q40_weight((float)vals[i].x - xmax, c);
-    const double bound = (double)top_p * (double)total;
-    uint64_t above = 0;
-    int i = 0;
+        csum_add(&tot, exp((vals[i].x - xmax) / Td));
+    const double M = csum_val(&tot);
+    const double bound = (double)top_p * M;
+    const double eps = (10.0 * M + (double)nk) * 0x1p-53;
+    CSum above = {0.0, 0.0};
+    double prev_gap = INFINITY, last_gap = INFINITY;
+    int i = 0, und = 0;
     double cut = vals[0].x;
     while (i < nk) {
         int e = i; /* the group of values equal to vals[i] */
-        uint64_t gm = 0;
+        CSum gm = {0.0, 0.0};
         while (e < nk && vals[e].x == vals[i].x) {
-            gm += oracle_q40_weight((float)vals[e].x - xmax, c);
+            csum_add(&gm, exp((vals[e].x - xmax) / Td));
             ++e;
         }
-        int keep = (i == 0) || ((double)above < bound);
+        const double a = csum_val(&above);
+        int keep = (i == 0) || (a < bound);
         if (g_mutant == MUT_TOPP_BELOW)
-            keep = (i == 0) || ((double)(above + gm) <= bound);
-        if (!keep)
+            keep = (i == 0) || (a + csum_val(&gm) <= bound);
+        const double gap = fabs(a - bound);
+        if (i > 0 && gap <= eps)
+            und = 1;
+        if (!keep) {
+            last_gap = gap; /* the first dropped group */
             break;
+        }
+        if (i > 0)
+            prev_gap = gap; /* the last kept group (so far) */
         cut = vals[i].x;
-        above += gm;
+        csum_add(&above, csum_val(&gm));
         i = e;
     }
+    if (margin)
+        *margin = fmin(prev_gap, last_gap);
+    if (total_out)
+        *total_out = M;
+    if (undecided)
+        *undecided = und;
     if (g_mutant == MUT_TOPP_FIRST && use_k) {
         /* mistaken order: the top-k cut taken after the nucleus */
         double ck = vals[top_k - 1].x;
@@ -386,7 +407,7 @@ static int processed_row(const void *x, int dtype, int64_t off, int V, double T,
     int bad = softmax_row(x, dtype, off, V, T, p);
     if (bad)
         return bad;
-    double cut = filter_cut(x, dtype, off, V, (float)T, top_k, top_p, vals);
+    double cut = filter_cut(x, dtype, off, V, (float)T, top_k, top_p, vals, NULL, NULL, NULL);
     if (cut == -INFINITY)
         return 0;
     double s = 0.0;
@@ -589,12 +610,22 @@ int oracle_softmax_row(const void *logits, int dtype, int64_t row, int V, double
     return bad;
 }
 
-/* The smallest kept logit of a row after top-k / top-p (-inf: no filter). */
-double oracle_filter_cut(const void *logits, int dtype, int64_t row, int V, float T, int top_k, float top_p)
+/* The smallest kept logit of a row after top-k / top-p (-inf: no filter);
+   info (or NULL) receives [margin, total mass, undecided] of the top-p
+   decision (filter_cut). */
+double oracle_filter_cut(const void *logits, int dtype, int64_t row, int V, float T, int top_k, float top_p,
+                         double *info)
 {
     ValIdx *vals = (ValIdx *)malloc(sizeof(ValIdx) * (size_t)(V > 0 ? V : 1));
-    double cut = filter_cut(logits, dtype, row * V, V, T, top_k, top_p, vals);
+    double margin, total;
+    int und;
+    double cut = filter_cut(logits, dtype, row * V, V, T, top_k, top_p, vals, &margin, &total, &und);
     free(vals);
+    if (info) {
+        info[0] = margin;
+        info[1] = total;
+        info[2] = (double)und;
+    }
     return cut;
 }
 

@@ -4,17 +4,21 @@ the target distribution of stochastic verification (CPU only).
 The pages require the ratio test, the residual and the bonus to use the
 processed distribution ("Chapter 10 Speculative Decoding (Code Walkthrough)",
 §5.1; "Speculative decoding: proposals and verified output", "The mechanism"
-step 1) without defining the transforms.  Pinned here:
-  - a hand-worked example with exact power-of-two weights (tests/golden);
-  - brute force on tiny inputs in exact rational arithmetic, from the
-    definitions restated independently (top-k: fewer than k tokens strictly
-    larger; top-p: the smallest upper set of mass >= top_p);
+step 1) without defining the transforms.  The oracle takes the plain
+definitions and decides the top-p boundary on the masses e^((x - x_max)/T)
+in fp64 with a stated error band.  Pinned here:
+  - a hand-worked example with power-of-two weights (tests/golden);
+  - brute force on tiny inputs, from the definitions restated independently
+    (top-k: fewer than k tokens strictly larger; top-p: the smallest upper
+    set of mass >= top_p): exact rationals on integer logits, and
+    50-digit arithmetic on real-valued logits at several temperatures;
+  - on rows of 128256 N(0,1) logits (fp32 and bf16), the kept set is the
+    smallest top set reaching top_p, checked with correctly rounded sums;
   - top_k = 1 (and top_p -> 0) turns stochastic verification into greedy
     verification, checked against the greedy oracle;
   - top_k >= V, top_p = 1 leave every output unchanged;
   - the committed token's distribution equals the processed distribution
     (midpoint grid over the uniforms), and acceptance = sum min(p', q);
-  - the fixed-point weight of the nucleus decision against 2^t;
   - -0 and +0 are one value at the cut, in every storage type;
   - six planted mistakes each fail at least one of these.
 """
@@ -27,7 +31,12 @@ import oracle
 from conftest import golden
 from oracle import DT_F32
 
-T_UNIT = float(np.float32(np.log2(np.e)))  # fp32(log2 e): the decision scale c is exactly 1
+# fp32(log2 e) as the temperature: masses e^(x/T) = 2^(x (1 + d)) with
+# d = 1.3e-8, so integer logits give (almost exactly) powers of two; where an
+# upper set's mass equals top_p times the total exactly in powers of two,
+# d > 0 moves it above that bound, as the strict test of the definition does
+# at an exact tie (the set's mean logit exceeds the row's)
+T_UNIT = float(np.float32(np.log2(np.e)))
 
 
 def _case_table():
@@ -198,21 +207,95 @@ def test_output_distribution_is_the_processed_target(name):
     assert abs(acc - np.minimum(pp, q).sum()) < 4e-3
 
 
-def test_q40_weight_against_powers_of_two():
-    for t in range(-64, 1):
-        assert oracle.q40_weight(float(t), 1.0) == (2 ** (40 + t) if t >= -40 else 0)
-    assert oracle.q40_weight(-65.0, 1.0) == 0 and oracle.q40_weight(-np.inf, 1.0) == 0
-    rng = np.random.default_rng(3)
-    for t in rng.uniform(-30, 0, size=4000).astype(np.float32):
-        want = 2.0 ** (40 + float(t))
-        got = oracle.q40_weight(float(t), 1.0)
-        assert abs(got - want) <= want * 2.5e-7 + 1.0, (t, got, want)
+def _exact_kept(x, T, top_k, top_p, dps=50):
+    """Kept set from the definitions with 50-digit masses e^((x - x_max)/T)."""
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = dps
+    V = len(x)
+    keep = [True] * V
+    if 0 < top_k < V:
+        keep = [sum(1 for u in x if u > x[v]) < top_k for v in range(V)]
+    margin = mp.inf
+    if top_p < 1.0:
+        xm = max(float(x[v]) for v in range(V) if keep[v])
+        w = [mp.e ** ((mp.mpf(float(x[v])) - xm) / mp.mpf(T)) if keep[v] else mp.mpf(0) for v in range(V)]
+        tot = sum(w)
+        bound = mp.mpf(float(np.float32(top_p))) * tot
+        vals = sorted({float(x[v]) for v in range(V) if keep[v]}, reverse=True)
+        for i, t in enumerate(vals):
+            above = sum(w[v] for v in range(V) if keep[v] and x[v] > t)
+            if i > 0:
+                margin = min(margin, abs(above - bound) / tot)
+            if i > 0 and not above < bound:
+                keep = [keep[v] and x[v] > t for v in range(V)]
+                break
+    return keep, margin
+
+
+def test_exact_arithmetic_on_tiny_real_rows():
+    """Real-valued logits at temperatures 0.37 .. 3: the kept set equals the
+    one computed with 50-digit masses (no decision here lies within 1e-12 of
+    its bound, far outside the oracle's fp64 band)."""
+    rng = np.random.default_rng(23)
+    n = 0
+    for _ in range(1500):
+        V = int(rng.integers(1, 9))
+        x = (rng.standard_normal(V) * rng.choice([0.5, 1.0, 3.0])).astype(np.float32)
+        if rng.random() < 0.3:  # some repeated values
+            x[rng.integers(0, V, size=V // 2)] = x[0]
+        T = float(np.float32(rng.choice([0.37, 1.0, 1.7, 3.0])))
+        top_k = int(rng.integers(0, V + 2))
+        top_p = float(np.float32(rng.choice([rng.random(), 0.0, 0.5, 0.9, 0.95, 1.0])))
+        keep, margin = _exact_kept(list(x), T, top_k, top_p)
+        if margin < 1e-12:
+            continue
+        p, bad = oracle.softmax_row(x[None], DT_F32, 0, T, top_k, top_p)
+        assert not bad
+        assert list(p > 0) == keep, (x, T, top_k, top_p, p)
+        n += 1
+    assert n > 1400
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("top_p", [0.5, 0.9, 0.95])
+def test_nucleus_is_the_smallest_top_set_on_full_size_rows(dt, top_p):
+    """Rows of V = 128256 N(0,1) logits (the vocabulary of the stochastic
+    workloads): with masses e^(x - x_max) summed by math.fsum (correctly
+    rounded), the mass strictly above the cut is below top_p times the total
+    and the mass at or above it reaches it -- the kept set is the smallest
+    top set reaching top_p.  The oracle's reported margin is the distance of
+    those two sums to the bound, and no decision falls in its error band."""
+    import math
+
+    from specgen import bf16_bits_to_f32, f32_to_bf16_bits
+
+    rng = np.random.default_rng(int(top_p * 100) + (dt == "bf16"))
+    V = 128256
+    tp = float(np.float32(top_p))
+    for _ in range(6):
+        x = rng.standard_normal(V).astype(np.float32)
+        if dt == "bf16":
+            xs = f32_to_bf16_bits(x)
+            xv, code = bf16_bits_to_f32(xs).astype(np.float64), oracle.DT_BF16
+        else:
+            xs, xv, code = x, x.astype(np.float64), DT_F32
+        cut, margin, total, undecided = oracle.filter_info(xs[None], code, 0, 1.0, 0, tp)
+        assert not undecided
+        w = np.exp(xv - xv.max())
+        M = math.fsum(w)
+        above = math.fsum(w[xv > cut])
+        upto = math.fsum(w[xv >= cut])
+        assert above < tp * M <= upto, (above / M, upto / M)
+        assert abs(total - M) <= 1e-12 * M
+        assert abs(min(tp * M - above, upto - tp * M) - margin) <= 1e-9 * M
+        assert cut in xv
 
 
 @pytest.mark.parametrize("mut", ["topk_strict", "topp_below", "ratio_unfiltered", "resid_unfiltered",
                                  "topp_first", "zero_sign_order"])
 def test_planted_mistakes_fail_a_pin(mut):
     checks = [test_worked_example, test_top_k_one_is_greedy, test_brute_force_tiny_rows,
+              test_exact_arithmetic_on_tiny_real_rows,
               lambda: test_signed_zeros_are_one_value("bf16"),
               lambda: [test_output_distribution_is_the_processed_target(n)
                        for n in ("k2", "k3", "p0625", "p0875", "k3p05625")]]
