@@ -109,7 +109,9 @@ VerifyArgs sample_args(const void *logits, float temperature, const int32_t *top
     a.filtered = (top_k || top_p) ? 1 : 0;
     a.top_k = top_k;
     a.top_p = top_p;
-    a.dec_scale = (float)(1.44269504088896340736 / (double)temperature);
+    const double dec = 1.44269504088896340736 / (double)temperature;
+    a.dec_hi = (float)dec;
+    a.dec_lo = (float)(dec - (double)a.dec_hi);
     return a;
 }
 

@@ -39,7 +39,7 @@ struct VerifyArgs {
     int filtered;
     const int32_t *top_k;  // [B] or null
     const float *top_p;    // [B] or null
-    float dec_scale;       // fp32(log2(e) / T), the scale of the top-p decision weights
+    float dec_hi, dec_lo;  // log2(e) / T as a float pair: the scale of the top-p decision weights
     float *row_cut;        // workspace: smallest kept logit per row
 };
 

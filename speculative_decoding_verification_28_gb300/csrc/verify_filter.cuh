@@ -12,13 +12,19 @@
 //     always kept);
 //   p = softmax(x / T) renormalised over the kept tokens.
 // The top-p boundary is decided on exact integer sums of fixed-point weights
-// Q = floor(2^40 * w), w = 2^t with t = fp32(fp32(x - x_max) * c) and
-// c = fp32(log2(e) / T): t = i + f, i = rint(t), |f| <= 1/2 (Cody-Waite range
-// reduction) and 2^f from its degree-7 Taylor polynomial (coefficients
-// (ln 2)^n / n! in fp32) by Horner's rule with fused multiply-adds.  Integer
-// sums do not depend on the order of summation, so the decision is
-// reproducible; the kept token probabilities use the same ex2-based softmax
-// as the unfiltered path.
+// Q = floor(2^40 * 2^t), t = (x - x_max) * log2(e) / T, computed to about
+// 2e-9 relative (DecScale, dec_weight below): x - x_max exactly (TwoSum),
+// t as a float-float product with log2(e)/T held as a float pair, 2^t as
+// 2^n * 2^(k/64) * 2^r (Tang's table-driven method: 64 float-float table
+// entries, |r| <= 1/128 plus the low part of t, 2^r - 1 from its degree-4
+// Taylor polynomial), and the floor taken from the float pair in integers
+// (within one unit of 2^-40).  The kept set then differs from the one the
+// real masses give only where the true mass above a value lies within ~4e-9
+// of top_p times the total (plus V * 2^-39 for the floors, in units of the
+// top mass).  Integer sums do not
+// depend on the order of summation, so the decision is reproducible; the
+// kept token probabilities use the same ex2-based softmax as the unfiltered
+// path.
 //
 // Two kernels, one CTA per target row each (rows j-major, skipped once an
 // earlier stop of the sequence is known, as in the statistics kernel).
@@ -96,68 +102,109 @@ struct KeyLevels<float> {
     static constexpr int kLevels = 3;
 };
 
-// Q40 weight of a logit at difference d = x - x_max (<= 0) and scale c
-__device__ __forceinline__ unsigned long long q40_weight(float d, float c)
+// The decision scale log2(e) / T as a float pair (hi + lo, ~48 bits) and
+// the shared-memory copy of the table 2^(k/64).
+struct DecScale {
+    float hi, lo;
+    const float2 *tab;
+};
+
+// 2^(k/64), k = 0..63, as float pairs hi + lo: hi = 2^(k/64) rounded to fp32,
+// lo = the rest rounded to fp32 (the table of Tang's table-driven exponential;
+// the pair is within 2^-48 of 2^(k/64) relative)
+static __constant__ float2 kExp2Tab64[64] = {
+    {0x1p+0f, 0.0f}, {0x1.02c9a4p+0f, -0x1.887fap-28f}, {0x1.059b0ep+0f, -0x1.9d4f52p-25f}, {0x1.087452p+0f, -0x1.e2990ep-26f},
+    {0x1.0b5586p+0f, 0x1.9f3122p-25f}, {0x1.0e3ec4p+0f, -0x1.a585ccp-25f}, {0x1.11301ep+0f, -0x1.fdb496p-25f}, {0x1.1429aap+0f, 0x1.d525bcp-25f},
+    {0x1.172b84p+0f, -0x1.c15742p-27f}, {0x1.1a35bep+0f, 0x1.6df96ep-25f}, {0x1.1d4874p+0f, -0x1.d2e8cap-25f}, {0x1.2063b8p+0f, 0x1.0c519ap-25f},
+    {0x1.2387a6p+0f, 0x1.ceac48p-25f}, {0x1.26b456p+0f, 0x1.789f38p-26f}, {0x1.29e9ep+0f, -0x1.5c0424p-25f}, {0x1.2d285ap+0f, 0x1.b900c2p-26f},
+    {0x1.306fep+0f, 0x1.4636e2p-25f}, {0x1.33c08cp+0f, -0x1.b37d2p-25f}, {0x1.371a74p+0f, -0x1.18aac6p-25f}, {0x1.3a7db4p+0f, -0x1.634c02p-25f},
+    {0x1.3dea64p+0f, 0x1.824684p-25f}, {0x1.4160a2p+0f, 0x1.f72e2ap-28f}, {0x1.44e086p+0f, 0x1.8624b4p-30f}, {0x1.486a2cp+0f, -0x1.47d866p-25f},
+    {0x1.4bfdaep+0f, -0x1.593abcp-25f}, {0x1.4f9b28p+0f, -0x1.2c5a6cp-25f}, {0x1.5342b6p+0f, -0x1.2c561p-25f}, {0x1.56f474p+0f, -0x1.295b04p-25f},
+    {0x1.5ab07ep+0f, -0x1.5bd5ecp-27f}, {0x1.5e76f2p+0f, -0x1.4a5bd6p-25f}, {0x1.6247ecp+0f, -0x1.f8b55p-25f}, {0x1.662388p+0f, 0x1.2a9112p-27f},
+    {0x1.6a09e6p+0f, 0x1.9fcef4p-26f}, {0x1.6dfb24p+0f, -0x1.cd72e8p-27f}, {0x1.71f75ep+0f, 0x1.1d8beep-25f}, {0x1.75feb6p+0f, -0x1.37b306p-25f},
+    {0x1.7a1148p+0f, -0x1.829fdp-25f}, {0x1.7e2f34p+0f, -0x1.261634p-25f}, {0x1.82589ap+0f, -0x1.accc7cp-26f}, {0x1.868d9ap+0f, -0x1.2edb44p-26f},
+    {0x1.8ace54p+0f, 0x1.15506ep-27f}, {0x1.8f1aeap+0f, -0x1.baa232p-26f}, {0x1.93737cp+0f, -0x1.e64744p-25f}, {0x1.97d82ap+0f, -0x1.0d8d84p-31f},
+    {0x1.9c4918p+0f, 0x1.51f848p-27f}, {0x1.a0c668p+0f, -0x1.2886a6p-26f}, {0x1.a5503cp+0f, -0x1.b83b54p-25f}, {0x1.a9e6b6p+0f, -0x1.50c048p-25f},
+    {0x1.ae89fap+0f, -0x1.a94b14p-26f}, {0x1.b33a2cp+0f, -0x1.ec3a82p-26f}, {0x1.b7f77p+0f, -0x1.a09438p-25f}, {0x1.bcc1eap+0f, -0x1.f687c6p-25f},
+    {0x1.c199bep+0f, -0x1.3d56b2p-27f}, {0x1.c67f12p+0f, 0x1.cafa2ap-25f}, {0x1.cb720ep+0f, -0x1.8837ccp-27f}, {0x1.d072d4p+0f, 0x1.40f13p-25f},
+    {0x1.d5818ep+0f, -0x1.822dbcp-27f}, {0x1.da9e6p+0f, 0x1.ed9942p-27f}, {0x1.dfc974p+0f, -0x1.908c94p-25f}, {0x1.e502eep+0f, 0x1.e2cffep-26f},
+    {0x1.ea4afap+0f, 0x1.52486cp-27f}, {0x1.efa1bep+0f, 0x1.cc2b44p-25f}, {0x1.f50766p+0f, -0x1.246ebp-26f}, {0x1.fa7c18p+0f, 0x1.9e90d8p-28f},
+};
+
+// all threads, before the first barrier of the kernel: the table into shared
+// memory (the weight's lookup index differs across a warp's lanes)
+__device__ __forceinline__ void dec_table_init(float2 *tab)
 {
-    const float t = __fmul_rn(d, c);
-    if (!(t >= -64.0f))
+    for (int i = threadIdx.x; i < 64; i += blockDim.x)
+        tab[i] = kExp2Tab64[i];
+}
+
+// 2^r - 1 for |r| <= 1/128 + 2^-18: Taylor coefficients (ln 2)^n / n!, n = 1..4
+// (the degree-5 term is below 4e-14)
+__device__ __forceinline__ float exp2m1_small(float r)
+{
+    float q = __fmaf_rn(0x1.3b2ab6p-7f, r, 0x1.c6b08ep-5f);
+    q = __fmaf_rn(q, r, 0x1.ebfbe0p-3f);
+    q = __fmaf_rn(q, r, 0x1.62e430p-1f);
+    return __fmul_rn(q, r);
+}
+
+// The Q weight from p + tl (the high and low parts of t <= 0): 2^t = 2^n *
+// 2^(k/64) * 2^r with j = rint(64 p), n = floor(j / 64), k = j mod 64 and
+// r = (p - j/64) + tl (p - j/64 is exact); w = T_hi + w_lo with
+// w_lo = T_hi * (2^r - 1) + T_lo (|w_lo| < 2^-6), and Q = floor(w * 2^(n+40))
+// from Z = w * 2^47 in integers: T_hi in [1, 2) is its 24-bit significand
+// m_h times 2^-23, and w_lo * 2^47 = A * 2^24 + B with A = floor(w_lo * 2^23)
+// and 0 <= B < 2^24, both exact fp32 values converted by 32-bit conversions
+// (B rounds only when |w_lo| < 2^-23, by less than one unit of 2^-47); then
+// Q = Z >> (7 - n), within one unit of the exact floor.
+__device__ __forceinline__ unsigned long long dec_q(float p, float tl, const float2 *tab)
+{
+    if (!(p >= -64.0f))  // 2^t < 2^-64: Q = 0 (also -inf and NaN)
         return 0ull;
-    const float i = rintf(t);
-    const float f = __fsub_rn(t, i);
-    float p = 0x1.ffcbfcp-17f;
-    p = __fmaf_rn(p, f, 0x1.430912p-13f);
-    p = __fmaf_rn(p, f, 0x1.5d87fep-10f);
-    p = __fmaf_rn(p, f, 0x1.3b2ab6p-7f);
-    p = __fmaf_rn(p, f, 0x1.c6b08ep-5f);
-    p = __fmaf_rn(p, f, 0x1.ebfbe0p-3f);
-    p = __fmaf_rn(p, f, 0x1.62e430p-1f);
-    p = __fmaf_rn(p, f, 1.0f);
-    const float scale = __int_as_float(((int)i + 40 + 127) << 23);  // 2^(i+40), i in [-64, 0]
-    return __float2ull_rz(__fmul_rn(p, scale));
+    const float j = rintf(__fmul_rn(p, 64.0f));
+    const float r = __fadd_rn(__fmaf_rn(j, -0.015625f, p), tl);
+    const float q = exp2m1_small(r);
+    const int ji = (int)j;
+    const float2 T = tab[ji & 63];
+    const float wl = __fmaf_rn(T.x, q, T.y);
+    const float a = floorf(__fmul_rn(wl, 0x1p23f));
+    const float b = __fmaf_rn(-a, 0x1p24f, __fmul_rn(wl, 0x1p47f));
+    const uint32_t mh_a = ((__float_as_uint(T.x) & 0x7FFFFFu) | 0x800000u) + (uint32_t)(int)a;
+    const unsigned long long Z = ((unsigned long long)mh_a << 24) + (unsigned long long)(uint32_t)b;
+    const int sh = 7 - (ji >> 6);  // 7 .. 71
+    return sh < 64 ? (Z >> sh) : 0ull;
 }
 
-// floor(p * 2^(i + 40)) for p in [0.5, 2) and i in [-65, 0] from integer
-// instructions only: the product is exact (a power-of-two scale of a normal
-// float), so it is p's 24-bit significand shifted by the product's exponent
-__device__ __forceinline__ unsigned long long q40_bits(float p, int i)
+// Q weight of a logit x against the row maximum xmax (x <= xmax)
+__device__ __forceinline__ unsigned long long dec_weight(float x, float xmax, const DecScale &dw)
 {
-    const uint32_t b = __float_as_uint(p);
-    const uint32_t m = (b & 0x7FFFFFu) | 0x800000u;
-    const int s = (int)(b >> 23) - 127 + i + 40 - 23;  // weight of the significand's lowest bit
-    if (s >= 0)
-        return (unsigned long long)m << s;
-    return s > -24 ? (unsigned long long)(m >> -s) : 0ull;
+    // d = dh + dl = x - xmax exactly (TwoSum)
+    const float dh = __fsub_rn(x, xmax);
+    const float bb = __fsub_rn(dh, x);
+    const float dl = __fadd_rn(__fsub_rn(x, __fsub_rn(dh, bb)), __fsub_rn(-xmax, bb));
+    // t = p + tl = d * (hi + lo) to ~2^-46 relative
+    const float p = __fmul_rn(dh, dw.hi);
+    const float e = __fmaf_rn(dh, dw.hi, -p);  // the product's rounding error, exactly
+    const float tl = __fmaf_rn(dh, dw.lo, __fmaf_rn(dl, dw.hi, e));
+    return dec_q(p, tl, dw.tab);
 }
 
-// q40_weight of two logits at once with paired fp32 instructions (FMUL2,
-// FADD2, FFMA2; every lane rounded to nearest, so each result is bit for bit
-// q40_weight's).  t is clamped at -65 before the integer scale is formed, so
-// an out-of-range t never reaches the conversion; such a t gives 0 anyway.
-// kBits: the last step by q40_bits instead of the float product and its
-// conversion to 64 bits (same result; no conversion unit).
-template <bool kBits = false>
-__device__ __forceinline__ void q40_weight2(float2 d, float c, unsigned long long &q0, unsigned long long &q1)
+// dec_weight of two logits, the float steps paired (FADD2 / FMUL2 / FFMA2;
+// each lane rounded as the scalar form, so the results are dec_weight's)
+__device__ __forceinline__ void dec_weight2(float x0, float x1, float xmax, const DecScale &dw,
+                                            unsigned long long &q0, unsigned long long &q1)
 {
-    const float2 t = __fmul2_rn(d, make_float2(c, c));
-    const float i0 = rintf(fmaxf(t.x, -65.0f)), i1 = rintf(fmaxf(t.y, -65.0f));
-    const float2 f = __fadd2_rn(t, make_float2(-i0, -i1));
-    float2 p = make_float2(0x1.ffcbfcp-17f, 0x1.ffcbfcp-17f);
-    p = __ffma2_rn(p, f, make_float2(0x1.430912p-13f, 0x1.430912p-13f));
-    p = __ffma2_rn(p, f, make_float2(0x1.5d87fep-10f, 0x1.5d87fep-10f));
-    p = __ffma2_rn(p, f, make_float2(0x1.3b2ab6p-7f, 0x1.3b2ab6p-7f));
-    p = __ffma2_rn(p, f, make_float2(0x1.c6b08ep-5f, 0x1.c6b08ep-5f));
-    p = __ffma2_rn(p, f, make_float2(0x1.ebfbe0p-3f, 0x1.ebfbe0p-3f));
-    p = __ffma2_rn(p, f, make_float2(0x1.62e430p-1f, 0x1.62e430p-1f));
-    p = __ffma2_rn(p, f, make_float2(1.0f, 1.0f));
-    if constexpr (kBits) {
-        q0 = (t.x >= -64.0f) ? q40_bits(p.x, (int)i0) : 0ull;
-        q1 = (t.y >= -64.0f) ? q40_bits(p.y, (int)i1) : 0ull;
-    } else {
-        const float2 sc = make_float2(__int_as_float(((int)i0 + 40 + 127) << 23), __int_as_float(((int)i1 + 40 + 127) << 23));
-        const float2 r = __fmul2_rn(p, sc);
-        q0 = (t.x >= -64.0f) ? __float2ull_rz(r.x) : 0ull;
-        q1 = (t.y >= -64.0f) ? __float2ull_rz(r.y) : 0ull;
-    }
+    const float2 x = make_float2(x0, x1), nm = make_float2(-xmax, -xmax);
+    const float2 dh = __fadd2_rn(x, nm);
+    const float2 bb = __fadd2_rn(dh, make_float2(-x0, -x1));
+    const float2 t1 = __fadd2_rn(dh, make_float2(-bb.x, -bb.y));
+    const float2 dl = __fadd2_rn(__fadd2_rn(x, make_float2(-t1.x, -t1.y)), __fadd2_rn(nm, make_float2(-bb.x, -bb.y)));
+    const float2 p = __fmul2_rn(dh, make_float2(dw.hi, dw.hi));
+    const float2 e = __ffma2_rn(dh, make_float2(dw.hi, dw.hi), make_float2(-p.x, -p.y));
+    const float2 tl = __ffma2_rn(dh, make_float2(dw.lo, dw.lo), __ffma2_rn(dl, make_float2(dw.hi, dw.hi), e));
+    q0 = dec_q(p.x, tl.x, dw.tab);
+    q1 = dec_q(p.y, tl.y, dw.tab);
 }
 
 // f(x) for every logit of the row: 16-byte vectors, scalar head and tail
@@ -243,8 +290,8 @@ __device__ __forceinline__ void hist_clear(FilterHist &h, int nb)
 // Counts (and Q masses) per digit of level l over the logits whose key is
 // >= lo_key and whose higher digits equal `prefix`.
 template <typename T, bool kMass, int NT>
-__device__ void hist_pass(const T *row, int V, int l, uint32_t prefix, uint32_t lo_key, float xmax, float cdec,
-                          FilterHist &h)
+__device__ void hist_pass(const T *row, int V, int l, uint32_t prefix, uint32_t lo_key, float xmax,
+                          const DecScale &dw, FilterHist &h)
 {
     const int sh = lvl_shift(l), msk = lvl_bins(l) - 1;
     const int shp = (l == 0) ? 0 : lvl_shift(l - 1);
@@ -255,7 +302,7 @@ __device__ void hist_pass(const T *row, int V, int l, uint32_t prefix, uint32_t 
         const int dg = (int)((key >> sh) & (uint32_t)msk);
         atomicAdd(&h.cnt[dg], 1u);
         if (kMass) {
-            const unsigned long long q = q40_weight(__fsub_rn(x, xmax), cdec);
+            const unsigned long long q = dec_weight(x, xmax, dw);
             atomicAdd(&h.mlo[dg], (unsigned int)(q & 0x3FFFull));
             atomicAdd(&h.mmid[dg], (unsigned int)((q >> 14) & 0x3FFFull));
             atomicAdd(&h.mhi[dg], (unsigned int)(q >> 28));
@@ -273,7 +320,7 @@ __device__ void hist_pass(const T *row, int V, int l, uint32_t prefix, uint32_t 
         auto add2 = [&](float x0, float x1) {
             const uint32_t k0 = order_key(x0), k1 = order_key(x1);
             unsigned long long q0, q1;
-            q40_weight2(__fadd2_rn(make_float2(x0, x1), make_float2(-xmax, -xmax)), cdec, q0, q1);
+            dec_weight2(x0, x1, xmax, dw, q0, q1);
             if (k0 >= lo_key) {
                 const int dg = (int)(k0 >> sh);
                 atomicAdd(&h.cnt[dg], 1u);
@@ -443,7 +490,7 @@ __device__ float row_max_pass(const T *row, int V, float *s_f)
 // at or above it.  Returns the smallest kept logit; kept_mass: the Q mass of
 // the kept logits.
 template <typename T, int NT>
-__device__ __forceinline__ float radix_cut(const T *row, int V, float xmax, float cdec, int tk, float tp, bool use_k,
+__device__ __forceinline__ float radix_cut(const T *row, int V, float xmax, const DecScale &dw, int tk, float tp, bool use_k,
                                            bool use_p, FilterHist &h, FilterSel &sel, unsigned int *s_wc,
                                            unsigned long long *s_wm, unsigned long long &kept_mass)
 {
@@ -459,9 +506,9 @@ __device__ __forceinline__ float radix_cut(const T *row, int V, float xmax, floa
             hist_clear<NT>(h, nb);
             __syncthreads();
             if (use_p)
-                hist_pass<T, false, NT>(row, V, l, prefix, 0u, xmax, cdec, h);
+                hist_pass<T, false, NT>(row, V, l, prefix, 0u, xmax, dw, h);
             else
-                hist_pass<T, true, NT>(row, V, l, prefix, 0u, xmax, cdec, h);
+                hist_pass<T, true, NT>(row, V, l, prefix, 0u, xmax, dw, h);
             __syncthreads();
             hist_select<false, NT>(h, nb, need, 0ull, 0.0f, false, sel, s_wc, s_wm);
             const int bin = sel.bin < 0 ? 0 : sel.bin;  // a digit is always found
@@ -481,7 +528,7 @@ __device__ __forceinline__ float radix_cut(const T *row, int V, float xmax, floa
             const int nb = lvl_bins(l);
             hist_clear<NT>(h, nb);
             __syncthreads();
-            hist_pass<T, true, NT>(row, V, l, prefix, K, xmax, cdec, h);
+            hist_pass<T, true, NT>(row, V, l, prefix, K, xmax, dw, h);
             __syncthreads();
             hist_select<true, NT>(h, nb, 0u, A, tp, l == 0, sel, s_wc, s_wm);
             const int bin = sel.bin < 0 ? 0 : sel.bin;  // a digit is always found
@@ -507,13 +554,16 @@ __global__ void __launch_bounds__(NT, NT >= 1024 ? 1 : (NT >= 512 ? 2 : 3)) veri
     __shared__ FilterSel sel;
     __shared__ float s_m, s_s, s_xmax;
     __shared__ int s_bad, s_skip;
+    __shared__ float2 s_e2[64];
     const float c = scale_of(a);
     const Unit u = decode_unit(a);
     const T *row = reinterpret_cast<const T *>(a.logits) + (size_t)u.row * a.V;
     const int t = threadIdx.x;
     if (t == 0)
         s_skip = (!u.needed || stopped_before(a.stop_enc, u.b, u.j)) ? 1 : 0;
+    dec_table_init(s_e2);
     __syncthreads();
+    const DecScale dw{a.dec_hi, a.dec_lo, s_e2};
     float cut = -INFINITY, s_kept = 0.0f;
     if (!s_skip) {
         const int tk = a.top_k ? a.top_k[u.b] : 0;
@@ -547,7 +597,7 @@ __global__ void __launch_bounds__(NT, NT >= 1024 ? 1 : (NT >= 512 ? 2 : 3)) veri
         s_kept = s_s;
         if (!s_skip && !s_bad && (use_k || use_p)) {
             unsigned long long kept_mass;
-            cut = radix_cut<T, NT>(row, a.V, s_xmax, a.dec_scale, tk, tp, use_k, use_p, h, sel, s_wc, s_wm, kept_mass);
+            cut = radix_cut<T, NT>(row, a.V, s_xmax, dw, tk, tp, use_k, use_p, h, sel, s_wc, s_wm, kept_mass);
             s_kept = (float)((double)kept_mass * 0x1p-40);
         }
     }
@@ -568,7 +618,7 @@ __global__ void __launch_bounds__(NT, NT >= 1024 ? 1 : (NT >= 512 ? 2 : 3)) veri
 // each bit pattern (16-bit counters, two per shared word; one shared atomic
 // per logit) and the rest works on the table: the row maximum is its highest
 // non-empty value, and the Q mass of a value is its count times the value's
-// weight q40_weight(x - x_max) -- the same weights and the same exact
+// weight dec_weight(x, x_max) -- the same weights and the same exact
 // integer sums as the radix selection, with one weight per distinct value
 // instead of one per logit per pass.  A block scan in descending value order
 // gives the k-th largest value and the top-p boundary; the thread range that
@@ -725,7 +775,7 @@ __device__ __forceinline__ unsigned long long u64_threshold(double bound)
 // masses) reaches the threshold `athr`; writes that key and the running mass
 // at it to *key_out / *mass_out (untouched when there is none).
 template <typename T, bool kCount>
-__device__ __forceinline__ void tab_walk(const unsigned int *tab, int tc, uint32_t kk, float xmax, float cdec,
+__device__ __forceinline__ void tab_walk(const unsigned int *tab, int tc, uint32_t kk, float xmax, const DecScale &dw,
                                          uint32_t c0, uint32_t need, unsigned long long m0, unsigned long long athr,
                                          int *key_out, unsigned long long *mass_out)
 {
@@ -737,7 +787,7 @@ __device__ __forceinline__ void tab_walk(const unsigned int *tab, int tc, uint32
     // an empty key's weight is not needed: x_max stands in (no inf or NaN)
     const float va = na ? Tab16<T>::value(ha) : xmax, vb = nb ? Tab16<T>::value(hb) : xmax;
     unsigned long long qa, qb;
-    q40_weight2<true>(__fadd2_rn(make_float2(va, vb), make_float2(-xmax, -xmax)), cdec, qa, qb);
+    dec_weight2(va, vb, xmax, dw, qa, qb);
     const unsigned long long ma = (unsigned long long)na * qa, mb = (unsigned long long)nb * qb;
     uint32_t ic = na + nb;
     unsigned long long im = ma + mb;
@@ -771,11 +821,13 @@ __device__ __forceinline__ void tab_walk(const unsigned int *tab, int tc, uint32
 // false when the table is unusable (a wrapped counter: the caller runs the
 // radix selection); else the row's maximum, its non-finite flag and, when
 // the row is filtered and finite, the cut and the kept Q mass.  s_i: 9 ints,
-// s_u: 5 u64 of shared scratch (every slot written once per row).
+// s_u: 5 u64, s_ml: kTabThreads u64 of shared scratch (every slot written
+// once per row).
 template <typename T>
-__device__ bool tab_select(unsigned int *tab, int V, float cdec, int tk, float tp, bool use_k, bool use_p,
+__device__ bool tab_select(unsigned int *tab, int V, const DecScale &dw, int tk, float tp, bool use_k, bool use_p,
                            float &xmax_out, bool &bad_out, float &cut_out, unsigned long long &kept_out,
-                           unsigned int *s_wc, unsigned long long *s_wm, int *s_i, unsigned long long *s_u)
+                           unsigned int *s_wc, unsigned long long *s_wm, int *s_i, unsigned long long *s_u,
+                           unsigned long long *s_ml)
 {
     const int t = threadIdx.x, lane = t & 31;
     const unsigned int *mine = tab + tab_base(t);
@@ -793,6 +845,7 @@ __device__ bool tab_select(unsigned int *tab, int V, float cdec, int tk, float t
         s_i[8] = -1;     // the top-p boundary key
     }
     __syncthreads();
+    s_ml[t] = 0ull;  // pass 2 writes the slots of non-empty blocks only
     // pass 1: count, highest and lowest non-empty key (words read in an order
     // rotated by the lane: no bank conflicts)
     const uint32_t pbase = 2u * (uint32_t)tab_base(t);
@@ -827,21 +880,40 @@ __device__ bool tab_select(unsigned int *tab, int V, float cdec, int tk, float t
     bad_out = kmax >= Tab16<T>::kPinfKey || kmin < Tab16<T>::kNinfKey || kmax <= Tab16<T>::kNinfKey;
     if (bad_out || !(use_k || use_p))
         return true;
-    // pass 2: Q masses, two values per word with paired weights (warps
-    // whose keys are all empty skip it)
-    unsigned long long ml = 0;
-    if (__any_sync(0xFFFFFFFFu, cl != 0u)) {
-#pragma unroll 8
-        for (int i = 0; i < 32; ++i) {  // branch-free: independent weights overlap
-            const int j = (i + lane) & 31;
-            const uint32_t x = mine[j];
-            const uint32_t h = pbase + 2u * (uint32_t)j;
-            const float v0 = (x & 0xFFFFu) ? Tab16<T>::value(h) : xmax, v1 = (x >> 16) ? Tab16<T>::value(h + 1u) : xmax;
-            unsigned long long q0, q1;
-            q40_weight2<true>(__fadd2_rn(make_float2(v0, v1), make_float2(-xmax, -xmax)), cdec, q0, q1);
-            ml += (unsigned long long)(x & 0xFFFFu) * q0 + (unsigned long long)(x >> 16) * q1;
+    // pass 2: Q masses, two values per word with paired weights.  The
+    // non-empty words form a band of values, which in the threads' own
+    // ranges would load a few warps only; so the table's 1024 blocks of 32
+    // words (block b = the range of one thread) are dealt out by warp --
+    // warp w takes blocks w, w + 32, ... -- each lane one word of the block,
+    // and the block's sum goes to its owner's slot (no atomics: each block
+    // has one warp).  Empty blocks are skipped by a ballot.
+    {
+        const int w = t >> 5;
+#pragma unroll 2
+        for (int i = 0; i < 32; ++i) {
+            const int blk = w + 32 * i;  // words 32 blk .. 32 blk + 31
+            const uint32_t word = 32u * (uint32_t)blk + (uint32_t)lane;
+            const uint32_t x = tab[word];
+            if (__ballot_sync(0xFFFFFFFFu, x != 0u) == 0u)
+                continue;
+            unsigned long long m = 0;
+            if (x != 0u) {
+                const uint32_t h = 2u * word;
+                const float v0 = (x & 0xFFFFu) ? Tab16<T>::value(h) : xmax,
+                            v1 = (x >> 16) ? Tab16<T>::value(h + 1u) : xmax;
+                unsigned long long q0, q1;
+                dec_weight2(v0, v1, xmax, dw, q0, q1);
+                m = (unsigned long long)(x & 0xFFFFu) * q0 + (unsigned long long)(x >> 16) * q1;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                m += __shfl_xor_sync(0xFFFFFFFFu, m, o);
+            if (lane == 0)  // the owner of block blk (tab_base inverted)
+                s_ml[blk < 512 ? 511 - blk : blk] = m;
         }
     }
+    __syncthreads();
+    const unsigned long long ml = s_ml[t];
     uint32_t c_ex;
     unsigned long long m_ex, m_tot;
     tab_scan(cl, ml, c_ex, m_ex, m_tot, s_wc, s_wm);
@@ -859,7 +931,7 @@ __device__ bool tab_select(unsigned int *tab, int V, float cdec, int tk, float t
         __syncthreads();
         tck = s_i[3];
         if (t < 32)
-            tab_walk<T, true>(tab, tck, 0u, xmax, cdec, (uint32_t)s_i[4], need, s_u[2], 0ull, s_i + 5, s_u);
+            tab_walk<T, true>(tab, tck, 0u, xmax, dw, (uint32_t)s_i[4], need, s_u[2], 0ull, s_i + 5, s_u);
         __syncthreads();
         kk = (uint32_t)s_i[5];
         tot_p = s_u[0];
@@ -889,7 +961,7 @@ __device__ bool tab_select(unsigned int *tab, int V, float cdec, int tk, float t
     __syncthreads();
     const int tcp = s_i[7];
     if (tcp >= 0 && t < 32)
-        tab_walk<T, false>(tab, tcp, kk, xmax, cdec, 0u, 0u, s_u[3], athr, s_i + 8, s_u + 1);
+        tab_walk<T, false>(tab, tcp, kk, xmax, dw, 0u, 0u, s_u[3], athr, s_i + 8, s_u + 1);
     __syncthreads();
     if (s_i[8] < 0) {  // no key reached the bound: the lowest key kept
         cut_out = Tab16<T>::value(key_pat(use_k ? kk : kmin));
@@ -915,8 +987,10 @@ __global__ void __launch_bounds__(kTabThreads, 1) verify_filter_tab_kernel(Verif
     __shared__ FilterSel sel;
     __shared__ int s_i[9];
     __shared__ unsigned long long s_u[5];
+    __shared__ unsigned long long s_ml[kTabThreads];
     __shared__ float s_m, s_s, s_xmax, s_cut;
     __shared__ int s_bad, s_skip;
+    __shared__ float2 s_e2[64];
     const float c = scale_of(a);
     const Unit u = decode_unit(a);
     const T *row = reinterpret_cast<const T *>(a.logits) + (size_t)u.row * a.V;
@@ -925,7 +999,9 @@ __global__ void __launch_bounds__(kTabThreads, 1) verify_filter_tab_kernel(Verif
         s_skip = (!u.needed || stopped_before(a.stop_enc, u.b, u.j)) ? 1 : 0;
         s_cut = -INFINITY;
     }
+    dec_table_init(s_e2);
     __syncthreads();
+    const DecScale dw{a.dec_hi, a.dec_lo, s_e2};
     if (!s_skip) {
         const int tk = a.top_k ? a.top_k[u.b] : 0;
         const float tp = a.top_p ? a.top_p[u.b] : 1.0f;
@@ -943,8 +1019,8 @@ __global__ void __launch_bounds__(kTabThreads, 1) verify_filter_tab_kernel(Verif
                 bool bad;
                 unsigned long long kept;
                 // block-uniform result (it derives from shared values only)
-                if (tab_select<T>(tab, a.V, a.dec_scale, tk, tp, use_k, use_p, xmax, bad, cutv, kept, s_wc, s_wm,
-                                  s_i, s_u)) {
+                if (tab_select<T>(tab, a.V, dw, tk, tp, use_k, use_p, xmax, bad, cutv, kept, s_wc, s_wm,
+                                  s_i, s_u, s_ml)) {
                     if (t == 0) {
                         s_m = xmax * c;
                         s_bad = bad ? 1 : 0;
@@ -958,7 +1034,7 @@ __global__ void __launch_bounds__(kTabThreads, 1) verify_filter_tab_kernel(Verif
                     float cr = -INFINITY;
                     unsigned long long km = 0ull;
                     if (!badm)
-                        cr = radix_cut<T, NT>(row, a.V, xm, a.dec_scale, tk, tp, use_k, use_p,
+                        cr = radix_cut<T, NT>(row, a.V, xm, dw, tk, tp, use_k, use_p,
                                               *reinterpret_cast<FilterHist *>(tab), sel, s_wc, s_wm, km);
                     if (t == 0) {
                         s_m = xm * c;

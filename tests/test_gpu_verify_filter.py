@@ -3,10 +3,13 @@ the CUDA path (spec_verify_sample_filtered) vs the CPU oracle.
 
 Same bar as the unfiltered stochastic tests (tokens and counts equal except
 counted boundary decisions of the ratio test or the draw; normalised draw
-distributions within 1e-6), plus: the kept set itself is exact -- wherever a
-sequence draws its bonus from the processed target distribution, the support
-of that distribution equals the oracle's.  Both sides decide the top-p
-boundary with the same stated fixed-point arithmetic, so it has no tolerance.
+distributions within 1e-6), plus: the kept set itself -- wherever a sequence
+draws its bonus from the processed target distribution, the support of that
+distribution equals the oracle's.  The oracle decides the top-p boundary on
+the real masses (fp64 with an error band); the kernel on fixed-point weights
+within ~2e-9 of them.  A kept set may differ only where the oracle's margin
+lies inside the kernel's bound; such rows count as boundary cases, under the
+same bar (fewer than 1e-4 of the decisions).
 """
 import numpy as np
 import pytest
@@ -139,6 +142,22 @@ def test_config5_shape_bf16():
           top_k=None, top_p=np.full(64, 0.95, np.float32))
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("top_p", [0.5, 0.9, 0.95])
+def test_kept_set_of_every_row(dtype, top_p):
+    """k = 0: every row is its sequence's bonus row, so the support of every
+    drawn distribution is the kernel's kept set for that row; 128 rows of
+    128256 N(0,1) logits (the stochastic workloads' vocabulary) against the
+    oracle's top-p on the real masses."""
+    B, V = 128, 128256
+    x, q, d, u = sample_round_inputs(B, 0, V, 0.5, seed=int(top_p * 1000) + (dtype == "bf16"), dtype=dtype)
+    before = STATS.get("kept_sets", 0) + STATS["boundary"]
+    check(x, DT_OF[dtype], q, d, u, top_k=None, top_p=np.full(B, top_p, np.float32))
+    # every row either had its kept set compared or was a counted boundary
+    # case (a top-p decision inside the kernel's bound, or a draw boundary)
+    assert STATS.get("kept_sets", 0) + STATS["boundary"] - before == B
+
+
 @pytest.mark.parametrize("V,dtype", [(32768, "bf16"), (50001, "f16"), (128256, "bf16"), (262144, "f16")])
 def test_table_form_16bit(V, dtype):
     """16-bit rows of at least 32768 logits: the cut from the table of value
@@ -203,6 +222,9 @@ def test_table_form_counter_wrap_and_bad_rows(dtype):
 
 
 def test_zz_filter_statistics():
+    """Every file above that shares the counters: kept sets compared, and
+    boundary cases (ratio test, draw, or a top-p decision inside the
+    kernel's bound) below 1e-4 of the decisions."""
     assert STATS.get("kept_sets", 0) > 500, STATS
     assert STATS["decisions"] > 20_000, STATS  # one boundary case would then be below 1e-4 of them
     assert STATS["boundary"] < 1e-4 * STATS["decisions"], STATS

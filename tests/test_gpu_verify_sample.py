@@ -86,11 +86,37 @@ def _boundary_explains(x, dt, q, d, u, T, b, o_out, o_na, o_ne, o_res, g_out, g_
     return bool(np.all(np.abs(c[lo:hi] - uu) <= TOL * uu))
 
 
+# The kernel's top-p decision weights are within ~2e-9 relative of the real
+# masses (plus the floor of each fixed-point weight, 2^-40 of the top mass),
+# so its kept set can differ from the oracle's only where the oracle's margin
+# |A - top_p M| (in units of the top mass) is below this bound.
+def kernel_topp_bound(total, V):
+    return 1e-8 * total + V * 2.0 ** -39
+
+
+def _kept_set_boundary(x, dt, T, b, rows, top_k, top_p):
+    """True when a top-p decision of one of the sequence's rows lies within
+    the kernel's arithmetic bound of the oracle's (counted, not a failure)."""
+    if top_p is None:
+        return False
+    k1, V = x.shape[1], x.shape[-1]
+    for j in rows:
+        if j >= k1:
+            continue
+        _, margin, total, _ = oracle.filter_info(x.reshape(-1, V), dt, b * k1 + j, T, *_filt(top_k, top_p, b))
+        if margin <= kernel_topp_bound(total, V):
+            STATS["kept_set_boundary"] = STATS.get("kept_set_boundary", 0) + 1
+            return True
+    return False
+
+
 def check(x, dt, q, d, u, T=1.0, draft_len=None, eos=-1, remaining=None, residual=True, top_k=None, top_p=None):
     """top_k / top_p: None, or per-sequence numpy arrays (int32 / fp32): the
     filtered entry point runs and the oracle applies the same transforms.
     Where filtering is on, the support of every drawn bonus distribution
-    (the kept set itself) must equal the oracle's exactly."""
+    (the kept set itself) must equal the oracle's, except where the oracle's
+    top-p margin lies within the kernel's arithmetic bound (a counted
+    boundary case)."""
     kw = dict(temperature=T, draft_len=None if draft_len is None else to_dev(draft_len), eos_id=eos,
               remaining=None if remaining is None else to_dev(remaining), want_residual=residual)
     if top_k is None and top_p is None:
@@ -112,9 +138,12 @@ def check(x, dt, q, d, u, T=1.0, draft_len=None, eos=-1, remaining=None, residua
             assert int(g_fl[b]) & 4
             continue
         same = (np.array_equal(g_out[b], o_out[b]) and g_na[b] == o_na[b] and g_ne[b] == o_ne[b])
+        used = range(int(max(o_ne[b], g_ne[b])) + 1)
         if not same:
-            assert _boundary_explains(x, dt, q, d, u, T, b, o_out, o_na[b], o_ne[b], o_res, g_out, g_na[b],
-                                      g_ne[b], int(kbs[b]), top_k, top_p), (b, g_out[b], o_out[b], g_na[b], o_na[b])
+            if not _kept_set_boundary(x, dt, T, b, used, top_k, top_p):
+                assert _boundary_explains(x, dt, q, d, u, T, b, o_out, o_na[b], o_ne[b], o_res, g_out, g_na[b],
+                                          g_ne[b], int(kbs[b]), top_k, top_p), (b, g_out[b], o_out[b], g_na[b],
+                                                                                 o_na[b])
             STATS["boundary"] += 1
             continue
         assert (int(g_fl[b]) & ~4) == (int(o_fl[b]) & ~4), (b, g_fl[b], o_fl[b])
@@ -124,9 +153,15 @@ def check(x, dt, q, d, u, T=1.0, draft_len=None, eos=-1, remaining=None, residua
             row = int(o_na[b])
             kb = int(kbs[b])
             if (top_k is not None or top_p is not None) and (row == kb or int(o_fl[b]) & 2):
-                assert np.array_equal(g_res[b] > 0, o_res[b] > 0), (b, np.flatnonzero(g_res[b] > 0)[:20],
-                                                                     np.flatnonzero(o_res[b] > 0)[:20])
+                if not np.array_equal(g_res[b] > 0, o_res[b] > 0):
+                    assert _kept_set_boundary(x, dt, T, b, [row], top_k, top_p), (
+                        b, np.flatnonzero(g_res[b] > 0)[:20], np.flatnonzero(o_res[b] > 0)[:20])
+                    STATS["boundary"] += 1
+                    continue
                 STATS["kept_sets"] = STATS.get("kept_sets", 0) + 1
+            if err.max() > RES_TOL and _kept_set_boundary(x, dt, T, b, [row], top_k, top_p):
+                STATS["boundary"] += 1  # the processed distribution itself differs by a boundary group
+                continue
             if err.max() > RES_TOL:
                 tol = residual_tolerance(x, dt, q, T, b, k1 - 1, row, row == kb, o_res[b], top_k, top_p)
                 assert (err <= tol).all(), (b, err.max(), tol[np.argmax(err - tol)])
