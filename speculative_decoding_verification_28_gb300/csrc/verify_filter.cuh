@@ -72,7 +72,7 @@ struct FilterSel {
     int bin;                       // selected digit
     unsigned int cnt_above;        // count of the digits above it (this level)
     unsigned long long mass_above; // Q mass of the digits above it (this level)
-    double bound;                  // top_p * total Q mass (set at the first top-p level)
+    unsigned long long athr;       // ceil(top_p * total Q mass) (set at the first top-p level)
     int low_thread;                // last thread holding a non-empty digit
 };
 
@@ -342,10 +342,37 @@ __device__ void hist_pass(const T *row, int V, int l, uint32_t prefix, uint32_t 
     }
 }
 
+// ceil(tp * M) for an fp32 0 <= tp < 1 and M < 2^63, exactly, in integers:
+// tp = m * 2^-s with a 24-bit m and s >= 24, so the product is m * M / 2^s
+// with m * M a 128-bit integer.  The top-p test "mass above < tp * M" is
+// then "mass above < ceil(tp * M)" for integer masses.
+__device__ __forceinline__ unsigned long long ceil_mul_frac(float tp, unsigned long long M)
+{
+    const uint32_t b = __float_as_uint(tp);
+    const uint32_t e = (b >> 23) & 0xFFu;
+    const unsigned long long m = (unsigned long long)((b & 0x7FFFFFu) | (e ? 0x800000u : 0u));
+    if ((b >> 31) || m == 0ull || M == 0ull)
+        return 0ull;                           // tp <= 0
+    const int sh = e ? 150 - (int)e : 149;     // tp = m * 2^-sh, sh >= 24 for tp < 1
+    const unsigned long long lo = m * M, hi = __umul64hi(m, M);
+    if (sh >= 128)
+        return 1ull;                           // 0 < tp * M < 1
+    unsigned long long q;
+    bool rem;
+    if (sh < 64) {
+        q = (lo >> sh) | (hi << (64 - sh));
+        rem = (lo & ((1ull << sh) - 1ull)) != 0ull;
+    } else {
+        q = sh == 64 ? hi : hi >> (sh - 64);
+        rem = lo != 0ull || (sh > 64 && (hi & ((1ull << (sh - 64)) - 1ull)) != 0ull);
+    }
+    return q + (rem ? 1ull : 0ull);
+}
+
 // First digit from the top whose inclusive cumulative count reaches `need`
 // (counts), or the first non-empty digit from the top with
-// double(base + cumulative mass) >= bound (masses; bound = top_p * total at
-// the first level).  With masses and no such digit, the lowest non-empty one.
+// base + cumulative mass >= ceil(top_p * total) (masses; the threshold is
+// formed at the first level).  With masses and no such digit, the lowest non-empty one.
 // Thread t owns digits nb-1-tP .. nb-P-tP (P = nb / NT), scanned in
 // descending order.  Ends with a barrier; the result is in `sel`.
 template <bool kMass, int NT>
@@ -389,10 +416,10 @@ __device__ void hist_select(const FilterHist &h, int nb, unsigned int need, unsi
         }
         total += s_wm[i];
     }
-    double bound = 0.0;
+    unsigned long long athr = 0ull;
     if (kMass)
-        bound = first_level ? (double)top_p * (double)total : sel.bound;
-    const bool earlier = kMass ? (cb > 0u && (double)(base + mb) >= bound) : (cb >= need);
+        athr = first_level ? ceil_mul_frac(top_p, total) : sel.athr;
+    const bool earlier = kMass ? (cb > 0u && base + mb >= athr) : (cb >= need);
     if (!earlier) {
         unsigned int cc = cb;
         unsigned long long mm = mb;
@@ -400,7 +427,7 @@ __device__ void hist_select(const FilterHist &h, int nb, unsigned int need, unsi
             const int bin = top - i;
             const unsigned int c1 = h.cnt[bin];
             const unsigned long long m1 = h.mass(bin);
-            const bool hit = kMass ? (c1 > 0u && (double)(base + mm + m1) >= bound) : (cc + c1 >= need);
+            const bool hit = kMass ? (c1 > 0u && base + mm + m1 >= athr) : (cc + c1 >= need);
             if (hit) {
                 sel.bin = bin;
                 sel.cnt_above = cc;
@@ -436,7 +463,7 @@ __device__ void hist_select(const FilterHist &h, int nb, unsigned int need, unsi
             sel.mass_above = m_at;
         }
         if (first_level && t == 0)
-            sel.bound = bound;
+            sel.athr = athr;
         __syncthreads();
     }
 }
@@ -659,18 +686,65 @@ __device__ __forceinline__ uint32_t rank_pat(int t, int r)
 __device__ __forceinline__ int tab_base(int t) { return t < 512 ? 0x3FE0 - 32 * t : 32 * t; }
 __device__ __forceinline__ uint32_t tab_half(uint32_t x, uint32_t h) { return (h & 1u) ? (x >> 16) : (x & 0xFFFFu); }
 
-// all threads: counts every logit of the row into the table (cleared before)
+// Element-wise minimum of two 16-byte vectors of 16-bit floats (NaN is not
+// propagated: a NaN anywhere already makes the row's maximum NaN).
 template <typename T>
-__device__ __forceinline__ void tab_count(const T *row, int V, unsigned int *tab)
+__device__ __forceinline__ uint32_t min_word16(uint32_t a, uint32_t b);
+template <>
+__device__ __forceinline__ uint32_t min_word16<__nv_bfloat16>(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+template <>
+__device__ __forceinline__ uint32_t min_word16<__half>(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("min.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+template <typename T>
+__device__ __forceinline__ float word_lo(uint32_t w)
+{
+    if constexpr (std::is_same<T, __nv_bfloat16>::value)
+        return __uint_as_float(w << 16);
+    else
+        return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
+}
+template <typename T>
+__device__ __forceinline__ float word_hi(uint32_t w)
+{
+    if constexpr (std::is_same<T, __nv_bfloat16>::value)
+        return __uint_as_float(w & 0xFFFF0000u);
+    else
+        return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+}
+
+// all threads: counts every logit of the row into the table (cleared
+// before), and finds the row's maximum (NaN-propagating: a NaN anywhere
+// gives NaN) and minimum on the way: warp w's go to s_mx[w] / s_mn[w]
+// (the caller's barrier publishes them)
+template <typename T>
+__device__ __forceinline__ void tab_count(const T *row, int V, unsigned int *tab, float *s_mx, float *s_mn)
 {
     constexpr int NT = kTabThreads;
     const ChunkSplit<T> cs(row, 0, V);
     const int t = threadIdx.x;
+    float mx = -INFINITY, mn = INFINITY;
     auto add = [&](uint32_t h) { atomicAdd(tab + (h >> 1), (h & 1u) ? 0x10000u : 1u); };
+    auto add1 = [&](unsigned short h) {
+        add(h);
+        const float v = word_lo<T>(h);
+        mx = max_nan(mx, v);
+        mn = fminf(mn, v);
+    };
     for (int v = t; v < cs.head_end; v += NT)
-        add(__ldg(reinterpret_cast<const unsigned short *>(row) + v));
+        add1(__ldg(reinterpret_cast<const unsigned short *>(row) + v));
     const T *body = row + cs.head_end;
     constexpr int U = 8;  // 128 KB of loads in flight per CTA (one CTA per SM)
+    bool any = false;
+    uint32_t wmx = 0u, wmn = 0u;  // running packed maximum / minimum of the vectors
     for (int base = 0; base < cs.nvec; base += U * NT) {
         uint4 r[U];
 #pragma unroll
@@ -689,19 +763,39 @@ __device__ __forceinline__ void tab_count(const T *row, int V, unsigned int *tab
                     add(w[e] & 0xFFFFu);
                     add(w[e] >> 16);
                 }
+                const uint32_t vx = max_word<T>(max_word<T>(r[u].x, r[u].y), max_word<T>(r[u].z, r[u].w));
+                const uint32_t vn =
+                    min_word16<T>(min_word16<T>(r[u].x, r[u].y), min_word16<T>(r[u].z, r[u].w));
+                wmx = any ? max_word<T>(wmx, vx) : vx;
+                wmn = any ? min_word16<T>(wmn, vn) : vn;
+                any = true;
             }
         }
     }
     for (int v = cs.tail_beg + t; v < V; v += NT)
-        add(__ldg(reinterpret_cast<const unsigned short *>(row) + v));
+        add1(__ldg(reinterpret_cast<const unsigned short *>(row) + v));
+    if (any) {
+        mx = max_nan(mx, max_nan(word_lo<T>(wmx), word_hi<T>(wmx)));
+        mn = fminf(mn, fminf(word_lo<T>(wmn), word_hi<T>(wmn)));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mx = max_nan(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+    }
+    if ((t & 31) == 0) {
+        s_mx[t >> 5] = mx;
+        s_mn[t >> 5] = mn;
+    }
 }
 
-// Block-wide exclusive prefix (thread order) of a count and a mass, with the
-// mass total; ends with a barrier.  s_wc: one slot per warp, s_wm: one per
-// warp and the total (warp 0 turns the warp totals into their exclusive
-// prefix by shuffles).
+// Block-wide exclusive prefix (thread order) of a count and a mass, with
+// both totals; ends with a barrier.  s_wc, s_wm: one slot per warp and the
+// total (warp 0 turns the warp totals into their exclusive prefix by
+// shuffles).
 __device__ __forceinline__ void tab_scan(uint32_t c, unsigned long long m, uint32_t &c_ex, unsigned long long &m_ex,
-                                         unsigned long long &m_tot, unsigned int *s_wc, unsigned long long *s_wm)
+                                         uint32_t &c_tot, unsigned long long &m_tot, unsigned int *s_wc,
+                                         unsigned long long *s_wm)
 {
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     uint32_t ic = c;
@@ -739,33 +833,16 @@ __device__ __forceinline__ void tab_scan(uint32_t c, unsigned long long m, uint3
         __syncwarp();
         s_wc[lane] = wc - wc0;
         s_wm[lane] = wm - wm0;
-        if (lane == 31)
-            s_wm[32] = wm;  // the block total
+        if (lane == 31) {  // the block totals
+            s_wc[32] = wc;
+            s_wm[32] = wm;
+        }
     }
     __syncthreads();
     c_ex = ic - c + s_wc[w];
     m_ex = im - m + s_wm[w];
+    c_tot = s_wc[32];
     m_tot = s_wm[32];
-}
-
-// The smallest integer A with double(A) >= bound (0 < bound < 2^63), so that
-// double(A) >= bound becomes A >= threshold.  floor(bound) lies within one
-// ulp of bound (at most 2^10 above 2^53), and rounding is monotonic: a
-// binary search over [floor - 1024, floor + 1].
-__device__ __forceinline__ unsigned long long u64_threshold(double bound)
-{
-    if (!(bound > 0.0))
-        return 0ull;
-    const unsigned long long a = (unsigned long long)bound;
-    unsigned long long lo = a > 1024ull ? a - 1024ull : 0ull, hi = a + 1ull;
-    while (lo < hi) {
-        const unsigned long long mid = lo + (hi - lo) / 2;
-        if ((double)mid >= bound)
-            hi = mid;
-        else
-            lo = mid + 1ull;
-    }
-    return hi;
 }
 
 // Warp 0 (all lanes): walks the 64 keys of thread tc in descending order,
@@ -817,85 +894,73 @@ __device__ __forceinline__ void tab_walk(const unsigned int *tab, int tc, uint32
     }
 }
 
+// 16-bit pattern of a value of the row (exact: the value came from one)
+template <typename T>
+__device__ __forceinline__ uint32_t pat_of(float v)
+{
+    if constexpr (std::is_same<T, __nv_bfloat16>::value)
+        return __float_as_uint(v) >> 16;
+    else
+        return (uint32_t)__half_as_ushort(__float2half_rn(v));
+}
+
 // Table selection (all threads, after tab_count and a barrier).  Returns
 // false when the table is unusable (a wrapped counter: the caller runs the
 // radix selection); else the row's maximum, its non-finite flag and, when
-// the row is filtered and finite, the cut and the kept Q mass.  s_i: 9 ints,
-// s_u: 5 u64, s_ml: kTabThreads u64 of shared scratch (every slot written
-// once per row).
+// the row is filtered and finite, the cut and the kept Q mass.  xmax / xmin:
+// the row's maximum (NaN-propagating) and minimum from tab_count.  s_i: 9
+// ints, s_u: 5 u64, s_cl / s_ml: kTabThreads u32 / u64 of shared scratch
+// (every slot written once per row).
 template <typename T>
-__device__ bool tab_select(unsigned int *tab, int V, const DecScale &dw, int tk, float tp, bool use_k, bool use_p,
-                           float &xmax_out, bool &bad_out, float &cut_out, unsigned long long &kept_out,
+__device__ bool tab_select(unsigned int *tab, int V, float xmax, float xmin, const DecScale &dw, int tk, float tp,
+                           bool use_k, bool use_p, bool &bad_out, float &cut_out, unsigned long long &kept_out,
                            unsigned int *s_wc, unsigned long long *s_wm, int *s_i, unsigned long long *s_u,
-                           unsigned long long *s_ml)
+                           unsigned int *s_cl, unsigned long long *s_ml)
 {
     const int t = threadIdx.x, lane = t & 31;
-    const unsigned int *mine = tab + tab_base(t);
+    s_cl[t] = 0u;  // the merged pass writes the slots of non-empty blocks only
+    s_ml[t] = 0ull;
     if (t == 0) {  // -0 (pattern 0x8000) joins +0 (pattern 0)
         const uint32_t nz = tab[0x4000] & 0xFFFFu, pz = tab[0] & 0xFFFFu;
         s_i[0] = (nz + pz > 0xFFFFu) ? 1 : 0;  // would wrap
         tab[0x4000] -= nz;
         tab[0] += nz;
-        s_i[1] = -1;     // highest non-empty key
-        s_i[2] = 0;      // total count
-        s_i[3] = -1;     // thread holding the k-th largest key
-        s_i[5] = -1;     // the k-th largest key
-        s_i[6] = 65536;  // lowest non-empty key
-        s_i[7] = -1;     // thread holding the top-p boundary
-        s_i[8] = -1;     // the top-p boundary key
+        s_i[3] = -1;  // thread holding the k-th largest key
+        s_i[5] = -1;  // the k-th largest key
+        s_i[7] = -1;  // thread holding the top-p boundary
+        s_i[8] = -1;  // the top-p boundary key
     }
+    // +inf or a NaN anywhere, or nothing above -inf
+    bad_out = !(xmax > -INFINITY && xmax < INFINITY);
     __syncthreads();
-    s_ml[t] = 0ull;  // pass 2 writes the slots of non-empty blocks only
-    // pass 1: count, highest and lowest non-empty key (words read in an order
-    // rotated by the lane: no bank conflicts)
-    const uint32_t pbase = 2u * (uint32_t)tab_base(t);
-    uint32_t cl = 0;
-    int top = -1, bot = 65536;
-#pragma unroll 8
-    for (int i = 0; i < 32; ++i) {  // branch-free: the loads and tests overlap
-        const int j = (i + lane) & 31;
-        const uint32_t x = mine[j];
-        const uint32_t n0 = x & 0xFFFFu, n1 = x >> 16;
-        cl += n0 + n1;
-        const uint32_t h = pbase + 2u * (uint32_t)j;
-        const int k0 = (int)pat_key(h), k1 = (int)pat_key(h + 1u);
-        top = max(top, max(n0 ? k0 : -1, n1 ? k1 : -1));
-        bot = min(bot, min(n0 ? k0 : 65536, n1 ? k1 : 65536));
-    }
-    const uint32_t cw = __reduce_add_sync(0xFFFFFFFFu, cl);
-    top = __reduce_max_sync(0xFFFFFFFFu, top);
-    bot = __reduce_min_sync(0xFFFFFFFFu, bot);
-    if (lane == 0) {
-        atomicAdd(s_i + 2, (int)cw);
-        atomicMax(s_i + 1, top);
-        atomicMin(s_i + 6, bot);
-    }
-    __syncthreads();
-    if (s_i[0] || s_i[2] != V)
-        return false;  // a counter wrapped (or would have)
-    const uint32_t kmax = (uint32_t)s_i[1], kmin = (uint32_t)s_i[6];
-    const float xmax = Tab16<T>::value(key_pat(kmax));
-    xmax_out = xmax;
-    // +inf or a NaN at the top, a NaN at the bottom, or nothing above -inf
-    bad_out = kmax >= Tab16<T>::kPinfKey || kmin < Tab16<T>::kNinfKey || kmax <= Tab16<T>::kNinfKey;
-    if (bad_out || !(use_k || use_p))
-        return true;
-    // pass 2: Q masses, two values per word with paired weights.  The
-    // non-empty words form a band of values, which in the threads' own
-    // ranges would load a few warps only; so the table's 1024 blocks of 32
-    // words (block b = the range of one thread) are dealt out by warp --
-    // warp w takes blocks w, w + 32, ... -- each lane one word of the block,
-    // and the block's sum goes to its owner's slot (no atomics: each block
-    // has one warp).  Empty blocks are skipped by a ballot.
+    if (bad_out)
+        return s_i[0] == 0;  // a wrap is not checked here: the row is undefined either way
+    if (xmax == 0.0f)
+        xmax = 0.0f;  // -0 counts as +0 (its key)
+    if (xmin == 0.0f)
+        xmin = 0.0f;
+    const uint32_t kmin = pat_key(pat_of<T>(xmin));
+    // one pass: each thread range's count and Q mass, two values per word
+    // with paired weights.  The non-empty words form a band of values, which
+    // in the threads' own ranges would load a few warps only; so the table's
+    // 1024 blocks of 32 words (block b = the range of one thread) are dealt
+    // out by warp -- warp w takes blocks w, w + 32, ... -- each lane one word
+    // of the block, and the block's sums go to its owner's slots (no atomics:
+    // each block has one warp).  A first sweep of ballots marks the
+    // non-empty blocks; only those are visited.
     {
         const int w = t >> 5;
-#pragma unroll 2
-        for (int i = 0; i < 32; ++i) {
+        uint32_t busy = 0u;  // bit i: block w + 32 i holds a count (independent loads)
+#pragma unroll 8
+        for (int i = 0; i < 32; ++i)
+            busy |= (__ballot_sync(0xFFFFFFFFu, tab[32u * (uint32_t)(w + 32 * i) + (uint32_t)lane] != 0u) != 0u ? 1u : 0u)
+                    << i;
+        while (busy) {
+            const int i = __ffs(busy) - 1;
+            busy &= busy - 1u;
             const int blk = w + 32 * i;  // words 32 blk .. 32 blk + 31
             const uint32_t word = 32u * (uint32_t)blk + (uint32_t)lane;
             const uint32_t x = tab[word];
-            if (__ballot_sync(0xFFFFFFFFu, x != 0u) == 0u)
-                continue;
             unsigned long long m = 0;
             if (x != 0u) {
                 const uint32_t h = 2u * word;
@@ -905,18 +970,25 @@ __device__ bool tab_select(unsigned int *tab, int V, const DecScale &dw, int tk,
                 dec_weight2(v0, v1, xmax, dw, q0, q1);
                 m = (unsigned long long)(x & 0xFFFFu) * q0 + (unsigned long long)(x >> 16) * q1;
             }
+            const uint32_t c = __reduce_add_sync(0xFFFFFFFFu, (x & 0xFFFFu) + (x >> 16));
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1)
                 m += __shfl_xor_sync(0xFFFFFFFFu, m, o);
-            if (lane == 0)  // the owner of block blk (tab_base inverted)
-                s_ml[blk < 512 ? 511 - blk : blk] = m;
+            if (lane == 0) {  // the owner of block blk (tab_base inverted)
+                const int own = blk < 512 ? 511 - blk : blk;
+                s_cl[own] = c;
+                s_ml[own] = m;
+            }
         }
     }
     __syncthreads();
+    const uint32_t cl = s_cl[t];
     const unsigned long long ml = s_ml[t];
-    uint32_t c_ex;
+    uint32_t c_ex, c_tot;
     unsigned long long m_ex, m_tot;
-    tab_scan(cl, ml, c_ex, m_ex, m_tot, s_wc, s_wm);
+    tab_scan(cl, ml, c_ex, m_ex, c_tot, m_tot, s_wc, s_wm);
+    if (s_i[0] || c_tot != (uint32_t)V)
+        return false;  // a counter wrapped (or would have)
     // top-k: the key where the count from the top reaches tk (ties kept)
     uint32_t kk = 0u;                  // lowest key top-k keeps
     unsigned long long tot_p = m_tot;  // Q mass of the logits top-k keeps
@@ -942,14 +1014,11 @@ __device__ bool tab_select(unsigned int *tab, int V, const DecScale &dw, int tk,
         return true;
     }
     // top-p among the keys >= kk: the first non-empty key from the top at
-    // which double(mass above + its mass) >= double(tp) * double(tot_p).  The
-    // running mass only grows, so that key lies in the one thread whose
-    // kept range holds a key, has its mass above below the bound (or nothing
-    // non-empty above) and reaches the bound within the range.
-    if (t == 0)  // double(A) >= double(tp) * double(tot_p) as an integer test
-        s_u[4] = u64_threshold((double)tp * (double)tot_p);
-    __syncthreads();
-    const unsigned long long athr = s_u[4];
+    // which mass above + its mass >= ceil(tp * tot_p).  The running mass only
+    // grows, so that key lies in the one thread whose kept range holds a key,
+    // has its mass above below the threshold (or nothing non-empty above) and
+    // reaches it within the range.
+    const unsigned long long athr = ceil_mul_frac(tp, tot_p);
     if (t <= tck) {
         const uint32_t cl_r = (t == tck) ? 1u : cl;  // thread tck keeps kk at least
         const unsigned long long ml_r = (t == tck) ? tot_p - m_ex : ml;
@@ -982,11 +1051,12 @@ __global__ void __launch_bounds__(kTabThreads, 1) verify_filter_tab_kernel(Verif
     constexpr int NT = kTabThreads;
     extern __shared__ __align__(16) unsigned int tab[];
     __shared__ float s_f[4 * NT / 32];
-    __shared__ unsigned int s_wc[NT / 32];
+    __shared__ unsigned int s_wc[NT / 32 + 1];
     __shared__ unsigned long long s_wm[NT / 32 + 1];
     __shared__ FilterSel sel;
     __shared__ int s_i[9];
     __shared__ unsigned long long s_u[5];
+    __shared__ unsigned int s_cl[kTabThreads];
     __shared__ unsigned long long s_ml[kTabThreads];
     __shared__ float s_m, s_s, s_xmax, s_cut;
     __shared__ int s_bad, s_skip;
@@ -1010,17 +1080,23 @@ __global__ void __launch_bounds__(kTabThreads, 1) verify_filter_tab_kernel(Verif
             for (int i = t; i < kTabWords / 4; i += NT)
                 reinterpret_cast<uint4 *>(tab)[i] = make_uint4(0u, 0u, 0u, 0u);  // 8 stores per thread
             __syncthreads();
-            tab_count<T>(row, a.V, tab);
+            tab_count<T>(row, a.V, tab, s_f, s_f + NT / 32);
             if (t == 0)
                 s_skip = stopped_before(a.stop_enc, u.b, u.j) ? 1 : 0;
             __syncthreads();
             if (!s_skip) {
-                float xmax, cutv;
+                // the warps' extremes, reduced by every warp (one per lane)
+                float xmax = s_f[t & 31], xmin = s_f[NT / 32 + (t & 31)], cutv;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    xmax = max_nan(xmax, __shfl_xor_sync(0xFFFFFFFFu, xmax, o));
+                    xmin = fminf(xmin, __shfl_xor_sync(0xFFFFFFFFu, xmin, o));
+                }
                 bool bad;
                 unsigned long long kept;
                 // block-uniform result (it derives from shared values only)
-                if (tab_select<T>(tab, a.V, dw, tk, tp, use_k, use_p, xmax, bad, cutv, kept, s_wc, s_wm,
-                                  s_i, s_u, s_ml)) {
+                if (tab_select<T>(tab, a.V, xmax, xmin, dw, tk, tp, use_k, use_p, bad, cutv, kept, s_wc, s_wm,
+                                  s_i, s_u, s_cl, s_ml)) {
                     if (t == 0) {
                         s_m = xmax * c;
                         s_bad = bad ? 1 : 0;
