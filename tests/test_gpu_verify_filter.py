@@ -174,20 +174,24 @@ def _bits16(x):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-def test_table_form_ties_and_signed_zeros(dtype):
-    """Logits quantised to quarters (many tokens per value, -0 and +0 both
+@pytest.mark.parametrize("step", [64, 4])
+def test_table_form_ties_and_signed_zeros(dtype, step):
+    """Logits quantised to 1/step (many tokens per value, -0 and +0 both
     present and equal): the k-th value and the top-p boundary fall inside
-    groups of equal logits, some at zero."""
-    rng = np.random.default_rng(61)
+    groups of equal logits, some at zero; at 1/64 a value holds a few
+    hundred tokens, at 1/4 several thousand."""
+    rng = np.random.default_rng(61 + step)
     B, k, V = 64, 3, 40000
     x, q, d, u = sample_round_inputs(B, k, V, 0.5, seed=62, dtype=dtype)
-    xf = np.round(rng.standard_normal(x.shape).astype(np.float32) * 4) / 4
+    xf = np.round(rng.standard_normal(x.shape).astype(np.float32) * step) / step
     xf[xf == 0] = np.where(rng.random(np.count_nonzero(xf == 0)) < 0.5, -0.0, 0.0)
     if dtype == "bf16":
         xs = (xf.view(np.uint32) >> 16).astype(np.uint16)
     else:
         xs = xf.astype(np.float16)
     assert (_bits16(xs) == 0x8000).any() and (_bits16(xs) == 0).any()
+    counts = np.unique(_bits16(xs)[0, 0], return_counts=True)[1]
+    assert (counts.max() < 1023) == (step == 64)
     tk, tp = _params(rng, B, V)
     check(xs, DT_OF[dtype], q, d, u, top_k=tk, top_p=tp)
     check(xs, DT_OF[dtype], q, d, u, top_k=np.full(B, 5000, np.int32), top_p=np.full(B, 0.6, np.float32))
@@ -197,7 +201,8 @@ def test_table_form_ties_and_signed_zeros(dtype):
 def test_table_form_counter_wrap_and_bad_rows(dtype):
     """Rows where more than 65535 logits share one value (a 16-bit counter
     wraps, or would when -0 joins +0): the row takes the radix selection and
-    matches all the same.  Rows with a NaN (either sign) or +inf are flagged."""
+    matches all the same.  Rows with 50000 masked (-inf) logits stay in the
+    table.  Rows with a NaN (either sign) or +inf are flagged."""
     rng = np.random.default_rng(71)
     B, k, V = 12, 2, 140000
     x, q, d, u = sample_round_inputs(B, k, V, 0.5, seed=72, dtype=dtype)
@@ -212,6 +217,12 @@ def test_table_form_counter_wrap_and_bad_rows(dtype):
             idx = rng.choice(V, 70000, replace=False)
             xb[b, j, idx[:40000]] = 0x0000
             xb[b, j, idx[40000:]] = 0x8000
+    ninf = 0xFF80 if dtype == "bf16" else 0xFC00
+    for b in range(2, B, 3):  # 50000 masked tokens (-inf), the proposals kept unmasked
+        for j in range(k + 1):
+            idx = rng.choice(V, 50000, replace=False)
+            idx = idx[~np.isin(idx, d[b])]
+            xb[b, j, idx] = ninf
     xb[2, 0, 17] = 0xFFC1 if dtype == "bf16" else 0xFE01   # negative NaN
     xb[5, 1, 99] = pinf                                     # +inf
     xb[8, 0, 1234] = 0x7FC1 if dtype == "bf16" else 0x7E01  # positive NaN
