@@ -92,10 +92,13 @@ __device__ void sample_row_decide(const VerifyArgs &a, const Unit &u, const T *r
 
 // One lane, after row u.row's results are stored: counts the row for its
 // sequence; true for the sequence's last row (whose warp then writes the
-// outputs with sample_seq_outputs).
-__device__ __forceinline__ bool sample_seq_count(const VerifyArgs &a, int b)
+// outputs with sample_seq_outputs).  wrote: the row stored results (a row
+// that did not -- one past its sequence's stop -- has nothing to publish
+// before the count, and its results are never read).
+__device__ __forceinline__ bool sample_seq_count(const VerifyArgs &a, int b, bool wrote = true)
 {
-    __threadfence();
+    if (wrote)
+        __threadfence();
     return atomicAdd(a.seq_cnt + b, 1) == a.k;
 }
 
@@ -147,12 +150,12 @@ __device__ __forceinline__ void sample_seq_outputs(const VerifyArgs &a, int b, i
 }
 
 // Warp 0 (all 32 lanes) after a row of sequence u.b is done: counts the row;
-// the sequence's last row writes the outputs.
-__device__ __forceinline__ void sample_seq_finish(const VerifyArgs &a, const Unit &u)
+// the sequence's last row writes the outputs.  wrote: as sample_seq_count.
+__device__ __forceinline__ void sample_seq_finish(const VerifyArgs &a, const Unit &u, bool wrote = true)
 {
     int last_row = 0;
     if ((threadIdx.x & 31) == 0)
-        last_row = sample_seq_count(a, u.b) ? 1 : 0;
+        last_row = sample_seq_count(a, u.b, wrote) ? 1 : 0;
     if (__shfl_sync(0xFFFFFFFFu, last_row, 0))
         sample_seq_outputs(a, u.b, u.kb, u.rem);
 }

@@ -635,7 +635,7 @@ __global__ void __launch_bounds__(NT, NT >= 1024 ? 1 : (NT >= 512 ? 2 : 3)) veri
         eval = (u.needed && !stopped_before(a.stop_enc, u.b, u.j)) ? 1 : 0;
     if (eval)
         sample_row_decide<T>(a, u, row, s_m, s_kept, cut, s_bad != 0);
-    sample_seq_finish(a, u);
+    sample_seq_finish(a, u, __shfl_sync(0xFFFFFFFFu, eval, 0) != 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -1065,9 +1065,15 @@ __global__ void __launch_bounds__(kTabThreads, 1) verify_filter_tab_kernel(Verif
     const Unit u = decode_unit(a);
     const T *row = reinterpret_cast<const T *>(a.logits) + (size_t)u.row * a.V;
     const int t = threadIdx.x;
+    // thread 0 carries the row's ratio-test inputs: the proposal now, the
+    // rest once the count pass is done, so that both load rounds are off
+    // the row's end
+    int y_in = -1;
+    RowInputs in{-1, 0.0f, 1.0f, 0.0f};
     if (t == 0) {
         s_skip = (!u.needed || stopped_before(a.stop_enc, u.b, u.j)) ? 1 : 0;
         s_cut = -INFINITY;
+        y_in = row_proposal(a, u);
     }
     dec_table_init(s_e2);
     __syncthreads();
@@ -1081,8 +1087,10 @@ __global__ void __launch_bounds__(kTabThreads, 1) verify_filter_tab_kernel(Verif
                 reinterpret_cast<uint4 *>(tab)[i] = make_uint4(0u, 0u, 0u, 0u);  // 8 stores per thread
             __syncthreads();
             tab_count<T>(row, a.V, tab, s_f, s_f + NT / 32);
-            if (t == 0)
+            if (t == 0) {
                 s_skip = stopped_before(a.stop_enc, u.b, u.j) ? 1 : 0;
+                in = row_inputs<T>(a, u, row, y_in);
+            }
             __syncthreads();
             if (!s_skip) {
                 // the warps' extremes, reduced by every warp (one per lane)
@@ -1139,9 +1147,12 @@ __global__ void __launch_bounds__(kTabThreads, 1) verify_filter_tab_kernel(Verif
     int eval = 0;
     if (t == 0)
         eval = (u.needed && !stopped_before(a.stop_enc, u.b, u.j)) ? 1 : 0;
-    if (eval)
-        sample_row_decide<T>(a, u, row, s_m, s_s, s_cut, s_bad != 0);
-    sample_seq_finish(a, u);
+    if (eval) {
+        if (in.y != y_in)  // the unfiltered path: the rest of the inputs now
+            in = row_inputs<T>(a, u, row, y_in);
+        row_decide(a, u, in, s_m, s_s, s_cut, s_bad != 0);
+    }
+    sample_seq_finish(a, u, __shfl_sync(0xFFFFFFFFu, eval, 0) != 0);
 }
 
 // Block size by the number of rows (one CTA per row): a row per SM at most
