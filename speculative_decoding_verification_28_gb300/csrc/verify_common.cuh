@@ -143,15 +143,21 @@ constexpr float kLog2e = 1.4426950408889634f;  // log2(e): e^x = 2^(x log2 e)
 // needed: once a stop before row j is recorded for the sequence, the row will
 // never be evaluated (the record only moves earlier), so the warp can drop
 // the rest of its chunk.  Lane 0 reads the word; the decision is warp-uniform.
+// The read is split in two so that it can travel with a batch of loads:
+// load() issues it (lane 0; the other lanes return 0), stopped() decides on
+// its value one batch later, when it has long arrived.  A decision on a word
+// read one batch earlier only drops a chunk later, never one that is needed.
 struct StopProbe {
     const int *stop_enc;
     int b, j;
-    __device__ __forceinline__ bool dropped() const
+    __device__ __forceinline__ int load() const
     {
-        int s = 0;
-        if ((threadIdx.x & 31) == 0)
-            s = stopped_before(stop_enc, b, j) ? 1 : 0;
-        return __shfl_sync(0xFFFFFFFFu, s, 0) != 0;
+        return ((threadIdx.x & 31) == 0) ? ld_relaxed(stop_enc + b) : 0;
+    }
+    __device__ __forceinline__ bool stopped(int enc) const
+    {
+        const int e = __shfl_sync(0xFFFFFFFFu, enc, 0);
+        return e > 0 && (kStopBase - e) < j;
     }
 };
 

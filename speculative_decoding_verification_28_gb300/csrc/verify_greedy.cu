@@ -58,8 +58,9 @@ __device__ uint64_t chunk_argmax(const T *row, int V, int lo, int hi, uint64_t *
         first = first == 0xFFFFFFFFu ? (uint32_t)(cs.head_end + t * VEC) : first;
     bool signalled = y < 0 || y >= V;  // warp-uniform
     float xy = INFINITY;
+    int enc = 0;  // the stop word, read with the previous batch
     for (int base = 0; base < cs.nvec; base += UNROLL * kGreedyThreads) {  // warp-uniform trip count
-        if (base > 0 && probe.dropped())
+        if (base > 0 && probe.stopped(enc))
             break;
         const int i = base + t;
         uint4 r[UNROLL];
@@ -69,6 +70,7 @@ __device__ uint64_t chunk_argmax(const T *row, int V, int lo, int hi, uint64_t *
             if (vi < cs.nvec)
                 r[u] = ld_stream16(body + (size_t)vi * VEC);
         }
+        enc = probe.load();  // in flight with the batch
         if (base == 0 && !signalled)
             xy = Storage<T>::at(row, y);  // after the batch's loads are in flight
 #pragma unroll

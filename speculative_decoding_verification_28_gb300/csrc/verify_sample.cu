@@ -109,6 +109,7 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
     float2 sa[2] = {make_float2(s, 0.0f), make_float2(0.0f, 0.0f)};
     int base = 0;
     bool dropped = false;
+    int enc = 0;  // the stop word, read with the previous full batch
     // one batch of NB vectors per thread starting at vector `base`; guarded
     // (the last, partial batch): vectors past the chunk's end read as -inf
     auto batch = [&](auto nb, auto guard) {
@@ -120,6 +121,8 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
             const int vi = base + t + u * NT;
             r[u] = (!kGuard || vi < cs.nvec) ? ld_stream16(body + (size_t)vi * VEC) : neg_inf_vec<T>();
         }
+        if (!kGuard)
+            enc = probe.load();  // in flight with the batch
         uint4 mx = r[0];
 #pragma unroll
         for (int u = 1; u < NB; ++u)
@@ -152,7 +155,7 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
     };
     // full batches of 8 vectors (128 bytes in flight per thread)
     for (; base + 8 * NT <= cs.nvec; base += 8 * NT) {  // warp-uniform trip count
-        if (base > 0 && probe.dropped()) {
+        if (base > 0 && probe.stopped(enc)) {
             dropped = true;
             break;
         }
@@ -160,7 +163,7 @@ __device__ void chunk_softmax_stats(const T *row, int lo, int hi, float c, float
     }
     // the rest (fewer than 8 vectors per thread): one guarded batch, with the
     // same single packed maximum and lazy rescale test
-    if (!dropped && base < cs.nvec && (base == 0 || !probe.dropped()))
+    if (!dropped && base < cs.nvec && (base == 0 || !probe.stopped(enc)))
         batch(std::integral_constant<int, 8>(), std::true_type());
     s = (sa[0].x + sa[0].y) + (sa[1].x + sa[1].y);
     if (m > -INFINITY && mt > m) {  // bring the sum to the exact maximum

@@ -138,6 +138,99 @@ def test_early_rejection_declines_when_unsure():
     run_both(x, oracle.DT_F32, d, repeat=2)
 
 
+# Larger batches (512 to 1152 target rows, several chunks per row): the cases
+# above at such sizes -- ragged chunks, stop rules, ties and NaN across chunk
+# boundaries, early rejection, acceptance 0 and 1, and one workspace shared
+# by calls of different k and V.
+BIG_B, BIG_K = 128, 4  # 640 rows
+
+
+@pytest.mark.parametrize("V", [1, 7, 16383, 16384, 16385, 2 * 16384 + 5, 40000])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_large_batch_ragged_vocab_sizes(V, dtype):
+    x, d = greedy_round_inputs(BIG_B, BIG_K, V, 0.6, 1.0, seed=300 + V, dtype=dtype)
+    run_both(x, DT_OF[dtype], d, repeat=2)
+
+
+@pytest.mark.parametrize("alpha", [0.0, 0.5, 1.0])
+def test_large_batch_acceptance_extremes(alpha):
+    """alpha 0: only row 0 of every sequence is needed; alpha 1: every row."""
+    x, d = greedy_round_inputs(64, 8, 50000, alpha, 1.0, seed=int(alpha * 10) + 310, dtype="bf16")
+    ref = run_both(x, oracle.DT_BF16, d, repeat=2)
+    if alpha == 1.0:
+        assert (ref[2] == 9).all()
+    if alpha == 0.0:
+        assert (ref[2] == 1).all()
+
+
+def test_large_batch_stop_rules_and_per_sequence_arguments():
+    rng = np.random.default_rng(17)
+    B, k, V = 128, 6, 20000
+    for trial in range(6):
+        x, d = greedy_round_inputs(B, k, V, 0.8, 1.0, seed=350 + trial, dtype="bf16")
+        dl = rng.integers(0, k + 1, size=B).astype(np.int32)
+        rem = rng.integers(-1, k + 3, size=B).astype(np.int32)
+        eos = int(rng.integers(0, V))
+        d[::5, 1] = eos
+        run_both(x, oracle.DT_BF16, d, draft_len=dl, eos=eos, remaining=rem)
+
+
+def test_large_batch_ties_nan_inf_and_signed_zero():
+    """The special rows of the small case, placed among 128 sequences, with
+    ties 16384 elements apart."""
+    B, k, V = BIG_B, 3, 3 * 16384 + 100
+    x, d = greedy_round_inputs(B, k, V, 0.5, 1.0, seed=360, dtype="f32")
+    x[0, :, :] = 1.0
+    x[1, :, [5, 16384 + 3, 2 * 16384 + 7]] = 20.0
+    x[2, :, 30000] = np.inf
+    x[2, :, 100] = np.inf
+    x[3, :, 40000] = np.nan
+    x[3, :, 30] = 25.0
+    x[3, 1, 10] = np.nan
+    x[4, :, :] = -np.inf
+    x[4, 2, 77] = -1.0
+    x[5, :, :] = -0.0
+    x[5, :, 4] = 0.0
+    d[:6] = np.array([[0, 0, 0], [5, 5, 1], [100, 30000, 100], [40000, 10, 40000], [0, 0, 77], [0, 4, 0]],
+                     np.int32)
+    run_both(x, oracle.DT_F32, d, repeat=2)
+
+
+def test_large_batch_early_rejection_declines_when_unsure():
+    rng = np.random.default_rng(93)
+    B, k, V = BIG_B, 4, 3 * 16384 + 37
+    x = rng.standard_normal((B, k + 1, V)).astype(np.float32)
+    d = rng.integers(0, V, (B, k)).astype(np.int32)
+    for b in range(B):
+        for j in range(k):
+            x[b, j, d[b, j]] = 10.0
+    x[0, 0, d[0, 0]] = np.nan
+    d[1, 0] = V + 3
+    x[2, 1, 7] = 10.0
+    d[2, 1] = max(int(d[2, 1]), 8)
+    x[2, 1, d[2, 1]] = 10.0
+    x[3, 0, d[3, 0]] = np.inf
+    x[4, 0, d[4, 0]] = -np.inf
+    x[5, 0, (d[5, 0] + 100) % V] = np.nan
+    x[6, 0, :] = -5.0
+    x[6, 0, d[6, 0]] = 1.0
+    x[6, 0, V - 2] = 2.0
+    run_both(x, oracle.DT_F32, d, repeat=2)
+
+
+def test_large_batch_calls_share_one_workspace():
+    """Every counter is returned to zero by every call: calls of different k
+    and V on one workspace stay exact."""
+    B = BIG_B
+    ws = sv.Workspace(B, sv.MAX_K, 40000, dev())
+    for trial, (k, V) in enumerate([(8, 40000), (2, 40000), (3, 1000), (1, 20000), (31, 700), (8, 40000)]):
+        x, d = greedy_round_inputs(B, k, V, 0.7, 2.0, seed=370 + trial, dtype="bf16")
+        o, na, ne = sv.spec_verify_greedy(logits_to_dev(x, oracle.DT_BF16), to_dev(d), workspace=ws)
+        ref = oracle.verify_greedy(x, oracle.DT_BF16, d)
+        assert np.array_equal(o.cpu().numpy(), ref[0]) and np.array_equal(ne.cpu().numpy(), ref[2])
+        assert np.array_equal(na.cpu().numpy(), ref[1])
+
+
 def test_empty_batch_is_a_noop():
     x = torch.zeros((0, 3, 100), dtype=torch.float32, device=dev())
     d = torch.zeros((0, 2), dtype=torch.int32, device=dev())
