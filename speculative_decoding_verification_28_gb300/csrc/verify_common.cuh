@@ -4,9 +4,9 @@
 // One CTA handles one unit (sequence b, row j, vocabulary chunk c).  Units are
 // numbered row-major over j first: all row-0 units of every sequence, then all
 // row-1 units, ...  Verification only needs rows up to the first stop of a
-// sequence (first rejection, EOS, budget, or the bonus row): "remaining
-// proposals were predicted under the wrong prefix; discard them and the later
-// verification rows" ("Chapter 10 Speculative Decoding (Code Walkthrough)",
+// sequence (first rejection, EOS, budget, or the bonus row): the proposals
+// after a rejection were drafted after a token that is not kept, so their
+// rows decide nothing ("Chapter 10 Speculative Decoding (Code Walkthrough)",
 // §4.2).  So each unit first looks at the earliest stop row already known for
 // its sequence and skips its reads when that row lies before it.  The known
 // stop can only move earlier, and a row is evaluated only if no earlier stop
