@@ -169,6 +169,22 @@ def test_table_form_16bit(V, dtype):
     check(x, DT_OF[dtype], q, d, u, top_k=tk, top_p=tp)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_table_form_stop_rules_and_per_sequence_arguments(dtype):
+    """The table form (16-bit rows of 40000 logits) with draft lengths, output
+    budgets (including none) and an EOS that some proposals carry, over 160
+    sequences -- more rows than SMs, so rows are skipped once a stop is known."""
+    rng = np.random.default_rng(21 + len(dtype))
+    B, k, V = 160, 5, 40000
+    x, q, d, u = sample_round_inputs(B, k, V, 0.5, seed=210 + len(dtype), dtype=dtype)
+    tk, tp = _params(rng, B, V)
+    dl = rng.integers(0, k + 1, size=B).astype(np.int32)
+    rem = rng.integers(-1, k + 3, size=B).astype(np.int32)
+    eos = int(rng.integers(0, V))
+    d[::6, 0] = eos
+    check(x, DT_OF[dtype], q, d, u, draft_len=dl, eos=eos, remaining=rem, top_k=tk, top_p=tp)
+
+
 def _bits16(x):
     return x.view(np.uint16) if x.dtype == np.float16 else x
 

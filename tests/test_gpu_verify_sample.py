@@ -241,6 +241,21 @@ def test_stop_rules_and_per_sequence_arguments():
         check(x, oracle.DT_BF16, q, d, u, draft_len=dl, eos=eos, remaining=rem)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_stop_rules_with_chunked_rows(dtype):
+    """The per-sequence arguments on rows split over several work units
+    (B=128, k=6: 896 rows of 40000 logits, three chunks each), so that a
+    row's stop, budget and draft length meet the chunk counters."""
+    rng = np.random.default_rng(13)
+    B, k, V = 128, 6, 40000
+    x, q, d, u = sample_round_inputs(B, k, V, 0.5, seed=60 + len(dtype), dtype=dtype)
+    dl = rng.integers(0, k + 1, size=B).astype(np.int32)
+    rem = rng.integers(-1, k + 3, size=B).astype(np.int32)
+    eos = int(rng.integers(0, V))
+    d[::7, 0] = eos
+    check(x, DT_OF[dtype], q, d, u, draft_len=dl, eos=eos, remaining=rem)
+
+
 def test_flags_and_degenerate_rows():
     V, k, B = 16, 2, 6
     rng = np.random.default_rng(3)
