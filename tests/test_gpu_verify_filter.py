@@ -185,6 +185,18 @@ def test_table_form_stop_rules_and_per_sequence_arguments(dtype):
     check(x, DT_OF[dtype], q, d, u, draft_len=dl, eos=eos, remaining=rem, top_k=tk, top_p=tp)
 
 
+@pytest.mark.parametrize("T", [0.6, 2.5])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_table_form_temperature(T, dtype):
+    """The table form with T != 1: its decision weights take log2(e) / T as
+    a float pair, and the kept probabilities the scaled softmax."""
+    rng = np.random.default_rng(int(T * 10) + len(dtype))
+    B, k, V = 48, 3, 40000
+    x, q, d, u = sample_round_inputs(B, k, V, 0.5, seed=int(T * 100) + len(dtype), dtype=dtype)
+    tk, tp = _params(rng, B, V)
+    check(x, DT_OF[dtype], q, d, u, T=T, top_k=tk, top_p=tp)
+
+
 def _bits16(x):
     return x.view(np.uint16) if x.dtype == np.float16 else x
 
