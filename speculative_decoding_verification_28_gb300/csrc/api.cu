@@ -24,7 +24,8 @@ int check_workspace(void *ws, size_t have, size_t need)
 
 int launched(cudaError_t e) { return e == cudaSuccess ? SPEC_OK : SPEC_ECUDA; }
 
-int check_verify_common(const void *logits, int dt, int B, int k, int V, const int32_t *draft,
+int check_verify_common(const void *logits, int dt, int B, int k, int V, const int32_t *draft, const int32_t *draft_len,
+                        const int32_t *remaining,
                         const int32_t *out_tokens, const int32_t *n_accept, const int32_t *n_emit)
 {
     if (B < 0 || k < 0 || k > SPEC_MAX_K || V < 1)
@@ -39,16 +40,18 @@ int check_verify_common(const void *logits, int dt, int B, int k, int V, const i
     if (units > INT_MAX)
         return SPEC_EINVAL;
     if (!aligned(logits, dtype_bytes(dt)) || !aligned(out_tokens, 4) || !aligned(n_accept, 4) ||
-        !aligned(n_emit, 4) || (draft && !aligned(draft, 4)))
+        !aligned(n_emit, 4) || (draft && !aligned(draft, 4)) || (draft_len && !aligned(draft_len, 4)) ||
+        (remaining && !aligned(remaining, 4)))
         return SPEC_EALIGN;
     return SPEC_OK;
 }
 
 // ---- verification: checks and arguments ----------------------------------
-int check_greedy(const void *logits, int dt, int B, int k, int V, const int32_t *draft, const int32_t *out_tokens,
+int check_greedy(const void *logits, int dt, int B, int k, int V, const int32_t *draft, const int32_t *draft_len,
+                 const int32_t *remaining, const int32_t *out_tokens,
                  const int32_t *n_accept, const int32_t *n_emit, void *workspace, size_t workspace_bytes)
 {
-    const int rc = check_verify_common(logits, dt, B, k, V, draft, out_tokens, n_accept, n_emit);
+    const int rc = check_verify_common(logits, dt, B, k, V, draft, draft_len, remaining, out_tokens, n_accept, n_emit);
     if (rc != SPEC_OK || B == 0)
         return rc;
     return check_workspace(workspace, workspace_bytes, spec_workspace_bytes(B, k, V));
@@ -56,10 +59,11 @@ int check_greedy(const void *logits, int dt, int B, int k, int V, const int32_t 
 
 int check_sample(const void *logits, int dt, float temperature, const int32_t *top_k, const float *top_p,
                  const float *draft_probs, const int32_t *draft, const float *uniforms, int B, int k, int V,
+                 const int32_t *draft_len, const int32_t *remaining,
                  const int32_t *out_tokens, const int32_t *n_accept, const int32_t *n_emit,
                  const float *out_residual, const uint32_t *flags, void *workspace, size_t workspace_bytes)
 {
-    const int rc = check_verify_common(logits, dt, B, k, V, draft, out_tokens, n_accept, n_emit);
+    const int rc = check_verify_common(logits, dt, B, k, V, draft, draft_len, remaining, out_tokens, n_accept, n_emit);
     if (rc != SPEC_OK || B == 0)
         return rc;
     if (!(temperature > 0.0f) || !(temperature <= 3.0e38f) || !uniforms || (k > 0 && !draft_probs))
@@ -122,7 +126,8 @@ int run_sample(const void *logits, spec_dtype dt, float temperature, const int32
                size_t workspace_bytes, void *cuda_stream)
 {
     const int rc = check_sample(logits, dt, temperature, top_k, top_p, draft_probs, draft, uniforms, B, k, V,
-                                out_tokens, n_accept, n_emit, out_residual, flags, workspace, workspace_bytes);
+                                draft_len, remaining, out_tokens, n_accept, n_emit, out_residual, flags, workspace,
+                                workspace_bytes);
     if (rc != SPEC_OK || B == 0)
         return rc;
     return launched(launch_verify_sample(sample_args(logits, temperature, top_k, top_p, draft_probs, draft, uniforms, B,
@@ -180,8 +185,8 @@ int spec_verify_greedy(const void *target_logits, spec_dtype dt, int B, int k, i
                        const int32_t *remaining, int32_t *out_tokens, int32_t *n_accept, int32_t *n_emit,
                        void *workspace, size_t workspace_bytes, void *cuda_stream)
 {
-    const int rc = check_greedy(target_logits, dt, B, k, V, draft_tokens, out_tokens, n_accept, n_emit, workspace,
-                                workspace_bytes);
+    const int rc = check_greedy(target_logits, dt, B, k, V, draft_tokens, draft_len, remaining, out_tokens, n_accept,
+                                n_emit, workspace, workspace_bytes);
     if (rc != SPEC_OK || B == 0)
         return rc;
     return launched(launch_verify_greedy(verify_args(target_logits, B, k, V, draft_tokens, draft_len, eos_id, remaining,
@@ -446,8 +451,8 @@ int spec_round_greedy(const void *target_logits, spec_dtype dt, int B, int k, in
                       int32_t *out_tokens, int32_t *n_accept, int32_t *n_emit, int32_t *len_new, int32_t *pad_new,
                       int32_t *width_new, int32_t *err, void *workspace, size_t workspace_bytes, void *cuda_stream)
 {
-    int rc = check_greedy(target_logits, dt, B, k, V, draft_tokens, out_tokens, n_accept, n_emit, workspace,
-                          workspace_bytes);
+    int rc = check_greedy(target_logits, dt, B, k, V, draft_tokens, draft_len, remaining, out_tokens, n_accept, n_emit,
+                          workspace, workspace_bytes);
     if (rc == SPEC_OK)
         rc = check_realign(caches, n_caches, B, S, len, pad, n_emit, len_new, pad_new, width_new, err, workspace,
                            workspace_bytes);
@@ -475,7 +480,8 @@ int spec_round_sample(const void *target_logits, spec_dtype dt, float temperatur
                       int32_t *width_new, int32_t *err, void *workspace, size_t workspace_bytes, void *cuda_stream)
 {
     int rc = check_sample(target_logits, dt, temperature, top_k, top_p, draft_probs, draft_tokens, uniforms, B, k, V,
-                          out_tokens, n_accept, n_emit, out_residual, flags, workspace, workspace_bytes);
+                          draft_len, remaining, out_tokens, n_accept, n_emit, out_residual, flags, workspace,
+                          workspace_bytes);
     if (rc == SPEC_OK)
         rc = check_realign(caches, n_caches, B, S, len, pad, n_emit, len_new, pad_new, width_new, err, workspace,
                            workspace_bytes);

@@ -69,7 +69,8 @@ extern "C" int spec_verify_greedy_static(const void *target_logits, spec_dtype d
     if ((long long)B * (k + 1) * verify_chunks(B, k, V) > 0x7FFFFFFFLL)
         return SPEC_EINVAL;
     if (!aligned_to(target_logits, dt == SPEC_F32 ? 4 : 2) || !aligned_to(out_tokens, 4) ||
-        !aligned_to(n_accept, 4) || !aligned_to(n_emit, 4) || (draft_tokens && !aligned_to(draft_tokens, 4)))
+        !aligned_to(n_accept, 4) || !aligned_to(n_emit, 4) || (draft_tokens && !aligned_to(draft_tokens, 4)) ||
+        (draft_len && !aligned_to(draft_len, 4)) || (remaining && !aligned_to(remaining, 4)))
         return SPEC_EALIGN;
     const Layout lay = make_layout(B, k, V);
     if (lay.total > SPEC_STATIC_SCRATCH_BYTES)

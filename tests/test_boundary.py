@@ -75,6 +75,23 @@ def test_greedy_argument_errors(lib):
     assert greedy(lib, B=0) == 0  # empty batch: valid no-op, nothing launched
 
 
+def test_per_sequence_arguments_must_be_aligned(lib):
+    """draft_len and remaining are int32 arrays: a misaligned one is refused
+    on the host (SPEC_EALIGN) by every verification entry point, before any
+    launch."""
+    for dl, rem in ((FAKE_ODD, None), (None, FAKE_ODD)):
+        assert lib.spec_verify_greedy(FAKE, 1, 2, 3, 100, FAKE, dl, -1, rem, FAKE, FAKE, FAKE, FAKE, 1 << 30,
+                                      None) == -5
+        assert lib.spec_verify_sample(FAKE, 0, 1.0, FAKE, FAKE, FAKE, 2, 2, 50, dl, -1, rem, FAKE, FAKE, FAKE, None,
+                                      None, FAKE, 1 << 30, None) == -5
+        assert lib.spec_verify_sample_filtered(FAKE, 0, 1.0, FAKE, None, FAKE, FAKE, FAKE, 2, 2, 50, dl, -1, rem,
+                                               FAKE, FAKE, FAKE, None, None, FAKE, 1 << 30, None) == -5
+        assert lib.spec_verify_greedy_static(FAKE, 1, 2, 3, 100, FAKE, dl, -1, rem, FAKE, FAKE, FAKE, None) == -5
+    # aligned ones pass the same checks (the greedy call then fails only on its
+    # missing workspace)
+    assert lib.spec_verify_greedy(FAKE, 1, 2, 3, 100, FAKE, FAKE, -1, FAKE, FAKE, FAKE, FAKE, None, 0, None) == -3
+
+
 def test_sample_argument_errors(lib):
     def sample(temp=1.0, u=FAKE, q=FAKE, k=2):
         return lib.spec_verify_sample(FAKE, 0, temp, q, FAKE, u, 2, k, 50, None, -1, None, FAKE, FAKE, FAKE, None,
